@@ -1,0 +1,247 @@
+"""Paged-attention oracle -- TEST INFRASTRUCTURE ONLY.
+
+A plain fp64 CPU implementation of the paged-attention hot path
+(``pa_oracle.cpp``), loaded with ctypes.  Only ``tests/``,
+``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg may import
+this package.  It shares no code with ``paged_kv_cache_50_gb300`` and never
+imports it; inputs come from the seeded generators in ``workloads``.
+
+Every function takes numpy arrays (bf16 data as ``uint16`` bit patterns, or
+``float64``) and returns fp64 results.  See ``pa_oracle.cpp`` for the
+page-by-page citations and the readings taken where the pages are silent.
+"""
+
+from __future__ import annotations
+
+import contextlib
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pa_oracle.cpp")
+_LIB = os.path.join(_HERE, "_build", "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``pa_oracle.cpp`` into ``_build/liboracle.so`` with g++."""
+    os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".{os.getpid()}.tmp"
+    cmd = ["g++", "-std=c++17", "-O2", "-fPIC", "-shared", "-pthread",
+           "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _bind(path):
+    lib = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    i32, i64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double
+    lib.oracle_reshape_and_cache.argtypes = [P, P, P, P, i64, i32, i32, i32, i64]
+    lib.oracle_reshape_and_cache.restype = i32
+    for name in ("oracle_paged_attention_bf16", "oracle_paged_attention_f64"):
+        fn = getattr(lib, name)
+        fn.argtypes = [P, P, P, i32, P, P, i32, i32, i32, i32, i32, i64, f64,
+                       i32, P, P, P, i32]
+        fn.restype = i32
+    for name in ("oracle_split_partials_bf16", "oracle_split_partials_f64"):
+        fn = getattr(lib, name)
+        fn.argtypes = [P, P, P, i32, P, i32, i32, i32, i32, i32, i64, f64,
+                       i32, P, i32]
+        fn.restype = i32
+    lib.oracle_lse_merge.argtypes = [P, i32, i32, i32, i32, P, P]
+    lib.oracle_lse_merge.restype = None
+    for name in ("oracle_mla_decode_bf16", "oracle_mla_decode_f64"):
+        fn = getattr(lib, name)
+        fn.argtypes = [P, P, P, i32, P, i32, i32, i32, i32, i32, i64, f64,
+                       P, P, P, i32]
+        fn.restype = i32
+    lib.oracle_bf16_to_f64.argtypes = [P, P, i64]
+    lib.oracle_bf16_to_f64.restype = None
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = _bind(build())
+        return _lib
+
+
+def build_variant(source_text: str, out_path: str) -> str:
+    """Compile an edited copy of the oracle source (the mutation tests plant
+    deliberate slips this way to show that the pins catch them)."""
+    src = out_path + ".cpp"
+    with open(src, "w") as f:
+        f.write(source_text)
+    subprocess.run(["g++", "-std=c++17", "-O1", "-fPIC", "-shared", "-pthread",
+                    "-fno-fast-math", "-ffp-contract=off", src, "-o", out_path], check=True)
+    return out_path
+
+
+def source_text() -> str:
+    with open(_SRC) as f:
+        return f.read()
+
+
+@contextlib.contextmanager
+def using_library(path: str):
+    """Route every oracle call to another build of the source for a while."""
+    global _lib
+    old = _load()
+    with _lock:
+        _lib = _bind(path)
+    try:
+        yield
+    finally:
+        with _lock:
+            _lib = old
+
+
+def default_threads() -> int:
+    return os.cpu_count() or 1
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _kind(a):
+    a = np.asarray(a)
+    if a.dtype == np.uint16:
+        return "bf16", a
+    return "f64", np.ascontiguousarray(a, dtype=np.float64)
+
+
+def reshape_and_cache(key, value, pool, slot_mapping, block_size):
+    """Returns a copy of ``pool`` ([nb, 2, bs, Hkv, d] uint16) with the new
+    key/value rows ([T, Hkv, d] uint16) written at ``slot_mapping`` [T]."""
+    lib = _load()
+    key = _c(key, np.uint16)
+    value = _c(value, np.uint16)
+    out = np.array(pool, dtype=np.uint16, copy=True, order="C")
+    slots = _c(slot_mapping, np.int64)
+    T, Hkv, d = key.shape
+    nb = out.shape[0]
+    rc = lib.oracle_reshape_and_cache(_ptr(key), _ptr(value), _ptr(out), _ptr(slots),
+                                      T, Hkv, d, block_size, nb)
+    if rc != 0:
+        raise ValueError("slot outside the pool")
+    return out
+
+
+def paged_attention(q, pool, block_table, query_start_loc, seq_lens, scale,
+                    causal=True, row_mask=None, threads=None):
+    """Varlen paged attention.  q [T, Hq, d]; pool [nb, 2, bs, Hkv, d]
+    (uint16 bf16 bits, or float64).  Returns (out [T, Hq, d], lse [T, Hq])
+    in fp64; rows not selected by ``row_mask`` are left at zero."""
+    lib = _load()
+    kq, q = _kind(q)
+    kp, pool = _kind(pool)
+    if kq != kp:
+        raise TypeError("q and pool must both be bf16 bits or both float64")
+    q = np.ascontiguousarray(q)
+    pool = np.ascontiguousarray(pool)
+    bt = _c(block_table, np.int32)
+    qsl = _c(query_start_loc, np.int32)
+    sl = _c(seq_lens, np.int32)
+    T, Hq, d = q.shape
+    nb, two, bs, Hkv, d2 = pool.shape
+    assert two == 2 and d2 == d
+    N = sl.shape[0]
+    out = np.zeros((T, Hq, d), np.float64)
+    lse = np.full((T, Hq), -np.inf, np.float64)
+    mask = None if row_mask is None else _c(row_mask, np.uint8)
+    fn = lib.oracle_paged_attention_bf16 if kq == "bf16" else lib.oracle_paged_attention_f64
+    rc = fn(_ptr(q), _ptr(pool), _ptr(bt), bt.shape[1], _ptr(qsl), _ptr(sl), N, Hq,
+            Hkv, d, bs, nb, float(scale), int(bool(causal)), _ptr(mask), _ptr(out),
+            _ptr(lse), threads or default_threads())
+    if rc != 0:
+        raise ValueError("invalid paged-attention input (block id or lengths)")
+    return out, lse
+
+
+def split_partials(q, pool, block_table, seq_lens, scale, num_splits, threads=None):
+    """Split-KV stage 1 for one query per request.  q [N, Hq, d].
+    Returns partials [N, Hq, S, d + 1] fp64 (normalised o, then lse)."""
+    lib = _load()
+    kq, q = _kind(q)
+    kp, pool = _kind(pool)
+    if kq != kp:
+        raise TypeError("q and pool must both be bf16 bits or both float64")
+    q = np.ascontiguousarray(q)
+    pool = np.ascontiguousarray(pool)
+    bt = _c(block_table, np.int32)
+    sl = _c(seq_lens, np.int32)
+    N, Hq, d = q.shape
+    nb, _, bs, Hkv, _ = pool.shape
+    out = np.zeros((N, Hq, num_splits, d + 1), np.float64)
+    fn = lib.oracle_split_partials_bf16 if kq == "bf16" else lib.oracle_split_partials_f64
+    rc = fn(_ptr(q), _ptr(pool), _ptr(bt), bt.shape[1], _ptr(sl), N, Hq, Hkv, d, bs,
+            nb, float(scale), int(num_splits), _ptr(out), threads or default_threads())
+    if rc != 0:
+        raise ValueError("invalid split-KV input")
+    return out
+
+
+def lse_merge(partials):
+    """Split-KV stage 2.  partials [N, H, S, dv + 1] -> (out [N, H, dv], lse [N, H])."""
+    lib = _load()
+    p = _c(partials, np.float64)
+    N, H, S, dv1 = p.shape
+    out = np.zeros((N, H, dv1 - 1), np.float64)
+    lse = np.zeros((N, H), np.float64)
+    lib.oracle_lse_merge(_ptr(p), N, H, S, dv1 - 1, _ptr(out), _ptr(lse))
+    return out, lse
+
+
+def mla_decode(q, pool, block_table, seq_lens, scale, kv_lora_rank=512,
+               rope_dim=64, req_mask=None, threads=None):
+    """MLA latent decode.  q [B, H, kv_lora_rank + rope_dim];
+    pool [nb, bs, kv_lora_rank + rope_dim].  Returns (out [B, H, kv_lora_rank],
+    lse [B, H]) fp64; requests not in ``req_mask`` are left at zero."""
+    lib = _load()
+    kq, q = _kind(q)
+    kp, pool = _kind(pool)
+    if kq != kp:
+        raise TypeError("q and pool must both be bf16 bits or both float64")
+    q = np.ascontiguousarray(q)
+    pool = np.ascontiguousarray(pool)
+    bt = _c(block_table, np.int32)
+    sl = _c(seq_lens, np.int32)
+    B, H, dk = q.shape
+    nb, bs, dk2 = pool.shape
+    assert dk == dk2 == kv_lora_rank + rope_dim
+    out = np.zeros((B, H, kv_lora_rank), np.float64)
+    lse = np.full((B, H), -np.inf, np.float64)
+    mask = None if req_mask is None else _c(req_mask, np.uint8)
+    fn = lib.oracle_mla_decode_bf16 if kq == "bf16" else lib.oracle_mla_decode_f64
+    rc = fn(_ptr(q), _ptr(pool), _ptr(bt), bt.shape[1], _ptr(sl), B, H, kv_lora_rank,
+            rope_dim, bs, nb, float(scale), _ptr(mask), _ptr(out), _ptr(lse),
+            threads or default_threads())
+    if rc != 0:
+        raise ValueError("invalid MLA input (block id)")
+    return out, lse
+
+
+def bf16_to_f64(bits):
+    """Exact widening of bf16 bit patterns (uint16) to float64."""
+    lib = _load()
+    b = _c(bits, np.uint16)
+    out = np.empty(b.shape, np.float64)
+    lib.oracle_bf16_to_f64(_ptr(b), _ptr(out), b.size)
+    return out

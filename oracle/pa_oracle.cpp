@@ -1,0 +1,394 @@
+// Paged-attention oracle: TEST INFRASTRUCTURE ONLY.
+//
+// A plain, slow, fp64 CPU restatement of what the paged-attention hot path
+// computes.  Only the tests, the smoke check and the benchmark's CPU-baseline
+// leg may load it; the product library never does, and this file shares no
+// code, header or constant with the CUDA path.
+//
+// Sources (page title, section):
+//  * "Attention Backends" (vLLM model-execution notes), section
+//    "What 'paged attention' requires of a kernel": the inputs (queries,
+//    new K/V, the whole cache, block_table[N, max_blocks], slot_mapping[T],
+//    query_start_loc[N+1], seq_lens[N]) and the two steps: (1) write the T new
+//    keys/values at slot_mapping, (2) for each request attend from its
+//    queries over its first seq_len tokens, fetched through its block_table
+//    row.  Section "Code": slot = block_table[pos / bs] * bs + pos % bs, and
+//    paged attention equals contiguous attention exactly.
+//  * "AttentionBackend: attention backend abstraction layer" (vllm-arch-zh),
+//    design-motivation list: the standard pool layout
+//    [num_blocks, 2, block_size, num_kv_heads, head_size] and the MLA pool
+//    [num_blocks, block_size, head_size]; LSE in natural log.
+//  * "Triton and MLA" (vllm-arch-zh, zh-TW), data-flow section: MLA decode is
+//    MQA over one 576-wide [kv_c 512 | k_pe 64] cache vector whose first 512
+//    entries are the value; split-KV partials carry their LSE in slot
+//    [Dv] of a [B, H, S, Dv + 1] fp32 workspace and are merged by LSE.
+//  * "Chapter 1: attention backends" (zero-to-sglang), section 2.1:
+//    O = softmax(Q K^T / sqrt(d_h) + M) V; section 3.1: split-KV partials
+//    merged with their softmax normalisers; section 4.1 / Fig. 5c: the
+//    online-softmax merge of two blocks.
+//
+// Every floating-point step is done in double.  bf16 inputs are widened
+// exactly (a bf16 bit pattern is the top half of an IEEE float).
+//
+// Readings where the pages are silent (each also listed in the design notes):
+//  * causal alignment is bottom-right: the qlen_i new queries of request i are
+//    its last qlen_i positions, and query row j sees positions <= its own;
+//  * GQA groups are contiguous: q head h reads kv head h / (Hq / Hkv);
+//  * split s of request i covers tokens [s*C_i, min((s+1)*C_i, seq_i)) with
+//    C_i = bs * ceil(ceil(seq_i / S) / bs); an empty split has o = 0 and
+//    lse = -inf;
+//  * a query with nothing visible (seq_len = 0) gives o = 0, lse = -inf.
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <limits>
+#include <thread>
+#include <vector>
+
+namespace {
+
+const double kNegInf = -std::numeric_limits<double>::infinity();
+
+inline double widen(uint16_t bits) {
+  uint32_t u = static_cast<uint32_t>(bits) << 16;
+  float f;
+  std::memcpy(&f, &u, sizeof f);
+  return static_cast<double>(f);
+}
+inline double widen(double x) { return x; }
+
+// Runs fn(item) for item in [0, n) on `threads` host threads.
+template <typename F>
+void parallel_for(int64_t n, int threads, F fn) {
+  if (threads <= 1 || n <= 1) {
+    for (int64_t i = 0; i < n; ++i) fn(i);
+    return;
+  }
+  std::atomic<int64_t> next(0);
+  std::vector<std::thread> pool;
+  int t = threads < n ? threads : static_cast<int>(n);
+  for (int k = 0; k < t; ++k) {
+    pool.emplace_back([&]() {
+      for (;;) {
+        int64_t i = next.fetch_add(1);
+        if (i >= n) break;
+        fn(i);
+      }
+    });
+  }
+  for (auto& th : pool) th.join();
+}
+
+// softmax(scale * q.K^T) V over n rows of K (width dk) and V (width dv).
+// K and V are contiguous [n][dk] / [n][dv] fp64 arrays.  Writes o[dv] and
+// the natural-log LSE.  n == 0 gives o = 0, lse = -inf.
+void attend(const double* q, const double* K, const double* V, int64_t n,
+            int dk, int dv, double scale, double* o, double* lse) {
+  for (int e = 0; e < dv; ++e) o[e] = 0.0;
+  if (n <= 0) {
+    *lse = kNegInf;
+    return;
+  }
+  std::vector<double> s(static_cast<size_t>(n));
+  double m = kNegInf;
+  for (int64_t p = 0; p < n; ++p) {
+    double acc = 0.0;
+    const double* k = K + p * dk;
+    for (int e = 0; e < dk; ++e) acc += q[e] * k[e];
+    s[p] = scale * acc;
+    if (s[p] > m) m = s[p];
+  }
+  double l = 0.0;
+  for (int64_t p = 0; p < n; ++p) {
+    s[p] = std::exp(s[p] - m);
+    l += s[p];
+  }
+  for (int64_t p = 0; p < n; ++p) {
+    const double w = s[p] / l;
+    const double* v = V + p * dv;
+    for (int e = 0; e < dv; ++e) o[e] += w * v[e];
+  }
+  *lse = m + std::log(l);
+}
+
+// Gathers the first seq_len tokens of kv head g of one request from the
+// standard pool [nb][2][bs][Hkv][d] into contiguous K[seq][d], V[seq][d].
+// Returns false if a block id is outside [0, nb).
+template <typename E>
+bool gather_standard(const E* pool, const int32_t* table_row, int64_t seq_len,
+                     int g, int Hkv, int d, int bs, int64_t nb,
+                     std::vector<double>& K, std::vector<double>& V) {
+  K.assign(static_cast<size_t>(seq_len) * d, 0.0);
+  V.assign(static_cast<size_t>(seq_len) * d, 0.0);
+  for (int64_t p = 0; p < seq_len; ++p) {
+    const int64_t blk = table_row[p / bs];
+    if (blk < 0 || blk >= nb) return false;
+    const int64_t off = p % bs;
+    const E* krow = pool + (((blk * 2 + 0) * bs + off) * Hkv + g) * d;
+    const E* vrow = pool + (((blk * 2 + 1) * bs + off) * Hkv + g) * d;
+    for (int e = 0; e < d; ++e) {
+      K[p * d + e] = widen(krow[e]);
+      V[p * d + e] = widen(vrow[e]);
+    }
+  }
+  return true;
+}
+
+template <typename E>
+int paged_attention(const E* q, const E* pool, const int32_t* block_table,
+                    int max_blocks, const int32_t* query_start_loc,
+                    const int32_t* seq_lens, int N, int Hq, int Hkv, int d,
+                    int bs, int64_t nb, double scale, int causal,
+                    const uint8_t* row_mask, double* out, double* lse,
+                    int threads) {
+  if (Hkv <= 0 || Hq % Hkv != 0 || bs <= 0 || d <= 0) return -1;
+  const int grp = Hq / Hkv;
+  std::atomic<int> bad(0);
+  parallel_for(static_cast<int64_t>(N) * Hkv, threads, [&](int64_t item) {
+    const int i = static_cast<int>(item / Hkv);
+    const int g = static_cast<int>(item % Hkv);
+    const int64_t q0 = query_start_loc[i], q1 = query_start_loc[i + 1];
+    const int64_t seq = seq_lens[i];
+    const int64_t qlen = q1 - q0;
+    if (qlen <= 0) return;
+    if (qlen > seq) {
+      bad = 1;
+      return;
+    }
+    bool any = row_mask == nullptr;
+    for (int64_t j = q0; j < q1 && !any; ++j) any = row_mask[j] != 0;
+    if (!any) return;
+    std::vector<double> K, V, qv(d);
+    if (!gather_standard(pool, block_table + static_cast<int64_t>(i) * max_blocks,
+                         seq, g, Hkv, d, bs, nb, K, V)) {
+      bad = 1;
+      return;
+    }
+    const int64_t ctx = seq - qlen;
+    for (int64_t j = q0; j < q1; ++j) {
+      if (row_mask && !row_mask[j]) continue;
+      const int64_t pos = ctx + (j - q0);          // absolute position of row j
+      const int64_t visible = causal ? pos + 1 : seq;
+      for (int r = 0; r < grp; ++r) {
+        const int h = g * grp + r;
+        const E* qr = q + (j * Hq + h) * d;
+        for (int e = 0; e < d; ++e) qv[e] = widen(qr[e]);
+        attend(qv.data(), K.data(), V.data(), visible, d, d, scale,
+               out + (j * Hq + h) * d, lse + j * Hq + h);
+      }
+    }
+  });
+  return bad ? -1 : 0;
+}
+
+// Split-KV stage 1 for one query per request (decode: the query sits at
+// position seq_i - 1 and sees every cached token).  partials is
+// [N][Hq][S][d + 1]: the split's normalised output then its LSE.
+template <typename E>
+int split_partials(const E* q, const E* pool, const int32_t* block_table,
+                   int max_blocks, const int32_t* seq_lens, int N, int Hq,
+                   int Hkv, int d, int bs, int64_t nb, double scale, int S,
+                   double* partials, int threads) {
+  if (Hkv <= 0 || Hq % Hkv != 0 || S <= 0 || bs <= 0) return -1;
+  const int grp = Hq / Hkv;
+  std::atomic<int> bad(0);
+  parallel_for(static_cast<int64_t>(N) * Hkv, threads, [&](int64_t item) {
+    const int i = static_cast<int>(item / Hkv);
+    const int g = static_cast<int>(item % Hkv);
+    const int64_t seq = seq_lens[i];
+    std::vector<double> K, V, qv(d);
+    if (!gather_standard(pool, block_table + static_cast<int64_t>(i) * max_blocks,
+                         seq, g, Hkv, d, bs, nb, K, V)) {
+      bad = 1;
+      return;
+    }
+    const int64_t per = (seq + S - 1) / S;              // ceil(seq / S)
+    const int64_t chunk = ((per + bs - 1) / bs) * bs;   // rounded up to blocks
+    for (int r = 0; r < grp; ++r) {
+      const int h = g * grp + r;
+      for (int e = 0; e < d; ++e) qv[e] = widen(q[(static_cast<int64_t>(i) * Hq + h) * d + e]);
+      for (int s = 0; s < S; ++s) {
+        int64_t a = s * chunk, b = a + chunk;
+        if (a > seq) a = seq;
+        if (b > seq) b = seq;
+        double* dst = partials + ((static_cast<int64_t>(i) * Hq + h) * S + s) * (d + 1);
+        attend(qv.data(), K.data() + a * d, V.data() + a * d, b - a, d, d,
+               scale, dst, dst + d);
+      }
+    }
+  });
+  return bad ? -1 : 0;
+}
+
+// MLA decode: one query per request, all H heads against the single latent
+// KV head.  The key is the whole dk = kv_lora_rank + rope_dim row, the value
+// its first kv_lora_rank entries.  pool is [nb][bs][dk].
+template <typename E>
+int mla_decode(const E* q, const E* pool, const int32_t* block_table,
+               int max_blocks, const int32_t* seq_lens, int B, int H,
+               int kv_lora_rank, int rope_dim, int bs, int64_t nb,
+               double scale, const uint8_t* req_mask, double* out, double* lse,
+               int threads) {
+  const int dk = kv_lora_rank + rope_dim, dv = kv_lora_rank;
+  if (bs <= 0 || dk <= 0) return -1;
+  std::atomic<int> bad(0);
+  parallel_for(B, threads, [&](int64_t b) {
+    if (req_mask && !req_mask[b]) return;
+    const int64_t seq = seq_lens[b];
+    std::vector<double> K(static_cast<size_t>(seq) * dk), V(static_cast<size_t>(seq) * dv), qv(dk);
+    const int32_t* row = block_table + b * max_blocks;
+    for (int64_t p = 0; p < seq; ++p) {
+      const int64_t blk = row[p / bs];
+      if (blk < 0 || blk >= nb) {
+        bad = 1;
+        return;
+      }
+      const E* c = pool + (blk * bs + p % bs) * dk;
+      for (int e = 0; e < dk; ++e) K[p * dk + e] = widen(c[e]);
+      for (int e = 0; e < dv; ++e) V[p * dv + e] = widen(c[e]);
+    }
+    for (int h = 0; h < H; ++h) {
+      for (int e = 0; e < dk; ++e) qv[e] = widen(q[(b * H + h) * dk + e]);
+      attend(qv.data(), K.data(), V.data(), seq, dk, dv, scale,
+             out + (b * H + h) * dv, lse + b * H + h);
+    }
+  });
+  return bad ? -1 : 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+// Step 1 of the paged-kernel contract: for every token t with
+// slot = slot_mapping[t] >= 0, copy key[t] / value[t] ([Hkv][d] each) into
+// pool[slot / bs][0 or 1][slot % bs].  A bit copy of 16-bit elements.
+// Returns -1 (and writes nothing more) on a slot outside the pool.
+int oracle_reshape_and_cache(const uint16_t* key, const uint16_t* value,
+                             uint16_t* pool, const int64_t* slot_mapping,
+                             int64_t num_tokens, int num_kv_heads, int head_size,
+                             int block_size, int64_t num_blocks) {
+  const int64_t row = static_cast<int64_t>(num_kv_heads) * head_size;
+  for (int64_t t = 0; t < num_tokens; ++t) {
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    const int64_t blk = slot / block_size, off = slot % block_size;
+    if (blk >= num_blocks) return -1;
+    std::memcpy(pool + ((blk * 2 + 0) * block_size + off) * row, key + t * row,
+                sizeof(uint16_t) * row);
+    std::memcpy(pool + ((blk * 2 + 1) * block_size + off) * row, value + t * row,
+                sizeof(uint16_t) * row);
+  }
+  return 0;
+}
+
+// Step 2 of the contract (varlen paged attention), bf16 inputs.
+// q [T][Hq][d], pool [nb][2][bs][Hkv][d], out [T][Hq][d] fp64,
+// lse [T][Hq] fp64 natural log.  row_mask (nullable, [T]) selects rows.
+int oracle_paged_attention_bf16(const uint16_t* q, const uint16_t* pool,
+                                const int32_t* block_table, int max_blocks,
+                                const int32_t* query_start_loc,
+                                const int32_t* seq_lens, int N, int Hq, int Hkv,
+                                int d, int bs, int64_t nb, double scale,
+                                int causal, const uint8_t* row_mask,
+                                double* out, double* lse, int threads) {
+  return paged_attention(q, pool, block_table, max_blocks, query_start_loc,
+                         seq_lens, N, Hq, Hkv, d, bs, nb, scale, causal,
+                         row_mask, out, lse, threads);
+}
+
+// Same as above with fp64 q and pool (used by the worked-example pins).
+int oracle_paged_attention_f64(const double* q, const double* pool,
+                               const int32_t* block_table, int max_blocks,
+                               const int32_t* query_start_loc,
+                               const int32_t* seq_lens, int N, int Hq, int Hkv,
+                               int d, int bs, int64_t nb, double scale,
+                               int causal, const uint8_t* row_mask, double* out,
+                               double* lse, int threads) {
+  return paged_attention(q, pool, block_table, max_blocks, query_start_loc,
+                         seq_lens, N, Hq, Hkv, d, bs, nb, scale, causal,
+                         row_mask, out, lse, threads);
+}
+
+// Split-KV stage 1 (decode, one query per request), bf16 / fp64 inputs.
+int oracle_split_partials_bf16(const uint16_t* q, const uint16_t* pool,
+                               const int32_t* block_table, int max_blocks,
+                               const int32_t* seq_lens, int N, int Hq, int Hkv,
+                               int d, int bs, int64_t nb, double scale,
+                               int num_splits, double* partials, int threads) {
+  return split_partials(q, pool, block_table, max_blocks, seq_lens, N, Hq, Hkv,
+                        d, bs, nb, scale, num_splits, partials, threads);
+}
+int oracle_split_partials_f64(const double* q, const double* pool,
+                              const int32_t* block_table, int max_blocks,
+                              const int32_t* seq_lens, int N, int Hq, int Hkv,
+                              int d, int bs, int64_t nb, double scale,
+                              int num_splits, double* partials, int threads) {
+  return split_partials(q, pool, block_table, max_blocks, seq_lens, N, Hq, Hkv,
+                        d, bs, nb, scale, num_splits, partials, threads);
+}
+
+// Split-KV stage 2: merge S partials per (request, head) by their LSE.
+// partials [N][H][S][dv + 1] -> out [N][H][dv], lse [N][H].
+//   M = max_s lse_s, w_s = exp(lse_s - M), o = sum_s w_s o_s / sum_s w_s,
+//   lse = M + ln(sum_s w_s).  All splits empty (M = -inf): o = 0, lse = -inf.
+void oracle_lse_merge(const double* partials, int N, int H, int S, int dv,
+                      double* out, double* lse) {
+  for (int64_t nh = 0; nh < static_cast<int64_t>(N) * H; ++nh) {
+    const double* base = partials + nh * S * (dv + 1);
+    double m = kNegInf;
+    for (int s = 0; s < S; ++s) {
+      const double l = base[s * (dv + 1) + dv];
+      if (l > m) m = l;
+    }
+    double* o = out + nh * dv;
+    for (int e = 0; e < dv; ++e) o[e] = 0.0;
+    if (m == kNegInf) {
+      lse[nh] = kNegInf;
+      continue;
+    }
+    double wsum = 0.0;
+    for (int s = 0; s < S; ++s) {
+      const double l = base[s * (dv + 1) + dv];
+      if (l == kNegInf) continue;
+      const double w = std::exp(l - m);
+      wsum += w;
+      for (int e = 0; e < dv; ++e) o[e] += w * base[s * (dv + 1) + e];
+    }
+    for (int e = 0; e < dv; ++e) o[e] /= wsum;
+    lse[nh] = m + std::log(wsum);
+  }
+}
+
+// MLA latent decode, bf16 / fp64 inputs.  q [B][H][dk], pool [nb][bs][dk],
+// out [B][H][kv_lora_rank], lse [B][H].  req_mask (nullable, [B]).
+int oracle_mla_decode_bf16(const uint16_t* q, const uint16_t* pool,
+                           const int32_t* block_table, int max_blocks,
+                           const int32_t* seq_lens, int B, int H,
+                           int kv_lora_rank, int rope_dim, int bs, int64_t nb,
+                           double scale, const uint8_t* req_mask, double* out,
+                           double* lse, int threads) {
+  return mla_decode(q, pool, block_table, max_blocks, seq_lens, B, H,
+                    kv_lora_rank, rope_dim, bs, nb, scale, req_mask, out, lse,
+                    threads);
+}
+int oracle_mla_decode_f64(const double* q, const double* pool,
+                          const int32_t* block_table, int max_blocks,
+                          const int32_t* seq_lens, int B, int H,
+                          int kv_lora_rank, int rope_dim, int bs, int64_t nb,
+                          double scale, const uint8_t* req_mask, double* out,
+                          double* lse, int threads) {
+  return mla_decode(q, pool, block_table, max_blocks, seq_lens, B, H,
+                    kv_lora_rank, rope_dim, bs, nb, scale, req_mask, out, lse,
+                    threads);
+}
+
+// Exact bf16 -> fp64 widening of n values (for callers that want the
+// oracle's view of a bf16 array).
+void oracle_bf16_to_f64(const uint16_t* src, double* dst, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) dst[i] = widen(src[i]);
+}
+
+}  // extern "C"

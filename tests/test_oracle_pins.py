@@ -1,0 +1,374 @@
+"""Pins for the fp64 oracle: checks against what the pages and plain
+mathematics fix, never against the oracle itself or the CUDA path.
+
+Each test names the page section it follows.  A plausible slip in the oracle
+(a dropped causal offset, a wrong GQA index, a transposed gather, a wrong LSE
+base or merge weight) makes at least one of these fail; see
+``test_oracle_mutants.py`` for that claim checked by planting such slips.
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from tests import bruteforce
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------------------
+# "Attention Backends", section "Code": the block-table worked example.
+# ---------------------------------------------------------------------------
+
+def _m1_inputs():
+    g = _golden("m1_block_table.json")
+    bs, dim, seq = g["block_size"], g["dim"], g["seq_len"]
+    keys = [[math.sin(i * 3 + d) for d in range(dim)] for i in range(seq)]
+    vals = [[math.cos(i * 5 + d * 2) for d in range(dim)] for i in range(seq)]
+    return g, keys, vals
+
+
+def _m1_pool(table, keys, vals, bs, nb, dim):
+    # Unused slots hold NaN: reading one would poison the result.
+    pool = np.full((nb, 2, bs, 1, dim), np.nan)
+    for pos in range(len(keys)):
+        blk, off = table[pos // bs], pos % bs
+        pool[blk, 0, off, 0] = keys[pos]
+        pool[blk, 1, off, 0] = vals[pos]
+    return pool
+
+
+def test_m1_slot_ranges(oracle_lib):
+    g, keys, vals = _m1_inputs()
+    bs, table = g["block_size"], g["block_table"]
+    slots = [table[p // bs] * bs + p % bs for p in range(g["seq_len"])]
+    r = g["printed_slot_ranges"]
+    assert slots[0:4] == list(range(r["positions 0-3"][0], r["positions 0-3"][1] + 1))
+    assert slots[4:8] == list(range(r["positions 4-7"][0], r["positions 4-7"][1] + 1))
+    assert slots[8:10] == list(range(r["positions 8-9"][0], r["positions 8-9"][1] + 1))
+    # The oracle's cache write puts token p at exactly that slot.
+    T, d = g["seq_len"], 8
+    rng = np.random.default_rng(0)
+    key = rng.integers(0, 1 << 16, size=(T, 1, d), dtype=np.uint16)
+    val = rng.integers(0, 1 << 16, size=(T, 1, d), dtype=np.uint16)
+    pool = np.zeros((g["num_blocks"], 2, bs, 1, d), np.uint16)
+    out = oracle_lib.reshape_and_cache(key, val, pool, np.array(slots), bs)
+    for p, s in enumerate(slots):
+        assert np.array_equal(out[s // bs, 0, s % bs], key[p])
+        assert np.array_equal(out[s // bs, 1, s % bs], val[p])
+    written = {(s // bs, s % bs) for s in slots}
+    for b in range(g["num_blocks"]):
+        for o in range(bs):
+            if (b, o) not in written:
+                assert not out[b, :, o].any()
+
+
+@pytest.mark.parametrize("table", [[6, 1, 4], [0, 1, 2], [7, 3, 5]])
+def test_m1_paged_equals_contiguous(oracle_lib, table):
+    g, keys, vals = _m1_inputs()
+    bs, dim, seq, nb = g["block_size"], g["dim"], g["seq_len"], g["num_blocks"]
+    scale = 1.0 / math.sqrt(dim)
+    q = np.array(g["query"], np.float64).reshape(1, 1, dim)
+    pool = _m1_pool(table, keys, vals, bs, nb, dim)
+    out, lse = oracle_lib.paged_attention(q, pool, np.array([table]), [0, 1], [seq], scale)
+    ref_o, ref_lse = bruteforce.attend(g["query"], keys, vals, scale)
+    np.testing.assert_allclose(out[0, 0], ref_o, rtol=0, atol=1e-13)
+    assert abs(lse[0, 0] - ref_lse) < 1e-13
+    # Bit-for-bit equality with the paper's scattered table (the page's claim).
+    pool0 = _m1_pool(g["block_table"], keys, vals, bs, nb, dim)
+    out0, lse0 = oracle_lib.paged_attention(q, pool0, np.array([g["block_table"]]), [0, 1],
+                                            [seq], scale)
+    assert np.array_equal(out, out0) and np.array_equal(lse, lse0)
+
+
+# ---------------------------------------------------------------------------
+# "Chapter 1: attention backends", section 4.1, Fig. 5c: online softmax and
+# the merge of two key blocks.
+# ---------------------------------------------------------------------------
+
+def test_fig5c_block_merge(oracle_lib):
+    g = _golden("fig5c_online_softmax.json")
+    v = g["values"]
+    scores = [0.0, 0.0, math.log(2.0), math.log(2.0)]   # weights 1:1:2:2
+    bs, nb = 2, 2
+    pool = np.zeros((nb, 2, bs, 1, 1))
+    for p in range(4):
+        pool[p // bs, 0, p % bs, 0, 0] = scores[p]
+        pool[p // bs, 1, p % bs, 0, 0] = v[p]
+    q = np.ones((1, 1, 1))
+    table = np.array([[0, 1]])
+    part = oracle_lib.split_partials(q, pool, table, [4], 1.0, 2)
+    o_a, lse_a = part[0, 0, 0, 0], part[0, 0, 0, 1]
+    o_b, lse_b = part[0, 0, 1, 0], part[0, 0, 1, 1]
+    assert abs(o_a - g["block_A_output"]) < 1e-12
+    assert abs(lse_a - math.log(2.0)) < 1e-12
+    assert abs(o_b - 35.0) < 1e-12 and abs(lse_b - math.log(4.0)) < 1e-12
+    out, lse = oracle_lib.lse_merge(part)
+    assert abs(out[0, 0, 0] - 170.0 / 6.0) < 1e-12
+    assert abs(out[0, 0, 0] - g["merged_output_approx"]) < 5e-3
+    assert abs(lse[0, 0] - math.log(6.0)) < 1e-12
+    assert abs(math.exp(lse_a - lse[0, 0]) - g["share_of_A_after_B"]) < 1e-12
+    # The merged result equals attention over the whole row (Fig. 5a).
+    full_o, full_lse = oracle_lib.paged_attention(q, pool, table, [0, 1], [4], 1.0)
+    assert abs(full_o[0, 0, 0] - out[0, 0, 0]) < 1e-12
+    assert abs(full_lse[0, 0] - lse[0, 0]) < 1e-12
+
+
+# ---------------------------------------------------------------------------
+# Closed forms of O = softmax(Q K^T / sqrt(d) + M) V ("Chapter 1", 2.1).
+# ---------------------------------------------------------------------------
+
+def _f64(bits):
+    return workloads.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def _gather(pool, table_row, seq, bs):
+    """numpy fancy-index gather of one request's K, V: [seq, Hkv, d]."""
+    pos = np.arange(seq)
+    blk = np.asarray(table_row)[pos // bs]
+    return pool[blk, 0, pos % bs], pool[blk, 1, pos % bs]
+
+
+def test_zero_query_gives_mean_of_visible_rows_causal(oracle_lib):
+    # q = 0: every visible score is 0, so o is the mean of the visible V rows
+    # and lse = ln(#visible).  With bottom-right causal alignment row j of a
+    # request with context c sees c + j + 1 positions.
+    b = workloads.make_paged_batch("zq", 11, [5, 40, 33], [5, 7, 1], 4, 2, 16, 16)
+    q = np.zeros_like(b.q)
+    out, lse = oracle_lib.paged_attention(q, b.pool, b.block_table, b.query_start_loc,
+                                          b.seq_lens, b.scale)
+    pool = _f64(b.pool)
+    grp = b.num_q_heads // b.num_kv_heads
+    for i in range(b.num_seqs):
+        _, V = _gather(pool, b.block_table[i], b.seq_lens[i], b.block_size)
+        ctx = b.seq_lens[i] - b.query_lens[i]
+        for j in range(b.query_lens[i]):
+            row = b.query_start_loc[i] + j
+            n = ctx + j + 1
+            for h in range(b.num_q_heads):
+                np.testing.assert_allclose(out[row, h], V[:n, h // grp].mean(axis=0),
+                                           rtol=0, atol=1e-13)
+                assert abs(lse[row, h] - math.log(n)) < 1e-13
+    # Non-causal: every row sees all seq_len positions.
+    out, lse = oracle_lib.paged_attention(q, b.pool, b.block_table, b.query_start_loc,
+                                          b.seq_lens, b.scale, causal=False)
+    for i in range(b.num_seqs):
+        rows = range(b.query_start_loc[i], b.query_start_loc[i + 1])
+        for row in rows:
+            assert np.allclose(lse[row], math.log(b.seq_lens[i]), atol=1e-13)
+
+
+def test_single_token_returns_that_value_row(oracle_lib):
+    b = workloads.make_paged_batch("one", 12, [1, 1], [1, 1], 4, 2, 64, 16, num_blocks=5)
+    out, lse = oracle_lib.paged_attention(b.q, b.pool, b.block_table, b.query_start_loc,
+                                          b.seq_lens, b.scale)
+    pool, q = _f64(b.pool), _f64(b.q)
+    for i in range(2):
+        blk = b.block_table[i, 0]
+        for h in range(4):
+            k, v = pool[blk, 0, 0, h // 2], pool[blk, 1, 0, h // 2]
+            assert np.array_equal(out[i, h], v)            # weight exactly 1
+            assert abs(lse[i, h] - b.scale * float(np.dot(q[i, h], k))) < 1e-12
+
+
+def test_gqa_head_mapping_and_row_sums(oracle_lib):
+    # V constant per kv head (value g + 1): q head h must return (h // grp) + 1.
+    # V = 1 everywhere checks that the softmax weights sum to one.
+    b = workloads.make_paged_batch("gqa", 13, [37, 64], [3, 2], 8, 2, 16, 16)
+    pool = _f64(b.pool)
+    for g in range(b.num_kv_heads):
+        pool[:, 1, :, g, :] = g + 1.0
+    q = _f64(b.q)
+    out, _ = oracle_lib.paged_attention(q, pool, b.block_table, b.query_start_loc,
+                                        b.seq_lens, b.scale)
+    for h in range(8):
+        np.testing.assert_allclose(out[:, h], h // 4 + 1.0, rtol=0, atol=1e-13)
+
+
+def test_gqa_equals_replicated_mha(oracle_lib):
+    b = workloads.make_paged_batch("rep", 14, [29, 50], [4, 1], 6, 2, 32, 16)
+    pool = b.pool
+    rep = np.repeat(pool, 3, axis=3)       # kv head g copied to heads 3g..3g+2
+    o1, l1 = oracle_lib.paged_attention(b.q, pool, b.block_table, b.query_start_loc,
+                                        b.seq_lens, b.scale)
+    o2, l2 = oracle_lib.paged_attention(b.q, rep, b.block_table, b.query_start_loc,
+                                        b.seq_lens, b.scale)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_matches_torch_sdpa_on_tiny_workload(oracle_lib):
+    # Library routine: torch's scaled_dot_product_attention in fp64 over the
+    # contiguous K/V with an explicit bottom-right causal mask.
+    b = workloads.tiny_paged()
+    pool = oracle_lib.reshape_and_cache(b.key, b.value, b.pool,
+                                        b.slot_mapping, b.block_size)
+    out, lse = oracle_lib.paged_attention(b.q, pool, b.block_table, b.query_start_loc,
+                                          b.seq_lens, b.scale)
+    P, q = _f64(pool), _f64(b.q)
+    grp = b.num_q_heads // b.num_kv_heads
+    for i in range(b.num_seqs):
+        K, V = _gather(P, b.block_table[i], b.seq_lens[i], b.block_size)
+        rows = slice(b.query_start_loc[i], b.query_start_loc[i + 1])
+        qi = torch.from_numpy(q[rows]).permute(1, 0, 2)                 # [Hq, L, d]
+        Ki = torch.from_numpy(K).permute(1, 0, 2).repeat_interleave(grp, 0)
+        Vi = torch.from_numpy(V).permute(1, 0, 2).repeat_interleave(grp, 0)
+        L, S = qi.shape[1], Ki.shape[1]
+        mask = torch.arange(S)[None, :] <= (S - L + torch.arange(L))[:, None]
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            qi, Ki, Vi, attn_mask=mask, scale=b.scale)
+        np.testing.assert_allclose(out[rows], ref.permute(1, 0, 2).numpy(), rtol=0, atol=1e-12)
+        s = torch.einsum("hld,hsd->hls", qi, Ki) * b.scale
+        s = s.masked_fill(~mask, -math.inf)
+        np.testing.assert_allclose(lse[rows], torch.logsumexp(s, -1).T.numpy(), rtol=0,
+                                   atol=1e-12)
+
+
+def test_matches_pure_python_bruteforce_on_tiny_workload(oracle_lib):
+    b = workloads.tiny_paged()
+    pool = oracle_lib.reshape_and_cache(b.key, b.value, b.pool, b.slot_mapping, b.block_size)
+    out, lse = oracle_lib.paged_attention(b.q, pool, b.block_table, b.query_start_loc,
+                                          b.seq_lens, b.scale)
+    P, q = _f64(pool), _f64(b.q)
+    grp = b.num_q_heads // b.num_kv_heads
+    for i in range(b.num_seqs):
+        seq, qlen = int(b.seq_lens[i]), int(b.query_lens[i])
+        for j in range(qlen):
+            row = int(b.query_start_loc[i]) + j
+            n = seq - qlen + j + 1
+            for h in range(b.num_q_heads):
+                keys, vals = [], []
+                for p in range(n):
+                    blk = int(b.block_table[i][p // b.block_size])
+                    keys.append(list(P[blk, 0, p % b.block_size, h // grp]))
+                    vals.append(list(P[blk, 1, p % b.block_size, h // grp]))
+                o, l = bruteforce.attend(list(q[row, h]), keys, vals, b.scale)
+                np.testing.assert_allclose(out[row, h], o, rtol=0, atol=1e-12)
+                assert abs(lse[row, h] - l) < 1e-12
+
+
+def test_block_permutation_invariance(oracle_lib):
+    b = workloads.make_paged_batch("perm", 15, [70, 33, 16], [3, 33, 1], 4, 4, 16, 16,
+                                   num_blocks=12)
+    o1, l1 = oracle_lib.paged_attention(b.q, b.pool, b.block_table, b.query_start_loc,
+                                        b.seq_lens, b.scale)
+    perm = np.random.default_rng(3).permutation(b.num_blocks)
+    new_pool = np.empty_like(b.pool)
+    new_pool[perm] = b.pool                     # block k moves to perm[k]
+    table = np.where(b.block_table >= 0, perm[np.maximum(b.block_table, 0)], -1)
+    o2, l2 = oracle_lib.paged_attention(b.q, new_pool, table, b.query_start_loc,
+                                        b.seq_lens, b.scale)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+# ---------------------------------------------------------------------------
+# Split-KV ("Chapter 1", 3.1; "Triton and MLA", data flow): splitting adds
+# parallelism but every key still takes part, so split + LSE merge equals the
+# unsplit result, and one split is the unsplit result.
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("S", [1, 2, 7, 256])
+def test_split_then_merge_equals_unsplit(oracle_lib, S):
+    b = workloads.make_paged_batch("split", 16, [300, 17, 1, 64], [1, 1, 1, 1], 8, 2, 32, 16)
+    unsplit_o, unsplit_l = oracle_lib.paged_attention(b.q, b.pool, b.block_table,
+                                                      b.query_start_loc, b.seq_lens, b.scale)
+    part = oracle_lib.split_partials(b.q, b.pool, b.block_table, b.seq_lens, b.scale, S)
+    o, l = oracle_lib.lse_merge(part)
+    np.testing.assert_allclose(o, unsplit_o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l, unsplit_l, rtol=0, atol=1e-12)
+    if S == 1:
+        assert np.array_equal(part[:, :, 0, :-1], unsplit_o)
+        assert np.array_equal(part[:, :, 0, -1], unsplit_l)
+    # Split boundaries: chunk C = bs * ceil(ceil(seq / S) / bs); splits past
+    # the end are empty (o = 0, lse = -inf).
+    for i, seq in enumerate(b.seq_lens):
+        per = -(-int(seq) // S)
+        chunk = -(-per // b.block_size) * b.block_size
+        for s in range(S):
+            empty = s * chunk >= seq
+            assert np.isneginf(part[i, :, s, -1]).all() == empty
+            if empty:
+                assert not part[i, :, s, :-1].any()
+
+
+def test_merge_ignores_empty_and_handles_all_empty(oracle_lib):
+    part = np.zeros((2, 1, 3, 3))
+    part[0, 0, 0] = [1.0, 2.0, 0.5]
+    part[0, 0, 1] = [0.0, 0.0, -np.inf]
+    part[0, 0, 2] = [3.0, 4.0, 0.5]
+    part[1, 0, :, 2] = -np.inf
+    o, l = oracle_lib.lse_merge(part)
+    np.testing.assert_allclose(o[0, 0], [2.0, 3.0], atol=1e-15)
+    assert abs(l[0, 0] - (0.5 + math.log(2.0))) < 1e-15
+    assert not o[1].any() and np.isneginf(l[1, 0])
+
+
+# ---------------------------------------------------------------------------
+# MLA ("Triton and MLA", data flow): MQA over one [kv_c | k_pe] vector, value
+# = its first kv_lora_rank entries.
+# ---------------------------------------------------------------------------
+
+def test_mla_equals_generic_single_kv_head(oracle_lib):
+    b = workloads.make_mla_batch("mla", 17, [70, 5, 128], 4, kv_lora_rank=40, rope_dim=8,
+                                 block_size=16)
+    o, l = oracle_lib.mla_decode(b.q, b.pool, b.block_table, b.seq_lens, b.scale, 40, 8)
+    # Standard layout with one kv head, K = V = the whole 48-wide row.
+    std = np.stack([b.pool, b.pool], axis=1)[:, :, :, None, :]
+    qsl = np.arange(b.batch + 1)
+    go, gl = oracle_lib.paged_attention(b.q, std, b.block_table, qsl, b.seq_lens, b.scale)
+    assert np.array_equal(o, go[:, :, :40]) and np.array_equal(l, gl)
+
+
+def test_mla_matches_bruteforce(oracle_lib):
+    b = workloads.make_mla_batch("mla_bf", 18, [9, 33], 3, kv_lora_rank=16, rope_dim=8,
+                                 block_size=16)
+    o, l = oracle_lib.mla_decode(b.q, b.pool, b.block_table, b.seq_lens, b.scale, 16, 8)
+    P, q = _f64(b.pool), _f64(b.q)
+    for i in range(b.batch):
+        rows = [P[b.block_table[i][p // 16], p % 16] for p in range(b.seq_lens[i])]
+        for h in range(3):
+            ro, rl = bruteforce.attend(list(q[i, h]), [list(r) for r in rows],
+                                       [list(r[:16]) for r in rows], b.scale)
+            np.testing.assert_allclose(o[i, h], ro, rtol=0, atol=1e-12)
+            assert abs(l[i, h] - rl) < 1e-12
+
+
+# ---------------------------------------------------------------------------
+# Cache write ("Attention Backends", paged-kernel contract step 1).
+# ---------------------------------------------------------------------------
+
+def test_cache_write_matches_numpy_scatter(oracle_lib):
+    b = workloads.tiny_paged()
+    out = oracle_lib.reshape_and_cache(b.key, b.value, b.pool, b.slot_mapping, b.block_size)
+    ref = b.pool.copy()
+    s = b.slot_mapping
+    ref[s // b.block_size, 0, s % b.block_size] = b.key
+    ref[s // b.block_size, 1, s % b.block_size] = b.value
+    assert np.array_equal(out, ref)
+    skip = b.slot_mapping.copy()
+    skip[1] = -1
+    out2 = oracle_lib.reshape_and_cache(b.key, b.value, b.pool, skip, b.block_size)
+    blk, off = s[1] // b.block_size, s[1] % b.block_size
+    assert np.array_equal(out2[blk, :, off], b.pool[blk, :, off])
+    bad = b.slot_mapping.copy()
+    bad[0] = b.num_blocks * b.block_size
+    with pytest.raises(ValueError):
+        oracle_lib.reshape_and_cache(b.key, b.value, b.pool, bad, b.block_size)
+
+
+def test_empty_request_gives_neg_inf_lse(oracle_lib):
+    b = workloads.make_paged_batch("empty", 19, [0, 20], [0, 1], 2, 1, 16, 16, num_blocks=3)
+    part = oracle_lib.split_partials(np.zeros((2, 2, 16), np.uint16), b.pool, b.block_table,
+                                     b.seq_lens, b.scale, 3)
+    o, l = oracle_lib.lse_merge(part)
+    assert np.isneginf(l[0]).all() and not o[0].any()
+    assert np.isfinite(l[1]).all()

@@ -1,0 +1,235 @@
+"""Seeded synthetic inputs for the paged-attention hot path.
+
+This module only draws random inputs and lays them out; it holds none of the
+attention arithmetic.  Both sides of every parity check -- the CUDA library
+and the fp64 oracle -- consume the arrays it returns, and neither side
+imports the other.
+
+Recipe (the same for every workload):
+  * numpy ``default_rng(seed)`` draws N(0, 1) float32 values, rounded to bf16
+    (round to nearest even) and kept as uint16 bit patterns;
+  * request lengths are integers drawn uniformly from inclusive ranges;
+  * the pool holds exactly sum_i ceil(seq_i / bs) blocks (unless a size is
+    given); a seeded permutation of the block ids is handed out to the
+    requests in order, so each request's blocks are scattered through the pool;
+  * the whole pool is first filled with N(0, 1) values, then the step's new
+    K/V (the last ``query_len`` positions of each request) are drawn and the
+    slot of each new token is slot = block_table[i][pos // bs] * bs + pos % bs
+    ("Attention Backends", section "Code");
+  * entries of ``block_table`` past a request's last block are -1, so a kernel
+    that read them would be caught.
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to bf16 (nearest even); returns uint16 bit patterns."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    bias = ((u >> 16) & 1) + np.uint32(0x7FFF)
+    return ((u + bias) >> 16).astype(np.uint16)
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bit patterns to float32."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def randn_bf16(rng: np.random.Generator, shape, chunk: int = 1 << 26) -> np.ndarray:
+    """N(0, 1) values rounded to bf16, as uint16 bits.  Drawn in chunks so
+    multi-GB pools do not need a float32 copy of the whole array."""
+    n = int(np.prod(shape))
+    out = np.empty(n, np.uint16)
+    for a in range(0, n, chunk):
+        b = min(n, a + chunk)
+        out[a:b] = f32_to_bf16_bits(rng.standard_normal(b - a, dtype=np.float32))
+    return out.reshape(shape)
+
+
+@dataclass
+class PagedBatch:
+    """One step of the standard-layout workload (pool [nb, 2, bs, Hkv, d])."""
+    name: str
+    seed: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_size: int
+    block_size: int
+    num_blocks: int
+    seq_lens: np.ndarray          # int32 [N]
+    query_lens: np.ndarray        # int32 [N]
+    query_start_loc: np.ndarray   # int32 [N + 1]
+    block_table: np.ndarray       # int32 [N, max_blocks], -1 past the end
+    slot_mapping: np.ndarray      # int64 [T]
+    q: np.ndarray                 # uint16 [T, Hq, d]
+    key: np.ndarray               # uint16 [T, Hkv, d] (new tokens)
+    value: np.ndarray             # uint16 [T, Hkv, d]
+    pool: np.ndarray              # uint16 [nb, 2, bs, Hkv, d] BEFORE the write
+    scale: float
+    causal: bool = True
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.seq_lens.shape[0])
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.query_start_loc[-1])
+
+    @property
+    def max_blocks_per_seq(self) -> int:
+        return int(self.block_table.shape[1])
+
+    def kv_bytes(self) -> int:
+        """Bytes of K and V a decode pass must read (bf16)."""
+        return int(self.seq_lens.astype(np.int64).sum()) * self.num_kv_heads * self.head_size * 2 * 2
+
+    def causal_flops(self) -> int:
+        """4 * d * Hq * sum_i(qlen_i * ctx_i + qlen_i (qlen_i + 1) / 2)."""
+        ql = self.query_lens.astype(np.int64)
+        ctx = self.seq_lens.astype(np.int64) - ql
+        pairs = int((ql * ctx + ql * (ql + 1) // 2).sum())
+        return 4 * self.head_size * self.num_q_heads * pairs
+
+
+def _assign_blocks(rng, seq_lens, block_size, num_blocks=None):
+    need = [(int(s) + block_size - 1) // block_size for s in seq_lens]
+    total = sum(need)
+    nb = total if num_blocks is None else int(num_blocks)
+    if nb < total:
+        raise ValueError("pool too small")
+    perm = rng.permutation(nb).astype(np.int32)
+    max_blocks = max(1, max(need) if need else 1)
+    table = np.full((len(seq_lens), max_blocks), -1, np.int32)
+    k = 0
+    for i, n in enumerate(need):
+        table[i, :n] = perm[k:k + n]
+        k += n
+    return table, nb
+
+
+def make_paged_batch(name, seed, seq_lens, query_lens, num_q_heads, num_kv_heads,
+                     head_size, block_size, num_blocks=None, scale=None,
+                     causal=True) -> PagedBatch:
+    rng = np.random.default_rng(seed)
+    seq_lens = np.asarray(seq_lens, np.int32)
+    query_lens = np.asarray(query_lens, np.int32)
+    assert np.all(query_lens <= seq_lens) and np.all(query_lens >= 0)
+    N = seq_lens.shape[0]
+    qsl = np.zeros(N + 1, np.int32)
+    qsl[1:] = np.cumsum(query_lens)
+    table, nb = _assign_blocks(rng, seq_lens, block_size, num_blocks)
+    T = int(qsl[-1])
+    slots = np.empty(T, np.int64)
+    for i in range(N):
+        ctx = int(seq_lens[i] - query_lens[i])
+        for j in range(int(query_lens[i])):
+            pos = ctx + j
+            slots[qsl[i] + j] = int(table[i, pos // block_size]) * block_size + pos % block_size
+    pool = randn_bf16(rng, (nb, 2, block_size, num_kv_heads, head_size))
+    q = randn_bf16(rng, (T, num_q_heads, head_size))
+    key = randn_bf16(rng, (T, num_kv_heads, head_size))
+    value = randn_bf16(rng, (T, num_kv_heads, head_size))
+    if scale is None:
+        scale = 1.0 / math.sqrt(head_size)
+    return PagedBatch(name, seed, num_q_heads, num_kv_heads, head_size, block_size, nb,
+                      seq_lens, query_lens, qsl, table, slots, q, key, value, pool,
+                      float(scale), causal)
+
+
+@dataclass
+class MLABatch:
+    """One decode step of the MLA latent workload (pool [nb, bs, 576])."""
+    name: str
+    seed: int
+    num_heads: int
+    kv_lora_rank: int
+    rope_dim: int
+    block_size: int
+    num_blocks: int
+    seq_lens: np.ndarray      # int32 [B]
+    block_table: np.ndarray   # int32 [B, max_blocks]
+    q: np.ndarray             # uint16 [B, H, kv_lora_rank + rope_dim]
+    pool: np.ndarray          # uint16 [nb, bs, kv_lora_rank + rope_dim]
+    scale: float
+
+    @property
+    def batch(self) -> int:
+        return int(self.seq_lens.shape[0])
+
+    @property
+    def max_blocks_per_seq(self) -> int:
+        return int(self.block_table.shape[1])
+
+    def kv_bytes(self) -> int:
+        return int(self.seq_lens.astype(np.int64).sum()) * (self.kv_lora_rank + self.rope_dim) * 2
+
+
+def make_mla_batch(name, seed, seq_lens, num_heads, kv_lora_rank=512, rope_dim=64,
+                   block_size=64, num_blocks=None, scale=None) -> MLABatch:
+    rng = np.random.default_rng(seed)
+    seq_lens = np.asarray(seq_lens, np.int32)
+    table, nb = _assign_blocks(rng, seq_lens, block_size, num_blocks)
+    dk = kv_lora_rank + rope_dim
+    pool = randn_bf16(rng, (nb, block_size, dk))
+    q = randn_bf16(rng, (seq_lens.shape[0], num_heads, dk))
+    if scale is None:
+        scale = 1.0 / math.sqrt(128 + rope_dim)
+    return MLABatch(name, seed, num_heads, kv_lora_rank, rope_dim, block_size, nb,
+                    seq_lens, table, q, pool, float(scale))
+
+
+# ---------------------------------------------------------------------------
+# The five named workloads.
+# ---------------------------------------------------------------------------
+
+def tiny_paged(seed: int = 1) -> PagedBatch:
+    """3 requests, seq_lens {5, 17, 40}, query_lens {5, 1, 1}, 4 q / 2 kv heads,
+    head_size 64, block_size 16, a 16-block pool, scale 1/8, causal."""
+    return make_paged_batch("tiny_paged_3req_d64", seed, [5, 17, 40], [5, 1, 1], 4, 2, 64,
+                            16, num_blocks=16, scale=1.0 / 8.0)
+
+
+def gqa_decode(seed: int = 2, num_seqs: int = 64, lo: int = 128, hi: int = 4096) -> PagedBatch:
+    """Llama-3-8B attention shape: 64 requests x 1 query, seq_lens U[128, 4096],
+    32 q / 8 kv heads, head_size 128, block_size 16."""
+    rng = np.random.default_rng(seed + 1000)
+    seq = rng.integers(lo, hi, size=num_seqs, endpoint=True).astype(np.int32)
+    return make_paged_batch(f"gqa_decode_{num_seqs}req_seq{lo}-{hi}_32q8kv_d128", seed, seq,
+                            np.ones(num_seqs, np.int32), 32, 8, 128, 16)
+
+
+def chunked_prefill(seed: int = 3, num_seqs: int = 16, qlo: int = 256, qhi: int = 2048,
+                    clo: int = 0, chi: int = 4096) -> PagedBatch:
+    """16 requests, new-query lengths U[256, 2048], cached prefix U[0, 4096],
+    32 q / 8 kv heads, head_size 128, block_size 16, causal."""
+    rng = np.random.default_rng(seed + 1000)
+    ql = rng.integers(qlo, qhi, size=num_seqs, endpoint=True).astype(np.int32)
+    ctx = rng.integers(clo, chi, size=num_seqs, endpoint=True).astype(np.int32)
+    return make_paged_batch(f"chunked_prefill_{num_seqs}req_32q8kv_d128", seed, ctx + ql, ql,
+                            32, 8, 128, 16)
+
+
+def long_decode(seed: int = 4, num_seqs: int = 8, seq_len: int = 131072) -> PagedBatch:
+    """Llama-3-70B attention shape: 8 requests x 1 query at seq_len 131072,
+    64 q / 8 kv heads, head_size 128, block_size 16."""
+    return make_paged_batch(f"long_decode_{num_seqs}x{seq_len}_64q8kv_d128", seed,
+                            np.full(num_seqs, seq_len, np.int32), np.ones(num_seqs, np.int32),
+                            64, 8, 128, 16)
+
+
+def mla_decode(seed: int = 5, batch: int = 128, lo: int = 1024, hi: int = 8192) -> MLABatch:
+    """DeepSeek-V3 shape: 128 requests x 1 query, 128 heads over one 576-wide
+    latent KV head (kv_c 512 | k_pe 64), value = first 512, seq_lens
+    U[1024, 8192], block_size 64, scale 1/sqrt(192)."""
+    rng = np.random.default_rng(seed + 1000)
+    seq = rng.integers(lo, hi, size=batch, endpoint=True).astype(np.int32)
+    return make_mla_batch(f"mla_decode_{batch}req_128h_576", seed, seq, 128, 512, 64, 64,
+                          scale=1.0 / math.sqrt(192.0))
+
