@@ -1,0 +1,526 @@
+"""Benchmark of the paged-attention hot path on one GB300 (or N replicas).
+
+Headline workload: the GQA decode batch with the Llama-3-8B attention shape
+(64 requests x 1 query, seq_lens U[128, 4096], 32 q / 8 kv heads, head_size
+128, block_size 16, bf16).  One step = the whole decode hot path on that
+batch: the cache write of the step's 64 new tokens, split-KV stage 1 with the
+page's split rule, and the LSE merge.  ``value`` is decode KV throughput in
+GB/s: the bytes of K and V the step must read (4096 B per token per kv-head
+pair, summed over the batch) divided by the time per step.
+
+Secondary lines in the same JSON record (same kernels, timed alone): the
+chunked-prefill workload (TFLOP/s of causal-visible work), the long-context
+split-KV decode (Llama-3-70B shape, 8 x 131072), and MLA latent decode
+(DeepSeek-V3 shape).
+
+``--impl reference`` times the fp64 CPU oracle on a bounded sample of the
+same workload instead (the only other place this script runs the oracle).
+Multi-GPU: ``torchrun --nproc-per-node N bench.py --gpus N`` runs N
+independent replicas (weak scaling; the path has no exchange step).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "decode KV GB/s (% HBM peak); prefill TFLOP/s (% bf16 peak); 1 GB300"
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained",
+                                                     p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK, source="fallback")
+
+
+def kernel_source_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "paged_kv_cache_50_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(summary_name, sha):
+    """DRAM bytes per launch recorded by an ncu capture of this kernel source
+    (``traffic_bytes_per_launch`` and ``source_sha`` lines in the summary under
+    profiles/); None if absent or if the kernel changed since."""
+    path = os.path.join(ROOT, "profiles", summary_name)
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_sha = re.search(r"source_sha:\s*([0-9a-f]+)", text)
+    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_sha or not m_tr or m_sha.group(1) != sha:
+        return None
+    return float(m_tr.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the GPU is busy."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def to_dev_bf16(bits, device):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(
+        torch.bfloat16)
+
+
+def to_dev(a, dtype, device):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device=device, dtype=dtype)
+
+
+def device_pool(shape, seed, device):
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return torch.randn(shape, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+
+
+# ---------------------------------------------------------------------------
+# Headline: GQA decode step (cache write + split-KV stage 1 + LSE merge).
+# ---------------------------------------------------------------------------
+
+class DecodeStep:
+    def __init__(self, pa, b, device, n_pools=4):
+        self.pa, self.b, self.device = pa, b, device
+        N, hq, d = b.num_seqs, b.num_q_heads, b.head_size
+        base = to_dev_bf16(b.pool, device)
+        # Several copies of the pool so that consecutive steps never find the
+        # previous step's K/V in L2 (4 x 0.53 GB >> 129 MB of L2).
+        self.pools = [base] + [base.clone() for _ in range(n_pools - 1)]
+        self.q = to_dev_bf16(b.q, device).view(N, hq, d)
+        self.key = to_dev_bf16(b.key, device)
+        self.value = to_dev_bf16(b.value, device)
+        self.slots = to_dev(b.slot_mapping, torch.int64, device)
+        self.table = to_dev(b.block_table, torch.int32, device)
+        self.seq = to_dev(b.seq_lens, torch.int32, device)
+        self.S = pa.pa_num_kv_splits(int(b.seq_lens.max()), pa.pa_device_sm_count())
+        self.ws = pa.decode_workspace(N, hq, self.S, d, device=device)
+        self.out = torch.empty((N, hq, d), dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty((N, hq), dtype=torch.float32, device=device)
+
+    def run(self, k, ev=None):
+        pa, pool = self.pa, self.pools[k % len(self.pools)]
+        pa.pa_reshape_and_cache(self.key, self.value, pool, self.slots)
+        if ev is not None:
+            ev[0].record()
+        pa.pa_decode_splitkv(self.q, pool, self.table, self.seq, self.b.scale, self.ws)
+        if ev is not None:
+            ev[1].record()
+        pa.pa_lse_merge(self.ws, self.out, self.lse)
+
+
+def run_e2e(pa, b, step, steps, warmup, device):
+    """Same step through the public API with the step's inputs in pinned host
+    memory: H2D copies of q / new K,V / slot_mapping / block_table / seq_lens,
+    the three calls, and a D2H read of out + lse, every step."""
+    N, hq, d = b.num_seqs, b.num_q_heads, b.head_size
+    h = {
+        "q": torch.from_numpy(b.q.view(np.int16)).view(torch.bfloat16).reshape(N, hq, d)
+        .pin_memory(),
+        "key": torch.from_numpy(b.key.view(np.int16)).view(torch.bfloat16).pin_memory(),
+        "value": torch.from_numpy(b.value.view(np.int16)).view(torch.bfloat16).pin_memory(),
+        "slots": torch.from_numpy(b.slot_mapping).pin_memory(),
+        "table": torch.from_numpy(b.block_table).pin_memory(),
+        "seq": torch.from_numpy(b.seq_lens).pin_memory(),
+    }
+    out_h = torch.empty((N, hq, d), dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty((N, hq), dtype=torch.float32).pin_memory()
+    dv = {"q": step.q, "key": step.key, "value": step.value, "slots": step.slots,
+          "table": step.table, "seq": step.seq}
+    h2d = sum(t.numel() * t.element_size() for t in h.values())
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+    stream = torch.cuda.current_stream()
+
+    def one(k):
+        for name, t in h.items():
+            dv[name].copy_(t, non_blocking=True)
+        step.run(k)
+        out_h.copy_(step.out, non_blocking=True)
+        lse_h.copy_(step.lse, non_blocking=True)
+        stream.synchronize()
+
+    for k in range(warmup):
+        one(k)
+    t0 = time.perf_counter()
+    for k in range(steps):
+        one(k)
+    dt = time.perf_counter() - t0
+    return dt, h2d, d2h
+
+
+def cpu_baseline_sample(b, budget_s=20.0, threads=None):
+    """The oracle, as it stands, on a bounded sample of the decode batch:
+    whole requests in order until ~budget_s of CPU work.  Returns
+    (GB/s of KV processed, threads, sample description)."""
+    import oracle
+    threads = threads or (os.cpu_count() or 1)
+    pool = oracle.reshape_and_cache(b.key, b.value, b.pool, b.slot_mapping, b.block_size)
+    done_bytes, elapsed, n = 0, 0.0, 0
+    order = list(range(b.num_seqs))
+    per_tok = b.num_kv_heads * b.head_size * 2 * 2
+    while elapsed < budget_s and n < len(order):
+        # Take a group of requests per call so the oracle's threads have work.
+        grp = order[n:n + max(1, threads)]
+        mask = np.zeros(b.num_tokens, np.uint8)
+        mask[grp] = 1
+        t0 = time.perf_counter()
+        oracle.paged_attention(b.q, pool, b.block_table, b.query_start_loc, b.seq_lens, b.scale,
+                               row_mask=mask, threads=threads)
+        elapsed += time.perf_counter() - t0
+        done_bytes += int(b.seq_lens[grp].astype(np.int64).sum()) * per_tok
+        n += len(grp)
+    return done_bytes / elapsed / 1e9, threads, (
+        f"oracle decode attention (fp64, paged gather + softmax) over the first {n} of "
+        f"{b.num_seqs} requests of the GQA decode batch, {elapsed:.1f} s")
+
+
+# ---------------------------------------------------------------------------
+# Secondary workloads (kernels timed alone, events on the launch stream).
+# ---------------------------------------------------------------------------
+
+def time_events(fn, reps, warmup=3):
+    for _ in range(warmup):
+        fn()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    torch.cuda.synchronize()
+    for e0, e1 in evs:
+        e0.record()
+        fn()
+        e1.record()
+    torch.cuda.synchronize()
+    return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)   # ms
+
+
+def l2_flusher(device):
+    buf = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    return lambda: buf.fill_(1)
+
+
+def secondary(pa, device, pk):
+    res = {}
+    flush = l2_flusher(device)
+    # Chunked prefill: varlen kernel.
+    b = workloads.chunked_prefill(with_pool=False)
+    pool = device_pool((b.num_blocks, 2, b.block_size, b.num_kv_heads, b.head_size), 3, device)
+    q = to_dev_bf16(b.q, device)
+    table, qsl = to_dev(b.block_table, torch.int32, device), to_dev(b.query_start_loc,
+                                                                     torch.int32, device)
+    seq = to_dev(b.seq_lens, torch.int32, device)
+    out = torch.empty_like(q)
+    lse = torch.empty((b.num_tokens, b.num_q_heads), dtype=torch.float32, device=device)
+    mq = int(b.query_lens.max())
+
+    def prefill():
+        pa.pa_varlen_fwd(q, pool, table, qsl, seq, mq, b.scale, out=out, lse=lse)
+    ms = _timed_with_flush(prefill, flush, 10)
+    tf = b.causal_flops() / (ms * 1e-3) / 1e12
+    res["chunked_prefill"] = {"workload": b.name, "kernel": "varlen_fwd", "ms": ms,
+                              "tflops": tf, "causal_flops": b.causal_flops(),
+                              "frac_of_bf16_peak": tf / pk["bf16_tflops"],
+                              "peak": "bf16_tflops (measured burst)" if pk["source"] == "measured"
+                              else "fallback"}
+    del pool, q, out
+    torch.cuda.empty_cache()
+
+    # Long-context split-KV decode (8 x 131072).
+    b = workloads.long_decode(with_pool=False)
+    pool = device_pool((b.num_blocks, 2, b.block_size, b.num_kv_heads, b.head_size), 4, device)
+    N, hq, d = b.num_seqs, b.num_q_heads, b.head_size
+    q = to_dev_bf16(b.q, device).view(N, hq, d)
+    table, seq = to_dev(b.block_table, torch.int32, device), to_dev(b.seq_lens, torch.int32,
+                                                                    device)
+    S = pa.pa_num_kv_splits(131072, pa.pa_device_sm_count())
+    ws = pa.decode_workspace(N, hq, S, d, device=device)
+    o = torch.empty((N, hq, d), dtype=torch.bfloat16, device=device)
+    lo = torch.empty((N, hq), dtype=torch.float32, device=device)
+    st1 = _timed_with_flush(lambda: pa.pa_decode_splitkv(q, pool, table, seq, b.scale, ws),
+                            flush, 10)
+    both = _timed_with_flush(lambda: pa.pa_decode(q, pool, table, seq, b.scale, ws, o, lo),
+                             flush, 10)
+    gbs = b.kv_bytes() / (st1 * 1e-3) / 1e9
+    res["long_decode"] = {"workload": b.name, "num_splits": S, "stage1_ms": st1,
+                          "decode_plus_merge_ms": both, "kv_bytes": b.kv_bytes(),
+                          "stage1_gbs": gbs, "frac_of_hbm_peak": gbs / pk["hbm_gbs"],
+                          "step_gbs": b.kv_bytes() / (both * 1e-3) / 1e9}
+    del pool, q, ws
+    torch.cuda.empty_cache()
+
+    # MLA latent decode.
+    m = workloads.mla_decode(with_pool=False)
+    pool = device_pool((m.num_blocks, m.block_size, m.kv_lora_rank + m.rope_dim), 5, device)
+    q = to_dev_bf16(m.q, device)
+    table, seq = to_dev(m.block_table, torch.int32, device), to_dev(m.seq_lens, torch.int32,
+                                                                    device)
+    S = mla_splits(m, pa.pa_device_sm_count())
+    ws = pa.decode_workspace(m.batch, m.num_heads, S, m.kv_lora_rank, device=device)
+    o = torch.empty((m.batch, m.num_heads, m.kv_lora_rank), dtype=torch.bfloat16, device=device)
+    lo = torch.empty((m.batch, m.num_heads), dtype=torch.float32, device=device)
+    ms = _timed_with_flush(lambda: pa.pa_mla_decode(q, pool, table, seq, m.scale, ws, o, lo),
+                           flush, 10)
+    gbs = m.kv_bytes() / (ms * 1e-3) / 1e9
+    flops = int(m.seq_lens.astype(np.int64).sum()) * m.num_heads * 2 * (
+        m.kv_lora_rank + m.rope_dim + m.kv_lora_rank)
+    res["mla_decode"] = {"workload": m.name, "num_splits": S, "ms": ms, "kv_bytes": m.kv_bytes(),
+                         "gbs": gbs, "frac_of_hbm_peak": gbs / pk["hbm_gbs"],
+                         "tflops": flops / (ms * 1e-3) / 1e12}
+    del pool, q, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def mla_splits(m, sms):
+    """Splits for the MLA workload: enough (request, split) CTAs for two
+    waves of 2 head groups per SM."""
+    return max(1, min(8, math.ceil(2 * sms / (m.batch * max(1, m.num_heads // 64)))))
+
+
+def _timed_with_flush(fn, flush, reps):
+    """Median of reps event-timed launches, L2 flushed before each."""
+    for _ in range(3):
+        flush()
+        fn()
+    times = []
+    for _ in range(reps):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    return statistics.median(times)
+
+
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["pa", "reference"], default="pa")
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    warmup = max(3, args.warmup)
+    world, rank, local = dist_env()
+
+    if args.impl == "reference":
+        return main_reference(args, warmup, world, rank)
+
+    import paged_kv_cache_50_gb300 as pa
+    from paged_kv_cache_50_gb300 import build as pa_build
+    if not os.path.exists(pa.LIB_PATH):
+        pa_build.build()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    pa.lib()
+    pk = peaks()
+
+    b = workloads.gqa_decode()
+    step = DecodeStep(pa, b, device)
+    kv_bytes = b.kv_bytes()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for k in range(warmup):
+        step.run(k)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record()
+    for k in range(args.steps):
+        step.run(k, ev[k])
+    t_end.record()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    if dist is not None:
+        t = torch.tensor([total_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * kv_bytes * args.steps / (total_ms * 1e-3) / 1e9
+    dec_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
+    achieved = kv_bytes / (dec_ms * 1e-3) / 1e9
+    sha = kernel_source_sha(["decode.cu", "pa_common.cuh"])
+    traffic = profiled_traffic("decode_splitkv_gqa_decode.md", sha)
+
+    e2e_dt, h2d, d2h = run_e2e(pa, b, step, args.steps, warmup, device)
+    e2e_value = world * kv_bytes * args.steps / e2e_dt / 1e9
+
+    sec = None
+    if not args.no_secondary and rank == 0:
+        sec = secondary(pa, device, pk)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, sample = cpu_baseline_sample(b)
+        cpu = {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        rec = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded numpy N(0,1) rounded to bf16; random block permutation)",
+            "config": {"workload": b.name, "num_seqs": b.num_seqs, "seq_lens": "U[128,4096]",
+                       "num_q_heads": 32, "num_kv_heads": 8, "head_size": 128,
+                       "block_size": 16, "num_splits": step.S, "kv_bytes_per_step": kv_bytes,
+                       "step": "cache write (64 tokens) + split-KV stage 1 + LSE merge",
+                       "l2": "inputs larger than L2: 4 rotating pool copies of "
+                             f"{kv_bytes / 1e9:.2f} GB", "parallelism": f"replicas x{world}"},
+            "clocks": clk,
+            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": 3 * args.steps,
+            "roofline": {"bound": "hbm", "kernel": "decode_splitkv_kernel<128,3>",
+                         "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
+                         "algorithmic_bytes_per_launch": kv_bytes,
+                         "kernel_ms": dec_ms,
+                         "peak_source": "MEASURED_PEAKS hbm_gbs (of measured)"
+                         if pk["source"] == "measured" else "fallback 6.8 TB/s (of fallback)"},
+            "cpu_baseline": cpu,
+            "secondary": sec,
+        }
+        print(json.dumps(rec), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main_reference(args, warmup, world, rank):
+    """Reference arm: the fp64 oracle on the host cores, each step a bounded
+    sample (8 requests) of the same GQA decode batch; rank 0 only."""
+    if rank != 0:
+        return
+    import oracle
+    b = workloads.gqa_decode()
+    pool = oracle.reshape_and_cache(b.key, b.value, b.pool, b.slot_mapping, b.block_size)
+    threads = os.cpu_count() or 1
+    per_tok = b.num_kv_heads * b.head_size * 2 * 2
+    group = 8
+
+    def one(k):
+        first = (k * group) % b.num_seqs
+        reqs = [(first + j) % b.num_seqs for j in range(group)]
+        mask = np.zeros(b.num_tokens, np.uint8)
+        mask[reqs] = 1
+        oracle.paged_attention(b.q, pool, b.block_table, b.query_start_loc, b.seq_lens, b.scale,
+                               row_mask=mask, threads=threads)
+        return int(b.seq_lens[reqs].astype(np.int64).sum()) * per_tok
+
+    for k in range(warmup):
+        one(k)
+    t0 = time.perf_counter()
+    done = 0
+    for k in range(args.steps):
+        done += one(k)
+    dt = time.perf_counter() - t0
+    value = done / dt / 1e9
+    sample = (f"fp64 oracle decode attention, {group} requests of the GQA decode batch per step "
+              "(cache write done once, outside the timed region)")
+    rec = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+           "steps": args.steps, "warmup": warmup, "ms_per_step": dt * 1e3 / args.steps,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "config": {"workload": b.name, "parallelism": "host threads"},
+           "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0},
+           "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                            "sample": sample}}
+    print(json.dumps(rec), flush=True)
+
+
+if __name__ == "__main__":
+    main()

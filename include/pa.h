@@ -1,0 +1,186 @@
+/*
+ * pa.h -- C ABI of the GB300 paged-attention library (libpa.so).
+ *
+ * The library implements the hot path that every paged-attention backend
+ * wraps, as the two-step kernel contract of "Attention Backends" (vLLM
+ * model-execution notes), section "What 'paged attention' requires of a
+ * kernel", states it: (1) write the step's new keys and values into the cache
+ * at slot_mapping; (2) for each request, attend from its queries over its
+ * first seq_len tokens, fetched block by block through its block_table row.
+ * Split-KV decode and the LSE merge follow "Chapter 1: attention backends"
+ * (zero-to-sglang), section 3.1, and the data-flow section of "Triton and
+ * MLA" (vllm-arch-zh); MLA latent decode follows the latter.
+ *
+ * Conventions for every entry point:
+ *  - Every data pointer is a DEVICE pointer owned by the caller; the library
+ *    allocates nothing, keeps no state beyond a cached SM count per device and
+ *    a device error word, and never synchronises the host.
+ *  - bf16 tensors are passed as `const void*` / `void*` and hold IEEE
+ *    bfloat16 values; every tensor is dense and row-major (C order) with the
+ *    shape stated below.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *    enqueued asynchronously on it.
+ *  - Arguments are validated on the host before anything is launched; a call
+ *    that returns anything but PA_OK has launched nothing (PA_ERR_CUDA: the
+ *    launch itself failed).
+ *  - Index types: block_table, query_start_loc and seq_lens are int32;
+ *    slot_mapping is int64.
+ *  - The standard KV pool is [num_blocks, 2, block_size, num_kv_heads,
+ *    head_size] (index 0 = keys, 1 = values), the layout "AttentionBackend:
+ *    attention backend abstraction layer" (vllm-arch-zh), design-motivation
+ *    list, gives for FlashAttention.  The MLA pool is [num_blocks, block_size,
+ *    kv_lora_rank + rope_dim] (same page; "Triton and MLA", design list).
+ *  - Block ids in block_table are checked on the device against num_blocks:
+ *    an id outside [0, num_blocks) is never dereferenced; its tokens are
+ *    treated as masked and PA_DEVERR_BLOCK_ID is recorded in the device error
+ *    word (read it with pa_get_device_error).  Entries past
+ *    ceil(seq_len / block_size) are never read.
+ *  - LSE outputs are fp32 natural-log (log-sum-exp of scale * q.k), matching
+ *    the "lse_base_on_e" convention of the abstraction-layer page.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_INVALID = 1,     /* bad argument: null pointer, size, divisibility */
+  PA_ERR_UNSUPPORTED = 2, /* valid on the pages but not built here (head size, width) */
+  PA_ERR_CUDA = 3         /* a CUDA launch or query failed */
+} pa_status;
+
+/* Device error word bits (pa_get_device_error). */
+#define PA_DEVERR_BLOCK_ID 1  /* a block_table entry outside [0, num_blocks) */
+#define PA_DEVERR_SLOT 2      /* a slot_mapping entry >= num_blocks * block_size */
+
+/* Shape of a standard-layout paged batch. */
+typedef struct pa_shape {
+  int num_seqs;           /* N: requests in the batch                          */
+  int num_q_heads;        /* Hq                                                 */
+  int num_kv_heads;       /* Hkv; Hq % Hkv == 0, q head h reads kv head h/(Hq/Hkv) */
+  int head_size;          /* d                                                  */
+  int block_size;         /* tokens per cache block; a positive multiple of 16  */
+  int num_blocks;         /* blocks in the pool                                 */
+  int max_blocks_per_seq; /* columns of block_table                             */
+} pa_shape;
+
+/*
+ * Step 1 of the kernel contract: the cache write.
+ *   For t < num_tokens with slot = slot_mapping[t] >= 0:
+ *     kv_cache[slot / bs, 0, slot % bs, :, :] = key[t, :, :]
+ *     kv_cache[slot / bs, 1, slot % bs, :, :] = value[t, :, :]
+ *   A bit copy.  slot < 0 skips the token.  A slot >= num_blocks * bs is not
+ *   written and sets PA_DEVERR_SLOT.
+ * key, value: [num_tokens, Hkv, d] bf16.  kv_cache: standard pool, in-out.
+ * Uses shape->num_kv_heads, head_size (a multiple of 8), block_size,
+ * num_blocks.  num_tokens == 0 is a no-op.
+ */
+pa_status pa_reshape_and_cache(const void* key, const void* value, void* kv_cache,
+                               const int64_t* slot_mapping, int num_tokens,
+                               const pa_shape* shape, void* stream);
+
+/*
+ * Step 2 of the kernel contract: varlen paged attention (prefill, chunked
+ * prefill, mixed batches).  For request i, rows j in
+ * [query_start_loc[i], query_start_loc[i+1]) are its qlen_i newest tokens:
+ * row j sits at position p_j = seq_lens[i] - qlen_i + (j - query_start_loc[i]).
+ * For q head h (kv head h / (Hq/Hkv)):
+ *   out[j, h, :] = softmax(scale * q[j, h, :] . K[p, :] for visible p) . V
+ *   lse[j, h]    = ln sum_p exp(scale * q[j, h, :] . K[p, :])
+ * where p is visible if p <= p_j (causal != 0) or p < seq_lens[i] (causal == 0);
+ * O = softmax(Q K^T / sqrt(d_h) + M) V of "Chapter 1: attention backends",
+ * section 2.1, with the mask M.
+ * q, out: [total_q, Hq, d] bf16.  lse: [total_q, Hq] fp32, nullable.
+ * query_start_loc: [N + 1], non-decreasing, query_start_loc[N] == total_q.
+ * seq_lens: [N] with seq_lens[i] >= qlen_i.  max_query_len >= every qlen_i
+ * (sizes the grid; rows beyond it are not computed).
+ * Supported: head_size in {64, 128}.  A row with nothing visible gets o = 0
+ * and lse = -inf.  total_q == 0 is a no-op.
+ */
+pa_status pa_varlen_fwd(const void* q, const void* kv_cache, const int32_t* block_table,
+                        const int32_t* query_start_loc, const int32_t* seq_lens,
+                        int total_q, int max_query_len, const pa_shape* shape,
+                        float scale, int causal, void* out, float* lse, void* stream);
+
+/*
+ * Split-count rule of "Triton and MLA", key-files list (_compute_num_kv_splits):
+ * min(ceil(max_seq_len / 512), 2 * sm_count), at least 1.  sm_count <= 0
+ * means the current device's SM count.
+ */
+int pa_num_kv_splits(int max_seq_len, int sm_count);
+
+/*
+ * Bytes of the split-KV workspace [num_seqs, num_q_heads, num_splits, dv + 1]
+ * fp32: each split's normalised partial output followed by its LSE ("the +1
+ * stores the LSE", data-flow section of "Triton and MLA").  0 on bad sizes.
+ */
+size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_splits, int dv);
+
+/*
+ * Split-KV decode, stage 1 (one query per request; the query attends over
+ * all seq_lens[i] cached tokens).  Split s of request i covers the tokens
+ * [s*C_i, min((s+1)*C_i, seq_i)) with C_i = bs * ceil(ceil(seq_i / S) / bs);
+ * for each q head h it writes the split's softmax-normalised output and LSE:
+ *   workspace[i, h, s, 0:d] = o_s,  workspace[i, h, s, d] = lse_s
+ * An empty split writes o_s = 0, lse_s = -inf.
+ * q: [N, Hq, d] bf16.  workspace: pa_decode_workspace_bytes(N, Hq, S, d) bytes.
+ * Supported: head_size in {64, 128}, Hq / Hkv <= 16.
+ */
+pa_status pa_decode_splitkv(const void* q, const void* kv_cache, const int32_t* block_table,
+                            const int32_t* seq_lens, const pa_shape* shape, float scale,
+                            int num_splits, float* workspace, void* stream);
+
+/*
+ * Split-KV stage 2: merge S partials per (request, head) by their LSE:
+ *   M = max_s lse_s,  w_s = exp(lse_s - M),
+ *   out = sum_s w_s o_s / sum_s w_s  (rounded to bf16),  lse = M + ln sum_s w_s.
+ * All partials empty: out = 0, lse = -inf.
+ * workspace: [num_seqs, num_q_heads, num_splits, dv + 1] fp32.
+ * out: [num_seqs, num_q_heads, dv] bf16.  lse: [num_seqs, num_q_heads], nullable.
+ */
+pa_status pa_lse_merge(const float* workspace, int num_seqs, int num_q_heads,
+                       int num_splits, int dv, void* out, float* lse, void* stream);
+
+/*
+ * MLA latent decode ("Triton and MLA", data flow: forward_mqa): MQA over a
+ * single latent KV head.  For request b and head h:
+ *   s_p = scale * q[b, h, :] . c[p, :]   (all kv_lora_rank + rope_dim entries)
+ *   out[b, h, :] = softmax(s) . c[:, 0:kv_lora_rank],  lse[b, h] = ln sum exp(s_p)
+ * where c[p] = kv_cache[block_table[b][p / bs], p % bs, :], p < seq_lens[b].
+ * q: [batch, num_heads, kv_lora_rank + rope_dim] bf16 (q_nope absorbed | q_pe).
+ * kv_cache: [num_blocks, block_size, kv_lora_rank + rope_dim] bf16.
+ * out: [batch, num_heads, kv_lora_rank] bf16.  lse: [batch, num_heads] fp32, nullable.
+ * The call runs split-KV stage 1 into `workspace`
+ * (pa_decode_workspace_bytes(batch, num_heads, num_splits, kv_lora_rank) bytes)
+ * and then the LSE merge.
+ * Supported: kv_lora_rank == 512, rope_dim == 64, num_heads a multiple of 16.
+ */
+pa_status pa_mla_decode(const void* q, const void* kv_cache, const int32_t* block_table,
+                        const int32_t* seq_lens, int batch, int num_heads, int kv_lora_rank,
+                        int rope_dim, int block_size, int num_blocks, int max_blocks_per_seq,
+                        float scale, int num_splits, float* workspace, void* out, float* lse,
+                        void* stream);
+
+/* Human-readable name of a status. */
+const char* pa_status_string(pa_status status);
+
+/*
+ * Reads and clears the current device's error word (PA_DEVERR_* bits set by
+ * earlier kernels).  Synchronises `stream` first.  *code receives the bits.
+ */
+pa_status pa_get_device_error(int* code, void* stream);
+
+/* SM count of the current device (cached per device); -1 on error. */
+int pa_device_sm_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

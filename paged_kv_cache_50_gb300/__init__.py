@@ -1,0 +1,243 @@
+"""Python binding of libpa.so, the GB300 paged-attention library.
+
+Argument marshalling only: each function checks that the torch tensors it is
+given have the dtype, device and contiguity the C ABI (``include/pa.h``)
+expects, passes their raw device pointers and the current CUDA stream, and
+raises :class:`PaError` on a non-OK status.  Every step of the computation
+runs in the library's CUDA kernels; there is no fallback.  If ``libpa.so``
+has not been built, every call raises.
+
+Function names follow the C ABI: ``pa_reshape_and_cache``, ``pa_varlen_fwd``,
+``pa_num_kv_splits``, ``pa_decode_workspace_bytes``, ``pa_decode_splitkv``,
+``pa_lse_merge``, ``pa_mla_decode``, ``pa_get_device_error``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libpa.so")
+
+PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_CUDA = 0, 1, 2, 3
+PA_DEVERR_BLOCK_ID, PA_DEVERR_SLOT = 1, 2
+
+_lock = threading.Lock()
+_lib = None
+
+
+class PaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}")
+
+
+class PaShape(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int), ("num_q_heads", ctypes.c_int),
+                ("num_kv_heads", ctypes.c_int), ("head_size", ctypes.c_int),
+                ("block_size", ctypes.c_int), ("num_blocks", ctypes.c_int),
+                ("max_blocks_per_seq", ctypes.c_int)]
+
+
+def lib() -> ctypes.CDLL:
+    """Loads libpa.so (once).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m paged_kv_cache_50_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        P, i32, f32, st = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_int
+        SP = ctypes.POINTER(PaShape)
+        L.pa_reshape_and_cache.argtypes = [P, P, P, P, i32, SP, P]
+        L.pa_varlen_fwd.argtypes = [P, P, P, P, P, i32, i32, SP, f32, i32, P, P, P]
+        L.pa_num_kv_splits.argtypes = [i32, i32]
+        L.pa_num_kv_splits.restype = i32
+        L.pa_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
+        L.pa_decode_workspace_bytes.restype = ctypes.c_size_t
+        L.pa_decode_splitkv.argtypes = [P, P, P, P, SP, f32, i32, P, P]
+        L.pa_lse_merge.argtypes = [P, i32, i32, i32, i32, P, P, P]
+        L.pa_mla_decode.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, i32, f32, i32, P,
+                                    P, P, P]
+        L.pa_status_string.argtypes = [st]
+        L.pa_status_string.restype = ctypes.c_char_p
+        L.pa_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int), P]
+        L.pa_device_sm_count.argtypes = []
+        L.pa_device_sm_count.restype = i32
+        for name in ("pa_reshape_and_cache", "pa_varlen_fwd", "pa_decode_splitkv",
+                     "pa_lse_merge", "pa_mla_decode", "pa_get_device_error"):
+            getattr(L, name).restype = st
+        _lib = L
+        return L
+
+
+def status_string(status: int) -> str:
+    return lib().pa_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != PA_OK:
+        raise PaError(status, what)
+
+
+def _dev(t: torch.Tensor, name: str, dtype: torch.dtype) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _opt(t, name, dtype):
+    return None if t is None else _dev(t, name, dtype)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _pool_shape(kv_cache: torch.Tensor, num_seqs: int, num_q_heads: int,
+                max_blocks: int) -> PaShape:
+    if kv_cache.dim() != 5 or kv_cache.shape[1] != 2:
+        raise ValueError("kv_cache must be [num_blocks, 2, block_size, num_kv_heads, head_size]")
+    nb, _, bs, hkv, d = kv_cache.shape
+    return PaShape(num_seqs, num_q_heads, hkv, d, bs, nb, max_blocks)
+
+
+def pa_reshape_and_cache(key, value, kv_cache, slot_mapping, stream=None) -> None:
+    """Writes key/value [T, Hkv, d] bf16 into kv_cache at slot_mapping [T] int64."""
+    shape = _pool_shape(kv_cache, 0, kv_cache.shape[3], 1)
+    T = key.shape[0]
+    if tuple(key.shape) != (T, shape.num_kv_heads, shape.head_size) or value.shape != key.shape:
+        raise ValueError("key/value must be [num_tokens, num_kv_heads, head_size]")
+    if slot_mapping.shape != (T,):
+        raise ValueError("slot_mapping must be [num_tokens]")
+    _check(lib().pa_reshape_and_cache(
+        _dev(key, "key", torch.bfloat16), _dev(value, "value", torch.bfloat16),
+        _dev(kv_cache, "kv_cache", torch.bfloat16), _dev(slot_mapping, "slot_mapping", torch.int64),
+        T, ctypes.byref(shape), _stream(stream)), "pa_reshape_and_cache")
+
+
+def pa_varlen_fwd(q, kv_cache, block_table, query_start_loc, seq_lens, max_query_len, scale,
+                  causal=True, out=None, lse=None, return_lse=True, stream=None):
+    """Varlen paged attention.  q [T, Hq, d] bf16 -> (out [T, Hq, d] bf16,
+    lse [T, Hq] fp32 or None)."""
+    T, hq, d = q.shape
+    N = seq_lens.shape[0]
+    if query_start_loc.shape != (N + 1,):
+        raise ValueError("query_start_loc must be [num_seqs + 1]")
+    if block_table.dim() != 2 or block_table.shape[0] != N:
+        raise ValueError("block_table must be [num_seqs, max_blocks]")
+    shape = _pool_shape(kv_cache, N, hq, block_table.shape[1])
+    if d != shape.head_size:
+        raise ValueError("q head_size does not match kv_cache")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((T, hq), dtype=torch.float32, device=q.device)
+    _check(lib().pa_varlen_fwd(
+        _dev(q, "q", torch.bfloat16), _dev(kv_cache, "kv_cache", torch.bfloat16),
+        _dev(block_table, "block_table", torch.int32),
+        _dev(query_start_loc, "query_start_loc", torch.int32),
+        _dev(seq_lens, "seq_lens", torch.int32), T, int(max_query_len), ctypes.byref(shape),
+        float(scale), int(bool(causal)), _dev(out, "out", torch.bfloat16),
+        _opt(lse, "lse", torch.float32), _stream(stream)), "pa_varlen_fwd")
+    return out, lse
+
+
+def pa_num_kv_splits(max_seq_len: int, sm_count: int = 0) -> int:
+    return int(lib().pa_num_kv_splits(int(max_seq_len), int(sm_count)))
+
+
+def pa_decode_workspace_bytes(num_seqs: int, num_q_heads: int, num_splits: int, dv: int) -> int:
+    return int(lib().pa_decode_workspace_bytes(num_seqs, num_q_heads, num_splits, dv))
+
+
+def pa_device_sm_count() -> int:
+    return int(lib().pa_device_sm_count())
+
+
+def decode_workspace(num_seqs, num_q_heads, num_splits, dv, device="cuda"):
+    """Allocates a [N, Hq, S, dv + 1] fp32 split-KV workspace (torch owns it)."""
+    return torch.empty((num_seqs, num_q_heads, num_splits, dv + 1), dtype=torch.float32,
+                       device=device)
+
+
+def pa_decode_splitkv(q, kv_cache, block_table, seq_lens, scale, workspace, stream=None) -> None:
+    """Split-KV stage 1: q [N, Hq, d] -> workspace [N, Hq, S, d + 1] fp32."""
+    N, hq, d = q.shape
+    if workspace.dim() != 4 or tuple(workspace.shape) [:2] != (N, hq) or workspace.shape[3] != d + 1:
+        raise ValueError("workspace must be [num_seqs, num_q_heads, num_splits, head_size + 1]")
+    shape = _pool_shape(kv_cache, N, hq, block_table.shape[1])
+    _check(lib().pa_decode_splitkv(
+        _dev(q, "q", torch.bfloat16), _dev(kv_cache, "kv_cache", torch.bfloat16),
+        _dev(block_table, "block_table", torch.int32), _dev(seq_lens, "seq_lens", torch.int32),
+        ctypes.byref(shape), float(scale), int(workspace.shape[2]),
+        _dev(workspace, "workspace", torch.float32), _stream(stream)), "pa_decode_splitkv")
+
+
+def pa_lse_merge(workspace, out=None, lse=None, return_lse=True, stream=None):
+    """Split-KV stage 2: workspace [N, H, S, dv + 1] -> (out [N, H, dv] bf16, lse [N, H])."""
+    N, H, S, dv1 = workspace.shape
+    if out is None:
+        out = torch.empty((N, H, dv1 - 1), dtype=torch.bfloat16, device=workspace.device)
+    if lse is None and return_lse:
+        lse = torch.empty((N, H), dtype=torch.float32, device=workspace.device)
+    _check(lib().pa_lse_merge(
+        _dev(workspace, "workspace", torch.float32), N, H, S, dv1 - 1,
+        _dev(out, "out", torch.bfloat16), _opt(lse, "lse", torch.float32), _stream(stream)),
+        "pa_lse_merge")
+    return out, lse
+
+
+def pa_decode(q, kv_cache, block_table, seq_lens, scale, workspace, out=None, lse=None,
+              stream=None):
+    """Both split-KV stages: stage 1 into ``workspace``, then the LSE merge."""
+    pa_decode_splitkv(q, kv_cache, block_table, seq_lens, scale, workspace, stream)
+    return pa_lse_merge(workspace, out, lse, stream=stream)
+
+
+def pa_mla_decode(q, kv_cache, block_table, seq_lens, scale, workspace, out=None, lse=None,
+                  kv_lora_rank=512, rope_dim=64, stream=None):
+    """MLA latent decode.  q [B, H, 576], kv_cache [nb, bs, 576] ->
+    (out [B, H, 512] bf16, lse [B, H] fp32)."""
+    B, H, dk = q.shape
+    if kv_cache.dim() != 3 or kv_cache.shape[2] != dk or dk != kv_lora_rank + rope_dim:
+        raise ValueError("kv_cache must be [num_blocks, block_size, kv_lora_rank + rope_dim]")
+    if workspace.dim() != 4 or tuple(workspace.shape[:2]) != (B, H) or \
+            workspace.shape[3] != kv_lora_rank + 1:
+        raise ValueError("workspace must be [batch, num_heads, num_splits, kv_lora_rank + 1]")
+    nb, bs, _ = kv_cache.shape
+    if out is None:
+        out = torch.empty((B, H, kv_lora_rank), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    _check(lib().pa_mla_decode(
+        _dev(q, "q", torch.bfloat16), _dev(kv_cache, "kv_cache", torch.bfloat16),
+        _dev(block_table, "block_table", torch.int32), _dev(seq_lens, "seq_lens", torch.int32),
+        B, H, kv_lora_rank, rope_dim, bs, nb, block_table.shape[1], float(scale),
+        int(workspace.shape[2]), _dev(workspace, "workspace", torch.float32),
+        _dev(out, "out", torch.bfloat16), _opt(lse, "lse", torch.float32), _stream(stream)),
+        "pa_mla_decode")
+    return out, lse
+
+
+def pa_get_device_error(stream=None) -> int:
+    """Synchronises the stream, returns and clears the PA_DEVERR_* bits."""
+    code = ctypes.c_int(0)
+    _check(lib().pa_get_device_error(ctypes.byref(code), _stream(stream)), "pa_get_device_error")
+    return code.value

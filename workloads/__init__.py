@@ -40,14 +40,26 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
-def randn_bf16(rng: np.random.Generator, shape, chunk: int = 1 << 26) -> np.ndarray:
-    """N(0, 1) values rounded to bf16, as uint16 bits.  Drawn in chunks so
-    multi-GB pools do not need a float32 copy of the whole array."""
+def randn_bf16(rng: np.random.Generator, shape, chunk: int = 1 << 22) -> np.ndarray:
+    """N(0, 1) values rounded to bf16 (nearest even), as uint16 bits.  Drawn
+    in small chunks through reused buffers, so multi-GB pools need no float32
+    copy of the whole array."""
     n = int(np.prod(shape))
     out = np.empty(n, np.uint16)
+    buf = np.empty(min(n, chunk), np.float32)
+    tmp = np.empty(min(n, chunk), np.uint32)
     for a in range(0, n, chunk):
-        b = min(n, a + chunk)
-        out[a:b] = f32_to_bf16_bits(rng.standard_normal(b - a, dtype=np.float32))
+        m = min(n, a + chunk) - a
+        f = buf[:m]
+        rng.standard_normal(m, dtype=np.float32, out=f)
+        u = f.view(np.uint32)
+        t = tmp[:m]
+        np.right_shift(u, 16, out=t)
+        t &= 1
+        t += 0x7FFF
+        t += u
+        t >>= 16
+        out[a:a + m] = t
     return out.reshape(shape)
 
 
@@ -116,7 +128,9 @@ def _assign_blocks(rng, seq_lens, block_size, num_blocks=None):
 
 def make_paged_batch(name, seed, seq_lens, query_lens, num_q_heads, num_kv_heads,
                      head_size, block_size, num_blocks=None, scale=None,
-                     causal=True) -> PagedBatch:
+                     causal=True, with_pool=True) -> PagedBatch:
+    """with_pool=False skips drawing the pool (``pool`` is None); the other
+    arrays are drawn exactly as with the pool, from a separate stream."""
     rng = np.random.default_rng(seed)
     seq_lens = np.asarray(seq_lens, np.int32)
     query_lens = np.asarray(query_lens, np.int32)
@@ -132,7 +146,8 @@ def make_paged_batch(name, seed, seq_lens, query_lens, num_q_heads, num_kv_heads
         for j in range(int(query_lens[i])):
             pos = ctx + j
             slots[qsl[i] + j] = int(table[i, pos // block_size]) * block_size + pos % block_size
-    pool = randn_bf16(rng, (nb, 2, block_size, num_kv_heads, head_size))
+    pool = randn_bf16(rng, (nb, 2, block_size, num_kv_heads, head_size)) if with_pool else None
+    rng = np.random.default_rng([seed, 1])
     q = randn_bf16(rng, (T, num_q_heads, head_size))
     key = randn_bf16(rng, (T, num_kv_heads, head_size))
     value = randn_bf16(rng, (T, num_kv_heads, head_size))
@@ -172,12 +187,13 @@ class MLABatch:
 
 
 def make_mla_batch(name, seed, seq_lens, num_heads, kv_lora_rank=512, rope_dim=64,
-                   block_size=64, num_blocks=None, scale=None) -> MLABatch:
+                   block_size=64, num_blocks=None, scale=None, with_pool=True) -> MLABatch:
     rng = np.random.default_rng(seed)
     seq_lens = np.asarray(seq_lens, np.int32)
     table, nb = _assign_blocks(rng, seq_lens, block_size, num_blocks)
     dk = kv_lora_rank + rope_dim
-    pool = randn_bf16(rng, (nb, block_size, dk))
+    pool = randn_bf16(rng, (nb, block_size, dk)) if with_pool else None
+    rng = np.random.default_rng([seed, 1])
     q = randn_bf16(rng, (seq_lens.shape[0], num_heads, dk))
     if scale is None:
         scale = 1.0 / math.sqrt(128 + rope_dim)
@@ -196,40 +212,42 @@ def tiny_paged(seed: int = 1) -> PagedBatch:
                             16, num_blocks=16, scale=1.0 / 8.0)
 
 
-def gqa_decode(seed: int = 2, num_seqs: int = 64, lo: int = 128, hi: int = 4096) -> PagedBatch:
+def gqa_decode(seed: int = 2, num_seqs: int = 64, lo: int = 128, hi: int = 4096,
+               **kw) -> PagedBatch:
     """Llama-3-8B attention shape: 64 requests x 1 query, seq_lens U[128, 4096],
     32 q / 8 kv heads, head_size 128, block_size 16."""
     rng = np.random.default_rng(seed + 1000)
     seq = rng.integers(lo, hi, size=num_seqs, endpoint=True).astype(np.int32)
     return make_paged_batch(f"gqa_decode_{num_seqs}req_seq{lo}-{hi}_32q8kv_d128", seed, seq,
-                            np.ones(num_seqs, np.int32), 32, 8, 128, 16)
+                            np.ones(num_seqs, np.int32), 32, 8, 128, 16, **kw)
 
 
 def chunked_prefill(seed: int = 3, num_seqs: int = 16, qlo: int = 256, qhi: int = 2048,
-                    clo: int = 0, chi: int = 4096) -> PagedBatch:
+                    clo: int = 0, chi: int = 4096, **kw) -> PagedBatch:
     """16 requests, new-query lengths U[256, 2048], cached prefix U[0, 4096],
     32 q / 8 kv heads, head_size 128, block_size 16, causal."""
     rng = np.random.default_rng(seed + 1000)
     ql = rng.integers(qlo, qhi, size=num_seqs, endpoint=True).astype(np.int32)
     ctx = rng.integers(clo, chi, size=num_seqs, endpoint=True).astype(np.int32)
     return make_paged_batch(f"chunked_prefill_{num_seqs}req_32q8kv_d128", seed, ctx + ql, ql,
-                            32, 8, 128, 16)
+                            32, 8, 128, 16, **kw)
 
 
-def long_decode(seed: int = 4, num_seqs: int = 8, seq_len: int = 131072) -> PagedBatch:
+def long_decode(seed: int = 4, num_seqs: int = 8, seq_len: int = 131072, **kw) -> PagedBatch:
     """Llama-3-70B attention shape: 8 requests x 1 query at seq_len 131072,
     64 q / 8 kv heads, head_size 128, block_size 16."""
     return make_paged_batch(f"long_decode_{num_seqs}x{seq_len}_64q8kv_d128", seed,
                             np.full(num_seqs, seq_len, np.int32), np.ones(num_seqs, np.int32),
-                            64, 8, 128, 16)
+                            64, 8, 128, 16, **kw)
 
 
-def mla_decode(seed: int = 5, batch: int = 128, lo: int = 1024, hi: int = 8192) -> MLABatch:
+def mla_decode(seed: int = 5, batch: int = 128, lo: int = 1024, hi: int = 8192,
+               **kw) -> MLABatch:
     """DeepSeek-V3 shape: 128 requests x 1 query, 128 heads over one 576-wide
     latent KV head (kv_c 512 | k_pe 64), value = first 512, seq_lens
     U[1024, 8192], block_size 64, scale 1/sqrt(192)."""
     rng = np.random.default_rng(seed + 1000)
     seq = rng.integers(lo, hi, size=batch, endpoint=True).astype(np.int32)
     return make_mla_batch(f"mla_decode_{batch}req_128h_576", seed, seq, 128, 512, 64, 64,
-                          scale=1.0 / math.sqrt(192.0))
+                          scale=1.0 / math.sqrt(192.0), **kw)
 
