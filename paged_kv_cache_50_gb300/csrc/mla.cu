@@ -200,7 +200,9 @@ mla_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
 #pragma unroll
     for (int nd = 0; nd < 32; ++nd) {
       const int col = half * 256 + nd * 8 + 2 * tid4;
-      *reinterpret_cast<float2*>(dst + col) = make_float2(o[nd][2 * r] * inv, o[nd][2 * r + 1] * inv);
+      // Rows of the workspace are Dv + 1 = 513 floats: only 4-byte aligned.
+      dst[col] = o[nd][2 * r] * inv;
+      dst[col + 1] = o[nd][2 * r + 1] * inv;
     }
     if (half == 0 && tid4 == 0)
       dst[C::kDv] = l_r[r] > 0.f ? (m_r[r] + log2f(l_r[r])) * kLn2 : -CUDART_INF_F;

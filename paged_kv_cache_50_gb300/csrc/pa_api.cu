@@ -52,6 +52,10 @@ bool shape_ok(const pa_shape* s) {
 
 pa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
 
+// The kernels move cache rows and MLA queries in 16-byte vectors and q / out
+// rows in 4-byte pairs.
+bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
 // Device address of the error word on the current device (looked up once per
 // device; a host-side symbol is not a device address).
 int* device_error_ptr() {
@@ -82,6 +86,9 @@ pa_status pa_reshape_and_cache(const void* key, const void* value, void* kv_cach
   if (num_tokens == 0) return PA_OK;
   if (key == nullptr || value == nullptr || kv_cache == nullptr || slot_mapping == nullptr)
     return PA_ERR_INVALID;
+  if (!aligned(key, 16) || !aligned(value, 16) || !aligned(kv_cache, 16) ||
+      !aligned(slot_mapping, 8))
+    return PA_ERR_INVALID;
   return from_cuda(pa::launch_reshape_and_cache(key, value, kv_cache, slot_mapping, num_tokens,
                                                 shape->num_kv_heads, shape->head_size,
                                                 shape->block_size, shape->num_blocks,
@@ -98,6 +105,8 @@ pa_status pa_varlen_fwd(const void* q, const void* kv_cache, const int32_t* bloc
   if (total_q == 0 || shape->num_seqs == 0 || max_query_len == 0) return PA_OK;
   if (q == nullptr || kv_cache == nullptr || block_table == nullptr ||
       query_start_loc == nullptr || seq_lens == nullptr || out == nullptr)
+    return PA_ERR_INVALID;
+  if (!aligned(q, 4) || !aligned(kv_cache, 16) || !aligned(out, 4) || !aligned(lse, 4))
     return PA_ERR_INVALID;
   return from_cuda(pa::launch_varlen_fwd(
       q, kv_cache, block_table, query_start_loc, seq_lens, shape->num_seqs, shape->num_q_heads,
@@ -145,6 +154,7 @@ pa_status pa_decode_splitkv(const void* q, const void* kv_cache, const int32_t* 
   if (q == nullptr || kv_cache == nullptr || block_table == nullptr || seq_lens == nullptr ||
       workspace == nullptr)
     return PA_ERR_INVALID;
+  if (!aligned(q, 4) || !aligned(kv_cache, 16) || !aligned(workspace, 4)) return PA_ERR_INVALID;
   return from_cuda(pa::launch_decode_splitkv(
       q, kv_cache, block_table, seq_lens, shape->num_seqs, shape->num_q_heads,
       shape->num_kv_heads, shape->head_size, shape->block_size, shape->num_blocks,
@@ -158,6 +168,7 @@ pa_status pa_lse_merge(const float* workspace, int num_seqs, int num_q_heads, in
     return PA_ERR_INVALID;
   if (num_seqs == 0) return PA_OK;
   if (workspace == nullptr || out == nullptr) return PA_ERR_INVALID;
+  if (!aligned(workspace, 4) || !aligned(out, 2) || !aligned(lse, 4)) return PA_ERR_INVALID;
   const long long nh = static_cast<long long>(num_seqs) * num_q_heads;
   if (nh > INT_MAX) return PA_ERR_INVALID;
   return from_cuda(pa::launch_lse_merge(workspace, static_cast<int>(nh), num_splits, dv, out, lse,
@@ -178,6 +189,9 @@ pa_status pa_mla_decode(const void* q, const void* kv_cache, const int32_t* bloc
   if (batch == 0) return PA_OK;
   if (q == nullptr || kv_cache == nullptr || block_table == nullptr || seq_lens == nullptr ||
       workspace == nullptr || out == nullptr)
+    return PA_ERR_INVALID;
+  if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(workspace, 4) || !aligned(out, 2) ||
+      !aligned(lse, 4))
     return PA_ERR_INVALID;
   return from_cuda(pa::launch_mla_decode(q, kv_cache, block_table, seq_lens, batch, num_heads,
                                          block_size, num_blocks, max_blocks_per_seq, scale,

@@ -157,3 +157,14 @@ def test_python_binding_refuses_cpu_tensors(pa):
     slots = torch.zeros(3, dtype=torch.int64)
     with pytest.raises(ValueError):
         pa.pa_reshape_and_cache(key, key, kv, slots)
+
+
+def test_misaligned_pointers_are_rejected(pa):
+    L = pa.lib()
+    s = _shape(pa)
+    # kv_cache must be 16-byte aligned (16-byte vector loads of cache rows).
+    assert L.pa_varlen_fwd(16, 8, 16, 16, 16, 4, 2, ctypes.byref(s), 0.1, 1, 16, NULL,
+                           NULL) == pa.PA_ERR_INVALID
+    assert L.pa_reshape_and_cache(16, 24, 16, 16, 4, ctypes.byref(s), NULL) == pa.PA_ERR_INVALID
+    assert L.pa_mla_decode(8, 16, 16, 16, 2, 128, 512, 64, 64, 8, 4, 0.1, 2, 16, 16, NULL,
+                           NULL) == pa.PA_ERR_INVALID
