@@ -213,9 +213,10 @@ def test_decode_edge_cases(pa):
     d = Dev(pa, b)
     q = workloads.randn_bf16(np.random.default_rng(5), (len(seq), 32, 128))
     d.q = to_dev_bf16(q)
-    qsl = np.arange(len(seq) + 1)
-    ref_o, ref_l = oracle.paged_attention(q, d.ref_pool(), b.block_table, qsl,
-                                          np.asarray(seq, np.int32), b.scale, causal=False)
+    # The oracle's decode: one split per request, merged (seq_len 0 allowed).
+    part = oracle.split_partials(q, d.ref_pool(), b.block_table, np.asarray(seq, np.int32),
+                                 b.scale, 1)
+    ref_o, ref_l = oracle.lse_merge(part)
     for S in (1, 3, 16):
         out, lse, _ = _decode(pa, d, S)
         assert_out_close(out, ref_o, f"edge S={S}")
