@@ -167,6 +167,30 @@ pa_status pa_mla_decode(const void* q, const void* kv_cache, const int32_t* bloc
                         float scale, int num_splits, float* workspace, void* out, float* lse,
                         void* stream);
 
+/* Size of the fixed device array pa_decode_noalloc keeps its split partials in. */
+#define PA_NOALLOC_WORKSPACE_BYTES (16u * 1024u * 1024u)
+
+/*
+ * Split-KV decode (stage 1 and the LSE merge, exactly as pa_decode_splitkv
+ * followed by pa_lse_merge) that allocates nothing and takes no workspace.
+ * The pages have no counterpart: this entry point exists for callers that
+ * cannot allocate device memory -- a host application that owns every device
+ * allocation and gives the library no allocator, or a path that must never
+ * call cudaMalloc -- and so cannot pass a workspace.  The split partials go
+ * to a fixed device array of PA_NOALLOC_WORKSPACE_BYTES inside the library,
+ * which every device that loads the library keeps until the process exits.
+ *   q: [N, Hq, d] bf16;  out: [N, Hq, d] bf16;  lse: [N, Hq] fp32, nullable.
+ * Returns PA_ERR_INVALID if N * Hq * num_splits * (d + 1) * 4 bytes exceeds
+ * PA_NOALLOC_WORKSPACE_BYTES (use fewer splits, or pa_decode_splitkv with a
+ * workspace of your own).  The first call on each device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current;
+ * make it before any stream capture begins.  All calls share the array:
+ * calls whose work may overlap on the GPU (unordered streams) race on it.
+ */
+pa_status pa_decode_noalloc(const void* q, const void* kv_cache, const int32_t* block_table,
+                            const int32_t* seq_lens, const pa_shape* shape, float scale,
+                            int num_splits, void* out, float* lse, void* stream);
+
 /* Human-readable name of a status. */
 const char* pa_status_string(pa_status status);
 

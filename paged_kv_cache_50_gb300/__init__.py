@@ -65,13 +65,14 @@ def lib() -> ctypes.CDLL:
         L.pa_lse_merge.argtypes = [P, i32, i32, i32, i32, P, P, P]
         L.pa_mla_decode.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, i32, f32, i32, P,
                                     P, P, P]
+        L.pa_decode_noalloc.argtypes = [P, P, P, P, SP, f32, i32, P, P, P]
         L.pa_status_string.argtypes = [st]
         L.pa_status_string.restype = ctypes.c_char_p
         L.pa_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int), P]
         L.pa_device_sm_count.argtypes = []
         L.pa_device_sm_count.restype = i32
         for name in ("pa_reshape_and_cache", "pa_varlen_fwd", "pa_decode_splitkv",
-                     "pa_lse_merge", "pa_mla_decode", "pa_get_device_error"):
+                     "pa_lse_merge", "pa_mla_decode", "pa_get_device_error", "pa_decode_noalloc"):
             getattr(L, name).restype = st
         _lib = L
         return L
@@ -233,6 +234,30 @@ def pa_mla_decode(q, kv_cache, block_table, seq_lens, scale, workspace, out=None
         int(workspace.shape[2]), _dev(workspace, "workspace", torch.float32),
         _dev(out, "out", torch.bfloat16), _opt(lse, "lse", torch.float32), _stream(stream)),
         "pa_mla_decode")
+    return out, lse
+
+
+PA_NOALLOC_WORKSPACE_BYTES = 16 * 1024 * 1024
+
+
+def pa_decode_noalloc(q, kv_cache, block_table, seq_lens, scale, num_splits, out=None,
+                      lse=None, stream=None):
+    """Split-KV decode with the partials in the library's fixed device array
+    (no workspace argument, nothing allocated by the library).  For callers
+    that cannot allocate device memory; calls that overlap on the GPU race
+    on the shared array.  ``out``/``lse`` are allocated here only if not
+    given."""
+    N, hq, d = q.shape
+    shape = _pool_shape(kv_cache, N, hq, block_table.shape[1])
+    if out is None:
+        out = torch.empty((N, hq, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((N, hq), dtype=torch.float32, device=q.device)
+    _check(lib().pa_decode_noalloc(
+        _dev(q, "q", torch.bfloat16), _dev(kv_cache, "kv_cache", torch.bfloat16),
+        _dev(block_table, "block_table", torch.int32), _dev(seq_lens, "seq_lens", torch.int32),
+        ctypes.byref(shape), float(scale), int(num_splits), _dev(out, "out", torch.bfloat16),
+        _opt(lse, "lse", torch.float32), _stream(stream)), "pa_decode_noalloc")
     return out, lse
 
 

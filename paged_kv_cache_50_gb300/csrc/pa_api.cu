@@ -73,6 +73,11 @@ int* device_error_ptr() {
 
 }  // namespace
 
+namespace pa {
+// The error word's device address for kernels launched from other files.
+int* device_error_word() { return device_error_ptr(); }
+}  // namespace pa
+
 extern "C" {
 
 pa_status pa_reshape_and_cache(const void* key, const void* value, void* kv_cache,
