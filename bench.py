@@ -171,7 +171,8 @@ class DecodeStep:
         self.slots = to_dev(b.slot_mapping, torch.int64, device)
         self.table = to_dev(b.block_table, torch.int32, device)
         self.seq = to_dev(b.seq_lens, torch.int32, device)
-        self.S = pa.pa_num_kv_splits(int(b.seq_lens.max()), pa.pa_device_sm_count())
+        self.max_seq = int(b.seq_lens.max())
+        self.S = pa.pa_num_kv_splits(self.max_seq, pa.pa_device_sm_count())
         self.ws = pa.decode_workspace(N, hq, self.S, d, device=device)
         self.out = torch.empty((N, hq, d), dtype=torch.bfloat16, device=device)
         self.lse = torch.empty((N, hq), dtype=torch.float32, device=device)
@@ -181,7 +182,8 @@ class DecodeStep:
         pa.pa_reshape_and_cache(self.key, self.value, pool, self.slots)
         if ev is not None:
             ev[0].record()
-        pa.pa_decode_splitkv(self.q, pool, self.table, self.seq, self.b.scale, self.ws)
+        pa.pa_decode_splitkv(self.q, pool, self.table, self.seq, self.b.scale, self.ws,
+                             self.max_seq)
         if ev is not None:
             ev[1].record()
         pa.pa_lse_merge(self.ws, self.out, self.lse)
@@ -226,7 +228,7 @@ def run_e2e(pa, b, step, steps, warmup, device):
     return dt, h2d, d2h
 
 
-def cpu_baseline_sample(b, budget_s=20.0, threads=None):
+def cpu_baseline_sample(b, budget_s=12.0, threads=None):
     """The oracle, as it stands, on a bounded sample of the decode batch:
     whole requests in order until ~budget_s of CPU work.  Returns
     (GB/s of KV processed, threads, sample description)."""
@@ -234,11 +236,12 @@ def cpu_baseline_sample(b, budget_s=20.0, threads=None):
     threads = threads or (os.cpu_count() or 1)
     pool = oracle.reshape_and_cache(b.key, b.value, b.pool, b.slot_mapping, b.block_size)
     done_bytes, elapsed, n = 0, 0.0, 0
-    order = list(range(b.num_seqs))
     per_tok = b.num_kv_heads * b.head_size * 2 * 2
-    while elapsed < budget_s and n < len(order):
-        # Take a group of requests per call so the oracle's threads have work.
-        grp = order[n:n + max(1, threads)]
+    group = max(1, threads)
+    while elapsed < budget_s:
+        # A group of requests per call (so the oracle's threads have work),
+        # cycling through the batch until the time budget is spent.
+        grp = [(n + j) % b.num_seqs for j in range(group)]
         mask = np.zeros(b.num_tokens, np.uint8)
         mask[grp] = 1
         t0 = time.perf_counter()
@@ -248,8 +251,8 @@ def cpu_baseline_sample(b, budget_s=20.0, threads=None):
         done_bytes += int(b.seq_lens[grp].astype(np.int64).sum()) * per_tok
         n += len(grp)
     return done_bytes / elapsed / 1e9, threads, (
-        f"oracle decode attention (fp64, paged gather + softmax) over the first {n} of "
-        f"{b.num_seqs} requests of the GQA decode batch, {elapsed:.1f} s")
+        f"oracle decode attention (fp64, paged gather + softmax), {n} request-decodes cycling "
+        f"through the {b.num_seqs}-request GQA decode batch, {elapsed:.1f} s of {threads} threads")
 
 
 # ---------------------------------------------------------------------------
@@ -312,9 +315,9 @@ def secondary(pa, device, pk):
     ws = pa.decode_workspace(N, hq, S, d, device=device)
     o = torch.empty((N, hq, d), dtype=torch.bfloat16, device=device)
     lo = torch.empty((N, hq), dtype=torch.float32, device=device)
-    st1 = _timed_with_flush(lambda: pa.pa_decode_splitkv(q, pool, table, seq, b.scale, ws),
+    st1 = _timed_with_flush(lambda: pa.pa_decode_splitkv(q, pool, table, seq, b.scale, ws, 131072),
                             flush, 10)
-    both = _timed_with_flush(lambda: pa.pa_decode(q, pool, table, seq, b.scale, ws, o, lo),
+    both = _timed_with_flush(lambda: pa.pa_decode(q, pool, table, seq, b.scale, ws, o, lo, 131072),
                              flush, 10)
     gbs = b.kv_bytes() / (st1 * 1e-3) / 1e9
     res["long_decode"] = {"workload": b.name, "num_splits": S, "stage1_ms": st1,
@@ -334,7 +337,9 @@ def secondary(pa, device, pk):
     ws = pa.decode_workspace(m.batch, m.num_heads, S, m.kv_lora_rank, device=device)
     o = torch.empty((m.batch, m.num_heads, m.kv_lora_rank), dtype=torch.bfloat16, device=device)
     lo = torch.empty((m.batch, m.num_heads), dtype=torch.float32, device=device)
-    ms = _timed_with_flush(lambda: pa.pa_mla_decode(q, pool, table, seq, m.scale, ws, o, lo),
+    mx = int(m.seq_lens.max())
+    ms = _timed_with_flush(lambda: pa.pa_mla_decode(q, pool, table, seq, m.scale, ws, o, lo,
+                                                    max_seq_len=mx),
                            flush, 10)
     gbs = m.kv_bytes() / (ms * 1e-3) / 1e9
     flops = int(m.seq_lens.astype(np.int64).sum()) * m.num_heads * 2 * (

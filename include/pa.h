@@ -124,17 +124,23 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_splits, 
 
 /*
  * Split-KV decode, stage 1 (one query per request; the query attends over
- * all seq_lens[i] cached tokens).  Split s of request i covers the tokens
- * [s*C_i, min((s+1)*C_i, seq_i)) with C_i = bs * ceil(ceil(seq_i / S) / bs);
- * for each q head h it writes the split's softmax-normalised output and LSE:
+ * all seq_lens[i] cached tokens).  The split count S is derived from the
+ * batch's longest sequence ("Triton and MLA", key files), so the sequence
+ * axis is cut the same way for every request: with
+ *   C = bs * ceil(ceil(max_seq_len / S) / bs),
+ * split s of request i covers the tokens [s*C, min((s+1)*C, seq_i)), and the
+ * last split (s = S-1) runs to seq_i (so a max_seq_len below the true maximum
+ * costs speed, never correctness).  For each q head h it writes the split's
+ * softmax-normalised output and natural-log LSE:
  *   workspace[i, h, s, 0:d] = o_s,  workspace[i, h, s, d] = lse_s
  * An empty split writes o_s = 0, lse_s = -inf.
  * q: [N, Hq, d] bf16.  workspace: pa_decode_workspace_bytes(N, Hq, S, d) bytes.
+ * max_seq_len >= 0: the batch's longest seq_len (sizes C).
  * Supported: head_size in {64, 128}, Hq / Hkv <= 16.
  */
 pa_status pa_decode_splitkv(const void* q, const void* kv_cache, const int32_t* block_table,
                             const int32_t* seq_lens, const pa_shape* shape, float scale,
-                            int num_splits, float* workspace, void* stream);
+                            int num_splits, int max_seq_len, float* workspace, void* stream);
 
 /*
  * Split-KV stage 2: merge S partials per (request, head) by their LSE:
@@ -157,15 +163,16 @@ pa_status pa_lse_merge(const float* workspace, int num_seqs, int num_q_heads,
  * kv_cache: [num_blocks, block_size, kv_lora_rank + rope_dim] bf16.
  * out: [batch, num_heads, kv_lora_rank] bf16.  lse: [batch, num_heads] fp32, nullable.
  * The call runs split-KV stage 1 into `workspace`
- * (pa_decode_workspace_bytes(batch, num_heads, num_splits, kv_lora_rank) bytes)
- * and then the LSE merge.
- * Supported: kv_lora_rank == 512, rope_dim == 64, num_heads a multiple of 16.
+ * (pa_decode_workspace_bytes(batch, num_heads, num_splits, kv_lora_rank) bytes,
+ * splits cut as for pa_decode_splitkv from max_seq_len) and then the LSE merge.
+ * Supported: kv_lora_rank == 512, rope_dim == 64, num_heads a multiple of 64,
+ * block_size a multiple of 32.
  */
 pa_status pa_mla_decode(const void* q, const void* kv_cache, const int32_t* block_table,
                         const int32_t* seq_lens, int batch, int num_heads, int kv_lora_rank,
                         int rope_dim, int block_size, int num_blocks, int max_blocks_per_seq,
-                        float scale, int num_splits, float* workspace, void* out, float* lse,
-                        void* stream);
+                        int max_seq_len, float scale, int num_splits, float* workspace, void* out,
+                        float* lse, void* stream);
 
 /* Size of the fixed device array pa_decode_noalloc keeps its split partials in. */
 #define PA_NOALLOC_WORKSPACE_BYTES (16u * 1024u * 1024u)
@@ -179,7 +186,8 @@ pa_status pa_mla_decode(const void* q, const void* kv_cache, const int32_t* bloc
  * call cudaMalloc -- and so cannot pass a workspace.  The split partials go
  * to a fixed device array of PA_NOALLOC_WORKSPACE_BYTES inside the library,
  * which every device that loads the library keeps until the process exits.
- *   q: [N, Hq, d] bf16;  out: [N, Hq, d] bf16;  lse: [N, Hq] fp32, nullable.
+ *   q: [N, Hq, d] bf16;  out: [N, Hq, d] bf16;  lse: [N, Hq] fp32, nullable;
+ *   max_seq_len as for pa_decode_splitkv.
  * Returns PA_ERR_INVALID if N * Hq * num_splits * (d + 1) * 4 bytes exceeds
  * PA_NOALLOC_WORKSPACE_BYTES (use fewer splits, or pa_decode_splitkv with a
  * workspace of your own).  The first call on each device looks up the
@@ -189,7 +197,8 @@ pa_status pa_mla_decode(const void* q, const void* kv_cache, const int32_t* bloc
  */
 pa_status pa_decode_noalloc(const void* q, const void* kv_cache, const int32_t* block_table,
                             const int32_t* seq_lens, const pa_shape* shape, float scale,
-                            int num_splits, void* out, float* lse, void* stream);
+                            int num_splits, int max_seq_len, void* out, float* lse,
+                            void* stream);
 
 /* Human-readable name of a status. */
 const char* pa_status_string(pa_status status);

@@ -56,7 +56,7 @@ def _bind(path):
     for name in ("oracle_split_partials_bf16", "oracle_split_partials_f64"):
         fn = getattr(lib, name)
         fn.argtypes = [P, P, P, i32, P, i32, i32, i32, i32, i32, i64, f64,
-                       i32, P, i32]
+                       i32, i64, P, i32]
         fn.restype = i32
     lib.oracle_lse_merge.argtypes = [P, i32, i32, i32, i32, P, P]
     lib.oracle_lse_merge.restype = None
@@ -175,9 +175,11 @@ def paged_attention(q, pool, block_table, query_start_loc, seq_lens, scale,
     return out, lse
 
 
-def split_partials(q, pool, block_table, seq_lens, scale, num_splits, threads=None):
+def split_partials(q, pool, block_table, seq_lens, scale, num_splits, max_seq_len=None,
+                   threads=None):
     """Split-KV stage 1 for one query per request.  q [N, Hq, d].
-    Returns partials [N, Hq, S, d + 1] fp64 (normalised o, then lse)."""
+    Returns partials [N, Hq, S, d + 1] fp64 (normalised o, then lse).
+    ``max_seq_len`` (default: the batch maximum) sizes the split chunk."""
     lib = _load()
     kq, q = _kind(q)
     kp, pool = _kind(pool)
@@ -190,9 +192,12 @@ def split_partials(q, pool, block_table, seq_lens, scale, num_splits, threads=No
     N, Hq, d = q.shape
     nb, _, bs, Hkv, _ = pool.shape
     out = np.zeros((N, Hq, num_splits, d + 1), np.float64)
+    if max_seq_len is None:
+        max_seq_len = int(sl.max()) if sl.size else 0
     fn = lib.oracle_split_partials_bf16 if kq == "bf16" else lib.oracle_split_partials_f64
     rc = fn(_ptr(q), _ptr(pool), _ptr(bt), bt.shape[1], _ptr(sl), N, Hq, Hkv, d, bs,
-            nb, float(scale), int(num_splits), _ptr(out), threads or default_threads())
+            nb, float(scale), int(num_splits), int(max_seq_len), _ptr(out),
+            threads or default_threads())
     if rc != 0:
         raise ValueError("invalid split-KV input")
     return out

@@ -34,8 +34,11 @@
 //  * causal alignment is bottom-right: the qlen_i new queries of request i are
 //    its last qlen_i positions, and query row j sees positions <= its own;
 //  * GQA groups are contiguous: q head h reads kv head h / (Hq / Hkv);
-//  * split s of request i covers tokens [s*C_i, min((s+1)*C_i, seq_i)) with
-//    C_i = bs * ceil(ceil(seq_i / S) / bs); an empty split has o = 0 and
+//  * the split count comes from the batch's longest sequence ("Triton and
+//    MLA", key files), so the sequence axis is cut uniformly for the whole
+//    batch: split s covers [s*C, (s+1)*C) of each request, clipped to its
+//    seq_len, with C = bs * ceil(ceil(max_seq_len / S) / bs), and the last
+//    split also takes any tokens past (S-1)*C; an empty split has o = 0 and
 //    lse = -inf;
 //  * a query with nothing visible (seq_len = 0) gives o = 0, lse = -inf.
 
@@ -183,6 +186,22 @@ int paged_attention(const E* q, const E* pool, const int32_t* block_table,
   return bad ? -1 : 0;
 }
 
+// Split boundaries.  The sequence axis is cut into S pieces of
+// C = bs * ceil(ceil(max_seq_len / S) / bs) tokens, the same for every
+// request of the batch (max_seq_len is the value the split count is computed
+// from); split s covers [s*C, (s+1)*C) clipped to the request, and the last
+// split also takes everything past (S-1)*C.
+inline void split_range(int64_t seq, int64_t max_seq, int S, int bs, int s,
+                        int64_t* a, int64_t* b) {
+  if (max_seq < 1) max_seq = 1;
+  const int64_t per = (max_seq + S - 1) / S;          // ceil(max_seq / S)
+  const int64_t chunk = ((per + bs - 1) / bs) * bs;   // rounded up to blocks
+  *a = s * chunk;
+  *b = (s == S - 1) ? seq : *a + chunk;
+  if (*a > seq) *a = seq;
+  if (*b > seq) *b = seq;
+}
+
 // Split-KV stage 1 for one query per request (decode: the query sits at
 // position seq_i - 1 and sees every cached token).  partials is
 // [N][Hq][S][d + 1]: the split's normalised output then its LSE.
@@ -190,7 +209,7 @@ template <typename E>
 int split_partials(const E* q, const E* pool, const int32_t* block_table,
                    int max_blocks, const int32_t* seq_lens, int N, int Hq,
                    int Hkv, int d, int bs, int64_t nb, double scale, int S,
-                   double* partials, int threads) {
+                   int64_t max_seq, double* partials, int threads) {
   if (Hkv <= 0 || Hq % Hkv != 0 || S <= 0 || bs <= 0) return -1;
   const int grp = Hq / Hkv;
   std::atomic<int> bad(0);
@@ -204,15 +223,12 @@ int split_partials(const E* q, const E* pool, const int32_t* block_table,
       bad = 1;
       return;
     }
-    const int64_t per = (seq + S - 1) / S;              // ceil(seq / S)
-    const int64_t chunk = ((per + bs - 1) / bs) * bs;   // rounded up to blocks
     for (int r = 0; r < grp; ++r) {
       const int h = g * grp + r;
       for (int e = 0; e < d; ++e) qv[e] = widen(q[(static_cast<int64_t>(i) * Hq + h) * d + e]);
       for (int s = 0; s < S; ++s) {
-        int64_t a = s * chunk, b = a + chunk;
-        if (a > seq) a = seq;
-        if (b > seq) b = seq;
+        int64_t a, b;
+        split_range(seq, max_seq, S, bs, s, &a, &b);
         double* dst = partials + ((static_cast<int64_t>(i) * Hq + h) * S + s) * (d + 1);
         attend(qv.data(), K.data() + a * d, V.data() + a * d, b - a, d, d,
                scale, dst, dst + d);
@@ -313,21 +329,24 @@ int oracle_paged_attention_f64(const double* q, const double* pool,
 }
 
 // Split-KV stage 1 (decode, one query per request), bf16 / fp64 inputs.
+// max_seq sizes the split chunk (see split_range).
 int oracle_split_partials_bf16(const uint16_t* q, const uint16_t* pool,
                                const int32_t* block_table, int max_blocks,
                                const int32_t* seq_lens, int N, int Hq, int Hkv,
                                int d, int bs, int64_t nb, double scale,
-                               int num_splits, double* partials, int threads) {
+                               int num_splits, int64_t max_seq, double* partials,
+                               int threads) {
   return split_partials(q, pool, block_table, max_blocks, seq_lens, N, Hq, Hkv,
-                        d, bs, nb, scale, num_splits, partials, threads);
+                        d, bs, nb, scale, num_splits, max_seq, partials, threads);
 }
 int oracle_split_partials_f64(const double* q, const double* pool,
                               const int32_t* block_table, int max_blocks,
                               const int32_t* seq_lens, int N, int Hq, int Hkv,
                               int d, int bs, int64_t nb, double scale,
-                              int num_splits, double* partials, int threads) {
+                              int num_splits, int64_t max_seq, double* partials,
+                              int threads) {
   return split_partials(q, pool, block_table, max_blocks, seq_lens, N, Hq, Hkv,
-                        d, bs, nb, scale, num_splits, partials, threads);
+                        d, bs, nb, scale, num_splits, max_seq, partials, threads);
 }
 
 // Split-KV stage 2: merge S partials per (request, head) by their LSE.

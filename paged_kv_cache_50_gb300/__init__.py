@@ -61,11 +61,11 @@ def lib() -> ctypes.CDLL:
         L.pa_num_kv_splits.restype = i32
         L.pa_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
         L.pa_decode_workspace_bytes.restype = ctypes.c_size_t
-        L.pa_decode_splitkv.argtypes = [P, P, P, P, SP, f32, i32, P, P]
+        L.pa_decode_splitkv.argtypes = [P, P, P, P, SP, f32, i32, i32, P, P]
         L.pa_lse_merge.argtypes = [P, i32, i32, i32, i32, P, P, P]
-        L.pa_mla_decode.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, i32, f32, i32, P,
-                                    P, P, P]
-        L.pa_decode_noalloc.argtypes = [P, P, P, P, SP, f32, i32, P, P, P]
+        L.pa_mla_decode.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, f32,
+                                    i32, P, P, P, P]
+        L.pa_decode_noalloc.argtypes = [P, P, P, P, SP, f32, i32, i32, P, P, P]
         L.pa_status_string.argtypes = [st]
         L.pa_status_string.restype = ctypes.c_char_p
         L.pa_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int), P]
@@ -178,17 +178,28 @@ def decode_workspace(num_seqs, num_q_heads, num_splits, dv, device="cuda"):
                        device=device)
 
 
-def pa_decode_splitkv(q, kv_cache, block_table, seq_lens, scale, workspace, stream=None) -> None:
-    """Split-KV stage 1: q [N, Hq, d] -> workspace [N, Hq, S, d + 1] fp32."""
+def _max_seq(seq_lens, max_seq_len):
+    """The batch's longest seq_len; read from the device (a sync) only if the
+    caller does not pass it."""
+    if max_seq_len is not None:
+        return int(max_seq_len)
+    return int(seq_lens.max().item()) if seq_lens.numel() else 0
+
+
+def pa_decode_splitkv(q, kv_cache, block_table, seq_lens, scale, workspace, max_seq_len=None,
+                      stream=None) -> None:
+    """Split-KV stage 1: q [N, Hq, d] -> workspace [N, Hq, S, d + 1] fp32.
+    ``max_seq_len`` sizes the split chunk (default: read from ``seq_lens``)."""
     N, hq, d = q.shape
-    if workspace.dim() != 4 or tuple(workspace.shape) [:2] != (N, hq) or workspace.shape[3] != d + 1:
+    if workspace.dim() != 4 or tuple(workspace.shape[:2]) != (N, hq) or workspace.shape[3] != d + 1:
         raise ValueError("workspace must be [num_seqs, num_q_heads, num_splits, head_size + 1]")
     shape = _pool_shape(kv_cache, N, hq, block_table.shape[1])
     _check(lib().pa_decode_splitkv(
         _dev(q, "q", torch.bfloat16), _dev(kv_cache, "kv_cache", torch.bfloat16),
         _dev(block_table, "block_table", torch.int32), _dev(seq_lens, "seq_lens", torch.int32),
         ctypes.byref(shape), float(scale), int(workspace.shape[2]),
-        _dev(workspace, "workspace", torch.float32), _stream(stream)), "pa_decode_splitkv")
+        _max_seq(seq_lens, max_seq_len), _dev(workspace, "workspace", torch.float32),
+        _stream(stream)), "pa_decode_splitkv")
 
 
 def pa_lse_merge(workspace, out=None, lse=None, return_lse=True, stream=None):
@@ -206,14 +217,14 @@ def pa_lse_merge(workspace, out=None, lse=None, return_lse=True, stream=None):
 
 
 def pa_decode(q, kv_cache, block_table, seq_lens, scale, workspace, out=None, lse=None,
-              stream=None):
+              max_seq_len=None, stream=None):
     """Both split-KV stages: stage 1 into ``workspace``, then the LSE merge."""
-    pa_decode_splitkv(q, kv_cache, block_table, seq_lens, scale, workspace, stream)
+    pa_decode_splitkv(q, kv_cache, block_table, seq_lens, scale, workspace, max_seq_len, stream)
     return pa_lse_merge(workspace, out, lse, stream=stream)
 
 
 def pa_mla_decode(q, kv_cache, block_table, seq_lens, scale, workspace, out=None, lse=None,
-                  kv_lora_rank=512, rope_dim=64, stream=None):
+                  kv_lora_rank=512, rope_dim=64, max_seq_len=None, stream=None):
     """MLA latent decode.  q [B, H, 576], kv_cache [nb, bs, 576] ->
     (out [B, H, 512] bf16, lse [B, H] fp32)."""
     B, H, dk = q.shape
@@ -230,10 +241,10 @@ def pa_mla_decode(q, kv_cache, block_table, seq_lens, scale, workspace, out=None
     _check(lib().pa_mla_decode(
         _dev(q, "q", torch.bfloat16), _dev(kv_cache, "kv_cache", torch.bfloat16),
         _dev(block_table, "block_table", torch.int32), _dev(seq_lens, "seq_lens", torch.int32),
-        B, H, kv_lora_rank, rope_dim, bs, nb, block_table.shape[1], float(scale),
-        int(workspace.shape[2]), _dev(workspace, "workspace", torch.float32),
-        _dev(out, "out", torch.bfloat16), _opt(lse, "lse", torch.float32), _stream(stream)),
-        "pa_mla_decode")
+        B, H, kv_lora_rank, rope_dim, bs, nb, block_table.shape[1],
+        _max_seq(seq_lens, max_seq_len), float(scale), int(workspace.shape[2]),
+        _dev(workspace, "workspace", torch.float32), _dev(out, "out", torch.bfloat16),
+        _opt(lse, "lse", torch.float32), _stream(stream)), "pa_mla_decode")
     return out, lse
 
 
@@ -241,7 +252,7 @@ PA_NOALLOC_WORKSPACE_BYTES = 16 * 1024 * 1024
 
 
 def pa_decode_noalloc(q, kv_cache, block_table, seq_lens, scale, num_splits, out=None,
-                      lse=None, stream=None):
+                      lse=None, max_seq_len=None, stream=None):
     """Split-KV decode with the partials in the library's fixed device array
     (no workspace argument, nothing allocated by the library).  For callers
     that cannot allocate device memory; calls that overlap on the GPU race
@@ -256,8 +267,9 @@ def pa_decode_noalloc(q, kv_cache, block_table, seq_lens, scale, num_splits, out
     _check(lib().pa_decode_noalloc(
         _dev(q, "q", torch.bfloat16), _dev(kv_cache, "kv_cache", torch.bfloat16),
         _dev(block_table, "block_table", torch.int32), _dev(seq_lens, "seq_lens", torch.int32),
-        ctypes.byref(shape), float(scale), int(num_splits), _dev(out, "out", torch.bfloat16),
-        _opt(lse, "lse", torch.float32), _stream(stream)), "pa_decode_noalloc")
+        ctypes.byref(shape), float(scale), int(num_splits), _max_seq(seq_lens, max_seq_len),
+        _dev(out, "out", torch.bfloat16), _opt(lse, "lse", torch.float32), _stream(stream)),
+        "pa_decode_noalloc")
     return out, lse
 
 

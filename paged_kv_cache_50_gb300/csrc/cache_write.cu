@@ -7,6 +7,7 @@
 // copies of Hkv*d*2 bytes.  One CTA per token, one 16-byte vector per thread
 // per step; every byte is read once and written once (HBM-bound).
 #include "pa_common.cuh"
+#include "pa_launch.h"
 
 namespace pa {
 

@@ -25,6 +25,7 @@
 #include <math_constants.h>
 
 #include "pa_common.cuh"
+#include "pa_launch.h"
 
 namespace pa {
 
@@ -56,7 +57,7 @@ __global__ void __launch_bounds__(128)
 decode_splitkv_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ cache,
                       const int32_t* __restrict__ block_table, const int32_t* __restrict__ seq_lens,
                       int max_blocks, int Hq, int Hkv, int bs, int num_blocks, float scale_log2,
-                      int S, float* __restrict__ ws, int* err) {
+                      int S, int chunk, float* __restrict__ ws, int* err) {
   using C = DecodeCfg<D, STAGES>;
   extern __shared__ __align__(128) uint8_t smem[];
   const int s = blockIdx.x, kvh = blockIdx.y, i = blockIdx.z;
@@ -65,11 +66,11 @@ decode_splitkv_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
   const int gid = lane >> 2, tid4 = lane & 3;
 
   const int seq = seq_lens[i];
-  const int per = (seq + S - 1) / S;
-  const int chunk = ((per + bs - 1) / bs) * bs;
+  // Split s covers [s*chunk, (s+1)*chunk) of the request (the last split runs
+  // to the end), chunk being one block-aligned size for the whole batch.
   const long long a0 = static_cast<long long>(s) * chunk;
   const int t0 = static_cast<int>(a0 < seq ? a0 : seq);
-  const int t1 = static_cast<int>(a0 + chunk < seq ? a0 + chunk : seq);
+  const int t1 = (s == S - 1) ? seq : static_cast<int>(a0 + chunk < seq ? a0 + chunk : seq);
   const int nsb = (t1 - t0 + 15) >> 4;
   const int my_n = nsb > warp ? (nsb - warp + C::kWarps - 1) / C::kWarps : 0;
 
@@ -316,45 +317,37 @@ lse_merge_kernel(const float* __restrict__ ws, int S, int dv, __nv_bfloat16* __r
 template <int D, int STAGES>
 static cudaError_t launch_decode_t(const void* q, const void* cache, const int32_t* block_table,
                                    const int32_t* seq_lens, int N, int Hq, int Hkv, int bs,
-                                   int num_blocks, int max_blocks, float scale, int S, float* ws,
-                                   int* err, cudaStream_t stream) {
+                                   int num_blocks, int max_blocks, float scale, int S, int chunk,
+                                   float* ws, int* err, cudaStream_t stream) {
   using C = DecodeCfg<D, STAGES>;
   auto kern = decode_splitkv_kernel<D, STAGES>;
-  static bool attr_set = false;  // per process; the attribute is per device function
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static DeviceFlags attr_set;
+  cudaError_t e = set_smem_once(kern, C::kSmemBytes, attr_set);
+  if (e != cudaSuccess) return e;
   dim3 grid(S, Hkv, N);
   kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(cache), block_table,
-      seq_lens, max_blocks, Hq, Hkv, bs, num_blocks, scale * kLog2e, S, ws, err);
+      seq_lens, max_blocks, Hq, Hkv, bs, num_blocks, scale * kLog2e, S, chunk, ws, err);
   return cudaGetLastError();
 }
 
 cudaError_t launch_decode_splitkv(const void* q, const void* cache, const int32_t* block_table,
                                   const int32_t* seq_lens, int N, int Hq, int Hkv, int d, int bs,
-                                  int num_blocks, int max_blocks, float scale, int S, float* ws,
-                                  int* err, cudaStream_t stream) {
+                                  int num_blocks, int max_blocks, float scale, int S, int chunk,
+                                  float* ws, int* err, cudaStream_t stream) {
   if (d == 128)
     return launch_decode_t<128, 3>(q, cache, block_table, seq_lens, N, Hq, Hkv, bs, num_blocks,
-                                   max_blocks, scale, S, ws, err, stream);
+                                   max_blocks, scale, S, chunk, ws, err, stream);
   return launch_decode_t<64, 4>(q, cache, block_table, seq_lens, N, Hq, Hkv, bs, num_blocks,
-                                max_blocks, scale, S, ws, err, stream);
+                                max_blocks, scale, S, chunk, ws, err, stream);
 }
 
 cudaError_t launch_lse_merge(const float* ws, int NH, int S, int dv, void* out, float* lse,
                              cudaStream_t stream) {
   const size_t smem = (static_cast<size_t>(S) + 32) * sizeof(float);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(lse_merge_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static DeviceFlags attr_set;
+  cudaError_t e = set_smem_once(lse_merge_kernel, 200 * 1024, attr_set);
+  if (e != cudaSuccess) return e;
   lse_merge_kernel<<<NH, 128, smem, stream>>>(ws, S, dv, static_cast<__nv_bfloat16*>(out), lse);
   return cudaGetLastError();
 }

@@ -23,18 +23,8 @@
 
 #include "pa.h"
 #include "pa_common.cuh"
+#include "pa_launch.h"
 
-namespace pa {
-
-cudaError_t launch_decode_splitkv(const void* q, const void* cache, const int32_t* block_table,
-                                  const int32_t* seq_lens, int N, int Hq, int Hkv, int d, int bs,
-                                  int num_blocks, int max_blocks, float scale, int S, float* ws,
-                                  int* err, cudaStream_t stream);
-cudaError_t launch_lse_merge(const float* ws, int NH, int S, int dv, void* out, float* lse,
-                             cudaStream_t stream);
-int* device_error_word();
-
-}  // namespace pa
 
 namespace {
 
@@ -63,12 +53,12 @@ float* noalloc_workspace() {
 extern "C" pa_status pa_decode_noalloc(const void* q, const void* kv_cache,
                                        const int32_t* block_table, const int32_t* seq_lens,
                                        const pa_shape* shape, float scale, int num_splits,
-                                       void* out, float* lse, void* stream) {
+                                       int max_seq_len, void* out, float* lse, void* stream) {
   if (shape == nullptr || shape->num_seqs < 0 || shape->num_q_heads <= 0 ||
       shape->num_kv_heads <= 0 || shape->head_size <= 0 || shape->block_size <= 0 ||
       shape->block_size % 16 != 0 || shape->num_blocks <= 0 || shape->max_blocks_per_seq <= 0 ||
       shape->num_q_heads % shape->num_kv_heads != 0 || shape->num_seqs > 65535 ||
-      shape->num_kv_heads > 65535 || num_splits < 1 || num_splits > 16384)
+      shape->num_kv_heads > 65535 || num_splits < 1 || num_splits > 16384 || max_seq_len < 0)
     return PA_ERR_INVALID;
   if (shape->head_size != 64 && shape->head_size != 128) return PA_ERR_UNSUPPORTED;
   if (shape->num_q_heads / shape->num_kv_heads > 16) return PA_ERR_UNSUPPORTED;
@@ -88,7 +78,9 @@ extern "C" pa_status pa_decode_noalloc(const void* q, const void* kv_cache,
   cudaError_t e = pa::launch_decode_splitkv(
       q, kv_cache, block_table, seq_lens, shape->num_seqs, shape->num_q_heads,
       shape->num_kv_heads, shape->head_size, shape->block_size, shape->num_blocks,
-      shape->max_blocks_per_seq, scale, num_splits, ws, pa::device_error_word(), st);
+      shape->max_blocks_per_seq, scale, num_splits,
+      static_cast<int>(pa::split_chunk(max_seq_len, num_splits, shape->block_size)), ws,
+      pa::device_error_word(), st);
   if (e != cudaSuccess) return PA_ERR_CUDA;
   e = pa::launch_lse_merge(ws, shape->num_seqs * shape->num_q_heads, num_splits,
                            shape->head_size, out, lse, st);

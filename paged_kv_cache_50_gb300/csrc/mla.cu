@@ -17,6 +17,7 @@
 #include <math_constants.h>
 
 #include "pa_common.cuh"
+#include "pa_launch.h"
 
 namespace pa {
 
@@ -42,7 +43,7 @@ __global__ void __launch_bounds__(256)
 mla_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ cache,
                   const int32_t* __restrict__ block_table, const int32_t* __restrict__ seq_lens,
                   int max_blocks, int H, int bs, int num_blocks, float scale_log2, int S,
-                  float* __restrict__ ws, int* err) {
+                  int chunk, float* __restrict__ ws, int* err) {
   using C = MlaCfg;
   extern __shared__ __align__(128) uint8_t smem[];
   const int hg = blockIdx.x, s = blockIdx.y, b = blockIdx.z;
@@ -52,11 +53,10 @@ mla_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   const int half = warp >> 2;          // value-column half
 
   const int seq = seq_lens[b];
-  const int per = (seq + S - 1) / S;
-  const int chunk = ((per + bs - 1) / bs) * bs;
+  // Split s covers [s*chunk, (s+1)*chunk) (the last split runs to the end).
   const long long a0 = static_cast<long long>(s) * chunk;
   const int t0 = static_cast<int>(a0 < seq ? a0 : seq);
-  const int t1 = static_cast<int>(a0 + chunk < seq ? a0 + chunk : seq);
+  const int t1 = (s == S - 1) ? seq : static_cast<int>(a0 + chunk < seq ? a0 + chunk : seq);
   const int ntiles = (t1 - t0 + C::kBN - 1) / C::kBN;
 
   const uint32_t qs = smem_u32(smem);
@@ -209,21 +209,18 @@ mla_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   }
 }
 
-cudaError_t launch_lse_merge(const float* ws, int NH, int S, int dv, void* out, float* lse,
-                             cudaStream_t stream);
-
 cudaError_t launch_mla_decode(const void* q, const void* cache, const int32_t* block_table,
                               const int32_t* seq_lens, int B, int H, int bs, int num_blocks,
-                              int max_blocks, float scale, int S, float* ws, void* out, float* lse,
-                              int* err, cudaStream_t stream) {
+                              int max_blocks, float scale, int S, int chunk, float* ws, void* out,
+                              float* lse, int* err, cudaStream_t stream) {
   using C = MlaCfg;
-  cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  static DeviceFlags attr_set;
+  cudaError_t e = set_smem_once(mla_decode_kernel, C::kSmemBytes, attr_set);
   if (e != cudaSuccess) return e;
   dim3 grid(H / C::kHeads, S, B);
   mla_decode_kernel<<<grid, C::kThreads, C::kSmemBytes, stream>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(cache), block_table,
-      seq_lens, max_blocks, H, bs, num_blocks, scale * kLog2e, S, ws, err);
+      seq_lens, max_blocks, H, bs, num_blocks, scale * kLog2e, S, chunk, ws, err);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_lse_merge(ws, B * H, S, C::kDv, out, lse, stream);

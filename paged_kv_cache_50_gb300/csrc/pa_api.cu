@@ -10,31 +10,12 @@
 
 #include "pa.h"
 #include "pa_common.cuh"
+#include "pa_launch.h"
 
 namespace pa {
 
 // The device error word (PA_DEVERR_* bits).  Kernels receive its address.
 __device__ int g_device_error = 0;
-
-cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* cache,
-                                     const int64_t* slot_mapping, int num_tokens,
-                                     int num_kv_heads, int head_size, int block_size,
-                                     int num_blocks, int* err, cudaStream_t stream);
-cudaError_t launch_decode_splitkv(const void* q, const void* cache, const int32_t* block_table,
-                                  const int32_t* seq_lens, int N, int Hq, int Hkv, int d, int bs,
-                                  int num_blocks, int max_blocks, float scale, int S, float* ws,
-                                  int* err, cudaStream_t stream);
-cudaError_t launch_lse_merge(const float* ws, int NH, int S, int dv, void* out, float* lse,
-                             cudaStream_t stream);
-cudaError_t launch_varlen_fwd(const void* q, const void* cache, const int32_t* block_table,
-                              const int32_t* qsl, const int32_t* seq_lens, int N, int Hq, int Hkv,
-                              int d, int bs, int num_blocks, int max_blocks, int max_query_len,
-                              float scale, int causal, void* out, float* lse,
-                              int* err, cudaStream_t stream);
-cudaError_t launch_mla_decode(const void* q, const void* cache, const int32_t* block_table,
-                              const int32_t* seq_lens, int B, int H, int bs, int num_blocks,
-                              int max_blocks, float scale, int S, float* ws, void* out, float* lse,
-                              int* err, cudaStream_t stream);
 
 }  // namespace pa
 
@@ -151,8 +132,9 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_splits, 
 
 pa_status pa_decode_splitkv(const void* q, const void* kv_cache, const int32_t* block_table,
                             const int32_t* seq_lens, const pa_shape* shape, float scale,
-                            int num_splits, float* workspace, void* stream) {
-  if (!shape_ok(shape) || num_splits < 1 || num_splits > kMaxSplits) return PA_ERR_INVALID;
+                            int num_splits, int max_seq_len, float* workspace, void* stream) {
+  if (!shape_ok(shape) || num_splits < 1 || num_splits > kMaxSplits || max_seq_len < 0)
+    return PA_ERR_INVALID;
   if (shape->head_size != 64 && shape->head_size != 128) return PA_ERR_UNSUPPORTED;
   if (shape->num_q_heads / shape->num_kv_heads > 16) return PA_ERR_UNSUPPORTED;
   if (shape->num_seqs == 0) return PA_OK;
@@ -163,7 +145,9 @@ pa_status pa_decode_splitkv(const void* q, const void* kv_cache, const int32_t* 
   return from_cuda(pa::launch_decode_splitkv(
       q, kv_cache, block_table, seq_lens, shape->num_seqs, shape->num_q_heads,
       shape->num_kv_heads, shape->head_size, shape->block_size, shape->num_blocks,
-      shape->max_blocks_per_seq, scale, num_splits, workspace, device_error_ptr(),
+      shape->max_blocks_per_seq, scale, num_splits,
+      static_cast<int>(pa::split_chunk(max_seq_len, num_splits, shape->block_size)), workspace,
+      device_error_ptr(),
       static_cast<cudaStream_t>(stream)));
 }
 
@@ -183,11 +167,12 @@ pa_status pa_lse_merge(const float* workspace, int num_seqs, int num_q_heads, in
 pa_status pa_mla_decode(const void* q, const void* kv_cache, const int32_t* block_table,
                         const int32_t* seq_lens, int batch, int num_heads, int kv_lora_rank,
                         int rope_dim, int block_size, int num_blocks, int max_blocks_per_seq,
-                        float scale, int num_splits, float* workspace, void* out, float* lse,
+                        int max_seq_len, float scale, int num_splits, float* workspace, void* out,
+                        float* lse,
                         void* stream) {
   if (batch < 0 || num_heads <= 0 || kv_lora_rank <= 0 || rope_dim < 0 || block_size <= 0 ||
       block_size % 16 != 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 || num_splits < 1 ||
-      num_splits > kMaxSplits || batch > kMaxGridYZ || num_splits > kMaxGridYZ)
+      num_splits > kMaxSplits || batch > kMaxGridYZ || num_splits > kMaxGridYZ || max_seq_len < 0)
     return PA_ERR_INVALID;
   if (kv_lora_rank != 512 || rope_dim != 64 || num_heads % 64 != 0 || block_size % 32 != 0)
     return PA_ERR_UNSUPPORTED;
@@ -200,7 +185,10 @@ pa_status pa_mla_decode(const void* q, const void* kv_cache, const int32_t* bloc
     return PA_ERR_INVALID;
   return from_cuda(pa::launch_mla_decode(q, kv_cache, block_table, seq_lens, batch, num_heads,
                                          block_size, num_blocks, max_blocks_per_seq, scale,
-                                         num_splits, workspace, out, lse, device_error_ptr(),
+                                         num_splits,
+                                         static_cast<int>(pa::split_chunk(max_seq_len, num_splits,
+                                                                          block_size)),
+                                         workspace, out, lse, device_error_ptr(),
                                          static_cast<cudaStream_t>(stream)));
 }
 

@@ -70,6 +70,32 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 __device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
 
+// Per-device "done" flags for one-time host set-up.
+struct DeviceFlags {
+  bool done[64] = {};
+};
+
+// Raises `kern`'s dynamic shared memory limit to `bytes` once per device.
+template <typename Kernel>
+inline cudaError_t set_smem_once(Kernel kern, int bytes, DeviceFlags& flags) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && flags.done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) flags.done[dev] = true;
+  return e;
+}
+
+// Tokens per split: the sequence axis of every request is cut at multiples
+// of chunk = bs * ceil(ceil(max_seq_len / S) / bs) (the last split of a
+// request runs to its end).
+inline long long split_chunk(int max_seq_len, int S, int bs) {
+  const long long m = max_seq_len > 0 ? max_seq_len : 1;
+  const long long per = (m + S - 1) / S;
+  return ((per + bs - 1) / bs) * bs;
+}
+
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 

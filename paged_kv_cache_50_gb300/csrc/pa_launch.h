@@ -1,0 +1,39 @@
+// Host-side launchers of the library's kernels (one per .cu file), used by the
+// C-ABI entry points.  Each returns the launch's cudaError_t.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* cache,
+                                     const int64_t* slot_mapping, int num_tokens,
+                                     int num_kv_heads, int head_size, int block_size,
+                                     int num_blocks, int* err, cudaStream_t stream);
+
+// Split-KV stage 1; `chunk` = tokens per split (split_chunk in pa_common.cuh).
+cudaError_t launch_decode_splitkv(const void* q, const void* cache, const int32_t* block_table,
+                                  const int32_t* seq_lens, int N, int Hq, int Hkv, int d, int bs,
+                                  int num_blocks, int max_blocks, float scale, int S, int chunk,
+                                  float* ws, int* err, cudaStream_t stream);
+
+cudaError_t launch_lse_merge(const float* ws, int NH, int S, int dv, void* out, float* lse,
+                             cudaStream_t stream);
+
+cudaError_t launch_varlen_fwd(const void* q, const void* cache, const int32_t* block_table,
+                              const int32_t* qsl, const int32_t* seq_lens, int N, int Hq, int Hkv,
+                              int d, int bs, int num_blocks, int max_blocks, int max_query_len,
+                              float scale, int causal, void* out, float* lse, int* err,
+                              cudaStream_t stream);
+
+// MLA stage 1 + merge.
+cudaError_t launch_mla_decode(const void* q, const void* cache, const int32_t* block_table,
+                              const int32_t* seq_lens, int B, int H, int bs, int num_blocks,
+                              int max_blocks, float scale, int S, int chunk, float* ws, void* out,
+                              float* lse, int* err, cudaStream_t stream);
+
+// Device address of the error word on the current device (nullptr on error).
+int* device_error_word();
+
+}  // namespace pa

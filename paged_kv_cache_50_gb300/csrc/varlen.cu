@@ -22,6 +22,7 @@
 #include <math_constants.h>
 
 #include "pa_common.cuh"
+#include "pa_launch.h"
 
 namespace pa {
 
@@ -262,8 +263,8 @@ static cudaError_t launch_varlen_t(const void* q, const void* cache, const int32
                                    float* lse, int* err, cudaStream_t stream) {
   using C = VarlenCfg<D>;
   auto kern = varlen_fwd_kernel<D>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::kSmemBytes);
+  static DeviceFlags attr_set;
+  cudaError_t e = set_smem_once(kern, C::kSmemBytes, attr_set);
   if (e != cudaSuccess) return e;
   const int grp = Hq / Hkv;
   const long long rows = static_cast<long long>(max_query_len) * grp;

@@ -96,20 +96,20 @@ def test_empty_calls_are_noops(pa):
     assert pa.lib().pa_reshape_and_cache(NULL, NULL, NULL, NULL, 0, ctypes.byref(s),
                                          NULL) == pa.PA_OK
     s0 = _shape(pa, num_seqs=0)
-    assert pa.lib().pa_decode_splitkv(NULL, NULL, NULL, NULL, ctypes.byref(s0), 0.1, 4, NULL,
+    assert pa.lib().pa_decode_splitkv(NULL, NULL, NULL, NULL, ctypes.byref(s0), 0.1, 4, 0, NULL,
                                       NULL) == pa.PA_OK
 
 
 def test_decode_rejects(pa):
     L = pa.lib()
     s = _shape(pa)
-    assert L.pa_decode_splitkv(1, 1, 1, 1, ctypes.byref(s), 0.1, 0, 1, NULL) == pa.PA_ERR_INVALID
-    assert L.pa_decode_splitkv(1, 1, 1, 1, ctypes.byref(s), 0.1, 20000, 1, NULL) == \
+    assert L.pa_decode_splitkv(1, 1, 1, 1, ctypes.byref(s), 0.1, 0, 64, 1, NULL) == pa.PA_ERR_INVALID
+    assert L.pa_decode_splitkv(1, 1, 1, 1, ctypes.byref(s), 0.1, 20000, 64, 1, NULL) == \
         pa.PA_ERR_INVALID
     big_group = _shape(pa, num_q_heads=64, num_kv_heads=2)
-    assert L.pa_decode_splitkv(1, 1, 1, 1, ctypes.byref(big_group), 0.1, 4, 1, NULL) == \
+    assert L.pa_decode_splitkv(1, 1, 1, 1, ctypes.byref(big_group), 0.1, 4, 64, 1, NULL) == \
         pa.PA_ERR_UNSUPPORTED
-    assert L.pa_decode_splitkv(1, 1, 1, 1, ctypes.byref(s), 0.1, 4, NULL, NULL) == \
+    assert L.pa_decode_splitkv(1, 1, 1, 1, ctypes.byref(s), 0.1, 4, 64, NULL, NULL) == \
         pa.PA_ERR_INVALID
     assert L.pa_lse_merge(1, 2, 8, 0, 128, 1, NULL, NULL) == pa.PA_ERR_INVALID
     assert L.pa_lse_merge(NULL, 2, 8, 4, 128, 1, NULL, NULL) == pa.PA_ERR_INVALID
@@ -134,7 +134,7 @@ def test_mla_rejects(pa):
         a = dict(args)
         a.update(kw)
         return L.pa_mla_decode(1, 1, 1, 1, a["batch"], a["num_heads"], a["kv_lora_rank"],
-                               a["rope_dim"], a["block_size"], a["num_blocks"], a["max_blocks"],
+                               a["rope_dim"], a["block_size"], a["num_blocks"], a["max_blocks"], 256,
                                a["scale"], a["num_splits"], 1, 1, NULL, NULL)
     assert call(kv_lora_rank=448) == pa.PA_ERR_UNSUPPORTED   # head sizes other than 576
     assert call(rope_dim=32) == pa.PA_ERR_UNSUPPORTED
@@ -166,5 +166,5 @@ def test_misaligned_pointers_are_rejected(pa):
     assert L.pa_varlen_fwd(16, 8, 16, 16, 16, 4, 2, ctypes.byref(s), 0.1, 1, 16, NULL,
                            NULL) == pa.PA_ERR_INVALID
     assert L.pa_reshape_and_cache(16, 24, 16, 16, 4, ctypes.byref(s), NULL) == pa.PA_ERR_INVALID
-    assert L.pa_mla_decode(8, 16, 16, 16, 2, 128, 512, 64, 64, 8, 4, 0.1, 2, 16, 16, NULL,
+    assert L.pa_mla_decode(8, 16, 16, 16, 2, 128, 512, 64, 64, 8, 4, 256, 0.1, 2, 16, 16, NULL,
                            NULL) == pa.PA_ERR_INVALID

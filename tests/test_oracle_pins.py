@@ -288,16 +288,34 @@ def test_split_then_merge_equals_unsplit(oracle_lib, S):
     if S == 1:
         assert np.array_equal(part[:, :, 0, :-1], unsplit_o)
         assert np.array_equal(part[:, :, 0, -1], unsplit_l)
-    # Split boundaries: chunk C = bs * ceil(ceil(seq / S) / bs); splits past
-    # the end are empty (o = 0, lse = -inf).
+    # Split boundaries: one chunk C = bs * ceil(ceil(max_seq / S) / bs) for
+    # the whole batch; splits past a request's end are empty (o = 0,
+    # lse = -inf).
+    per = -(-int(b.seq_lens.max()) // S)
+    chunk = -(-per // b.block_size) * b.block_size
+    P, q = _f64(b.pool), _f64(b.q)
+    grp = b.num_q_heads // b.num_kv_heads
     for i, seq in enumerate(b.seq_lens):
-        per = -(-int(seq) // S)
-        chunk = -(-per // b.block_size) * b.block_size
+        K, _ = _gather(P, b.block_table[i], seq, b.block_size)
         for s in range(S):
-            empty = s * chunk >= seq
+            a = min(s * chunk, seq)
+            e = seq if s == S - 1 else min((s + 1) * chunk, seq)
+            empty = a >= e
             assert np.isneginf(part[i, :, s, -1]).all() == empty
             if empty:
                 assert not part[i, :, s, :-1].any()
+                continue
+            # The split's LSE is the log-sum-exp of exactly its tokens' scores.
+            for h in range(b.num_q_heads):
+                sc = b.scale * K[a:e, h // grp] @ q[i, h]
+                ref = sc.max() + math.log(np.exp(sc - sc.max()).sum())
+                assert abs(part[i, h, s, -1] - ref) < 1e-12
+    # An understated max_seq_len only makes the last split longer.
+    part2 = oracle_lib.split_partials(b.q, b.pool, b.block_table, b.seq_lens, b.scale, S,
+                                      max_seq_len=17)
+    o2, l2 = oracle_lib.lse_merge(part2)
+    np.testing.assert_allclose(o2, unsplit_o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l2, unsplit_l, rtol=0, atol=1e-12)
 
 
 def test_merge_ignores_empty_and_handles_all_empty(oracle_lib):

@@ -62,8 +62,8 @@ def _noalloc_cabi(pa, d, S):
     shape = pa.PaShape(N, 32, 8, 128, 16, b.num_blocks, b.max_blocks_per_seq)
     rc = pa.lib().pa_decode_noalloc(
         d["q"].data_ptr(), d["pool"].data_ptr(), d["table"].data_ptr(), d["seq"].data_ptr(),
-        ctypes.byref(shape), ctypes.c_float(b.scale), S, out.data_ptr(), lse.data_ptr(),
-        torch.cuda.current_stream().cuda_stream)
+        ctypes.byref(shape), ctypes.c_float(b.scale), S, int(b.seq_lens.max()), out.data_ptr(),
+        lse.data_ptr(), torch.cuda.current_stream().cuda_stream)
     assert rc == pa.PA_OK, pa.status_string(rc)
     return out, lse
 
@@ -86,6 +86,6 @@ def test_noalloc_rejects_sizes_beyond_the_array(pa):
     S = limit // (N * hq * (d + 1) * 4) + 1       # one split too many
     shape = pa.PaShape(N, hq, 8, d, 16, 100, 10)
     rc = pa.lib().pa_decode_noalloc(16, 16, 16, 16, ctypes.byref(shape), ctypes.c_float(0.1), S,
-                                    16, None, None)
+                                    4096, 16, None, None)
     assert rc == pa.PA_ERR_INVALID
     assert np.prod([N, hq, S - 1, d + 1]) * 4 <= limit
