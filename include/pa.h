@@ -58,6 +58,7 @@ typedef enum pa_status {
 /* Device error word bits (pa_get_device_error). */
 #define PA_DEVERR_BLOCK_ID 1  /* a block_table entry outside [0, num_blocks) */
 #define PA_DEVERR_SLOT 2      /* a slot_mapping entry >= num_blocks * block_size */
+#define PA_DEVERR_TIMEOUT 4   /* a kernel gave up a bounded wait; its outputs are invalid */
 
 /* Shape of a standard-layout paged batch. */
 typedef struct pa_shape {

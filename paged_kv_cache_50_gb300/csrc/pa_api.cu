@@ -92,9 +92,9 @@ pa_status pa_varlen_fwd(const void* q, const void* kv_cache, const int32_t* bloc
   if (q == nullptr || kv_cache == nullptr || block_table == nullptr ||
       query_start_loc == nullptr || seq_lens == nullptr || out == nullptr)
     return PA_ERR_INVALID;
-  if (!aligned(q, 4) || !aligned(kv_cache, 16) || !aligned(out, 4) || !aligned(lse, 4))
+  if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(lse, 4))
     return PA_ERR_INVALID;
-  return from_cuda(pa::launch_varlen_fwd(
+  return from_cuda(pa::launch_varlen_tc(
       q, kv_cache, block_table, query_start_loc, seq_lens, shape->num_seqs, shape->num_q_heads,
       shape->num_kv_heads, shape->head_size, shape->block_size, shape->num_blocks,
       shape->max_blocks_per_seq, max_query_len, scale, causal ? 1 : 0, out, lse,

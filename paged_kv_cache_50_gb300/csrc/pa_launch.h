@@ -27,6 +27,13 @@ cudaError_t launch_varlen_fwd(const void* q, const void* cache, const int32_t* b
                               float scale, int causal, void* out, float* lse, int* err,
                               cudaStream_t stream);
 
+// The same operation on tcgen05 tensor cores with TMA-gathered K/V.
+cudaError_t launch_varlen_tc(const void* q, const void* cache, const int32_t* block_table,
+                             const int32_t* qsl, const int32_t* seq_lens, int N, int Hq, int Hkv,
+                             int d, int bs, int num_blocks, int max_blocks, int max_query_len,
+                             float scale, int causal, void* out, float* lse, int* err,
+                             cudaStream_t stream);
+
 // MLA stage 1 + merge.
 cudaError_t launch_mla_decode(const void* q, const void* cache, const int32_t* block_table,
                               const int32_t* seq_lens, int B, int H, int bs, int num_blocks,

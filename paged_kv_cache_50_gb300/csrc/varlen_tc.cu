@@ -1,0 +1,468 @@
+// Varlen paged attention on the 5th-generation tensor cores (tcgen05 + TMEM)
+// with TMA-gathered K/V: step 2 of the paged-kernel contract ("Attention
+// Backends", section "What 'paged attention' requires of a kernel") computed
+// as O = softmax(Q K^T * scale + M) V ("Chapter 1: attention backends",
+// section 2.1) with the FlashAttention tiling and online softmax of section
+// 4.1.
+//
+// CTA = (tile of 128 packed rows, kv head, request); a packed row is one
+// (query row, q head of the kv group) pair, so the Hq/Hkv heads sharing a kv
+// head share every K/V tile.  Warp roles (192 threads):
+//   warps 0-3  softmax: thread t owns packed row t = TMEM lane t.  Loads its
+//              Q row into shared memory, then per 128-token tile reads its
+//              S row from TMEM (tcgen05.ld), masks (causal, bottom-right),
+//              runs the online softmax in the log2 domain, writes its P row
+//              (bf16) to shared memory, and finally scales its O row out of
+//              TMEM into the output;
+//   warp 4     MMA issue (one thread): S(j) = Q K(j)^T into one of two TMEM
+//              S buffers, O += P(j) V(j) into the TMEM O accumulator;
+//   warp 5     K/V producer (one thread): per 16-token piece of a cache block
+//              one TMA box per 64-column half, through the block table.
+// The MMA thread issues S(j+1) before waiting for P(j), so the tensor core
+// computes the next scores while the softmax warps work on the current ones.
+// O is rescaled (TMEM load, scale, store) only when a row's running max grows
+// by more than 2^8; otherwise P keeps the older reference max, which keeps
+// the final O / l exact.
+//
+// Shared memory (128-byte swizzled, 1024-byte aligned atoms):
+//   Q    [D/64 halves][128 rows][128 B]
+//   K,V  2 stages x {K, V} x [D/64 halves][128 tokens][128 B]
+//   P    2 buffers x [2 token halves][128 rows][128 B]
+// TMEM: S buffers at columns 0 and 128, O at 256 (512 columns allocated).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <math_constants.h>
+
+#include <mutex>
+
+#include "pa_common.cuh"
+#include "pa_launch.h"
+#include "tc_common.cuh"
+
+namespace pa {
+
+template <int D>
+struct TcCfg {
+  static constexpr int kBM = 128;                     // packed rows per CTA
+  static constexpr int kBN = 128;                     // tokens per K/V tile
+  static constexpr int kHalves = D / 64;              // 128-byte column groups of a row
+  static constexpr int kQBytes = kBM * D * 2;
+  static constexpr int kTileBytes = kBN * D * 2;      // one K (or V) tile
+  static constexpr int kStageBytes = 2 * kTileBytes;  // K + V
+  static constexpr int kPBytes = kBM * kBN * 2;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffKV = kQBytes;
+  static constexpr int kOffP = kOffKV + 2 * kStageBytes;
+  static constexpr int kOffBar = kOffP + 2 * kPBytes;
+  static constexpr int kSmemBytes = kOffBar + 256 + 1024;   // barriers + alignment slack
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+  static constexpr int kThreads = 192;
+  static constexpr int kPieceBytes = 16 * 128;        // one TMA box: 16 rows x 128 B
+};
+
+// Byte offset of 16-byte chunk `c` (0..7) of row `r` in a 128-byte swizzled
+// [rows][128 B] region.
+__device__ __forceinline__ uint32_t sw128(int r, int c) {
+  return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+enum TcBar { kQFull = 0, kKvFull = 1, kKvEmpty = 3, kSFull = 5, kSFree = 7, kPFull = 9,
+             kPvDone = 11, kFinal = 13, kNumBars = 14 };
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16* __restrict__ q,
+                 const int32_t* __restrict__ block_table, const int32_t* __restrict__ qsl,
+                 const int32_t* __restrict__ seq_lens, int max_blocks, int Hq, int Hkv, int bs,
+                 int num_blocks, float scale_log2, int causal, __nv_bfloat16* __restrict__ out,
+                 float* __restrict__ lse, int* err) {
+  using C = TcCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* sgen = smem_raw + (sbase - raw);
+
+  // A kernel that already gave up a wait leaves the rest of the grid to exit
+  // at once instead of timing out CTA after CTA.
+  if (err != nullptr && (*reinterpret_cast<volatile int*>(err) & PA_DEVERR_TIMEOUT)) return;
+  const int i = blockIdx.z, kvh = blockIdx.y;
+  const int qt = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);  // heavy tiles first
+  const int grp = Hq / Hkv;
+  const int q0 = qsl[i];
+  const int qlen = qsl[i + 1] - q0;
+  const int rows_total = qlen * grp;
+  const int row0 = qt * C::kBM;
+  if (row0 >= rows_total) return;
+  const int seq = seq_lens[i];
+  const int ctx = seq - qlen;
+  const int last_row = min(row0 + C::kBM, rows_total) - 1;
+  int kv_end = causal ? ctx + last_row / grp + 1 : seq;
+  kv_end = max(0, min(kv_end, seq));
+  const int ntiles = (kv_end + C::kBN - 1) / C::kBN;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int32_t* table = block_table + static_cast<int64_t>(i) * max_blocks;
+
+  const uint32_t bars = sbase + C::kOffBar;
+  auto BAR = [&](int k) { return bars + 8u * static_cast<uint32_t>(k); };
+  const uint32_t tmem_slot = bars + 8u * kNumBars;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + C::kOffBar + 8 * kNumBars + 8);
+
+  if (threadIdx.x == 0) {
+    tc::mbar_init(BAR(kQFull), 128);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(BAR(kKvFull + b), 1);
+      tc::mbar_init(BAR(kKvEmpty + b), 1);
+      tc::mbar_init(BAR(kSFull + b), 1);
+      tc::mbar_init(BAR(kSFree + b), 128);
+      tc::mbar_init(BAR(kPFull + b), 128);
+      tc::mbar_init(BAR(kPvDone + b), 1);
+    }
+    tc::mbar_init(BAR(kFinal), 1);
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  __syncwarp();
+  if (warp == 0) tc::tmem_alloc(tmem_slot, C::kTmemCols);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sgen + C::kOffBar + 8 * kNumBars);
+
+  auto fail = [&]() {
+    record_error(err, PA_DEVERR_TIMEOUT);
+    *abort_flag = 1;
+  };
+  // Piece p (16 tokens) of tile j is loaded iff it starts before kv_end and
+  // its block id is valid.
+  auto piece_block = [&](int tok) -> int {
+    if (tok >= kv_end) return -1;
+    const int blk = block_at(table, tok / bs, max_blocks);
+    return (blk >= 0 && blk < num_blocks) ? blk : -2;
+  };
+
+  if (warp < 4) {
+    // ------------------------------------------------------------ softmax
+    const int t = threadIdx.x;
+    const int pr = row0 + t;
+    const bool valid = pr < rows_total;
+    const int qi = valid ? pr / grp : 0;
+    const int hh = valid ? pr % grp : 0;
+    const int64_t qoff = (static_cast<int64_t>(q0 + qi) * Hq + kvh * grp + hh) * D;
+    int lim = valid ? (causal ? ctx + qi + 1 : seq) : 0;
+    lim = max(0, min(lim, seq));
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(q + qoff);
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) {
+        uint4 v = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+        const uint32_t dst = sbase + C::kOffQ + (c >> 3) * (C::kBM * 128) + sw128(t, c & 7);
+        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v.x), "r"(v.y),
+                     "r"(v.z), "r"(v.w)
+                     : "memory");
+      }
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(BAR(kQFull));
+    }
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // TMEM loads and stores are warp-collective: every decision to skip or
+    // stop is taken for the whole warp.
+    auto wait_warp = [&](uint32_t b, uint32_t parity) -> bool {
+      const bool w = __all_sync(0xffffffffu, tc::mbar_wait(b, parity));
+      if (!w) fail();
+      return w;
+    };
+    float m_used = -CUDART_INF_F, l = 0.f;
+    for (int j = 0; j < ntiles; ++j) {
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+      const int sb = j & 1;
+      if (!wait_warp(BAR(kSFull + sb), (j >> 1) & 1)) break;
+      tc::tc_fence_after();
+      float s[C::kBN];
+      {
+        const uint32_t ta = tmem + lane_base + (sb ? C::kColS1 : C::kColS0);
+#pragma unroll
+        for (int c = 0; c < C::kBN / 32; ++c) {
+          uint32_t r[32];
+          tc::tmem_ld32(ta + c * 32, r);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[e]);
+        }
+      }
+      tc::tc_fence_before();
+      tc::mbar_arrive(BAR(kSFree + sb));
+
+      const int tok0 = j * C::kBN;
+      uint32_t vm = 0;   // loaded pieces
+#pragma unroll
+      for (int p = 0; p < C::kBN / 16; ++p) vm |= (piece_block(tok0 + 16 * p) >= 0 ? 1u : 0u) << p;
+      float mx = -CUDART_INF_F;
+#pragma unroll
+      for (int c = 0; c < C::kBN; ++c) {
+        const bool vis = (tok0 + c < lim) && ((vm >> (c >> 4)) & 1u);
+        s[c] = vis ? s[c] * scale_log2 : -CUDART_INF_F;
+        mx = fmaxf(mx, s[c]);
+      }
+      const float m_new = fmaxf(m_used, mx);
+      const bool need = m_new > m_used + 8.f;
+      const float alpha = need ? exp2f(m_used - m_new) : 1.f;
+      if (need) m_used = m_new;
+      if (__any_sync(0xffffffffu, need) && j > 0) {
+        // Rescale this warp's O rows once PV(j-1) has landed.
+        if (!wait_warp(BAR(kPvDone + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) break;
+        tc::tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          const uint32_t ta = tmem + lane_base + C::kColO + c * 32;
+          tc::tmem_ld32(ta, r);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+          tc::tmem_st32(ta, r);
+        }
+        tc::tmem_wait_st();
+      }
+      l *= alpha;
+      // P buffer sb is free once PV(j-2) has completed.
+      if (j >= 2 && !wait_warp(BAR(kPvDone + sb), ((j - 2) >> 1) & 1)) break;
+      const float mu = m_used == -CUDART_INF_F ? 0.f : m_used;
+      const uint32_t pbase = sbase + C::kOffP + sb * C::kPBytes;
+#pragma unroll
+      for (int c8 = 0; c8 < C::kBN / 8; ++c8) {
+        float p[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          p[e] = exp2f(s[c8 * 8 + e] - mu);
+          l += p[e];
+        }
+        const uint32_t dst = pbase + (c8 >> 3) * (C::kBM * 128) + sw128(t, c8 & 7);
+        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst),
+                     "r"(pack_bf16(p[0], p[1])), "r"(pack_bf16(p[2], p[3])),
+                     "r"(pack_bf16(p[4], p[5])), "r"(pack_bf16(p[6], p[7]))
+                     : "memory");
+      }
+      // V rows that must contribute nothing: past seq_len (stale or unset
+      // cache contents) or in pieces that were not loaded.
+      {
+        const int tok = tok0 + t;
+        const bool row_ok = tok < seq && ((vm >> (t >> 4)) & 1u);
+        if (!row_ok) {
+          const uint32_t vbase = sbase + C::kOffKV + sb * C::kStageBytes + C::kTileBytes;
+#pragma unroll
+          for (int h = 0; h < C::kHalves; ++h)
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const uint32_t dst = vbase + h * (C::kBN * 128) + sw128(t, c);
+              asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(dst), "r"(0u) : "memory");
+            }
+        }
+      }
+      tc::fence_proxy_async_smem();
+      tc::tc_fence_before();
+      tc::mbar_arrive(BAR(kPFull + sb));
+    }
+    // ------------------------------------------------------------ epilogue
+    bool ok = !__any_sync(0xffffffffu, *abort_flag != 0) && ntiles > 0;
+    if (ok) ok = wait_warp(BAR(kPvDone + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1);
+    tc::tc_fence_after();
+    if (ok) {   // warp-uniform
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      uint4* dst = reinterpret_cast<uint4*>(out + qoff);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        tc::tmem_ld32(tmem + lane_base + C::kColO + c * 32, r);
+        tc::tmem_wait_ld();
+        if (valid) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 w;
+            w.x = pack_bf16(__uint_as_float(r[v * 8 + 0]) * inv, __uint_as_float(r[v * 8 + 1]) * inv);
+            w.y = pack_bf16(__uint_as_float(r[v * 8 + 2]) * inv, __uint_as_float(r[v * 8 + 3]) * inv);
+            w.z = pack_bf16(__uint_as_float(r[v * 8 + 4]) * inv, __uint_as_float(r[v * 8 + 5]) * inv);
+            w.w = pack_bf16(__uint_as_float(r[v * 8 + 6]) * inv, __uint_as_float(r[v * 8 + 7]) * inv);
+            dst[c * 4 + v] = w;
+          }
+        }
+      }
+      if (valid && lse != nullptr)
+        lse[qoff / D] = l > 0.f ? (m_used + log2f(l)) * kLn2 : -CUDART_INF_F;
+    } else if (valid) {
+      // Nothing visible (or an aborted CTA): o = 0, lse = -inf.
+      uint4* dst = reinterpret_cast<uint4*>(out + qoff);
+      for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+      if (lse != nullptr) lse[qoff / D] = -CUDART_INF_F;
+    }
+  } else if (warp == 4) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, C::kBN, 0, 0);
+      constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, D, 0, 1);
+      const uint32_t qs = sbase + C::kOffQ;
+      bool ok = ntiles == 0 || tc::mbar_wait(BAR(kQFull), 0);
+      if (!ok) fail();
+      auto issue_s = [&](int j) -> bool {
+        const int st = j & 1;
+        if (!tc::mbar_wait(BAR(kKvFull + st), (j >> 1) & 1)) return false;
+        if (j >= 2 && !tc::mbar_wait(BAR(kSFree + st), ((j - 2) >> 1) & 1)) return false;
+        tc::tc_fence_after();
+        const uint32_t ks = sbase + C::kOffKV + st * C::kStageBytes;
+        const uint32_t dS = tmem + (st ? C::kColS1 : C::kColS0);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * (C::kBM * 128) + (k & 3) * 32;
+          const uint32_t koff = (k >> 2) * (C::kBN * 128) + (k & 3) * 32;
+          tc::mma_bf16_ss(dS, tc::smem_desc_sw128(qs + off, 16, 1024),
+                          tc::smem_desc_sw128(ks + koff, 16, 1024), idesc_s, k > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(BAR(kSFull + st));
+        return true;
+      };
+      if (ok && ntiles > 0) ok = issue_s(0);
+      for (int j = 0; ok && j < ntiles; ++j) {
+        if (*abort_flag) { ok = false; break; }
+        if (j + 1 < ntiles && !issue_s(j + 1)) { ok = false; break; }
+        const int st = j & 1;
+        if (!tc::mbar_wait(BAR(kPFull + st), (j >> 1) & 1)) { ok = false; break; }
+        tc::tc_fence_after();
+        const uint32_t ps = sbase + C::kOffP + st * C::kPBytes;
+        const uint32_t vs = sbase + C::kOffKV + st * C::kStageBytes + C::kTileBytes;
+#pragma unroll
+        for (int k = 0; k < C::kBN / 16; ++k) {
+          const uint32_t poff = (k >> 2) * (C::kBM * 128) + (k & 3) * 32;
+          tc::mma_bf16_ss(tmem + C::kColO, tc::smem_desc_sw128(ps + poff, 16, 1024),
+                          tc::smem_desc_sw128(vs + k * 16 * 128, C::kBN * 128, 1024), idesc_o,
+                          (j > 0 || k > 0) ? 1u : 0u);
+        }
+        tc::mma_commit(BAR(kPvDone + st));
+        tc::mma_commit(BAR(kKvEmpty + st));
+      }
+      if (!ok && !*abort_flag) fail();
+      // Everything issued has completed before TMEM is released.
+      tc::mma_commit(BAR(kFinal));
+      if (!tc::mbar_wait(BAR(kFinal), 0)) fail();
+    }
+  } else {
+    // ------------------------------------------------------------ K/V producer
+    if (lane == 0) {
+      tc::tma_prefetch_desc(&kv_map);
+      int issued = 0;
+      for (int j = 0; j < ntiles; ++j) {
+        if (*abort_flag) break;
+        const int st = j & 1;
+        if (j >= 2 && !tc::mbar_wait(BAR(kKvEmpty + st), ((j - 2) >> 1) & 1)) { fail(); break; }
+        const int tok0 = j * C::kBN;
+        int blks[C::kBN / 16];
+        uint32_t bytes = 0;
+#pragma unroll
+        for (int p = 0; p < C::kBN / 16; ++p) {
+          blks[p] = piece_block(tok0 + 16 * p);
+          if (blks[p] == -2) record_error(err, PA_DEVERR_BLOCK_ID);
+          if (blks[p] >= 0) bytes += 2u * C::kHalves * C::kPieceBytes;
+        }
+        const uint32_t full = BAR(kKvFull + st);
+        tc::mbar_arrive_expect_tx(full, bytes);
+        const uint32_t ks = sbase + C::kOffKV + st * C::kStageBytes;
+        const uint32_t vs = ks + C::kTileBytes;
+#pragma unroll
+        for (int p = 0; p < C::kBN / 16; ++p) {
+          if (blks[p] < 0) continue;
+          const int off = (tok0 + 16 * p) % bs;
+#pragma unroll
+          for (int h = 0; h < C::kHalves; ++h) {
+            const uint32_t d = h * (C::kBN * 128) + p * C::kPieceBytes;
+            tc::tma_load_5d(ks + d, &kv_map, full, h * 64, kvh, off, 0, blks[p]);
+            tc::tma_load_5d(vs + d, &kv_map, full, h * 64, kvh, off, 1, blks[p]);
+          }
+        }
+        issued = j + 1;
+      }
+      // No copy may still be landing when the CTA exits.
+      for (int j = max(0, issued - 2); j < issued; ++j)
+        if (!tc::mbar_wait(BAR(kKvFull + (j & 1)), (j >> 1) & 1)) fail();
+    }
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 5-D view of the standard pool [nb][2][bs][Hkv][d] (innermost first) with a
+// 64-element x 1 head x 16 token box and 128-byte swizzle.
+bool make_kv_map(CUtensorMap* map, const void* cache, int nb, int bs, int Hkv, int d) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[5] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(Hkv),
+                              static_cast<cuuint64_t>(bs), 2, static_cast<cuuint64_t>(nb)};
+  const cuuint64_t row = static_cast<cuuint64_t>(d) * 2;
+  const cuuint64_t strides[4] = {row, row * Hkv, row * Hkv * bs, row * Hkv * bs * 2};
+  const cuuint32_t box[5] = {64, 1, 16, 1, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(cache), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+template <int D>
+static cudaError_t launch_varlen_tc_t(const void* q, const void* cache, const int32_t* block_table,
+                                      const int32_t* qsl, const int32_t* seq_lens, int N, int Hq,
+                                      int Hkv, int bs, int num_blocks, int max_blocks,
+                                      int max_query_len, float scale, int causal, void* out,
+                                      float* lse, int* err, cudaStream_t stream) {
+  using C = TcCfg<D>;
+  CUtensorMap map;
+  if (!make_kv_map(&map, cache, num_blocks, bs, Hkv, D)) return cudaErrorInvalidValue;
+  auto kern = varlen_tc_kernel<D>;
+  static DeviceFlags attr_set;
+  cudaError_t e = set_smem_once(kern, C::kSmemBytes, attr_set);
+  if (e != cudaSuccess) return e;
+  const long long rows = static_cast<long long>(max_query_len) * (Hq / Hkv);
+  dim3 grid(static_cast<unsigned>((rows + C::kBM - 1) / C::kBM), Hkv, N);
+  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(
+      map, static_cast<const __nv_bfloat16*>(q), block_table, qsl, seq_lens, max_blocks, Hq, Hkv,
+      bs, num_blocks, scale * kLog2e, causal, static_cast<__nv_bfloat16*>(out), lse, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_varlen_tc(const void* q, const void* cache, const int32_t* block_table,
+                             const int32_t* qsl, const int32_t* seq_lens, int N, int Hq, int Hkv,
+                             int d, int bs, int num_blocks, int max_blocks, int max_query_len,
+                             float scale, int causal, void* out, float* lse, int* err,
+                             cudaStream_t stream) {
+  if (d == 128)
+    return launch_varlen_tc_t<128>(q, cache, block_table, qsl, seq_lens, N, Hq, Hkv, bs,
+                                   num_blocks, max_blocks, max_query_len, scale, causal, out, lse,
+                                   err, stream);
+  return launch_varlen_tc_t<64>(q, cache, block_table, qsl, seq_lens, N, Hq, Hkv, bs, num_blocks,
+                                max_blocks, max_query_len, scale, causal, out, lse, err, stream);
+}
+
+}  // namespace pa
