@@ -18,6 +18,9 @@
 //              S buffers, O += P(j) V(j) into the TMEM O accumulator;
 //   warp 5     K/V producer (one thread): per 16-token piece of a cache block
 //              one TMA box per 64-column half, through the block table.
+// K and V travel in separate rings: a K stage is released as soon as S(j)
+// has been computed and a V stage once PV(j) has, and the producer runs K two
+// tiles ahead of V, so the loads of later tiles overlap the current softmax.
 // The MMA thread issues S(j+1) before waiting for P(j), so the tensor core
 // computes the next scores while the softmax warps work on the current ones.
 // O is rescaled (TMEM load, scale, store) only when a row's running max grows
@@ -26,8 +29,9 @@
 //
 // Shared memory (128-byte swizzled, 1024-byte aligned atoms):
 //   Q    [D/64 halves][128 rows][128 B]
-//   K,V  2 stages x {K, V} x [D/64 halves][128 tokens][128 B]
-//   P    2 buffers x [2 token halves][128 rows][128 B]
+//   K    3 stages x [D/64 halves][128 tokens][128 B]
+//   V    2 stages x [D/64 halves][128 tokens][128 B]
+//   P    [2 token halves][128 rows][128 B]
 // TMEM: S buffers at columns 0 and 128, O at 256 (512 columns allocated).
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -46,14 +50,16 @@ struct TcCfg {
   static constexpr int kBM = 128;                     // packed rows per CTA
   static constexpr int kBN = 128;                     // tokens per K/V tile
   static constexpr int kHalves = D / 64;              // 128-byte column groups of a row
+  static constexpr int kKStages = 3;
+  static constexpr int kVStages = 2;
   static constexpr int kQBytes = kBM * D * 2;
   static constexpr int kTileBytes = kBN * D * 2;      // one K (or V) tile
-  static constexpr int kStageBytes = 2 * kTileBytes;  // K + V
   static constexpr int kPBytes = kBM * kBN * 2;
   static constexpr int kOffQ = 0;
-  static constexpr int kOffKV = kQBytes;
-  static constexpr int kOffP = kOffKV + 2 * kStageBytes;
-  static constexpr int kOffBar = kOffP + 2 * kPBytes;
+  static constexpr int kOffK = kQBytes;
+  static constexpr int kOffV = kOffK + kKStages * kTileBytes;
+  static constexpr int kOffP = kOffV + kVStages * kTileBytes;
+  static constexpr int kOffBar = kOffP + kPBytes;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;   // barriers + alignment slack
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
@@ -67,8 +73,25 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) {
   return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
-enum TcBar { kQFull = 0, kKvFull = 1, kKvEmpty = 3, kSFull = 5, kSFree = 7, kPFull = 9,
-             kPvDone = 11, kFinal = 13, kNumBars = 14 };
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+enum TcBar {
+  kQFull = 0,
+  kKFull = 1,    // 3
+  kKEmpty = 4,   // 3
+  kVFull = 7,    // 2
+  kVEmpty = 9,   // 2
+  kSFull = 11,   // 2
+  kSFree = 13,   // 2
+  kPFull = 15,
+  kPvDone = 16,
+  kFinal = 17,
+  kNumBars = 18
+};
 
 template <int D>
 __global__ void __launch_bounds__(192, 1)
@@ -111,14 +134,18 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
 
   if (threadIdx.x == 0) {
     tc::mbar_init(BAR(kQFull), 128);
+    for (int b = 0; b < C::kKStages; ++b) {
+      tc::mbar_init(BAR(kKFull + b), 1);
+      tc::mbar_init(BAR(kKEmpty + b), 1);
+    }
     for (int b = 0; b < 2; ++b) {
-      tc::mbar_init(BAR(kKvFull + b), 1);
-      tc::mbar_init(BAR(kKvEmpty + b), 1);
+      tc::mbar_init(BAR(kVFull + b), 1);
+      tc::mbar_init(BAR(kVEmpty + b), 1);
       tc::mbar_init(BAR(kSFull + b), 1);
       tc::mbar_init(BAR(kSFree + b), 128);
-      tc::mbar_init(BAR(kPFull + b), 128);
-      tc::mbar_init(BAR(kPvDone + b), 1);
     }
+    tc::mbar_init(BAR(kPFull), 128);
+    tc::mbar_init(BAR(kPvDone), 1);
     tc::mbar_init(BAR(kFinal), 1);
     *abort_flag = 0;
     tc::fence_barrier_init();
@@ -134,8 +161,9 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
     record_error(err, PA_DEVERR_TIMEOUT);
     *abort_flag = 1;
   };
-  // Piece p (16 tokens) of tile j is loaded iff it starts before kv_end and
-  // its block id is valid.
+  // The 16-token piece starting at `tok` is loaded iff it starts before
+  // kv_end and its block id is valid; returns the block id, -1 (past the
+  // visible range) or -2 (invalid id).
   auto piece_block = [&](int tok) -> int {
     if (tok >= kv_end) return -1;
     const int blk = block_at(table, tok / bs, max_blocks);
@@ -177,9 +205,14 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
     for (int j = 0; j < ntiles; ++j) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
       const int sb = j & 1;
+      const int tok0 = j * C::kBN;
+      uint32_t vm = 0;   // loaded pieces of this tile
+#pragma unroll
+      for (int p = 0; p < C::kBN / 16; ++p) vm |= (piece_block(tok0 + 16 * p) >= 0 ? 1u : 0u) << p;
       if (!wait_warp(BAR(kSFull + sb), (j >> 1) & 1)) break;
       tc::tc_fence_after();
       float s[C::kBN];
+      float mx = -CUDART_INF_F;
       {
         const uint32_t ta = tmem + lane_base + (sb ? C::kColS1 : C::kColS0);
 #pragma unroll
@@ -188,30 +221,35 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
           tc::tmem_ld32(ta + c * 32, r);
           tc::tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[e]);
+          for (int e = 0; e < 32; ++e) {
+            const int col = c * 32 + e;
+            const bool vis = (tok0 + col < lim) && ((vm >> (col >> 4)) & 1u);
+            s[col] = vis ? __uint_as_float(r[e]) * scale_log2 : -CUDART_INF_F;
+            mx = fmaxf(mx, s[col]);
+          }
         }
       }
       tc::tc_fence_before();
       tc::mbar_arrive(BAR(kSFree + sb));
 
-      const int tok0 = j * C::kBN;
-      uint32_t vm = 0;   // loaded pieces
-#pragma unroll
-      for (int p = 0; p < C::kBN / 16; ++p) vm |= (piece_block(tok0 + 16 * p) >= 0 ? 1u : 0u) << p;
-      float mx = -CUDART_INF_F;
-#pragma unroll
-      for (int c = 0; c < C::kBN; ++c) {
-        const bool vis = (tok0 + c < lim) && ((vm >> (c >> 4)) & 1u);
-        s[c] = vis ? s[c] * scale_log2 : -CUDART_INF_F;
-        mx = fmaxf(mx, s[c]);
-      }
       const float m_new = fmaxf(m_used, mx);
       const bool need = m_new > m_used + 8.f;
-      const float alpha = need ? exp2f(m_used - m_new) : 1.f;
+      const float alpha = need ? ex2(m_used - m_new) : 1.f;
       if (need) m_used = m_new;
+      const float mu = m_used == -CUDART_INF_F ? 0.f : m_used;
+      // P = exp2(s - m_used) in registers first (the P buffer may still be
+      // in use by PV(j-1)).
+      uint32_t pk[C::kBN / 2];
+      l *= alpha;
+#pragma unroll
+      for (int c = 0; c < C::kBN / 2; ++c) {
+        const float p0 = ex2(s[2 * c] - mu), p1 = ex2(s[2 * c + 1] - mu);
+        l += p0 + p1;
+        pk[c] = pack_bf16(p0, p1);
+      }
+      // PV(j-1) must be done before O is rescaled or the P buffer rewritten.
+      if (j > 0 && !wait_warp(BAR(kPvDone), (j - 1) & 1)) break;
       if (__any_sync(0xffffffffu, need) && j > 0) {
-        // Rescale this warp's O rows once PV(j-1) has landed.
-        if (!wait_warp(BAR(kPvDone + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) break;
         tc::tc_fence_after();
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -225,32 +263,25 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
         }
         tc::tmem_wait_st();
       }
-      l *= alpha;
-      // P buffer sb is free once PV(j-2) has completed.
-      if (j >= 2 && !wait_warp(BAR(kPvDone + sb), ((j - 2) >> 1) & 1)) break;
-      const float mu = m_used == -CUDART_INF_F ? 0.f : m_used;
-      const uint32_t pbase = sbase + C::kOffP + sb * C::kPBytes;
+      {
+        const uint32_t pbase = sbase + C::kOffP;
 #pragma unroll
-      for (int c8 = 0; c8 < C::kBN / 8; ++c8) {
-        float p[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          p[e] = exp2f(s[c8 * 8 + e] - mu);
-          l += p[e];
+        for (int c8 = 0; c8 < C::kBN / 8; ++c8) {
+          const uint32_t dst = pbase + (c8 >> 3) * (C::kBM * 128) + sw128(t, c8 & 7);
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(pk[4 * c8]),
+                       "r"(pk[4 * c8 + 1]), "r"(pk[4 * c8 + 2]), "r"(pk[4 * c8 + 3])
+                       : "memory");
         }
-        const uint32_t dst = pbase + (c8 >> 3) * (C::kBM * 128) + sw128(t, c8 & 7);
-        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst),
-                     "r"(pack_bf16(p[0], p[1])), "r"(pack_bf16(p[2], p[3])),
-                     "r"(pack_bf16(p[4], p[5])), "r"(pack_bf16(p[6], p[7]))
-                     : "memory");
       }
       // V rows that must contribute nothing: past seq_len (stale or unset
-      // cache contents) or in pieces that were not loaded.
+      // cache contents) or in pieces that were not loaded.  Zeroed once the
+      // tile's V has landed.
       {
         const int tok = tok0 + t;
         const bool row_ok = tok < seq && ((vm >> (t >> 4)) & 1u);
         if (!row_ok) {
-          const uint32_t vbase = sbase + C::kOffKV + sb * C::kStageBytes + C::kTileBytes;
+          if (!tc::mbar_wait(BAR(kVFull + sb), (j >> 1) & 1)) fail();
+          const uint32_t vbase = sbase + C::kOffV + sb * C::kTileBytes;
 #pragma unroll
           for (int h = 0; h < C::kHalves; ++h)
 #pragma unroll
@@ -262,11 +293,11 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
       }
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
-      tc::mbar_arrive(BAR(kPFull + sb));
+      tc::mbar_arrive(BAR(kPFull));
     }
     // ------------------------------------------------------------ epilogue
     bool ok = !__any_sync(0xffffffffu, *abort_flag != 0) && ntiles > 0;
-    if (ok) ok = wait_warp(BAR(kPvDone + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1);
+    if (ok) ok = wait_warp(BAR(kPvDone), (ntiles - 1) & 1);
     tc::tc_fence_after();
     if (ok) {   // warp-uniform
       const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -305,12 +336,12 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
       bool ok = ntiles == 0 || tc::mbar_wait(BAR(kQFull), 0);
       if (!ok) fail();
       auto issue_s = [&](int j) -> bool {
-        const int st = j & 1;
-        if (!tc::mbar_wait(BAR(kKvFull + st), (j >> 1) & 1)) return false;
-        if (j >= 2 && !tc::mbar_wait(BAR(kSFree + st), ((j - 2) >> 1) & 1)) return false;
+        const int ks_i = j % C::kKStages, sb = j & 1;
+        if (!tc::mbar_wait(BAR(kKFull + ks_i), (j / C::kKStages) & 1)) return false;
+        if (j >= 2 && !tc::mbar_wait(BAR(kSFree + sb), ((j - 2) >> 1) & 1)) return false;
         tc::tc_fence_after();
-        const uint32_t ks = sbase + C::kOffKV + st * C::kStageBytes;
-        const uint32_t dS = tmem + (st ? C::kColS1 : C::kColS0);
+        const uint32_t ks = sbase + C::kOffK + ks_i * C::kTileBytes;
+        const uint32_t dS = tmem + (sb ? C::kColS1 : C::kColS0);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * (C::kBM * 128) + (k & 3) * 32;
@@ -318,18 +349,20 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
           tc::mma_bf16_ss(dS, tc::smem_desc_sw128(qs + off, 16, 1024),
                           tc::smem_desc_sw128(ks + koff, 16, 1024), idesc_s, k > 0 ? 1u : 0u);
         }
-        tc::mma_commit(BAR(kSFull + st));
+        tc::mma_commit(BAR(kSFull + sb));
+        tc::mma_commit(BAR(kKEmpty + ks_i));
         return true;
       };
       if (ok && ntiles > 0) ok = issue_s(0);
       for (int j = 0; ok && j < ntiles; ++j) {
         if (*abort_flag) { ok = false; break; }
         if (j + 1 < ntiles && !issue_s(j + 1)) { ok = false; break; }
-        const int st = j & 1;
-        if (!tc::mbar_wait(BAR(kPFull + st), (j >> 1) & 1)) { ok = false; break; }
+        const int vb = j & 1;
+        if (!tc::mbar_wait(BAR(kPFull), j & 1)) { ok = false; break; }
+        if (!tc::mbar_wait(BAR(kVFull + vb), (j >> 1) & 1)) { ok = false; break; }
         tc::tc_fence_after();
-        const uint32_t ps = sbase + C::kOffP + st * C::kPBytes;
-        const uint32_t vs = sbase + C::kOffKV + st * C::kStageBytes + C::kTileBytes;
+        const uint32_t ps = sbase + C::kOffP;
+        const uint32_t vs = sbase + C::kOffV + vb * C::kTileBytes;
 #pragma unroll
         for (int k = 0; k < C::kBN / 16; ++k) {
           const uint32_t poff = (k >> 2) * (C::kBM * 128) + (k & 3) * 32;
@@ -337,8 +370,8 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
                           tc::smem_desc_sw128(vs + k * 16 * 128, C::kBN * 128, 1024), idesc_o,
                           (j > 0 || k > 0) ? 1u : 0u);
         }
-        tc::mma_commit(BAR(kPvDone + st));
-        tc::mma_commit(BAR(kKvEmpty + st));
+        tc::mma_commit(BAR(kPvDone));
+        tc::mma_commit(BAR(kVEmpty + vb));
       }
       if (!ok && !*abort_flag) fail();
       // Everything issued has completed before TMEM is released.
@@ -349,40 +382,60 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
     // ------------------------------------------------------------ K/V producer
     if (lane == 0) {
       tc::tma_prefetch_desc(&kv_map);
-      int issued = 0;
-      for (int j = 0; j < ntiles; ++j) {
-        if (*abort_flag) break;
-        const int st = j & 1;
-        if (j >= 2 && !tc::mbar_wait(BAR(kKvEmpty + st), ((j - 2) >> 1) & 1)) { fail(); break; }
+      // Issues the K (which = 0) or V (which = 1) tile j into `dst`.
+      auto issue = [&](int j, int which, uint32_t dst, uint32_t full) {
         const int tok0 = j * C::kBN;
         int blks[C::kBN / 16];
         uint32_t bytes = 0;
 #pragma unroll
         for (int p = 0; p < C::kBN / 16; ++p) {
           blks[p] = piece_block(tok0 + 16 * p);
-          if (blks[p] == -2) record_error(err, PA_DEVERR_BLOCK_ID);
-          if (blks[p] >= 0) bytes += 2u * C::kHalves * C::kPieceBytes;
+          if (blks[p] == -2 && which == 0) record_error(err, PA_DEVERR_BLOCK_ID);
+          if (blks[p] >= 0) bytes += C::kHalves * C::kPieceBytes;
         }
-        const uint32_t full = BAR(kKvFull + st);
         tc::mbar_arrive_expect_tx(full, bytes);
-        const uint32_t ks = sbase + C::kOffKV + st * C::kStageBytes;
-        const uint32_t vs = ks + C::kTileBytes;
 #pragma unroll
         for (int p = 0; p < C::kBN / 16; ++p) {
           if (blks[p] < 0) continue;
           const int off = (tok0 + 16 * p) % bs;
 #pragma unroll
-          for (int h = 0; h < C::kHalves; ++h) {
-            const uint32_t d = h * (C::kBN * 128) + p * C::kPieceBytes;
-            tc::tma_load_5d(ks + d, &kv_map, full, h * 64, kvh, off, 0, blks[p]);
-            tc::tma_load_5d(vs + d, &kv_map, full, h * 64, kvh, off, 1, blks[p]);
-          }
+          for (int h = 0; h < C::kHalves; ++h)
+            tc::tma_load_5d(dst + h * (C::kBN * 128) + p * C::kPieceBytes, &kv_map, full, h * 64,
+                            kvh, off, which, blks[p]);
         }
-        issued = j + 1;
+      };
+      auto issue_k = [&](int j) -> bool {
+        const int st = j % C::kKStages;
+        if (j >= C::kKStages &&
+            !tc::mbar_wait(BAR(kKEmpty + st), ((j / C::kKStages) - 1) & 1))
+          return false;
+        issue(j, 0, sbase + C::kOffK + st * C::kTileBytes, BAR(kKFull + st));
+        return true;
+      };
+      auto issue_v = [&](int j) -> bool {
+        const int st = j & 1;
+        if (j >= 2 && !tc::mbar_wait(BAR(kVEmpty + st), ((j >> 1) - 1) & 1)) return false;
+        issue(j, 1, sbase + C::kOffV + st * C::kTileBytes, BAR(kVFull + st));
+        return true;
+      };
+      int k_issued = 0, v_issued = 0;
+      bool ok = true;
+      for (; ok && k_issued < min(2, ntiles); ++k_issued) ok = issue_k(k_issued);
+      for (int j = 0; ok && j < ntiles; ++j) {
+        if (*abort_flag) break;
+        if (j + 2 < ntiles) {
+          if (!issue_k(j + 2)) { ok = false; break; }
+          k_issued = j + 3;
+        }
+        if (!issue_v(j)) { ok = false; break; }
+        v_issued = j + 1;
       }
+      if (!ok) fail();
       // No copy may still be landing when the CTA exits.
-      for (int j = max(0, issued - 2); j < issued; ++j)
-        if (!tc::mbar_wait(BAR(kKvFull + (j & 1)), (j >> 1) & 1)) fail();
+      for (int j = max(0, k_issued - C::kKStages); j < k_issued; ++j)
+        if (!tc::mbar_wait(BAR(kKFull + j % C::kKStages), (j / C::kKStages) & 1)) fail();
+      for (int j = max(0, v_issued - 2); j < v_issued; ++j)
+        if (!tc::mbar_wait(BAR(kVFull + (j & 1)), (j >> 1) & 1)) fail();
     }
   }
 
