@@ -211,26 +211,42 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
       for (int p = 0; p < C::kBN / 16; ++p) vm |= (piece_block(tok0 + 16 * p) >= 0 ? 1u : 0u) << p;
       if (!wait_warp(BAR(kSFull + sb), (j >> 1) & 1)) break;
       tc::tc_fence_after();
+      // Raw scores of this row: all four 32-column loads in flight at once.
       float s[C::kBN];
-      float mx = -CUDART_INF_F;
       {
         const uint32_t ta = tmem + lane_base + (sb ? C::kColS1 : C::kColS0);
+        uint32_t r[C::kBN / 32][32];
 #pragma unroll
-        for (int c = 0; c < C::kBN / 32; ++c) {
-          uint32_t r[32];
-          tc::tmem_ld32(ta + c * 32, r);
-          tc::tmem_wait_ld();
+        for (int c = 0; c < C::kBN / 32; ++c) tc::tmem_ld32(ta + c * 32, r[c]);
+        tc::tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int col = c * 32 + e;
-            const bool vis = (tok0 + col < lim) && ((vm >> (col >> 4)) & 1u);
-            s[col] = vis ? __uint_as_float(r[e]) * scale_log2 : -CUDART_INF_F;
-            mx = fmaxf(mx, s[col]);
-          }
-        }
+        for (int c = 0; c < C::kBN / 32; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[c][e]);
       }
       tc::tc_fence_before();
       tc::mbar_arrive(BAR(kSFree + sb));
+      // Mask only where some column is not visible (the diagonal tile, the
+      // end of the sequence, an unloaded piece).
+      if (!(tok0 + C::kBN <= lim && vm == (1u << (C::kBN / 16)) - 1u)) {
+#pragma unroll
+        for (int col = 0; col < C::kBN; ++col) {
+          const bool vis = (tok0 + col < lim) && ((vm >> (col >> 4)) & 1u);
+          s[col] = vis ? s[col] : -CUDART_INF_F;
+        }
+      }
+      // Row max over 8 independent chains (scale > 0, so max then scale).
+      float mx;
+      {
+        float m8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m8[k] = s[k];
+#pragma unroll
+        for (int col = 8; col < C::kBN; ++col) m8[col & 7] = fmaxf(m8[col & 7], s[col]);
+        mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        mx *= scale_log2;
+      }
 
       const float m_new = fmaxf(m_used, mx);
       const bool need = m_new > m_used + 8.f;
@@ -240,12 +256,16 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
       // P = exp2(s - m_used) in registers first (the P buffer may still be
       // in use by PV(j-1)).
       uint32_t pk[C::kBN / 2];
-      l *= alpha;
+      {
+        float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < C::kBN / 2; ++c) {
-        const float p0 = ex2(s[2 * c] - mu), p1 = ex2(s[2 * c + 1] - mu);
-        l += p0 + p1;
-        pk[c] = pack_bf16(p0, p1);
+        for (int c = 0; c < C::kBN / 2; ++c) {
+          const float p0 = ex2(fmaf(s[2 * c], scale_log2, -mu));
+          const float p1 = ex2(fmaf(s[2 * c + 1], scale_log2, -mu));
+          l8[c & 7] += p0 + p1;
+          pk[c] = pack_bf16(p0, p1);
+        }
+        l = l * alpha + (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
       }
       // PV(j-1) must be done before O is rescaled or the P buffer rewritten.
       if (j > 0 && !wait_warp(BAR(kPvDone), (j - 1) & 1)) break;
