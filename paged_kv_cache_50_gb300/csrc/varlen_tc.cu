@@ -16,8 +16,8 @@
 //              TMEM into the output;
 //   warp 4     MMA issue (one thread): S(j) = Q K(j)^T into one of two TMEM
 //              S buffers, O += P(j) V(j) into the TMEM O accumulator;
-//   warp 5     K/V producer (one thread): per 16-token piece of a cache block
-//              one TMA box per 64-column half, through the block table.
+//   warp 5     K/V producer: per 16-token piece of a cache block one TMA box
+//              per 64-column half, through the block table, one box per lane.
 // K and V travel in separate rings: a K stage is released as soon as S(j)
 // has been computed and a V stage once PV(j) has, and the producer runs K two
 // tiles ahead of V, so the loads of later tiles overlap the current softmax.
@@ -400,56 +400,54 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
     }
   } else {
     // ------------------------------------------------------------ K/V producer
-    if (lane == 0) {
-      tc::tma_prefetch_desc(&kv_map);
-      // Issues the K (which = 0) or V (which = 1) tile j into `dst`.
-      auto issue = [&](int j, int which, uint32_t dst, uint32_t full) {
-        const int tok0 = j * C::kBN;
-        int blks[C::kBN / 16];
-        uint32_t bytes = 0;
-#pragma unroll
-        for (int p = 0; p < C::kBN / 16; ++p) {
-          blks[p] = piece_block(tok0 + 16 * p);
-          if (blks[p] == -2 && which == 0) record_error(err, PA_DEVERR_BLOCK_ID);
-          if (blks[p] >= 0) bytes += C::kHalves * C::kPieceBytes;
-        }
-        tc::mbar_arrive_expect_tx(full, bytes);
-#pragma unroll
-        for (int p = 0; p < C::kBN / 16; ++p) {
-          if (blks[p] < 0) continue;
-          const int off = (tok0 + 16 * p) % bs;
-#pragma unroll
-          for (int h = 0; h < C::kHalves; ++h)
-            tc::tma_load_5d(dst + h * (C::kBN * 128) + p * C::kPieceBytes, &kv_map, full, h * 64,
-                            kvh, off, which, blks[p]);
-        }
-      };
-      auto issue_k = [&](int j) -> bool {
-        const int st = j % C::kKStages;
-        if (j >= C::kKStages &&
-            !tc::mbar_wait(BAR(kKEmpty + st), ((j / C::kKStages) - 1) & 1))
-          return false;
-        issue(j, 0, sbase + C::kOffK + st * C::kTileBytes, BAR(kKFull + st));
-        return true;
-      };
-      auto issue_v = [&](int j) -> bool {
-        const int st = j & 1;
-        if (j >= 2 && !tc::mbar_wait(BAR(kVEmpty + st), ((j >> 1) - 1) & 1)) return false;
-        issue(j, 1, sbase + C::kOffV + st * C::kTileBytes, BAR(kVFull + st));
-        return true;
-      };
-      int k_issued = 0, v_issued = 0;
-      bool ok = true;
-      for (; ok && k_issued < min(2, ntiles); ++k_issued) ok = issue_k(k_issued);
-      for (int j = 0; ok && j < ntiles; ++j) {
-        if (*abort_flag) break;
-        if (j + 2 < ntiles) {
-          if (!issue_k(j + 2)) { ok = false; break; }
-          k_issued = j + 3;
-        }
-        if (!issue_v(j)) { ok = false; break; }
-        v_issued = j + 1;
+    // The whole warp issues: lane p * halves + h loads 64-column half h of the
+    // tile's 16-token piece p, so a tile's boxes are issued in parallel.
+    if (lane == 0) tc::tma_prefetch_desc(&kv_map);
+    const int pc = lane / C::kHalves, hc = lane % C::kHalves;
+    const bool box_lane = lane < (C::kBN / 16) * C::kHalves;
+    auto issue = [&](int j, int which, uint32_t dst, uint32_t full) {
+      const int tok0 = j * C::kBN;
+      const int blk = box_lane ? piece_block(tok0 + 16 * pc) : -1;
+      const unsigned loaded = __ballot_sync(0xffffffffu, blk >= 0);
+      const unsigned bad = __ballot_sync(0xffffffffu, blk == -2);
+      if (lane == 0) {
+        if (bad != 0u && which == 0) record_error(err, PA_DEVERR_BLOCK_ID);
+        tc::mbar_arrive_expect_tx(full, static_cast<uint32_t>(__popc(loaded)) * C::kPieceBytes);
       }
+      __syncwarp();
+      if (blk >= 0)
+        tc::tma_load_5d(dst + hc * (C::kBN * 128) + pc * C::kPieceBytes, &kv_map, full, hc * 64,
+                        kvh, (tok0 + 16 * pc) % bs, which, blk);
+    };
+    auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, tc::mbar_wait(bar, parity));
+    };
+    auto issue_k = [&](int j) -> bool {
+      const int st = j % C::kKStages;
+      if (j >= C::kKStages && !wait_all(BAR(kKEmpty + st), ((j / C::kKStages) - 1) & 1))
+        return false;
+      issue(j, 0, sbase + C::kOffK + st * C::kTileBytes, BAR(kKFull + st));
+      return true;
+    };
+    auto issue_v = [&](int j) -> bool {
+      const int st = j & 1;
+      if (j >= 2 && !wait_all(BAR(kVEmpty + st), ((j >> 1) - 1) & 1)) return false;
+      issue(j, 1, sbase + C::kOffV + st * C::kTileBytes, BAR(kVFull + st));
+      return true;
+    };
+    int k_issued = 0, v_issued = 0;
+    bool ok = true;
+    for (; ok && k_issued < min(2, ntiles); ++k_issued) ok = issue_k(k_issued);
+    for (int j = 0; ok && j < ntiles; ++j) {
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+      if (j + 2 < ntiles) {
+        if (!issue_k(j + 2)) { ok = false; break; }
+        k_issued = j + 3;
+      }
+      if (!issue_v(j)) { ok = false; break; }
+      v_issued = j + 1;
+    }
+    if (lane == 0) {
       if (!ok) fail();
       // No copy may still be landing when the CTA exits.
       for (int j = max(0, k_issued - C::kKStages); j < k_issued; ++j)
