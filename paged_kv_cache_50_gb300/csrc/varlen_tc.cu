@@ -202,13 +202,15 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
       return w;
     };
     float m_used = -CUDART_INF_F, l = 0.f;
+    int piece_next = lane < C::kBN / 16 ? piece_block(16 * lane) : -1;
     for (int j = 0; j < ntiles; ++j) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
       const int sb = j & 1;
       const int tok0 = j * C::kBN;
-      uint32_t vm = 0;   // loaded pieces of this tile
-#pragma unroll
-      for (int p = 0; p < C::kBN / 16; ++p) vm |= (piece_block(tok0 + 16 * p) >= 0 ? 1u : 0u) << p;
+      // Loaded pieces of this tile (one table entry per lane, fetched during
+      // the previous tile) and the next tile's entries, fetched now.
+      const uint32_t vm = __ballot_sync(0xffffffffu, piece_next >= 0) & ((1u << (C::kBN / 16)) - 1u);
+      piece_next = lane < C::kBN / 16 ? piece_block(tok0 + C::kBN + 16 * lane) : -1;
       if (!wait_warp(BAR(kSFull + sb), (j >> 1) & 1)) break;
       tc::tc_fence_after();
       // Raw scores of this row: all four 32-column loads in flight at once.
