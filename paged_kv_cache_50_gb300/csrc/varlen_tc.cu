@@ -20,7 +20,8 @@
 //              per 64-column half, through the block table, one box per lane.
 // K and V travel in separate rings: a K stage is released as soon as S(j)
 // has been computed and a V stage once PV(j) has, and the producer runs K two
-// tiles ahead of V, so the loads of later tiles overlap the current softmax.
+// tiles ahead of V, so the loads of later tiles overlap the current softmax;
+// P is double-buffered, so the softmax of tile j+1 never waits for PV(j).
 // The MMA thread issues S(j+1) before waiting for P(j), so the tensor core
 // computes the next scores while the softmax warps work on the current ones.
 // O is rescaled (TMEM load, scale, store) only when a row's running max grows
@@ -29,9 +30,9 @@
 //
 // Shared memory (128-byte swizzled, 1024-byte aligned atoms):
 //   Q    [D/64 halves][128 rows][128 B]
-//   K    3 stages x [D/64 halves][128 tokens][128 B]
+//   K    2 stages x [D/64 halves][128 tokens][128 B]
 //   V    2 stages x [D/64 halves][128 tokens][128 B]
-//   P    [2 token halves][128 rows][128 B]
+//   P    2 buffers x [2 token halves][128 rows][128 B]
 // TMEM: S buffers at columns 0 and 128, O at 256 (512 columns allocated).
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -50,7 +51,7 @@ struct TcCfg {
   static constexpr int kBM = 128;                     // packed rows per CTA
   static constexpr int kBN = 128;                     // tokens per K/V tile
   static constexpr int kHalves = D / 64;              // 128-byte column groups of a row
-  static constexpr int kKStages = 3;
+  static constexpr int kKStages = 2;
   static constexpr int kVStages = 2;
   static constexpr int kQBytes = kBM * D * 2;
   static constexpr int kTileBytes = kBN * D * 2;      // one K (or V) tile
@@ -59,7 +60,7 @@ struct TcCfg {
   static constexpr int kOffK = kQBytes;
   static constexpr int kOffV = kOffK + kKStages * kTileBytes;
   static constexpr int kOffP = kOffV + kVStages * kTileBytes;
-  static constexpr int kOffBar = kOffP + kPBytes;
+  static constexpr int kOffBar = kOffP + 2 * kPBytes;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;   // barriers + alignment slack
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
@@ -79,16 +80,17 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Barriers; every pair is indexed by tile parity (stage or buffer j & 1).
 enum TcBar {
   kQFull = 0,
-  kKFull = 1,    // 3
-  kKEmpty = 4,   // 3
-  kVFull = 7,    // 2
-  kVEmpty = 9,   // 2
-  kSFull = 11,   // 2
-  kSFree = 13,   // 2
-  kPFull = 15,
-  kPvDone = 16,
+  kKFull = 1,
+  kKEmpty = 3,
+  kVFull = 5,
+  kVEmpty = 7,
+  kSFull = 9,
+  kSFree = 11,
+  kPFull = 13,
+  kPvDone = 15,
   kFinal = 17,
   kNumBars = 18
 };
@@ -134,18 +136,16 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
 
   if (threadIdx.x == 0) {
     tc::mbar_init(BAR(kQFull), 128);
-    for (int b = 0; b < C::kKStages; ++b) {
+    for (int b = 0; b < 2; ++b) {
       tc::mbar_init(BAR(kKFull + b), 1);
       tc::mbar_init(BAR(kKEmpty + b), 1);
-    }
-    for (int b = 0; b < 2; ++b) {
       tc::mbar_init(BAR(kVFull + b), 1);
       tc::mbar_init(BAR(kVEmpty + b), 1);
       tc::mbar_init(BAR(kSFull + b), 1);
       tc::mbar_init(BAR(kSFree + b), 128);
+      tc::mbar_init(BAR(kPFull + b), 128);
+      tc::mbar_init(BAR(kPvDone + b), 1);
     }
-    tc::mbar_init(BAR(kPFull), 128);
-    tc::mbar_init(BAR(kPvDone), 1);
     tc::mbar_init(BAR(kFinal), 1);
     *abort_flag = 0;
     tc::fence_barrier_init();
@@ -269,9 +269,11 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
         }
         l = l * alpha + (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
       }
-      // PV(j-1) must be done before O is rescaled or the P buffer rewritten.
-      if (j > 0 && !wait_warp(BAR(kPvDone), (j - 1) & 1)) break;
+      // P buffer sb was last read by PV(j-2); O may only be rescaled once
+      // PV(j-1) has landed.
+      if (j >= 2 && !wait_warp(BAR(kPvDone + sb), ((j >> 1) - 1) & 1)) break;
       if (__any_sync(0xffffffffu, need) && j > 0) {
+        if (!wait_warp(BAR(kPvDone + (sb ^ 1)), ((j - 1) >> 1) & 1)) break;
         tc::tc_fence_after();
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -286,7 +288,7 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
         tc::tmem_wait_st();
       }
       {
-        const uint32_t pbase = sbase + C::kOffP;
+        const uint32_t pbase = sbase + C::kOffP + sb * C::kPBytes;
 #pragma unroll
         for (int c8 = 0; c8 < C::kBN / 8; ++c8) {
           const uint32_t dst = pbase + (c8 >> 3) * (C::kBM * 128) + sw128(t, c8 & 7);
@@ -315,11 +317,11 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
       }
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
-      tc::mbar_arrive(BAR(kPFull));
+      tc::mbar_arrive(BAR(kPFull + sb));
     }
     // ------------------------------------------------------------ epilogue
     bool ok = !__any_sync(0xffffffffu, *abort_flag != 0) && ntiles > 0;
-    if (ok) ok = wait_warp(BAR(kPvDone), (ntiles - 1) & 1);
+    if (ok) ok = wait_warp(BAR(kPvDone + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1);
     tc::tc_fence_after();
     if (ok) {   // warp-uniform
       const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -358,8 +360,8 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
       bool ok = ntiles == 0 || tc::mbar_wait(BAR(kQFull), 0);
       if (!ok) fail();
       auto issue_s = [&](int j) -> bool {
-        const int ks_i = j % C::kKStages, sb = j & 1;
-        if (!tc::mbar_wait(BAR(kKFull + ks_i), (j / C::kKStages) & 1)) return false;
+        const int ks_i = j & 1, sb = j & 1;
+        if (!tc::mbar_wait(BAR(kKFull + ks_i), (j >> 1) & 1)) return false;
         if (j >= 2 && !tc::mbar_wait(BAR(kSFree + sb), ((j - 2) >> 1) & 1)) return false;
         tc::tc_fence_after();
         const uint32_t ks = sbase + C::kOffK + ks_i * C::kTileBytes;
@@ -380,10 +382,10 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
         if (*abort_flag) { ok = false; break; }
         if (j + 1 < ntiles && !issue_s(j + 1)) { ok = false; break; }
         const int vb = j & 1;
-        if (!tc::mbar_wait(BAR(kPFull), j & 1)) { ok = false; break; }
+        if (!tc::mbar_wait(BAR(kPFull + vb), (j >> 1) & 1)) { ok = false; break; }
         if (!tc::mbar_wait(BAR(kVFull + vb), (j >> 1) & 1)) { ok = false; break; }
         tc::tc_fence_after();
-        const uint32_t ps = sbase + C::kOffP;
+        const uint32_t ps = sbase + C::kOffP + vb * C::kPBytes;
         const uint32_t vs = sbase + C::kOffV + vb * C::kTileBytes;
 #pragma unroll
         for (int k = 0; k < C::kBN / 16; ++k) {
@@ -392,7 +394,7 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
                           tc::smem_desc_sw128(vs + k * 16 * 128, C::kBN * 128, 1024), idesc_o,
                           (j > 0 || k > 0) ? 1u : 0u);
         }
-        tc::mma_commit(BAR(kPvDone));
+        tc::mma_commit(BAR(kPvDone + vb));
         tc::mma_commit(BAR(kVEmpty + vb));
       }
       if (!ok && !*abort_flag) fail();
@@ -403,13 +405,17 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
   } else {
     // ------------------------------------------------------------ K/V producer
     // The whole warp issues: lane p * halves + h loads 64-column half h of the
-    // tile's 16-token piece p, so a tile's boxes are issued in parallel.
+    // tile's 16-token piece p, so a tile's boxes are issued in parallel.  The
+    // lane's block ids are fetched a tile ahead; V(j) goes out before K(j+2)
+    // (PV(j) needs it first) and reuses K(j)'s block ids.
     if (lane == 0) tc::tma_prefetch_desc(&kv_map);
     const int pc = lane / C::kHalves, hc = lane % C::kHalves;
     const bool box_lane = lane < (C::kBN / 16) * C::kHalves;
-    auto issue = [&](int j, int which, uint32_t dst, uint32_t full) {
+    auto block_of = [&](int j) -> int {
+      return (box_lane && j < ntiles) ? piece_block(j * C::kBN + 16 * pc) : -1;
+    };
+    auto issue = [&](int j, int blk, int which, uint32_t dst, uint32_t full) {
       const int tok0 = j * C::kBN;
-      const int blk = box_lane ? piece_block(tok0 + 16 * pc) : -1;
       const unsigned loaded = __ballot_sync(0xffffffffu, blk >= 0);
       const unsigned bad = __ballot_sync(0xffffffffu, blk == -2);
       if (lane == 0) {
@@ -424,36 +430,42 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
     auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, tc::mbar_wait(bar, parity));
     };
-    auto issue_k = [&](int j) -> bool {
-      const int st = j % C::kKStages;
-      if (j >= C::kKStages && !wait_all(BAR(kKEmpty + st), ((j / C::kKStages) - 1) & 1))
-        return false;
-      issue(j, 0, sbase + C::kOffK + st * C::kTileBytes, BAR(kKFull + st));
+    // K(j) and V(j) go to stage j & 1; stage reuse waits for S(j-2) / PV(j-2).
+    auto issue_k = [&](int j, int blk) -> bool {
+      const int st = j & 1;
+      if (j >= 2 && !wait_all(BAR(kKEmpty + st), ((j >> 1) - 1) & 1)) return false;
+      issue(j, blk, 0, sbase + C::kOffK + st * C::kTileBytes, BAR(kKFull + st));
       return true;
     };
-    auto issue_v = [&](int j) -> bool {
+    auto issue_v = [&](int j, int blk) -> bool {
       const int st = j & 1;
       if (j >= 2 && !wait_all(BAR(kVEmpty + st), ((j >> 1) - 1) & 1)) return false;
-      issue(j, 1, sbase + C::kOffV + st * C::kTileBytes, BAR(kVFull + st));
+      issue(j, blk, 1, sbase + C::kOffV + st * C::kTileBytes, BAR(kVFull + st));
       return true;
     };
+    int b0 = block_of(0), b1 = block_of(1), b2 = block_of(2);   // tiles j, j+1, j+2
     int k_issued = 0, v_issued = 0;
     bool ok = true;
-    for (; ok && k_issued < min(2, ntiles); ++k_issued) ok = issue_k(k_issued);
+    if (ntiles > 0) { ok = issue_k(0, b0); k_issued = 1; }
+    if (ok && ntiles > 1) { ok = issue_k(1, b1); k_issued = 2; }
     for (int j = 0; ok && j < ntiles; ++j) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+      if (!issue_v(j, b0)) { ok = false; break; }
+      v_issued = j + 1;
+      const int b3 = block_of(j + 3);   // in flight while K(j+2) waits for its stage
       if (j + 2 < ntiles) {
-        if (!issue_k(j + 2)) { ok = false; break; }
+        if (!issue_k(j + 2, b2)) { ok = false; break; }
         k_issued = j + 3;
       }
-      if (!issue_v(j)) { ok = false; break; }
-      v_issued = j + 1;
+      b0 = b1;
+      b1 = b2;
+      b2 = b3;
     }
     if (lane == 0) {
       if (!ok) fail();
       // No copy may still be landing when the CTA exits.
-      for (int j = max(0, k_issued - C::kKStages); j < k_issued; ++j)
-        if (!tc::mbar_wait(BAR(kKFull + j % C::kKStages), (j / C::kKStages) & 1)) fail();
+      for (int j = max(0, k_issued - 2); j < k_issued; ++j)
+        if (!tc::mbar_wait(BAR(kKFull + (j & 1)), (j >> 1) & 1)) fail();
       for (int j = max(0, v_issued - 2); j < v_issued; ++j)
         if (!tc::mbar_wait(BAR(kVFull + (j & 1)), (j >> 1) & 1)) fail();
     }
