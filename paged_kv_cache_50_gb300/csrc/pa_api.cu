@@ -183,7 +183,7 @@ pa_status pa_mla_decode(const void* q, const void* kv_cache, const int32_t* bloc
   if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(workspace, 4) || !aligned(out, 2) ||
       !aligned(lse, 4))
     return PA_ERR_INVALID;
-  return from_cuda(pa::launch_mla_decode(q, kv_cache, block_table, seq_lens, batch, num_heads,
+  return from_cuda(pa::launch_mla_tc(q, kv_cache, block_table, seq_lens, batch, num_heads,
                                          block_size, num_blocks, max_blocks_per_seq, scale,
                                          num_splits,
                                          static_cast<int>(pa::split_chunk(max_seq_len, num_splits,

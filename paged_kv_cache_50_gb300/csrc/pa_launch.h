@@ -34,7 +34,13 @@ cudaError_t launch_varlen_tc(const void* q, const void* cache, const int32_t* bl
                              float scale, int causal, void* out, float* lse, int* err,
                              cudaStream_t stream);
 
-// MLA stage 1 + merge.
+// MLA stage 1 on tcgen05 tensor cores + merge.
+cudaError_t launch_mla_tc(const void* q, const void* cache, const int32_t* block_table,
+                          const int32_t* seq_lens, int B, int H, int bs, int num_blocks,
+                          int max_blocks, float scale, int S, int chunk, float* ws, void* out,
+                          float* lse, int* err, cudaStream_t stream);
+
+// MLA stage 1 (warp-level mma) + merge.
 cudaError_t launch_mla_decode(const void* q, const void* cache, const int32_t* block_table,
                               const int32_t* seq_lens, int B, int H, int bs, int num_blocks,
                               int max_blocks, float scale, int S, int chunk, float* ws, void* out,
