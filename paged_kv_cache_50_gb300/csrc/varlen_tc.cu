@@ -95,7 +95,7 @@ enum TcBar {
   kNumBars = 18
 };
 
-template <int D>
+template <int D, int CL>
 __global__ void __launch_bounds__(192, 1)
 varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16* __restrict__ q,
                  const int32_t* __restrict__ block_table, const int32_t* __restrict__ qsl,
@@ -108,20 +108,22 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t* sgen = smem_raw + (sbase - raw);
 
-  // A kernel that already gave up a wait leaves the rest of the grid to exit
-  // at once instead of timing out CTA after CTA.
-  if (err != nullptr && (*reinterpret_cast<volatile int*>(err) & PA_DEVERR_TIMEOUT)) return;
   const int i = blockIdx.z, kvh = blockIdx.y;
   const int qt = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);  // heavy tiles first
+  // The CL CTAs of a cluster take CL consecutive q tiles of the same request
+  // and kv head and share every K/V tile: each CTA gathers 1/CL of a tile's
+  // boxes and the TMA multicasts them into all CL CTAs.
+  const int rank = CL > 1 ? static_cast<int>(tc::cluster_rank()) : 0;
+  const int qt_hi = qt + rank, qt_lo = qt_hi - (CL - 1);
   const int grp = Hq / Hkv;
   const int q0 = qsl[i];
   const int qlen = qsl[i + 1] - q0;
   const int rows_total = qlen * grp;
-  const int row0 = qt * C::kBM;
-  if (row0 >= rows_total) return;
+  if (qt_lo * C::kBM >= rows_total) return;   // the whole cluster is idle
+  const int row0 = qt * C::kBM;                // this CTA's rows (may all be past the end)
   const int seq = seq_lens[i];
   const int ctx = seq - qlen;
-  const int last_row = min(row0 + C::kBM, rows_total) - 1;
+  const int last_row = min((qt_hi + 1) * C::kBM, rows_total) - 1;   // the cluster's last row
   int kv_end = causal ? ctx + last_row / grp + 1 : seq;
   kv_end = max(0, min(kv_end, seq));
   const int ntiles = (kv_end + C::kBN - 1) / C::kBN;
@@ -138,9 +140,9 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
     tc::mbar_init(BAR(kQFull), 128);
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(BAR(kKFull + b), 1);
-      tc::mbar_init(BAR(kKEmpty + b), 1);
+      tc::mbar_init(BAR(kKEmpty + b), CL);   // released by every CTA of the cluster
       tc::mbar_init(BAR(kVFull + b), 1);
-      tc::mbar_init(BAR(kVEmpty + b), 1);
+      tc::mbar_init(BAR(kVEmpty + b), CL);
       tc::mbar_init(BAR(kSFull + b), 1);
       tc::mbar_init(BAR(kSFree + b), 128);
       tc::mbar_init(BAR(kPFull + b), 128);
@@ -153,9 +155,20 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
   __syncwarp();
   if (warp == 0) tc::tmem_alloc(tmem_slot, C::kTmemCols);
   tc::tc_fence_before();
-  __syncthreads();
+  // Every barrier of the cluster is initialised before any CTA multicasts.
+  if (CL > 1)
+    tc::cluster_sync();
+  else
+    __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sgen + C::kOffBar + 8 * kNumBars);
+  constexpr uint16_t kMask = static_cast<uint16_t>((1u << CL) - 1u);
+  auto release = [&](uint32_t bar) {   // frees a K/V stage in every CTA of the cluster
+    if (CL > 1)
+      tc::mma_commit_mc(bar, kMask);
+    else
+      tc::mma_commit(bar);
+  };
 
   auto fail = [&]() {
     record_error(err, PA_DEVERR_TIMEOUT);
@@ -374,7 +387,7 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
                           tc::smem_desc_sw128(ks + koff, 16, 1024), idesc_s, k > 0 ? 1u : 0u);
         }
         tc::mma_commit(BAR(kSFull + sb));
-        tc::mma_commit(BAR(kKEmpty + ks_i));
+        release(BAR(kKEmpty + ks_i));
         return true;
       };
       if (ok && ntiles > 0) ok = issue_s(0);
@@ -395,7 +408,7 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
                           (j > 0 || k > 0) ? 1u : 0u);
         }
         tc::mma_commit(BAR(kPvDone + vb));
-        tc::mma_commit(BAR(kVEmpty + vb));
+        release(BAR(kVEmpty + vb));
       }
       if (!ok && !*abort_flag) fail();
       // Everything issued has completed before TMEM is released.
@@ -404,13 +417,15 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
     }
   } else {
     // ------------------------------------------------------------ K/V producer
-    // The whole warp issues: lane p * halves + h loads 64-column half h of the
-    // tile's 16-token piece p, so a tile's boxes are issued in parallel.  The
-    // lane's block ids are fetched a tile ahead; V(j) goes out before K(j+2)
-    // (PV(j) needs it first) and reuses K(j)'s block ids.
+    // Lane p looks after the tile's 16-token piece p: its block id (fetched a
+    // tile ahead) and, if p % CL is this CTA's rank, its TMA boxes (one per
+    // 64-column half), multicast to the whole cluster.  Every CTA expects
+    // the bytes of all loaded pieces on its own barrier.  V(j) goes out before
+    // K(j+2) (PV(j) needs it first) and reuses K(j)'s block ids.
     if (lane == 0) tc::tma_prefetch_desc(&kv_map);
-    const int pc = lane / C::kHalves, hc = lane % C::kHalves;
-    const bool box_lane = lane < (C::kBN / 16) * C::kHalves;
+    const int pc = lane;
+    const bool box_lane = lane < C::kBN / 16;
+    const bool my_piece = box_lane && (pc % CL) == rank;
     auto block_of = [&](int j) -> int {
       return (box_lane && j < ntiles) ? piece_block(j * C::kBN + 16 * pc) : -1;
     };
@@ -419,13 +434,22 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
       const unsigned loaded = __ballot_sync(0xffffffffu, blk >= 0);
       const unsigned bad = __ballot_sync(0xffffffffu, blk == -2);
       if (lane == 0) {
-        if (bad != 0u && which == 0) record_error(err, PA_DEVERR_BLOCK_ID);
-        tc::mbar_arrive_expect_tx(full, static_cast<uint32_t>(__popc(loaded)) * C::kPieceBytes);
+        if (bad != 0u && which == 0 && rank == 0) record_error(err, PA_DEVERR_BLOCK_ID);
+        tc::mbar_arrive_expect_tx(
+            full, static_cast<uint32_t>(__popc(loaded)) * C::kHalves * C::kPieceBytes);
       }
       __syncwarp();
-      if (blk >= 0)
-        tc::tma_load_5d(dst + hc * (C::kBN * 128) + pc * C::kPieceBytes, &kv_map, full, hc * 64,
-                        kvh, (tok0 + 16 * pc) % bs, which, blk);
+      if (my_piece && blk >= 0) {
+#pragma unroll
+        for (int h = 0; h < C::kHalves; ++h) {
+          const uint32_t d = dst + h * (C::kBN * 128) + pc * C::kPieceBytes;
+          if (CL > 1)
+            tc::tma_load_5d_mc(d, &kv_map, full, kMask, h * 64, kvh, (tok0 + 16 * pc) % bs, which,
+                               blk);
+          else
+            tc::tma_load_5d(d, &kv_map, full, h * 64, kvh, (tok0 + 16 * pc) % bs, which, blk);
+        }
+      }
     };
     auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, tc::mbar_wait(bar, parity));
@@ -477,6 +501,9 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, C::kTmemCols);
   }
+  // No CTA leaves while a peer may still multicast into its shared memory or
+  // arrive on its barriers.
+  if (CL > 1) tc::cluster_sync();
 }
 
 // ---------------------------------------------------------------- host side
@@ -516,7 +543,7 @@ bool make_kv_map(CUtensorMap* map, const void* cache, int nb, int bs, int Hkv, i
 
 }  // namespace
 
-template <int D>
+template <int D, int CL>
 static cudaError_t launch_varlen_tc_t(const void* q, const void* cache, const int32_t* block_table,
                                       const int32_t* qsl, const int32_t* seq_lens, int N, int Hq,
                                       int Hkv, int bs, int num_blocks, int max_blocks,
@@ -525,17 +552,32 @@ static cudaError_t launch_varlen_tc_t(const void* q, const void* cache, const in
   using C = TcCfg<D>;
   CUtensorMap map;
   if (!make_kv_map(&map, cache, num_blocks, bs, Hkv, D)) return cudaErrorInvalidValue;
-  auto kern = varlen_tc_kernel<D>;
+  auto kern = varlen_tc_kernel<D, CL>;
   static DeviceFlags attr_set;
   cudaError_t e = set_smem_once(kern, C::kSmemBytes, attr_set);
   if (e != cudaSuccess) return e;
   const long long rows = static_cast<long long>(max_query_len) * (Hq / Hkv);
-  dim3 grid(static_cast<unsigned>((rows + C::kBM - 1) / C::kBM), Hkv, N);
-  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(
-      map, static_cast<const __nv_bfloat16*>(q), block_table, qsl, seq_lens, max_blocks, Hq, Hkv,
-      bs, num_blocks, scale * kLog2e, causal, static_cast<__nv_bfloat16*>(out), lse, err);
-  return cudaGetLastError();
+  long long tiles = (rows + C::kBM - 1) / C::kBM;
+  tiles = (tiles + CL - 1) / CL * CL;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(tiles), Hkv, N);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, map, static_cast<const __nv_bfloat16*>(q), block_table,
+                            qsl, seq_lens, max_blocks, Hq, Hkv, bs, num_blocks, scale * kLog2e,
+                            causal, static_cast<__nv_bfloat16*>(out), lse, err);
 }
+
+// CTAs per cluster sharing K/V tiles by multicast.
+constexpr int kVarlenCluster = 4;
 
 cudaError_t launch_varlen_tc(const void* q, const void* cache, const int32_t* block_table,
                              const int32_t* qsl, const int32_t* seq_lens, int N, int Hq, int Hkv,
@@ -543,10 +585,10 @@ cudaError_t launch_varlen_tc(const void* q, const void* cache, const int32_t* bl
                              float scale, int causal, void* out, float* lse, int* err,
                              cudaStream_t stream) {
   if (d == 128)
-    return launch_varlen_tc_t<128>(q, cache, block_table, qsl, seq_lens, N, Hq, Hkv, bs,
+    return launch_varlen_tc_t<128, kVarlenCluster>(q, cache, block_table, qsl, seq_lens, N, Hq, Hkv, bs,
                                    num_blocks, max_blocks, max_query_len, scale, causal, out, lse,
                                    err, stream);
-  return launch_varlen_tc_t<64>(q, cache, block_table, qsl, seq_lens, N, Hq, Hkv, bs, num_blocks,
+  return launch_varlen_tc_t<64, kVarlenCluster>(q, cache, block_table, qsl, seq_lens, N, Hq, Hkv, bs, num_blocks,
                                 max_blocks, max_query_len, scale, causal, out, lse, err, stream);
 }
 
