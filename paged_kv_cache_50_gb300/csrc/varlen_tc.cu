@@ -5,35 +5,36 @@
 // section 2.1) with the FlashAttention tiling and online softmax of section
 // 4.1.
 //
-// CTA = (tile of 128 packed rows, kv head, request); a packed row is one
-// (query row, q head of the kv group) pair, so the Hq/Hkv heads sharing a kv
-// head share every K/V tile.  Warp roles (192 threads):
-//   warps 0-3  softmax: thread t owns packed row t = TMEM lane t.  Loads its
-//              Q row into shared memory, then per 128-token tile reads its
-//              S row from TMEM (tcgen05.ld), masks (causal, bottom-right),
-//              runs the online softmax in the log2 domain, writes its P row
-//              (bf16) to shared memory, and finally scales its O row out of
-//              TMEM into the output;
-//   warp 4     MMA issue (one thread): S(j) = Q K(j)^T into one of two TMEM
-//              S buffers, O += P(j) V(j) into the TMEM O accumulator;
-//   warp 5     K/V producer: per 16-token piece of a cache block one TMA box
-//              per 64-column half, through the block table, one box per lane.
-// K and V travel in separate rings: a K stage is released as soon as S(j)
-// has been computed and a V stage once PV(j) has, and the producer runs K two
-// tiles ahead of V, so the loads of later tiles overlap the current softmax;
-// P is double-buffered, so the softmax of tile j+1 never waits for PV(j).
-// The MMA thread issues S(j+1) before waiting for P(j), so the tensor core
-// computes the next scores while the softmax warps work on the current ones.
-// O is rescaled (TMEM load, scale, store) only when a row's running max grows
-// by more than 2^8; otherwise P keeps the older reference max, which keeps
-// the final O / l exact.
+// CTA = (256 packed rows as two Q tiles of 128, kv head, request); a packed
+// row is one (query row, q head of the kv group) pair, so the Hq/Hkv heads
+// sharing a kv head share every K/V tile.  Warp roles (384 threads):
+//   warps 0-3 / 4-7  two softmax warpgroups, one per Q tile: thread t of a
+//              group owns row t of its tile = TMEM lane t.  Per 128-token K/V
+//              tile it reads its S row from TMEM, masks (causal,
+//              bottom-right), runs the online softmax in the log2 domain and
+//              writes its P row (bf16, two per 32-bit column) back into TMEM
+//              over the S row it came from;
+//   warp 8     MMA issue (one thread): S_x(j) = Q_x K(j)^T, then
+//              O_x += P_x(j) V(j) with the A operand (P) read from TMEM;
+//   warp 9     K/V producer: per 16-token piece of a cache block one TMA box
+//              per 64-column half, through the block table;
+//   warps 10-11 idle (they complete the third warpgroup, which hands its
+//              registers to the softmax warpgroups).
+// The two Q tiles interleave on the tensor core: PV_0(j), S_0(j+1),
+// PV_1(j), S_1(j+1), ... so each softmax warpgroup works on one tile while
+// the MMAs of the other proceed.  The tensor pipe runs in issue order, so
+// once S_x(j) has landed PV_x(j-1) has too: the softmax may rescale O_x (TMEM
+// load, scale, store) without another wait; it does so only when a row's
+// running max grows by more than 2^8 (P keeps the older reference max
+// otherwise, which keeps O / l exact).
+// Clusters of CL CTAs (consecutive q tiles of one request and kv head) share
+// every K/V tile: each CTA gathers 1/CL of the boxes and the TMA multicasts
+// them to all; a stage is released cluster-wide by a multicast tcgen05.commit.
 //
 // Shared memory (128-byte swizzled, 1024-byte aligned atoms):
-//   Q    [D/64 halves][128 rows][128 B]
-//   K    2 stages x [D/64 halves][128 tokens][128 B]
-//   V    2 stages x [D/64 halves][128 tokens][128 B]
-//   P    2 buffers x [2 token halves][128 rows][128 B]
-// TMEM: S buffers at columns 0 and 128, O at 256 (512 columns allocated).
+//   Q    2 tiles x [D/64 halves][128 rows][128 B]
+//   K, V 2 stages each x [D/64 halves][128 tokens][128 B]
+// TMEM (512 columns): S_0/P_0 at 0, S_1/P_1 at 128, O_0 at 256, O_1 at 384.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math_constants.h>
@@ -48,24 +49,27 @@ namespace pa {
 
 template <int D>
 struct TcCfg {
-  static constexpr int kBM = 128;                     // packed rows per CTA
+  static constexpr int kBM = 128;                     // rows per Q tile
+  static constexpr int kRows = 2 * kBM;               // packed rows per CTA
   static constexpr int kBN = 128;                     // tokens per K/V tile
   static constexpr int kHalves = D / 64;              // 128-byte column groups of a row
-  static constexpr int kKStages = 2;
-  static constexpr int kVStages = 2;
-  static constexpr int kQBytes = kBM * D * 2;
+  static constexpr int kQBytes = kBM * D * 2;         // one Q tile
   static constexpr int kTileBytes = kBN * D * 2;      // one K (or V) tile
-  static constexpr int kPBytes = kBM * kBN * 2;
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kQBytes;
-  static constexpr int kOffV = kOffK + kKStages * kTileBytes;
-  static constexpr int kOffP = kOffV + kVStages * kTileBytes;
-  static constexpr int kOffBar = kOffP + 2 * kPBytes;
+  static constexpr int kOffK = 2 * kQBytes;
+  static constexpr int kOffV = kOffK + 2 * kTileBytes;
+  static constexpr int kOffBar = kOffV + 2 * kTileBytes;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;   // barriers + alignment slack
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
-  static constexpr int kThreads = 192;
+  static constexpr int kThreads = 384;
+  // Registers per thread: softmax warpgroups 0-1 raise theirs, warpgroup 2
+  // (MMA issue, producer, two idle warps) lowers its own.  The launch must
+  // hold at least 256 * kRegSoftmax + 128 * kRegOther registers.
+  static constexpr uint32_t kRegSoftmax = 216;
+  static constexpr uint32_t kRegOther = 56;
   static constexpr int kPieceBytes = 16 * 128;        // one TMA box: 16 rows x 128 B
+  __host__ __device__ static constexpr uint32_t col_s(int x) { return 128u * x; }
+  __host__ __device__ static constexpr uint32_t col_o(int x) { return 256u + 128u * x; }
 };
 
 // Byte offset of 16-byte chunk `c` (0..7) of row `r` in a 128-byte swizzled
@@ -80,23 +84,22 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Barriers; every pair is indexed by tile parity (stage or buffer j & 1).
+// Barriers; pairs are indexed by stage (j & 1) or by Q tile x.
 enum TcBar {
   kQFull = 0,
   kKFull = 1,
   kKEmpty = 3,
   kVFull = 5,
   kVEmpty = 7,
-  kSFull = 9,
-  kSFree = 11,
-  kPFull = 13,
-  kPvDone = 15,
-  kFinal = 17,
-  kNumBars = 18
+  kSFull = 9,    // [x]
+  kPFull = 11,   // [x]
+  kODone = 13,   // [x]
+  kFinal = 15,
+  kNumBars = 16
 };
 
 template <int D, int CL>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(384, 1)
 varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16* __restrict__ q,
                  const int32_t* __restrict__ block_table, const int32_t* __restrict__ qsl,
                  const int32_t* __restrict__ seq_lens, int max_blocks, int Hq, int Hkv, int bs,
@@ -110,20 +113,17 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
 
   const int i = blockIdx.z, kvh = blockIdx.y;
   const int qt = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);  // heavy tiles first
-  // The CL CTAs of a cluster take CL consecutive q tiles of the same request
-  // and kv head and share every K/V tile: each CTA gathers 1/CL of a tile's
-  // boxes and the TMA multicasts them into all CL CTAs.
   const int rank = CL > 1 ? static_cast<int>(tc::cluster_rank()) : 0;
-  const int qt_hi = qt + rank, qt_lo = qt_hi - (CL - 1);
+  const int qt_hi = qt + rank, qt_lo = qt_hi - (CL - 1);   // the cluster's CTA tiles
   const int grp = Hq / Hkv;
   const int q0 = qsl[i];
   const int qlen = qsl[i + 1] - q0;
   const int rows_total = qlen * grp;
-  if (qt_lo * C::kBM >= rows_total) return;   // the whole cluster is idle
-  const int row0 = qt * C::kBM;                // this CTA's rows (may all be past the end)
+  if (qt_lo * C::kRows >= rows_total) return;   // the whole cluster is idle
+  const int row0 = qt * C::kRows;               // this CTA's rows (may all be past the end)
   const int seq = seq_lens[i];
   const int ctx = seq - qlen;
-  const int last_row = min((qt_hi + 1) * C::kBM, rows_total) - 1;   // the cluster's last row
+  const int last_row = min((qt_hi + 1) * C::kRows, rows_total) - 1;   // the cluster's last row
   int kv_end = causal ? ctx + last_row / grp + 1 : seq;
   kv_end = max(0, min(kv_end, seq));
   const int ntiles = (kv_end + C::kBN - 1) / C::kBN;
@@ -137,16 +137,15 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + C::kOffBar + 8 * kNumBars + 8);
 
   if (threadIdx.x == 0) {
-    tc::mbar_init(BAR(kQFull), 128);
+    tc::mbar_init(BAR(kQFull), C::kRows);
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(BAR(kKFull + b), 1);
       tc::mbar_init(BAR(kKEmpty + b), CL);   // released by every CTA of the cluster
       tc::mbar_init(BAR(kVFull + b), 1);
       tc::mbar_init(BAR(kVEmpty + b), CL);
       tc::mbar_init(BAR(kSFull + b), 1);
-      tc::mbar_init(BAR(kSFree + b), 128);
-      tc::mbar_init(BAR(kPFull + b), 128);
-      tc::mbar_init(BAR(kPvDone + b), 1);
+      tc::mbar_init(BAR(kPFull + b), C::kBM);
+      tc::mbar_init(BAR(kODone + b), 1);
     }
     tc::mbar_init(BAR(kFinal), 1);
     *abort_flag = 0;
@@ -169,7 +168,6 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
     else
       tc::mma_commit(bar);
   };
-
   auto fail = [&]() {
     record_error(err, PA_DEVERR_TIMEOUT);
     *abort_flag = 1;
@@ -183,10 +181,16 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
     return (blk >= 0 && blk < num_blocks) ? blk : -2;
   };
 
-  if (warp < 4) {
+  if (warp < 8)
+    tc::reg_alloc<C::kRegSoftmax>();
+  else
+    tc::reg_dealloc<C::kRegOther>();
+
+  if (warp < 8) {
     // ------------------------------------------------------------ softmax
-    const int t = threadIdx.x;
-    const int pr = row0 + t;
+    const int x = warp >> 2;                 // Q tile of this warpgroup
+    const int t = threadIdx.x & 127;         // row within the tile = TMEM lane
+    const int pr = row0 + x * C::kBM + t;
     const bool valid = pr < rows_total;
     const int qi = valid ? pr / grp : 0;
     const int hh = valid ? pr % grp : 0;
@@ -195,10 +199,11 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
     lim = max(0, min(lim, seq));
     {
       const uint4* src = reinterpret_cast<const uint4*>(q + qoff);
+      const uint32_t qb = sbase + C::kOffQ + x * C::kQBytes;
 #pragma unroll
       for (int c = 0; c < D / 8; ++c) {
         uint4 v = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-        const uint32_t dst = sbase + C::kOffQ + (c >> 3) * (C::kBM * 128) + sw128(t, c & 7);
+        const uint32_t dst = qb + (c >> 3) * (C::kBM * 128) + sw128(t, c & 7);
         asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v.x), "r"(v.y),
                      "r"(v.z), "r"(v.w)
                      : "memory");
@@ -206,7 +211,8 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(BAR(kQFull));
     }
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t ts = tmem + lane_base + C::col_s(x), to = tmem + lane_base + C::col_o(x);
     // TMEM loads and stores are warp-collective: every decision to skip or
     // stop is taken for the whole warp.
     auto wait_warp = [&](uint32_t b, uint32_t parity) -> bool {
@@ -218,29 +224,24 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
     int piece_next = lane < C::kBN / 16 ? piece_block(16 * lane) : -1;
     for (int j = 0; j < ntiles; ++j) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-      const int sb = j & 1;
       const int tok0 = j * C::kBN;
       // Loaded pieces of this tile (one table entry per lane, fetched during
       // the previous tile) and the next tile's entries, fetched now.
       const uint32_t vm = __ballot_sync(0xffffffffu, piece_next >= 0) & ((1u << (C::kBN / 16)) - 1u);
       piece_next = lane < C::kBN / 16 ? piece_block(tok0 + C::kBN + 16 * lane) : -1;
-      if (!wait_warp(BAR(kSFull + sb), (j >> 1) & 1)) break;
+      if (!wait_warp(BAR(kSFull + x), j & 1)) break;
       tc::tc_fence_after();
-      // Raw scores of this row: all four 32-column loads in flight at once.
       float s[C::kBN];
       {
-        const uint32_t ta = tmem + lane_base + (sb ? C::kColS1 : C::kColS0);
         uint32_t r[C::kBN / 32][32];
 #pragma unroll
-        for (int c = 0; c < C::kBN / 32; ++c) tc::tmem_ld32(ta + c * 32, r[c]);
+        for (int c = 0; c < C::kBN / 32; ++c) tc::tmem_ld32(ts + c * 32, r[c]);
         tc::tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < C::kBN / 32; ++c)
 #pragma unroll
           for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[c][e]);
       }
-      tc::tc_fence_before();
-      tc::mbar_arrive(BAR(kSFree + sb));
       // Mask only where some column is not visible (the diagonal tile, the
       // end of the sequence, an unloaded piece).
       if (!(tok0 + C::kBN <= lim && vm == (1u << (C::kBN / 16)) - 1u)) {
@@ -250,7 +251,6 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
           s[col] = vis ? s[col] : -CUDART_INF_F;
         }
       }
-      // Row max over 8 independent chains (scale > 0, so max then scale).
       float mx;
       {
         float m8[8];
@@ -262,63 +262,53 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
                    fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
         mx *= scale_log2;
       }
-
       const float m_new = fmaxf(m_used, mx);
       const bool need = m_new > m_used + 8.f;
       const float alpha = need ? ex2(m_used - m_new) : 1.f;
       if (need) m_used = m_new;
       const float mu = m_used == -CUDART_INF_F ? 0.f : m_used;
-      // P = exp2(s - m_used) in registers first (the P buffer may still be
-      // in use by PV(j-1)).
-      uint32_t pk[C::kBN / 2];
-      {
-        float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int c = 0; c < C::kBN / 2; ++c) {
-          const float p0 = ex2(fmaf(s[2 * c], scale_log2, -mu));
-          const float p1 = ex2(fmaf(s[2 * c + 1], scale_log2, -mu));
-          l8[c & 7] += p0 + p1;
-          pk[c] = pack_bf16(p0, p1);
-        }
-        l = l * alpha + (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
-      }
-      // P buffer sb was last read by PV(j-2); O may only be rescaled once
-      // PV(j-1) has landed.
-      if (j >= 2 && !wait_warp(BAR(kPvDone + sb), ((j >> 1) - 1) & 1)) break;
+      // S_x(j) has landed, hence PV_x(j-1) too: O_x may be rescaled now.
       if (__any_sync(0xffffffffu, need) && j > 0) {
-        if (!wait_warp(BAR(kPvDone + (sb ^ 1)), ((j - 1) >> 1) & 1)) break;
-        tc::tc_fence_after();
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
-          const uint32_t ta = tmem + lane_base + C::kColO + c * 32;
-          tc::tmem_ld32(ta, r);
+          tc::tmem_ld32(to + c * 32, r);
           tc::tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-          tc::tmem_st32(ta, r);
+          tc::tmem_st32(to + c * 32, r);
         }
-        tc::tmem_wait_st();
       }
+      // P = exp2(s * scale_log2 - m_used) as bf16 pairs over the first 64
+      // columns of the S row.
       {
-        const uint32_t pbase = sbase + C::kOffP + sb * C::kPBytes;
+        float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c8 = 0; c8 < C::kBN / 8; ++c8) {
-          const uint32_t dst = pbase + (c8 >> 3) * (C::kBM * 128) + sw128(t, c8 & 7);
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(pk[4 * c8]),
-                       "r"(pk[4 * c8 + 1]), "r"(pk[4 * c8 + 2]), "r"(pk[4 * c8 + 3])
-                       : "memory");
+        for (int c16 = 0; c16 < C::kBN / 32; ++c16) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int c = c16 * 16 + e;
+            const float p0 = ex2(fmaf(s[2 * c], scale_log2, -mu));
+            const float p1 = ex2(fmaf(s[2 * c + 1], scale_log2, -mu));
+            l8[e & 7] += p0 + p1;
+            pk[e] = pack_bf16(p0, p1);
+          }
+          tc::tmem_st16(ts + c16 * 16, pk);
         }
+        l = l * alpha + (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
       }
+      tc::tmem_wait_st();
       // V rows that must contribute nothing: past seq_len (stale or unset
       // cache contents) or in pieces that were not loaded.  Zeroed once the
-      // tile's V has landed.
-      {
+      // tile's V has landed, by the first warpgroup (one row per thread),
+      // before P_0(j) is published; PV_1(j) is issued after PV_0(j).
+      if (x == 0) {
         const int tok = tok0 + t;
         const bool row_ok = tok < seq && ((vm >> (t >> 4)) & 1u);
         if (!row_ok) {
-          if (!tc::mbar_wait(BAR(kVFull + sb), (j >> 1) & 1)) fail();
-          const uint32_t vbase = sbase + C::kOffV + sb * C::kTileBytes;
+          if (!tc::mbar_wait(BAR(kVFull + (j & 1)), (j >> 1) & 1)) fail();
+          const uint32_t vbase = sbase + C::kOffV + (j & 1) * C::kTileBytes;
 #pragma unroll
           for (int h = 0; h < C::kHalves; ++h)
 #pragma unroll
@@ -327,14 +317,14 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
               asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(dst), "r"(0u) : "memory");
             }
         }
+        tc::fence_proxy_async_smem();
       }
-      tc::fence_proxy_async_smem();
       tc::tc_fence_before();
-      tc::mbar_arrive(BAR(kPFull + sb));
+      tc::mbar_arrive(BAR(kPFull + x));
     }
     // ------------------------------------------------------------ epilogue
     bool ok = !__any_sync(0xffffffffu, *abort_flag != 0) && ntiles > 0;
-    if (ok) ok = wait_warp(BAR(kPvDone + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1);
+    if (ok) ok = wait_warp(BAR(kODone + x), (ntiles - 1) & 1);
     tc::tc_fence_after();
     if (ok) {   // warp-uniform
       const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -342,7 +332,7 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
-        tc::tmem_ld32(tmem + lane_base + C::kColO + c * 32, r);
+        tc::tmem_ld32(to + c * 32, r);
         tc::tmem_wait_ld();
         if (valid) {
 #pragma unroll
@@ -364,58 +354,68 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
       for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
       if (lse != nullptr) lse[qoff / D] = -CUDART_INF_F;
     }
-  } else if (warp == 4) {
+  } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
       constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, C::kBN, 0, 0);
       constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, D, 0, 1);
-      const uint32_t qs = sbase + C::kOffQ;
       bool ok = ntiles == 0 || tc::mbar_wait(BAR(kQFull), 0);
       if (!ok) fail();
-      auto issue_s = [&](int j) -> bool {
-        const int ks_i = j & 1, sb = j & 1;
-        if (!tc::mbar_wait(BAR(kKFull + ks_i), (j >> 1) & 1)) return false;
-        if (j >= 2 && !tc::mbar_wait(BAR(kSFree + sb), ((j - 2) >> 1) & 1)) return false;
-        tc::tc_fence_after();
-        const uint32_t ks = sbase + C::kOffK + ks_i * C::kTileBytes;
-        const uint32_t dS = tmem + (sb ? C::kColS1 : C::kColS0);
+      // S_x(j) = Q_x K(j)^T into the S columns of tile x.
+      auto issue_s = [&](int xq, int j) {
+        const uint32_t qs = sbase + C::kOffQ + xq * C::kQBytes;
+        const uint32_t ks = sbase + C::kOffK + (j & 1) * C::kTileBytes;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * (C::kBM * 128) + (k & 3) * 32;
           const uint32_t koff = (k >> 2) * (C::kBN * 128) + (k & 3) * 32;
-          tc::mma_bf16_ss(dS, tc::smem_desc_sw128(qs + off, 16, 1024),
+          tc::mma_bf16_ss(tmem + C::col_s(xq), tc::smem_desc_sw128(qs + off, 16, 1024),
                           tc::smem_desc_sw128(ks + koff, 16, 1024), idesc_s, k > 0 ? 1u : 0u);
         }
-        tc::mma_commit(BAR(kSFull + sb));
-        release(BAR(kKEmpty + ks_i));
-        return true;
+        tc::mma_commit(BAR(kSFull + xq));
       };
-      if (ok && ntiles > 0) ok = issue_s(0);
-      for (int j = 0; ok && j < ntiles; ++j) {
-        if (*abort_flag) { ok = false; break; }
-        if (j + 1 < ntiles && !issue_s(j + 1)) { ok = false; break; }
-        const int vb = j & 1;
-        if (!tc::mbar_wait(BAR(kPFull + vb), (j >> 1) & 1)) { ok = false; break; }
-        if (!tc::mbar_wait(BAR(kVFull + vb), (j >> 1) & 1)) { ok = false; break; }
-        tc::tc_fence_after();
-        const uint32_t ps = sbase + C::kOffP + vb * C::kPBytes;
-        const uint32_t vs = sbase + C::kOffV + vb * C::kTileBytes;
+      // O_x += P_x(j) V(j); P_x is read from TMEM, 8 columns (16 bf16) per
+      // 16-token step.
+      auto issue_pv = [&](int xq, int j) {
+        const uint32_t vs = sbase + C::kOffV + (j & 1) * C::kTileBytes;
 #pragma unroll
-        for (int k = 0; k < C::kBN / 16; ++k) {
-          const uint32_t poff = (k >> 2) * (C::kBM * 128) + (k & 3) * 32;
-          tc::mma_bf16_ss(tmem + C::kColO, tc::smem_desc_sw128(ps + poff, 16, 1024),
+        for (int k = 0; k < C::kBN / 16; ++k)
+          tc::mma_bf16_ts(tmem + C::col_o(xq), tmem + C::col_s(xq) + k * 8,
                           tc::smem_desc_sw128(vs + k * 16 * 128, C::kBN * 128, 1024), idesc_o,
                           (j > 0 || k > 0) ? 1u : 0u);
+        tc::mma_commit(BAR(kODone + xq));
+      };
+      auto wait_k = [&](int j) { return tc::mbar_wait(BAR(kKFull + (j & 1)), (j >> 1) & 1); };
+      if (ok && ntiles > 0) {
+        ok = wait_k(0);
+        if (ok) {
+          tc::tc_fence_after();
+          issue_s(0, 0);
+          issue_s(1, 0);
+          release(BAR(kKEmpty + 0));
         }
-        tc::mma_commit(BAR(kPvDone + vb));
-        release(BAR(kVEmpty + vb));
+      }
+      for (int j = 0; ok && j < ntiles; ++j) {
+        if (*abort_flag) { ok = false; break; }
+        const bool more = j + 1 < ntiles;
+        if (!tc::mbar_wait(BAR(kVFull + (j & 1)), (j >> 1) & 1)) { ok = false; break; }
+        if (more && !wait_k(j + 1)) { ok = false; break; }
+        for (int xq = 0; xq < 2 && ok; ++xq) {
+          if (!tc::mbar_wait(BAR(kPFull + xq), j & 1)) { ok = false; break; }
+          tc::tc_fence_after();
+          issue_pv(xq, j);
+          if (more) issue_s(xq, j + 1);
+        }
+        if (!ok) break;
+        release(BAR(kVEmpty + (j & 1)));
+        if (more) release(BAR(kKEmpty + ((j + 1) & 1)));
       }
       if (!ok && !*abort_flag) fail();
       // Everything issued has completed before TMEM is released.
       tc::mma_commit(BAR(kFinal));
       if (!tc::mbar_wait(BAR(kFinal), 0)) fail();
     }
-  } else {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ K/V producer
     // Lane p looks after the tile's 16-token piece p: its block id (fetched a
     // tile ahead) and, if p % CL is this CTA's rank, its TMA boxes (one per
@@ -556,8 +556,19 @@ static cudaError_t launch_varlen_tc_t(const void* q, const void* cache, const in
   static DeviceFlags attr_set;
   cudaError_t e = set_smem_once(kern, C::kSmemBytes, attr_set);
   if (e != cudaSuccess) return e;
+  // The register hand-over between warpgroups waits for registers that the
+  // launch must actually hold; refuse to launch a build that does not.
+  static const bool regs_ok = [&] {
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return false;
+    const long long have = static_cast<long long>(fa.numRegs) * C::kThreads;
+    const long long need = 256LL * C::kRegSoftmax + 128LL * C::kRegOther;
+    return fa.numRegs >= static_cast<int>(C::kRegOther) &&
+           fa.numRegs <= static_cast<int>(C::kRegSoftmax) && have >= need;
+  }();
+  if (!regs_ok) return cudaErrorInvalidConfiguration;
   const long long rows = static_cast<long long>(max_query_len) * (Hq / Hkv);
-  long long tiles = (rows + C::kBM - 1) / C::kBM;
+  long long tiles = (rows + C::kRows - 1) / C::kRows;
   tiles = (tiles + CL - 1) / CL * CL;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(tiles), Hkv, N);
@@ -577,7 +588,7 @@ static cudaError_t launch_varlen_tc_t(const void* q, const void* cache, const in
 }
 
 // CTAs per cluster sharing K/V tiles by multicast.
-constexpr int kVarlenCluster = 4;
+constexpr int kVarlenCluster = 2;
 
 cudaError_t launch_varlen_tc(const void* q, const void* cache, const int32_t* block_table,
                              const int32_t* qsl, const int32_t* seq_lens, int N, int Hq, int Hkv,
@@ -585,11 +596,12 @@ cudaError_t launch_varlen_tc(const void* q, const void* cache, const int32_t* bl
                              float scale, int causal, void* out, float* lse, int* err,
                              cudaStream_t stream) {
   if (d == 128)
-    return launch_varlen_tc_t<128, kVarlenCluster>(q, cache, block_table, qsl, seq_lens, N, Hq, Hkv, bs,
-                                   num_blocks, max_blocks, max_query_len, scale, causal, out, lse,
-                                   err, stream);
-  return launch_varlen_tc_t<64, kVarlenCluster>(q, cache, block_table, qsl, seq_lens, N, Hq, Hkv, bs, num_blocks,
-                                max_blocks, max_query_len, scale, causal, out, lse, err, stream);
+    return launch_varlen_tc_t<128, kVarlenCluster>(q, cache, block_table, qsl, seq_lens, N, Hq,
+                                                   Hkv, bs, num_blocks, max_blocks, max_query_len,
+                                                   scale, causal, out, lse, err, stream);
+  return launch_varlen_tc_t<64, kVarlenCluster>(q, cache, block_table, qsl, seq_lens, N, Hq, Hkv,
+                                                bs, num_blocks, max_blocks, max_query_len, scale,
+                                                causal, out, lse, err, stream);
 }
 
 }  // namespace pa
