@@ -278,10 +278,8 @@ def l2_flusher(device):
     return lambda: buf.fill_(1)
 
 
-def secondary(pa, device, pk):
-    res = {}
-    flush = l2_flusher(device)
-    # Chunked prefill: varlen kernel.
+def bench_prefill(pa, device, pk, flush, reps=10):
+    """Chunked prefill: the varlen kernel on its own."""
     b = workloads.chunked_prefill(with_pool=False)
     pool = device_pool((b.num_blocks, 2, b.block_size, b.num_kv_heads, b.head_size), 3, device)
     q = to_dev_bf16(b.q, device)
@@ -294,17 +292,20 @@ def secondary(pa, device, pk):
 
     def prefill():
         pa.pa_varlen_fwd(q, pool, table, qsl, seq, mq, b.scale, out=out, lse=lse)
-    ms = _timed_with_flush(prefill, flush, 10)
+    ms = _timed_with_flush(prefill, flush, reps)
     tf = b.causal_flops() / (ms * 1e-3) / 1e12
-    res["chunked_prefill"] = {"workload": b.name, "kernel": "varlen_fwd", "ms": ms,
+    res = {"workload": b.name, "kernel": "varlen_fwd", "ms": ms,
                               "tflops": tf, "causal_flops": b.causal_flops(),
                               "frac_of_bf16_peak": tf / pk["bf16_tflops"],
                               "peak": "bf16_tflops (measured burst)" if pk["source"] == "measured"
                               else "fallback"}
     del pool, q, out
     torch.cuda.empty_cache()
+    return res
 
-    # Long-context split-KV decode (8 x 131072).
+
+def bench_long_decode(pa, device, pk, flush, reps=10):
+    """Long-context split-KV decode (8 x 131072)."""
     b = workloads.long_decode(with_pool=False)
     pool = device_pool((b.num_blocks, 2, b.block_size, b.num_kv_heads, b.head_size), 4, device)
     N, hq, d = b.num_seqs, b.num_q_heads, b.head_size
@@ -316,18 +317,21 @@ def secondary(pa, device, pk):
     o = torch.empty((N, hq, d), dtype=torch.bfloat16, device=device)
     lo = torch.empty((N, hq), dtype=torch.float32, device=device)
     st1 = _timed_with_flush(lambda: pa.pa_decode_splitkv(q, pool, table, seq, b.scale, ws, 131072),
-                            flush, 10)
+                            flush, reps)
     both = _timed_with_flush(lambda: pa.pa_decode(q, pool, table, seq, b.scale, ws, o, lo, 131072),
-                             flush, 10)
+                             flush, reps)
     gbs = b.kv_bytes() / (st1 * 1e-3) / 1e9
-    res["long_decode"] = {"workload": b.name, "num_splits": S, "stage1_ms": st1,
+    res = {"workload": b.name, "num_splits": S, "stage1_ms": st1,
                           "decode_plus_merge_ms": both, "kv_bytes": b.kv_bytes(),
                           "stage1_gbs": gbs, "frac_of_hbm_peak": gbs / pk["hbm_gbs"],
                           "step_gbs": b.kv_bytes() / (both * 1e-3) / 1e9}
     del pool, q, ws
     torch.cuda.empty_cache()
+    return res
 
-    # MLA latent decode.
+
+def bench_mla(pa, device, pk, flush, reps=10):
+    """MLA latent decode (DeepSeek-V3 shape)."""
     m = workloads.mla_decode(with_pool=False)
     pool = device_pool((m.num_blocks, m.block_size, m.kv_lora_rank + m.rope_dim), 5, device)
     q = to_dev_bf16(m.q, device)
@@ -340,16 +344,25 @@ def secondary(pa, device, pk):
     mx = int(m.seq_lens.max())
     ms = _timed_with_flush(lambda: pa.pa_mla_decode(q, pool, table, seq, m.scale, ws, o, lo,
                                                     max_seq_len=mx),
-                           flush, 10)
+                           flush, reps)
     gbs = m.kv_bytes() / (ms * 1e-3) / 1e9
     flops = int(m.seq_lens.astype(np.int64).sum()) * m.num_heads * 2 * (
         m.kv_lora_rank + m.rope_dim + m.kv_lora_rank)
-    res["mla_decode"] = {"workload": m.name, "num_splits": S, "ms": ms, "kv_bytes": m.kv_bytes(),
+    res = {"workload": m.name, "num_splits": S, "ms": ms, "kv_bytes": m.kv_bytes(),
                          "gbs": gbs, "frac_of_hbm_peak": gbs / pk["hbm_gbs"],
                          "tflops": flops / (ms * 1e-3) / 1e12}
     del pool, q, ws
     torch.cuda.empty_cache()
     return res
+
+
+SECONDARY = {"chunked_prefill": bench_prefill, "long_decode": bench_long_decode,
+             "mla_decode": bench_mla}
+
+
+def secondary(pa, device, pk):
+    flush = l2_flusher(device)
+    return {name: fn(pa, device, pk, flush) for name, fn in SECONDARY.items()}
 
 
 def mla_splits(m, sms):
@@ -385,6 +398,9 @@ def main():
     ap.add_argument("--impl", choices=["pa", "reference"], default="pa")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=sorted(SECONDARY),
+                    help="time one secondary workload alone (--steps launches) and print its "
+                         "record; a small command for profiler captures")
     args = ap.parse_args()
     warmup = max(3, args.warmup)
     world, rank, local = dist_env()
@@ -404,6 +420,11 @@ def main():
         dist.init_process_group("nccl", device_id=device)
     pa.lib()
     pk = peaks()
+    if args.only is not None:
+        rec = SECONDARY[args.only](pa, device, pk, l2_flusher(device), reps=args.steps)
+        if rank == 0:
+            print(json.dumps({"only": args.only, **rec}), flush=True)
+        return
 
     b = workloads.gqa_decode()
     step = DecodeStep(pa, b, device)

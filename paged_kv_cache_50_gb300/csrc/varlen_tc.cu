@@ -8,18 +8,21 @@
 // CTA = (256 packed rows as two Q tiles of 128, kv head, request); a packed
 // row is one (query row, q head of the kv group) pair, so the Hq/Hkv heads
 // sharing a kv head share every K/V tile.  Warp roles (384 threads):
-//   warps 0-3 / 4-7  two softmax warpgroups, one per Q tile: thread t of a
+//   warp 0     MMA issue (one thread): S_x(j) = Q_x K(j)^T, then
+//              O_x += P_x(j) V(j) with the A operand (P) read from TMEM;
+//   warp 1     K/V producer: per 16-token piece of a cache block one TMA box
+//              per 64-column half, through the block table;
+//   warps 2-3  idle (they complete the first warpgroup, which hands its
+//              registers to the softmax warpgroups);
+//   warps 4-7 / 8-11  two softmax warpgroups, one per Q tile: thread t of a
 //              group owns row t of its tile = TMEM lane t.  Per 128-token K/V
 //              tile it reads its S row from TMEM, masks (causal,
 //              bottom-right), runs the online softmax in the log2 domain and
 //              writes its P row (bf16, two per 32-bit column) back into TMEM
-//              over the S row it came from;
-//   warp 8     MMA issue (one thread): S_x(j) = Q_x K(j)^T, then
-//              O_x += P_x(j) V(j) with the A operand (P) read from TMEM;
-//   warp 9     K/V producer: per 16-token piece of a cache block one TMA box
-//              per 64-column half, through the block table;
-//   warps 10-11 idle (they complete the third warpgroup, which hands its
-//              registers to the softmax warpgroups).
+//              over the S row it came from.
+// The MMA and producer warps have the lowest warp ids: each shares its
+// scheduler with two busy softmax warps, and the low ids keep them from being
+// starved of issue slots.
 // The two Q tiles interleave on the tensor core: PV_0(j), S_0(j+1),
 // PV_1(j), S_1(j+1), ... so each softmax warpgroup works on one tile while
 // the MMAs of the other proceed.  The tensor pipe runs in issue order, so
@@ -62,8 +65,8 @@ struct TcCfg {
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;   // barriers + alignment slack
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kThreads = 384;
-  // Registers per thread: softmax warpgroups 0-1 raise theirs, warpgroup 2
-  // (MMA issue, producer, two idle warps) lowers its own.  The launch must
+  // Registers per thread: the softmax warpgroups 1-2 raise theirs,
+  // warpgroup 0 (MMA issue, producer, two idle warps) lowers its own.  The launch must
   // hold at least 256 * kRegSoftmax + 128 * kRegOther registers.
   static constexpr uint32_t kRegSoftmax = 216;
   static constexpr uint32_t kRegOther = 56;
@@ -76,6 +79,12 @@ struct TcCfg {
 // [rows][128 B] region.
 __device__ __forceinline__ uint32_t sw128(int r, int c) {
   return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float y;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -92,11 +101,15 @@ enum TcBar {
   kVFull = 5,
   kVEmpty = 7,
   kSFull = 9,    // [x]
-  kPFull = 11,   // [x]
-  kODone = 13,   // [x]
-  kFinal = 15,
-  kNumBars = 16
+  kPLo = 11,     // [x] P columns of tokens 0-63 written
+  kPHi = 13,     // [x] P columns of tokens 64-127 written
+  kODone = 15,   // [x]
+  kFinal = 17,
+  kNumBars = 18
 };
+// After the barriers: the TMEM base address (4 B, padded to 8), the abort
+// flag (4 B, padded to 8) and a ring of 4 tile descriptors (4 B each).
+constexpr int kPieceRing = 4;
 
 template <int D, int CL>
 __global__ void __launch_bounds__(384, 1)
@@ -135,6 +148,11 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
   auto BAR = [&](int k) { return bars + 8u * static_cast<uint32_t>(k); };
   const uint32_t tmem_slot = bars + 8u * kNumBars;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + C::kOffBar + 8 * kNumBars + 8);
+  // Ring of loaded-piece masks: the producer writes (j << 8) | mask for tile
+  // j into slot j % kPieceRing before it issues K(j); the softmax reads it
+  // once S(j) has landed.  The tag makes the slot self-validating.
+  volatile uint32_t* piece_ring =
+      reinterpret_cast<volatile uint32_t*>(sgen + C::kOffBar + 8 * kNumBars + 16);
 
   if (threadIdx.x == 0) {
     tc::mbar_init(BAR(kQFull), C::kRows);
@@ -144,7 +162,8 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
       tc::mbar_init(BAR(kVFull + b), 1);
       tc::mbar_init(BAR(kVEmpty + b), CL);
       tc::mbar_init(BAR(kSFull + b), 1);
-      tc::mbar_init(BAR(kPFull + b), C::kBM);
+      tc::mbar_init(BAR(kPLo + b), C::kBM);
+      tc::mbar_init(BAR(kPHi + b), C::kBM);
       tc::mbar_init(BAR(kODone + b), 1);
     }
     tc::mbar_init(BAR(kFinal), 1);
@@ -181,14 +200,14 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
     return (blk >= 0 && blk < num_blocks) ? blk : -2;
   };
 
-  if (warp < 8)
+  if (warp >= 4)
     tc::reg_alloc<C::kRegSoftmax>();
   else
     tc::reg_dealloc<C::kRegOther>();
 
-  if (warp < 8) {
+  if (warp >= 4) {
     // ------------------------------------------------------------ softmax
-    const int x = warp >> 2;                 // Q tile of this warpgroup
+    const int x = (warp >> 2) - 1;           // Q tile of this warpgroup
     const int t = threadIdx.x & 127;         // row within the tile = TMEM lane
     const int pr = row0 + x * C::kBM + t;
     const bool valid = pr < rows_total;
@@ -221,16 +240,24 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
       return w;
     };
     float m_used = -CUDART_INF_F, l = 0.f;
-    int piece_next = lane < C::kBN / 16 ? piece_block(16 * lane) : -1;
     for (int j = 0; j < ntiles; ++j) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
       const int tok0 = j * C::kBN;
-      // Loaded pieces of this tile (one table entry per lane, fetched during
-      // the previous tile) and the next tile's entries, fetched now.
-      const uint32_t vm = __ballot_sync(0xffffffffu, piece_next >= 0) & ((1u << (C::kBN / 16)) - 1u);
-      piece_next = lane < C::kBN / 16 ? piece_block(tok0 + C::kBN + 16 * lane) : -1;
       if (!wait_warp(BAR(kSFull + x), j & 1)) break;
       tc::tc_fence_after();
+      // Loaded pieces of this tile, from the producer's ring (written before
+      // K(j) was issued, so normally visible at the first read).
+      uint32_t vm;
+      {
+        const uint32_t tag = static_cast<uint32_t>(j) << 8;
+        uint32_t w = piece_ring[j % kPieceRing];
+        for (int n = 0; (w & ~0xffu) != tag && n < tc::kWaitPolls; ++n) w = piece_ring[j % kPieceRing];
+        if (!__all_sync(0xffffffffu, (w & ~0xffu) == tag)) {
+          fail();
+          break;
+        }
+        vm = w & 0xffu;
+      }
       float s[C::kBN];
       {
         uint32_t r[C::kBN / 32][32];
@@ -253,13 +280,15 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
       }
       float mx;
       {
+        // Eight independent chains of 3-input maxima, then their maximum.
         float m8[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) m8[k] = s[k];
+        for (int k = 0; k < 8; ++k) m8[k] = fmaxf(s[k], s[8 + k]);
 #pragma unroll
-        for (int col = 8; col < C::kBN; ++col) m8[col & 7] = fmaxf(m8[col & 7], s[col]);
-        mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        for (int col = 16; col < C::kBN; col += 16)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) m8[k] = max3(m8[k], s[col + k], s[col + 8 + k]);
+        mx = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
         mx *= scale_log2;
       }
       const float m_new = fmaxf(m_used, mx);
@@ -279,26 +308,6 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
           tc::tmem_st32(to + c * 32, r);
         }
       }
-      // P = exp2(s * scale_log2 - m_used) as bf16 pairs over the first 64
-      // columns of the S row.
-      {
-        float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int c16 = 0; c16 < C::kBN / 32; ++c16) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int c = c16 * 16 + e;
-            const float p0 = ex2(fmaf(s[2 * c], scale_log2, -mu));
-            const float p1 = ex2(fmaf(s[2 * c + 1], scale_log2, -mu));
-            l8[e & 7] += p0 + p1;
-            pk[e] = pack_bf16(p0, p1);
-          }
-          tc::tmem_st16(ts + c16 * 16, pk);
-        }
-        l = l * alpha + (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
-      }
-      tc::tmem_wait_st();
       // V rows that must contribute nothing: past seq_len (stale or unset
       // cache contents) or in pieces that were not loaded.  Zeroed once the
       // tile's V has landed, by the first warpgroup (one row per thread),
@@ -319,8 +328,31 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
         }
         tc::fence_proxy_async_smem();
       }
-      tc::tc_fence_before();
-      tc::mbar_arrive(BAR(kPFull + x));
+      // P = exp2(s * scale_log2 - m_used) as bf16 pairs over the first 64
+      // columns of the S row, published in two halves (tokens 0-63, 64-127)
+      // so that the first half of PV_x(j) runs while the second is computed.
+      {
+        float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c16 = 0; c16 < C::kBN / 32; ++c16) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int c = c16 * 16 + e;
+            const float p0 = ex2(fmaf(s[2 * c], scale_log2, -mu));
+            const float p1 = ex2(fmaf(s[2 * c + 1], scale_log2, -mu));
+            l8[e & 7] += p0 + p1;
+            pk[e] = pack_bf16(p0, p1);
+          }
+          tc::tmem_st16(ts + c16 * 16, pk);
+          if (c16 == C::kBN / 64 - 1 || c16 == C::kBN / 32 - 1) {
+            tc::tmem_wait_st();
+            tc::tc_fence_before();
+            tc::mbar_arrive(BAR((c16 == C::kBN / 32 - 1 ? kPHi : kPLo) + x));
+          }
+        }
+        l = l * alpha + (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
+      }
     }
     // ------------------------------------------------------------ epilogue
     bool ok = !__any_sync(0xffffffffu, *abort_flag != 0) && ntiles > 0;
@@ -354,7 +386,7 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
       for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
       if (lse != nullptr) lse[qoff / D] = -CUDART_INF_F;
     }
-  } else if (warp == 8) {
+  } else if (warp == 0) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
       constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, C::kBN, 0, 0);
@@ -374,16 +406,15 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
         }
         tc::mma_commit(BAR(kSFull + xq));
       };
-      // O_x += P_x(j) V(j); P_x is read from TMEM, 8 columns (16 bf16) per
-      // 16-token step.
-      auto issue_pv = [&](int xq, int j) {
+      // O_x += P_x(j) V(j) over the 16-token steps [k0, k0 + 4); P_x is read
+      // from TMEM, 8 columns (16 bf16) per step.
+      auto issue_pv = [&](int xq, int j, int k0) {
         const uint32_t vs = sbase + C::kOffV + (j & 1) * C::kTileBytes;
 #pragma unroll
-        for (int k = 0; k < C::kBN / 16; ++k)
+        for (int k = k0; k < k0 + C::kBN / 32; ++k)
           tc::mma_bf16_ts(tmem + C::col_o(xq), tmem + C::col_s(xq) + k * 8,
                           tc::smem_desc_sw128(vs + k * 16 * 128, C::kBN * 128, 1024), idesc_o,
                           (j > 0 || k > 0) ? 1u : 0u);
-        tc::mma_commit(BAR(kODone + xq));
       };
       auto wait_k = [&](int j) { return tc::mbar_wait(BAR(kKFull + (j & 1)), (j >> 1) & 1); };
       if (ok && ntiles > 0) {
@@ -401,9 +432,13 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
         if (!tc::mbar_wait(BAR(kVFull + (j & 1)), (j >> 1) & 1)) { ok = false; break; }
         if (more && !wait_k(j + 1)) { ok = false; break; }
         for (int xq = 0; xq < 2 && ok; ++xq) {
-          if (!tc::mbar_wait(BAR(kPFull + xq), j & 1)) { ok = false; break; }
+          if (!tc::mbar_wait(BAR(kPLo + xq), j & 1)) { ok = false; break; }
           tc::tc_fence_after();
-          issue_pv(xq, j);
+          issue_pv(xq, j, 0);
+          if (!tc::mbar_wait(BAR(kPHi + xq), j & 1)) { ok = false; break; }
+          tc::tc_fence_after();
+          issue_pv(xq, j, C::kBN / 32);
+          tc::mma_commit(BAR(kODone + xq));
           if (more) issue_s(xq, j + 1);
         }
         if (!ok) break;
@@ -415,7 +450,7 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
       tc::mma_commit(BAR(kFinal));
       if (!tc::mbar_wait(BAR(kFinal), 0)) fail();
     }
-  } else if (warp == 9) {
+  } else if (warp == 1) {
     // ------------------------------------------------------------ K/V producer
     // Lane p looks after the tile's 16-token piece p: its block id (fetched a
     // tile ahead) and, if p % CL is this CTA's rank, its TMA boxes (one per
@@ -435,6 +470,7 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
       const unsigned bad = __ballot_sync(0xffffffffu, blk == -2);
       if (lane == 0) {
         if (bad != 0u && which == 0 && rank == 0) record_error(err, PA_DEVERR_BLOCK_ID);
+        if (which == 0) piece_ring[j % kPieceRing] = (static_cast<uint32_t>(j) << 8) | (loaded & 0xffu);
         tc::mbar_arrive_expect_tx(
             full, static_cast<uint32_t>(__popc(loaded)) * C::kHalves * C::kPieceBytes);
       }
