@@ -2,30 +2,65 @@
 // data-flow section: MQA over one latent KV head).  The cache row of a token
 // is the 576-wide [kv_c (512) | k_pe (64)] vector: the key is the whole row,
 // the value its first 512 entries, so every cache byte is read from HBM once
-// and serves both products.  Split-KV stage 1: each CTA writes its split's
+// and serves both products.  Split-KV stage 1: each split writes its
 // normalised partial output and LSE to the [B, H, S, 513] fp32 workspace;
 // the LSE merge finishes the call.
 //
-// CTA = (split, request, group of 128 heads); the 128 heads form the M = 128
-// rows of every MMA (a last partial group computes spare rows it never stores).  192 threads:
-//   warps 0-3  softmax: thread t owns head t = TMEM lane t;
-//   warp 4     MMA issue (one thread);
-//   warp 5     TMA producer: Q once (9 boxes of 64 columns x 128 heads), then
-//              per 32-token tile 9 boxes of 64 columns x 32 tokens, one per
-//              lane, from the token's cache block (block_size % 32 == 0).
-// Tensor memory holds 512 fp32 columns per lane, exactly one 128 x 512 output,
-// which leaves no room for the scores.  So O[:, 0:448] accumulates in TMEM
-// columns 0-447, and columns 448-511 (region X) serve in turn as
-//   S(j)    = Q K(j)^T             (32 columns), read by the softmax warps;
-//   T(j)    = P(j) V(j)[:, 448:512] (64 columns), added by the softmax warps
-//             into the last 64 output columns they keep in registers.
-// Per tile: S(j) -> softmax -> P(j) -> PV(j) (O[:, 0:448] and T(j)) -> T(j)
-// read back -> X free -> S(j+1).  O is rescaled only when a head's running
-// max grows by more than 2^8 (exact: P keeps the older reference max).
+// One (split, request, group of 128 heads) is computed by a cluster of two
+// CTAs.  The 128 heads form the M = 128 rows of every MMA.  A 128 x 576 query
+// (144 KB) and a 128 x 512 fp32 output (all 512 TMEM columns) do not fit one
+// CTA next to a K tile and the scores, so the pair splits both:
+//   * the contraction: CTA r holds the query / key columns of latent chunks
+//     [256r, 256r + 256) and rope half [512 + 32r, 512 + 32r + 32); it computes
+//     the partial scores S_r(j) = Q_r K_r(j)^T of a 64-token tile (N = 64);
+//   * the output: CTA r accumulates O[:, 256r : 256r + 256], whose values are
+//     exactly the latent columns it already holds.
+// The partial scores are exchanged through distributed shared memory
+// (st.async into the peer's buffer, completing bytes on the peer's barrier)
+// as 16-bit fixed point: the SM-to-SM path moves only ~12 bytes per clock,
+// and halving the bytes keeps the exchange behind the tensor core.  Each
+// head row of a tile is scaled by a power of two 2^(15 - E) with
+// 2^E > max |S_peer| over the row's visible tokens, rounded to int16 and
+// decoded exactly, so the error of a score is at most 2^(E - 16) <
+// max |S_peer| / 32768 (f16 would allow 2^-12 of each value, ~8x more for the
+// largest scores, which dominate the LSE).  CTA r then holds
+// S = S_r + decode(S_peer) and runs the online softmax on it; each CTA's
+// output half and row sum come from its own P, so each half is normalised
+// consistently.  P goes
+// to its own TMEM buffer and PV takes it from there, so the next scores can
+// be computed into the S buffer as soon as the S of the tile has been read.
 //
-// Shared memory: Q [9 chunks][128 heads][128 B] (144 KB, 128-byte swizzle),
-// K/V tiles 2 stages x [9 chunks][32 tokens][128 B] (72 KB), P [128 heads]
-// [32 tokens] bf16 in the unswizzled 8 x 16-byte core-matrix layout (8 KB).
+// 352 threads per CTA:
+//   warps 0-3  softmax: thread t owns head t = TMEM lane t;
+//   warps 4-7  exchange: as soon as S_r(j) has landed, thread t sends row t
+//              of it to the peer, while the softmax warps still work on tile
+//              j - 1 (the scores are double-buffered, so S_r(j) is computed
+//              during the softmax of j - 1);
+//   warp 8     MMA issue (one thread): S(j+2) as soon as S(j) has been read
+//              (and K(j+2) has landed), PV(j) as soon as P(j) is written,
+//              whichever comes first, so the scores of the next tiles are
+//              computed while the softmax works on the current one;
+//   warp 9     TMA producer: its query columns once, then per 64-token tile
+//              two 32-token halves (each inside one cache block, since
+//              block_size % 32 == 0) of 4 latent boxes (64 columns) and one
+//              rope box (32 columns), through the block table;
+//   warp 10    exchange helper: once the softmax warps have read the peer's
+//              partial scores of a tile, tells the peer its buffer is free
+//              (a thread with no remote stores of its own in flight, so the
+//              cluster-scope release does not wait for them).
+// O is rescaled only when a head's running max grows by more than 2^8
+// (exact: P keeps the older reference max).
+//
+// Shared memory per CTA (1024-byte aligned regions):
+//   Q     4 latent chunks [128 heads][128 B] (128-byte swizzle) + rope half
+//         [128 heads][64 B] (64-byte swizzle)                         72 KB
+//   K/V   3 stages x (4 latent chunks [64 tokens][128 B] + rope half
+//         [64 tokens][64 B])                                          108 KB
+//   X     2 buffers of the peer's partial scores, [9 chunks][128 heads]
+//         [16 B]: 8 chunks of 8 int16 scores, then the row's exponent E, so
+//         that one warp-wide store or load covers 512 contiguous bytes 36 KB
+// TMEM: S buffers at columns 0 and 64, P buffers (bf16 pairs) at 128 and 160,
+// O half at columns 256-511.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math_constants.h>
@@ -39,26 +74,43 @@
 namespace pa {
 
 struct MlaTcCfg {
-  static constexpr int kDk = 576, kDv = 512, kH = 128, kBN = 32;
-  static constexpr int kChunks = kDk / 64;                 // 9 column chunks of 64
+  static constexpr int kDk = 576, kDv = 512, kH = 128, kBN = 64, kBox = 32;
+  static constexpr int kLat = 4;                           // latent chunks per CTA
   static constexpr int kQChunkBytes = kH * 128;            // 16 KB
-  static constexpr int kKChunkBytes = kBN * 128;           // 4 KB
-  static constexpr int kStageBytes = kChunks * kKChunkBytes;  // 36 KB
-  static constexpr int kPBytes = kH * kBN * 2;             // 8 KB
+  static constexpr int kQRopeBytes = kH * 64;              // 8 KB
+  static constexpr int kKChunkBytes = kBN * 128;           // 8 KB
+  static constexpr int kKRopeBytes = kBN * 64;             // 4 KB
+  static constexpr int kStageBytes = kLat * kKChunkBytes + kKRopeBytes;   // 36 KB
+  static constexpr int kStages = 3;
+  static constexpr int kHalfBytes = kBox * (kLat * 128 + 64);           // 18 KB per 32 tokens
+  static constexpr int kXBytes = kH * 9 * 16;              // 18 KB per buffer
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kChunks * kQChunkBytes;     // 144 KB
-  static constexpr int kOffP = kOffK + 2 * kStageBytes;    // 216 KB
-  static constexpr int kOffBar = kOffP + kPBytes;          // 224 KB
+  static constexpr int kOffQr = kLat * kQChunkBytes;       // 64 KB
+  static constexpr int kOffK = kOffQr + kQRopeBytes;       // 72 KB
+  static constexpr int kOffX = kOffK + kStages * kStageBytes;   // 180 KB
+  static constexpr int kOffBar = kOffX + 2 * kXBytes;      // 216 KB
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColX = 448;                   // S / tail region
-  static constexpr int kMainCols = 448;
-  static constexpr int kTailCols = kDv - kMainCols;        // 64
-  static constexpr int kThreads = 192;
+  static constexpr uint32_t kColP = 128;
+  static constexpr uint32_t kColO = 256;
+  static constexpr int kThreads = 352;
 };
 
-enum MlaBar { kMQFull = 0, kMKFull = 1, kMKEmpty = 3, kMSFull = 5, kMPFull = 6, kMPvDone = 7,
-              kMXFree = 8, kMFinal = 9, kMNumBars = 10 };
+enum MlaBar {
+  kMQFull = 0,
+  kMKFull = 1,    // [3]
+  kMKEmpty = 4,   // [3]
+  kMSFull = 7,    // [2]
+  kMXFull = 9,    // [2] the peer's partial scores have arrived in buffer b
+  kMXEmpty = 11,  // [2] the peer has consumed buffer b of the scores this CTA sent
+  kMPFull = 13,   // [2] P buffer b written
+  kMPDone = 15,   // [2] PV of P buffer b completed
+  kMFinal = 17,
+  kMXRead = 18,   // [2] the softmax warps have read exchange buffer b
+  kMSRead = 20,   // [2] the softmax and exchange warps have read S buffer b
+  kMNumBars = 22
+};
+constexpr int kMlaRing = 4;   // tile descriptors passed from the producer
 
 __device__ __forceinline__ uint32_t msw128(int r, int c) {
   return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
@@ -70,19 +122,42 @@ __device__ __forceinline__ float mex2(float x) {
   return y;
 }
 
-// Shared-memory descriptor of an unswizzled K-major tile: 8-row x 16-byte
-// core matrices, `lbo` bytes apart along K and `sbo` bytes apart along M/N.
-__device__ __forceinline__ uint64_t smem_desc_noswz(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFF);
-  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16;
-  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32;
-  d |= static_cast<uint64_t>(1) << 46;
-  return d;
+__device__ __forceinline__ float mmax3(float a, float b, float c) {
+  float y;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
 }
 
-__global__ void __launch_bounds__(192, 1)
-mla_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap c_map,
+// Byte offset of 16-byte chunk c (0-8) of head row t in an exchange buffer.
+__device__ __forceinline__ uint32_t xoff(int t, int c) {
+  return static_cast<uint32_t>(c * 2048 + t * 16);
+}
+
+// Integer <-> float conversions through the 1.5 * 2^23 bias: adding it to a
+// float of magnitude below 2^22 rounds to an integer (nearest even) held in
+// the low mantissa bits, and the reverse subtraction is exact.  This keeps
+// the exchange on the FMA / integer pipes.
+constexpr float kRoundBias = 12582912.0f;       // 1.5 * 2^23
+constexpr int kRoundBiasBits = 0x4B400000;
+
+// x * mul rounded to the nearest int16 (saturating), two per 32-bit word.
+__device__ __forceinline__ uint32_t pack_q16(float lo, float hi, float mul) {
+  int a = __float_as_int(fmaf(lo, mul, kRoundBias)) - kRoundBiasBits;
+  int b = __float_as_int(fmaf(hi, mul, kRoundBias)) - kRoundBiasBits;
+  a = min(max(a, -32767), 32767);
+  b = min(max(b, -32767), 32767);
+  return (static_cast<uint32_t>(a) & 0xffffu) | (static_cast<uint32_t>(b) << 16);
+}
+
+// The signed 16-bit value q times `unit`, exactly (|q| < 2^15, unit a power
+// of two).
+__device__ __forceinline__ float dequant(int q, float unit, float bias_unit) {
+  return fmaf(__int_as_float(kRoundBiasBits + q), unit, -bias_unit);
+}
+
+__global__ void __launch_bounds__(352, 1)
+mla_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap qr_map,
+              const __grid_constant__ CUtensorMap c_map, const __grid_constant__ CUtensorMap cr_map,
               const int32_t* __restrict__ block_table, const int32_t* __restrict__ seq_lens,
               int max_blocks, int H, int bs, int num_blocks, float scale_log2, int S, int chunk,
               float* __restrict__ ws, int* err) {
@@ -91,9 +166,10 @@ mla_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t* sgen = smem_raw + (sbase - raw);
-  if (err != nullptr && (*reinterpret_cast<volatile int*>(err) & PA_DEVERR_TIMEOUT)) return;
 
-  const int s = blockIdx.x, b = blockIdx.y, hg = blockIdx.z;   // hg: group of 128 heads
+  const uint32_t rank = tc::cluster_rank();           // 0 or 1
+  const uint32_t peer = rank ^ 1u;
+  const int s = blockIdx.x >> 1, b = blockIdx.y, hg = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int seq = seq_lens[b];
   const long long a0 = static_cast<long long>(s) * chunk;
@@ -106,25 +182,37 @@ mla_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__
   auto BAR = [&](int k) { return bars + 8u * static_cast<uint32_t>(k); };
   const uint32_t tmem_slot = bars + 8u * kMNumBars;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + C::kOffBar + 8 * kMNumBars + 8);
+  volatile uint32_t* ring =
+      reinterpret_cast<volatile uint32_t*>(sgen + C::kOffBar + 8 * kMNumBars + 16);
 
   if (threadIdx.x == 0) {
     tc::mbar_init(BAR(kMQFull), 1);
-    for (int k = 0; k < 2; ++k) {
+    for (int k = 0; k < C::kStages; ++k) {
       tc::mbar_init(BAR(kMKFull + k), 1);
       tc::mbar_init(BAR(kMKEmpty + k), 1);
     }
-    tc::mbar_init(BAR(kMSFull), 1);
-    tc::mbar_init(BAR(kMPFull), 128);
-    tc::mbar_init(BAR(kMPvDone), 1);
-    tc::mbar_init(BAR(kMXFree), 128);
+    tc::mbar_init(BAR(kMSFull + 0), 1);
+    tc::mbar_init(BAR(kMSFull + 1), 1);
+    for (int k = 0; k < 2; ++k) {
+      tc::mbar_init(BAR(kMXFull + k), 1);
+      tc::mbar_init(BAR(kMXEmpty + k), 1);   // the peer's exchange helper
+      tc::mbar_init(BAR(kMXRead + k), 128);
+    }
+    for (int k = 0; k < 2; ++k) {
+      tc::mbar_init(BAR(kMPFull + k), 128);
+      tc::mbar_init(BAR(kMPDone + k), 1);
+    }
     tc::mbar_init(BAR(kMFinal), 1);
+    tc::mbar_init(BAR(kMSRead + 0), 256);
+    tc::mbar_init(BAR(kMSRead + 1), 256);
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
   __syncwarp();
   if (warp == 0) tc::tmem_alloc(tmem_slot, C::kTmemCols);
   tc::tc_fence_before();
-  __syncthreads();
+  // Both CTAs' barriers are initialised before either sends to the other.
+  tc::cluster_sync();
   tc::tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sgen + C::kOffBar + 8 * kMNumBars);
 
@@ -132,243 +220,418 @@ mla_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__
     record_error(err, PA_DEVERR_TIMEOUT);
     *abort_flag = 1;
   };
-  // Block id of tile j (its 32 tokens lie in one cache block), or -1.
-  auto tile_block = [&](int j) -> int {
-    const int tok = t0 + j * C::kBN;
-    const int blk = block_at(table, tok / bs, max_blocks);
-    return (blk >= 0 && blk < num_blocks) ? blk : -1;
-  };
 
   if (warp < 4) {
     // ------------------------------------------------------------ softmax
-    const int t = threadIdx.x;   // head
+    const int t = threadIdx.x;   // head within the group
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    auto wait_warp = [&](uint32_t bar, uint32_t parity) -> bool {
-      const bool w = __all_sync(0xffffffffu, tc::mbar_wait(bar, parity));
+    const uint32_t to = tmem + lane_base + C::kColO;
+    const uint32_t xs = sbase + C::kOffX;
+    auto all_ok = [&](bool w) -> bool {
+      w = __all_sync(0xffffffffu, w);
       if (!w) fail();
       return w;
     };
     float m_used = -CUDART_INF_F, l = 0.f;
-    float tail[C::kTailCols];
-#pragma unroll
-    for (int e = 0; e < C::kTailCols; ++e) tail[e] = 0.f;
     for (int j = 0; j < ntiles; ++j) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-      const int tok0 = t0 + j * C::kBN;
-      const bool tile_ok = tile_block(j) >= 0;
-      const int lim = tile_ok ? min(C::kBN, t1 - tok0) : 0;   // visible tokens of the tile
-      if (!wait_warp(BAR(kMSFull), j & 1)) break;
+      const int buf = j & 1;
+      const uint32_t ts = tmem + lane_base + 64u * buf;
+      if (!all_ok(tc::mbar_wait(BAR(kMSFull + buf), (j >> 1) & 1))) break;
       tc::tc_fence_after();
       float sc[C::kBN];
       {
-        uint32_t r[32];
-        tc::tmem_ld32(tmem + lane_base + C::kColX, r);
+        uint32_t r[2][32];
+        tc::tmem_ld32(ts, r[0]);
+        tc::tmem_ld32(ts + 32, r[1]);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < C::kBN; ++e) sc[e] = e < lim ? __uint_as_float(r[e]) : -CUDART_INF_F;
+        for (int e = 0; e < 32; ++e) {
+          sc[e] = __uint_as_float(r[0][e]);
+          sc[32 + e] = __uint_as_float(r[1][e]);
+        }
+      }
+      tc::tc_fence_before();
+      tc::mbar_arrive(BAR(kMSRead + buf));
+      // Add the peer's partial scores (sent by its exchange warps).
+      if (t == 0) tc::mbar_arrive_expect_tx(BAR(kMXFull + buf), C::kXBytes);
+      if (!all_ok(tc::mbar_wait_cluster(BAR(kMXFull + buf), (j >> 1) & 1))) break;
+      {
+        const uint32_t xb = xs + buf * C::kXBytes;
+        int e_row;
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(e_row) : "r"(xb + xoff(t, 8)) : "memory");
+        const float unit = __uint_as_float(static_cast<uint32_t>(112 + e_row) << 23);  // 2^(E-15)
+        const float bias_unit = kRoundBias * unit;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t v[4];
+          asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+                       : "r"(xb + xoff(t, c))
+                       : "memory");
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int lo = static_cast<int>(v[e] << 16) >> 16, hi = static_cast<int>(v[e]) >> 16;
+            sc[8 * c + 2 * e] += dequant(lo, unit, bias_unit);
+            sc[8 * c + 2 * e + 1] += dequant(hi, unit, bias_unit);
+          }
+        }
+      }
+      tc::mbar_arrive(BAR(kMXRead + buf));
+      // Loaded halves of this tile, from the producer's ring.
+      uint32_t vm;
+      {
+        const uint32_t tag = static_cast<uint32_t>(j) << 8;
+        uint32_t w = ring[j % kMlaRing];
+        for (int n = 0; (w & ~0xffu) != tag && n < tc::kWaitPolls; ++n) w = ring[j % kMlaRing];
+        if (!all_ok((w & ~0xffu) == tag)) break;
+        vm = w & 0x3u;
+      }
+      const int tok0 = t0 + j * C::kBN;
+      const int nvis = min(C::kBN, t1 - tok0);   // tokens of the tile inside the split
+      if (nvis < C::kBN || vm != 0x3u) {
+#pragma unroll
+        for (int e = 0; e < C::kBN; ++e) {
+          const bool vis = e < nvis && ((vm >> (e >> 5)) & 1u);
+          sc[e] = vis ? sc[e] : -CUDART_INF_F;
+        }
       }
       float mx;
       {
-        float m4[4] = {sc[0], sc[1], sc[2], sc[3]};
+        float m8[8];
 #pragma unroll
-        for (int e = 4; e < C::kBN; ++e) m4[e & 3] = fmaxf(m4[e & 3], sc[e]);
-        mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * scale_log2;
+        for (int k = 0; k < 8; ++k) m8[k] = fmaxf(sc[k], sc[8 + k]);
+#pragma unroll
+        for (int e = 16; e < C::kBN; e += 16)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) m8[k] = mmax3(m8[k], sc[e + k], sc[e + 8 + k]);
+        mx = mmax3(mmax3(m8[0], m8[1], m8[2]), mmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+        mx *= scale_log2;
       }
       const float m_new = fmaxf(m_used, mx);
       const bool need = m_new > m_used + 8.f;
       const float alpha = need ? mex2(m_used - m_new) : 1.f;
       if (need) m_used = m_new;
       const float mu = m_used == -CUDART_INF_F ? 0.f : m_used;
-      uint32_t pk[C::kBN / 2];
-      {
-        float l4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int c = 0; c < C::kBN / 2; ++c) {
-          const float p0 = mex2(fmaf(sc[2 * c], scale_log2, -mu));
-          const float p1 = mex2(fmaf(sc[2 * c + 1], scale_log2, -mu));
-          l4[c & 3] += p0 + p1;
-          pk[c] = pack_bf16(p0, p1);
-        }
-        l = l * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
-      }
-      // PV(j-1) and its tail have completed (X was freed before S(j)), so O
-      // can be rescaled here.
+      // Rescale O once PV(j-1) and PV(j-2) have completed (PV(j-3) has:
+      // it was issued before S(j)).
       if (__any_sync(0xffffffffu, need) && j > 0) {
+        if (j >= 2 && !all_ok(tc::mbar_wait(BAR(kMPDone + buf), ((j >> 1) - 1) & 1))) break;
+        if (!all_ok(tc::mbar_wait(BAR(kMPDone + (buf ^ 1)), ((j - 1) >> 1) & 1))) break;
+        tc::tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < C::kMainCols / 32; ++c) {
+        for (int c = 0; c < 256 / 32; ++c) {
           uint32_t r[32];
-          const uint32_t ta = tmem + lane_base + c * 32;
-          tc::tmem_ld32(ta, r);
+          tc::tmem_ld32(to + c * 32, r);
           tc::tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-          tc::tmem_st32(ta, r);
-        }
-        tc::tmem_wait_st();
-#pragma unroll
-        for (int e = 0; e < C::kTailCols; ++e) tail[e] *= alpha;
-      }
-      // P row t: 32 tokens = 4 core-matrix columns of 16 bytes.
-      {
-        const uint32_t pbase = sbase + C::kOffP;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint32_t dst = pbase + ((t >> 3) * 4 + c) * 128 + (t & 7) * 16;
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(pk[4 * c]),
-                       "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
-                       : "memory");
+          tc::tmem_st32(to + c * 32, r);
         }
       }
-      // Value rows of tokens the tile must not contribute (past the split or
-      // the whole tile when its block id is invalid) are zeroed: they may
-      // hold anything.
-      if (t < C::kBN && t >= lim) {
-        const uint32_t vb = sbase + C::kOffK + (j & 1) * C::kStageBytes;
+      // Value rows that must contribute nothing (past the split, or in a half
+      // that was not loaded) are zeroed: they may hold anything.
+      if (t < C::kBN && !(t < nvis && ((vm >> (t >> 5)) & 1u))) {
+        const uint32_t vb = sbase + C::kOffK + (j % C::kStages) * C::kStageBytes;
 #pragma unroll
-        for (int ch = 0; ch < C::kDv / 64; ++ch)
+        for (int ch = 0; ch < C::kLat; ++ch)
 #pragma unroll
           for (int c = 0; c < 8; ++c)
             asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(vb + ch * C::kKChunkBytes +
                                                                      msw128(t, c)),
                          "r"(0u)
                          : "memory");
+        tc::fence_proxy_async_smem();
       }
-      tc::fence_proxy_async_smem();
-      tc::tc_fence_before();
-      tc::mbar_arrive(BAR(kMPFull));
-      // Tail T(j) = P(j) V(j)[:, 448:512] lands in X together with PV(j).
-      if (!wait_warp(BAR(kMPvDone), j & 1)) break;
+      // P = exp2(s * scale_log2 - m_used), bf16 pairs into P buffer `buf`,
+      // once PV(j-2) has read it.
+      if (j >= 2 && !all_ok(tc::mbar_wait(BAR(kMPDone + buf), ((j >> 1) - 1) & 1))) break;
       tc::tc_fence_after();
+      const uint32_t tp = tmem + lane_base + C::kColP + 32u * buf;
       {
-        uint32_t r[2][32];
-        tc::tmem_ld32(tmem + lane_base + C::kColX, r[0]);
-        tc::tmem_ld32(tmem + lane_base + C::kColX + 32, r[1]);
-        tc::tmem_wait_ld();
+        float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          tail[e] += __uint_as_float(r[0][e]);
-          tail[32 + e] += __uint_as_float(r[1][e]);
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int c = h * 16 + e;
+            const float p0 = mex2(fmaf(sc[2 * c], scale_log2, -mu));
+            const float p1 = mex2(fmaf(sc[2 * c + 1], scale_log2, -mu));
+            l8[e & 7] += p0 + p1;
+            pk[e] = pack_bf16(p0, p1);
+          }
+          tc::tmem_st16(tp + h * 16, pk);
         }
+        l = l * alpha + (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
       }
+      tc::tmem_wait_st();
       tc::tc_fence_before();
-      tc::mbar_arrive(BAR(kMXFree));
+      tc::mbar_arrive(BAR(kMPFull + buf));
     }
     // ------------------------------------------------------------ epilogue
-    const bool ok = !__any_sync(0xffffffffu, *abort_flag != 0) && ntiles > 0;
+    bool ok = !__any_sync(0xffffffffu, *abort_flag != 0) && ntiles > 0;
+    // Every MMA has completed once the final commit has landed.
+    if (ok) ok = all_ok(tc::mbar_wait(BAR(kMFinal), 0));
     tc::tc_fence_after();
     const int head = hg * C::kH + t;
     float* dst = ws + ((static_cast<int64_t>(b) * H + head) * S + s) * (C::kDv + 1);
-    if (head >= H) {
-      // A row of the last, partial head group: computed, never stored.
-    } else if (ok) {
+    if (ok) {   // warp-uniform: TMEM loads are collective
       const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
-      for (int c = 0; c < C::kMainCols / 32; ++c) {
+      for (int c = 0; c < 256 / 32; ++c) {
         uint32_t r[32];
-        tc::tmem_ld32(tmem + lane_base + c * 32, r);
+        tc::tmem_ld32(to + c * 32, r);
         tc::tmem_wait_ld();
+        if (head < H) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) dst[c * 32 + e] = __uint_as_float(r[e]) * inv;
+          for (int e = 0; e < 32; ++e) dst[256 * rank + c * 32 + e] = __uint_as_float(r[e]) * inv;
+        }
       }
-#pragma unroll
-      for (int e = 0; e < C::kTailCols; ++e) dst[C::kMainCols + e] = tail[e] * inv;
-      dst[C::kDv] = l > 0.f ? (m_used + log2f(l)) * kLn2 : -CUDART_INF_F;
-    } else {
-      for (int e = 0; e < C::kDv; ++e) dst[e] = 0.f;
-      dst[C::kDv] = -CUDART_INF_F;
+      if (head < H && rank == 0)
+        dst[C::kDv] = l > 0.f ? (m_used + log2f(l)) * kLn2 : -CUDART_INF_F;
+    } else if (head < H) {
+      // Nothing visible (or an aborted pair): o = 0, lse = -inf.
+      for (int e = 0; e < 256; ++e) dst[256 * rank + e] = 0.f;
+      if (rank == 0) dst[C::kDv] = -CUDART_INF_F;
     }
-  } else if (warp == 4) {
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ exchange
+    const int t = threadIdx.x - 128;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t x_peer = tc::map_to_rank(sbase + C::kOffX, peer);
+    const uint32_t xfull_peer = tc::map_to_rank(BAR(kMXFull), peer);
+    for (int j = 0; j < ntiles; ++j) {
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+      const int buf = j & 1;
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(BAR(kMSFull + buf), (j >> 1) & 1))) {
+        fail();
+        break;
+      }
+      tc::tc_fence_after();
+      uint32_t r[2][32];
+      tc::tmem_ld32(tmem + lane_base + 64u * buf, r[0]);
+      tc::tmem_ld32(tmem + lane_base + 64u * buf + 32, r[1]);
+      tc::tmem_wait_ld();
+      // Visible tokens of the tile (descriptor from the producer's ring, read
+      // before S buffer `buf` is released): the others may hold anything and
+      // are sent as 0.
+      uint32_t vm;
+      {
+        const uint32_t tag = static_cast<uint32_t>(j) << 8;
+        uint32_t w = ring[j % kMlaRing];
+        for (int n = 0; (w & ~0xffu) != tag && n < tc::kWaitPolls; ++n) w = ring[j % kMlaRing];
+        if (!__all_sync(0xffffffffu, (w & ~0xffu) == tag)) {
+          fail();
+          break;
+        }
+        vm = w & 0x3u;
+      }
+      tc::tc_fence_before();
+      tc::mbar_arrive(BAR(kMSRead + buf));
+      const int nvis = min(C::kBN, t1 - (t0 + j * C::kBN));
+      float v[C::kBN];
+      float amax = 0.f;
+#pragma unroll
+      for (int e = 0; e < C::kBN; ++e) {
+        const bool vis = e < nvis && ((vm >> (e >> 5)) & 1u);
+        v[e] = vis ? __uint_as_float(r[e >> 5][e & 31]) : 0.f;
+        amax = fmaxf(amax, fabsf(v[e]));
+      }
+      // E with max |v| < 2^E (E = -100 for an all-zero row), and 2^(15 - E).
+      const int ebits = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu);
+      const int e_row = ebits == 0 ? -100 : min(ebits - 126, 127);
+      const float mul = __uint_as_float(static_cast<uint32_t>(142 - e_row) << 23);
+      // The peer has consumed what this CTA sent into buffer `buf` two
+      // tiles ago.
+      if (j >= 2 &&
+          !__all_sync(0xffffffffu,
+                      tc::mbar_wait_cluster(BAR(kMXEmpty + buf), ((j >> 1) - 1) & 1))) {
+        fail();
+        break;
+      }
+      const uint32_t dst = x_peer + buf * C::kXBytes;
+      const uint32_t full = xfull_peer + 8u * buf;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int e = c * 8;
+        tc::st_async_v4(dst + xoff(t, c), pack_q16(v[e], v[e + 1], mul),
+                        pack_q16(v[e + 2], v[e + 3], mul), pack_q16(v[e + 4], v[e + 5], mul),
+                        pack_q16(v[e + 6], v[e + 7], mul), full);
+      }
+      tc::st_async_v4(dst + xoff(t, 8), static_cast<uint32_t>(e_row), 0u, 0u, 0u, full);
+    }
+  } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
       constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, C::kBN, 0, 0);
-      constexpr uint32_t idesc_o256 = tc::idesc_bf16_f32(128, 256, 0, 1);
-      constexpr uint32_t idesc_o192 = tc::idesc_bf16_f32(128, 192, 0, 1);
-      constexpr uint32_t idesc_t64 = tc::idesc_bf16_f32(128, 64, 0, 1);
-      const uint32_t qs = sbase + C::kOffQ, ps = sbase + C::kOffP;
-      bool ok = ntiles == 0 || tc::mbar_wait(BAR(kMQFull), 0);
-      for (int j = 0; ok && j < ntiles; ++j) {
-        if (*abort_flag) { ok = false; break; }
-        const int st = j & 1;
-        if (!tc::mbar_wait(BAR(kMKFull + st), (j >> 1) & 1)) { ok = false; break; }
-        if (j > 0 && !tc::mbar_wait(BAR(kMXFree), (j - 1) & 1)) { ok = false; break; }
-        tc::tc_fence_after();
-        const uint32_t ks = sbase + C::kOffK + st * C::kStageBytes;
-        // S(j) = Q K(j)^T over the 576 columns: 9 chunks x 4 K-steps.
-#pragma unroll 1
-        for (int c = 0; c < C::kChunks; ++c) {
+      constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, 256, 0, 1);
+      const uint32_t qs = sbase + C::kOffQ, qr = sbase + C::kOffQr;
+      // S(j) = Q_r K_r(j)^T into S buffer j & 1: 4 latent chunks x 4 K-steps
+      // (128-byte swizzle) and the rope half, 2 K-steps (64-byte swizzle).
+      auto issue_s = [&](int j) {
+        const uint32_t ks = sbase + C::kOffK + (j % C::kStages) * C::kStageBytes;
+        const uint32_t d = tmem + 64u * (j & 1);
+#pragma unroll
+        for (int c = 0; c < C::kLat; ++c)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            tc::mma_bf16_ss(tmem + C::kColX,
-                            tc::smem_desc_sw128(qs + c * C::kQChunkBytes + kk * 32, 16, 1024),
+            tc::mma_bf16_ss(d, tc::smem_desc_sw128(qs + c * C::kQChunkBytes + kk * 32, 16, 1024),
                             tc::smem_desc_sw128(ks + c * C::kKChunkBytes + kk * 32, 16, 1024),
                             idesc_s, (c > 0 || kk > 0) ? 1u : 0u);
-        }
-        tc::mma_commit(BAR(kMSFull));
-        if (!tc::mbar_wait(BAR(kMPFull), j & 1)) { ok = false; break; }
-        tc::tc_fence_after();
-        // O[:, 0:448] += P V[:, 0:448];  X = P V[:, 448:512].
 #pragma unroll
-        for (int k = 0; k < C::kBN / 16; ++k) {
-          const uint64_t pd = smem_desc_noswz(ps + k * 2 * 128, 128, 512);
-          const uint32_t vrow = ks + k * 16 * 128;
-          const uint32_t acc = (j > 0 || k > 0) ? 1u : 0u;
-          tc::mma_bf16_ss(tmem + 0, pd, tc::smem_desc_sw128(vrow, C::kKChunkBytes, 1024),
-                          idesc_o256, acc);
-          tc::mma_bf16_ss(tmem + 256, pd,
-                          tc::smem_desc_sw128(vrow + 4 * C::kKChunkBytes, C::kKChunkBytes, 1024),
-                          idesc_o192, acc);
-          tc::mma_bf16_ss(tmem + C::kColX, pd,
-                          tc::smem_desc_sw128(vrow + 7 * C::kKChunkBytes, C::kKChunkBytes, 1024),
-                          idesc_t64, k > 0 ? 1u : 0u);
+        for (int kk = 0; kk < 2; ++kk)
+          tc::mma_bf16_ss(d, tc::smem_desc_sw64(qr + kk * 32, 512),
+                          tc::smem_desc_sw64(ks + C::kLat * C::kKChunkBytes + kk * 32, 512),
+                          idesc_s, 1u);
+        tc::mma_commit(BAR(kMSFull + (j & 1)));
+      };
+      auto wait_k = [&](int j) {
+        return tc::mbar_wait(BAR(kMKFull + j % C::kStages), (j / C::kStages) & 1);
+      };
+      // O_r += P(j) V_r(j): P from TMEM (8 columns = 16 tokens per K-step),
+      // V_r = the 4 latent chunks of the stage, N = 256.
+      auto issue_pv = [&](int j) {
+        const uint32_t vs = sbase + C::kOffK + (j % C::kStages) * C::kStageBytes;
+        const uint32_t pa = tmem + C::kColP + 32u * (j & 1);
+#pragma unroll
+        for (int k = 0; k < C::kBN / 16; ++k)
+          tc::mma_bf16_ts(tmem + C::kColO, pa + k * 8,
+                          tc::smem_desc_sw128(vs + k * 16 * 128, C::kKChunkBytes, 1024), idesc_o,
+                          (j > 0 || k > 0) ? 1u : 0u);
+        tc::mma_commit(BAR(kMPDone + (j & 1)));
+        tc::mma_commit(BAR(kMKEmpty + j % C::kStages));
+      };
+      bool ok = ntiles == 0 || tc::mbar_wait(BAR(kMQFull), 0);
+      for (int j = 0; ok && j < 2 && j < ntiles; ++j) {
+        ok = wait_k(j);
+        if (ok) {
+          tc::tc_fence_after();
+          issue_s(j);
         }
-        tc::mma_commit(BAR(kMPvDone));
-        tc::mma_commit(BAR(kMKEmpty + st));
+      }
+      // Per tile j: S(j+2) into S buffer j & 1 once S(j) has been read from
+      // it and K(j+2) has landed, and PV(j) once P(j) is written, in
+      // whichever order they become ready.
+      for (int j = 0; ok && j < ntiles; ++j) {
+        bool s_done = j + 2 >= ntiles, pv_done = false;
+        int n = 0;
+        for (; n < tc::kWaitPolls && !(s_done && pv_done); ++n) {
+          if (*abort_flag) break;
+          if (!s_done && tc::mbar_try_wait(BAR(kMSRead + (j & 1)), (j >> 1) & 1) &&
+              tc::mbar_try_wait(BAR(kMKFull + (j + 2) % C::kStages), ((j + 2) / C::kStages) & 1)) {
+            tc::tc_fence_after();
+            issue_s(j + 2);
+            s_done = true;
+          }
+          if (!pv_done && tc::mbar_try_wait(BAR(kMPFull + (j & 1)), (j >> 1) & 1)) {
+            tc::tc_fence_after();
+            issue_pv(j);
+            pv_done = true;
+          }
+        }
+        if (!(s_done && pv_done)) ok = false;
       }
       if (!ok && !*abort_flag) fail();
       tc::mma_commit(BAR(kMFinal));
       if (!tc::mbar_wait(BAR(kMFinal), 0)) fail();
     }
-  } else {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ TMA producer
+    // Lane i < 10 owns box i % 5 (latent chunk 0-3, or the rope half) of the
+    // 32-token half i / 5 of every tile.
     if (lane == 0) {
       tc::tma_prefetch_desc(&q_map);
+      tc::tma_prefetch_desc(&qr_map);
       tc::tma_prefetch_desc(&c_map);
+      tc::tma_prefetch_desc(&cr_map);
     }
+    const int half = lane / 5, box = lane % 5;
+    const bool box_lane = lane < 10;
+    if (ntiles > 0) {
+      if (lane == 0)
+        tc::mbar_arrive_expect_tx(BAR(kMQFull), C::kLat * C::kQChunkBytes + C::kQRopeBytes);
+      __syncwarp();
+      const int row = b * H + hg * C::kH;
+      if (lane < C::kLat)
+        tc::tma_load_2d_(sbase + C::kOffQ + lane * C::kQChunkBytes, &q_map, BAR(kMQFull),
+                         256 * static_cast<int>(rank) + 64 * lane, row);
+      else if (lane == C::kLat)
+        tc::tma_load_2d_(sbase + C::kOffQr, &qr_map, BAR(kMQFull), 512 + 32 * static_cast<int>(rank),
+                         row);
+    }
+    // Half `half` of tile j lies inside the split iff its first token does.
+    auto in_split = [&](int j) -> bool {
+      return box_lane && j < ntiles && t0 + j * C::kBN + half * C::kBox < t1;
+    };
+    // Raw table entry of that half (-1 outside the split or past the table).
+    // Loaded three tiles ahead and validated only when used, so that the
+    // load's latency never stalls the issue of the current tile.
+    auto raw_block = [&](int j) -> int {
+      if (!in_split(j)) return -1;
+      const int idx = (t0 + j * C::kBN + half * C::kBox) / bs;
+      return idx < max_blocks ? __ldg(table + idx) : -1;
+    };
     auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, tc::mbar_wait(bar, parity));
     };
-    if (ntiles > 0) {
-      if (lane == 0) tc::mbar_arrive_expect_tx(BAR(kMQFull), C::kChunks * C::kQChunkBytes);
-      __syncwarp();
-      if (lane < C::kChunks)
-        tc::tma_load_2d_(sbase + C::kOffQ + lane * C::kQChunkBytes, &q_map, BAR(kMQFull),
-                         lane * 64, b * H + hg * C::kH);
-    }
     int issued = 0;
     bool ok = true;
-    int blk_next = ntiles > 0 ? tile_block(0) : -1;
+    int r0 = raw_block(0), r1 = raw_block(1), r2 = raw_block(2);
     for (int j = 0; j < ntiles; ++j) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-      const int st = j & 1;
-      if (j >= 2 && !wait_all(BAR(kMKEmpty + st), ((j >> 1) - 1) & 1)) { ok = false; break; }
-      const int blk = blk_next;
-      blk_next = j + 1 < ntiles ? tile_block(j + 1) : -1;
+      const int st = j % C::kStages;
+      if (j >= C::kStages && !wait_all(BAR(kMKEmpty + st), ((j / C::kStages) - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      const int r3 = raw_block(j + 3);
+      // The id, -1 (outside the split) or -2 (invalid id).
+      const int blk = !in_split(j) ? -1 : (r0 >= 0 && r0 < num_blocks) ? r0 : -2;
+      r0 = r1;
+      r1 = r2;
+      r2 = r3;
+      // Lanes 0 and 5 speak for halves 0 and 1.
+      const unsigned loaded = __ballot_sync(0xffffffffu, blk >= 0);
+      const unsigned bad = __ballot_sync(0xffffffffu, blk == -2);
+      const uint32_t mask = ((loaded >> 0) & 1u) | (((loaded >> 5) & 1u) << 1);
       const uint32_t full = BAR(kMKFull + st);
       if (lane == 0) {
-        if (blk < 0) record_error(err, PA_DEVERR_BLOCK_ID);
-        tc::mbar_arrive_expect_tx(full, blk >= 0 ? C::kStageBytes : 0u);
+        if (bad != 0u) record_error(err, PA_DEVERR_BLOCK_ID);
+        ring[j % kMlaRing] = (static_cast<uint32_t>(j) << 8) | mask;
+        tc::mbar_arrive_expect_tx(full, static_cast<uint32_t>(__popc(mask)) * C::kHalfBytes);
       }
       __syncwarp();
-      if (blk >= 0 && lane < C::kChunks)
-        tc::tma_load_3d(sbase + C::kOffK + st * C::kStageBytes + lane * C::kKChunkBytes, &c_map,
-                        full, lane * 64, (t0 + j * C::kBN) % bs, blk);
+      if (blk >= 0) {
+        const uint32_t stage = sbase + C::kOffK + st * C::kStageBytes;
+        const int tok = (t0 + j * C::kBN + half * C::kBox) % bs;
+        if (box < C::kLat)
+          tc::tma_load_3d(stage + box * C::kKChunkBytes + half * (C::kBox * 128), &c_map, full,
+                          256 * static_cast<int>(rank) + 64 * box, tok, blk);
+        else
+          tc::tma_load_3d(stage + C::kLat * C::kKChunkBytes + half * (C::kBox * 64), &cr_map, full,
+                          512 + 32 * static_cast<int>(rank), tok, blk);
+      }
       issued = j + 1;
     }
     if (lane == 0) {
       if (!ok) fail();
+      // No copy may still be landing when the CTA exits.
       if (ntiles > 0 && !tc::mbar_wait(BAR(kMQFull), 0)) fail();
-      for (int j = max(0, issued - 2); j < issued; ++j)
-        if (!tc::mbar_wait(BAR(kMKFull + (j & 1)), (j >> 1) & 1)) fail();
+      for (int j = max(0, issued - C::kStages); j < issued; ++j)
+        if (!tc::mbar_wait(BAR(kMKFull + j % C::kStages), (j / C::kStages) & 1)) fail();
+    }
+  } else if (warp == 10 && lane == 0) {
+    // ------------------------------------------------------------ exchange helper
+    const uint32_t xempty_peer = tc::map_to_rank(BAR(kMXEmpty), peer);
+    for (int j = 0; j < ntiles; ++j) {
+      bool w = false;
+      for (int n = 0; n < tc::kWaitPolls && !w; ++n) {
+        w = tc::mbar_try_wait(BAR(kMXRead + (j & 1)), (j >> 1) & 1);
+        if (!w && *abort_flag) break;
+      }
+      if (!w) break;
+      tc::mbar_arrive_remote(xempty_peer + 8u * (j & 1));
     }
   }
 
@@ -378,6 +641,9 @@ mla_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, C::kTmemCols);
   }
+  // Neither CTA leaves while the other may still write into its shared
+  // memory or arrive on its barriers.
+  tc::cluster_sync();
 }
 
 // ---------------------------------------------------------------- host side
@@ -399,13 +665,13 @@ PFN_cuTensorMapEncodeTiled_v12000 mla_encode_fn() {
 }
 
 bool encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
-            const cuuint64_t* strides, const cuuint32_t* box) {
+            const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swz) {
   auto fn = mla_encode_fn();
   if (fn == nullptr) return false;
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides,
-            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -415,28 +681,45 @@ cudaError_t launch_mla_tc(const void* q, const void* cache, const int32_t* block
                           int max_blocks, float scale, int S, int chunk, float* ws, void* out,
                           float* lse, int* err, cudaStream_t stream) {
   using C = MlaTcCfg;
-  CUtensorMap q_map, c_map;
+  // Query [B*H rows][576]: 64-column latent boxes and 32-column rope boxes of
+  // 128 heads.  Cache [nb][bs][576]: the same boxes over 32 tokens.
+  CUtensorMap q_map, qr_map, c_map, cr_map;
   {
     const cuuint64_t dims[2] = {C::kDk, static_cast<cuuint64_t>(B) * H};
     const cuuint64_t strides[1] = {C::kDk * 2};
     const cuuint32_t box[2] = {64, C::kH};
-    if (!encode(&q_map, q, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    const cuuint32_t box_r[2] = {32, C::kH};
+    if (!encode(&q_map, q, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode(&qr_map, q, 2, dims, strides, box_r, CU_TENSOR_MAP_SWIZZLE_64B))
+      return cudaErrorInvalidValue;
   }
   {
     const cuuint64_t dims[3] = {C::kDk, static_cast<cuuint64_t>(bs),
                                 static_cast<cuuint64_t>(num_blocks)};
     const cuuint64_t strides[2] = {C::kDk * 2, static_cast<cuuint64_t>(C::kDk) * 2 * bs};
-    const cuuint32_t box[3] = {64, C::kBN, 1};
-    if (!encode(&c_map, cache, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    const cuuint32_t box[3] = {64, C::kBox, 1};
+    const cuuint32_t box_r[3] = {32, C::kBox, 1};
+    if (!encode(&c_map, cache, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode(&cr_map, cache, 3, dims, strides, box_r, CU_TENSOR_MAP_SWIZZLE_64B))
+      return cudaErrorInvalidValue;
   }
   static DeviceFlags attr_set;
   cudaError_t e = set_smem_once(mla_tc_kernel, C::kSmemBytes, attr_set);
   if (e != cudaSuccess) return e;
-  dim3 grid(S, B, (H + C::kH - 1) / C::kH);
-  mla_tc_kernel<<<grid, C::kThreads, C::kSmemBytes, stream>>>(
-      q_map, c_map, block_table, seq_lens, max_blocks, H, bs, num_blocks, scale * kLog2e, S,
-      chunk, ws, err);
-  e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * S, B, (H + C::kH - 1) / C::kH);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, mla_tc_kernel, q_map, qr_map, c_map, cr_map, block_table, seq_lens,
+                         max_blocks, H, bs, num_blocks, scale * kLog2e, S, chunk, ws, err);
   if (e != cudaSuccess) return e;
   return launch_lse_merge(ws, B * H, S, C::kDv, out, lse, stream);
 }

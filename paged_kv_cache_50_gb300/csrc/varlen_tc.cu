@@ -191,14 +191,6 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
     record_error(err, PA_DEVERR_TIMEOUT);
     *abort_flag = 1;
   };
-  // The 16-token piece starting at `tok` is loaded iff it starts before
-  // kv_end and its block id is valid; returns the block id, -1 (past the
-  // visible range) or -2 (invalid id).
-  auto piece_block = [&](int tok) -> int {
-    if (tok >= kv_end) return -1;
-    const int blk = block_at(table, tok / bs, max_blocks);
-    return (blk >= 0 && blk < num_blocks) ? blk : -2;
-  };
 
   if (warp >= 4)
     tc::reg_alloc<C::kRegSoftmax>();
@@ -452,8 +444,9 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ K/V producer
-    // Lane p looks after the tile's 16-token piece p: its block id (fetched a
-    // tile ahead) and, if p % CL is this CTA's rank, its TMA boxes (one per
+    // Lane p looks after the tile's 16-token piece p: its block id (loaded
+    // three tiles ahead and validated only when used, so the load's latency
+    // never stalls an issue) and, if p % CL is this CTA's rank, its TMA boxes (one per
     // 64-column half), multicast to the whole cluster.  Every CTA expects
     // the bytes of all loaded pieces on its own barrier.  V(j) goes out before
     // K(j+2) (PV(j) needs it first) and reuses K(j)'s block ids.
@@ -461,8 +454,17 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
     const int pc = lane;
     const bool box_lane = lane < C::kBN / 16;
     const bool my_piece = box_lane && (pc % CL) == rank;
-    auto block_of = [&](int j) -> int {
-      return (box_lane && j < ntiles) ? piece_block(j * C::kBN + 16 * pc) : -1;
+    auto in_range = [&](int j) -> bool {
+      return box_lane && j < ntiles && j * C::kBN + 16 * pc < kv_end;
+    };
+    auto raw_of = [&](int j) -> int {
+      if (!in_range(j)) return -1;
+      const int idx = (j * C::kBN + 16 * pc) / bs;
+      return idx < max_blocks ? __ldg(table + idx) : -1;
+    };
+    // The piece's block id, -1 (not visible) or -2 (invalid id).
+    auto valid_of = [&](int j, int raw) -> int {
+      return !in_range(j) ? -1 : (raw >= 0 && raw < num_blocks) ? raw : -2;
     };
     auto issue = [&](int j, int blk, int which, uint32_t dst, uint32_t full) {
       const int tok0 = j * C::kBN;
@@ -503,23 +505,23 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
       issue(j, blk, 1, sbase + C::kOffV + st * C::kTileBytes, BAR(kVFull + st));
       return true;
     };
-    int b0 = block_of(0), b1 = block_of(1), b2 = block_of(2);   // tiles j, j+1, j+2
+    int r0 = raw_of(0), r1 = raw_of(1), r2 = raw_of(2);   // tiles j, j+1, j+2 (raw)
     int k_issued = 0, v_issued = 0;
     bool ok = true;
-    if (ntiles > 0) { ok = issue_k(0, b0); k_issued = 1; }
-    if (ok && ntiles > 1) { ok = issue_k(1, b1); k_issued = 2; }
+    if (ntiles > 0) { ok = issue_k(0, valid_of(0, r0)); k_issued = 1; }
+    if (ok && ntiles > 1) { ok = issue_k(1, valid_of(1, r1)); k_issued = 2; }
     for (int j = 0; ok && j < ntiles; ++j) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-      if (!issue_v(j, b0)) { ok = false; break; }
+      if (!issue_v(j, valid_of(j, r0))) { ok = false; break; }
       v_issued = j + 1;
-      const int b3 = block_of(j + 3);   // in flight while K(j+2) waits for its stage
+      const int r3 = raw_of(j + 3);   // in flight while K(j+2) waits for its stage
       if (j + 2 < ntiles) {
-        if (!issue_k(j + 2, b2)) { ok = false; break; }
+        if (!issue_k(j + 2, valid_of(j + 2, r2))) { ok = false; break; }
         k_issued = j + 3;
       }
-      b0 = b1;
-      b1 = b2;
-      b2 = b3;
+      r0 = r1;
+      r1 = r2;
+      r2 = r3;
     }
     if (lane == 0) {
       if (!ok) fail();
