@@ -366,9 +366,11 @@ def secondary(pa, device, pk):
 
 
 def mla_splits(m, sms):
-    """Splits for the MLA workload: enough (request, split) CTAs for two
-    waves of 2 head groups per SM."""
-    return max(1, min(8, math.ceil(2 * sms / (m.batch * max(1, m.num_heads // 64)))))
+    """Splits for the MLA workload: each (request, split, 128-head group) runs
+    on a pair of SMs, so enough splits to give every pair slot one unit, and
+    no more (each split adds a 128 x 513 fp32 partial per request)."""
+    groups = max(1, (m.num_heads + 127) // 128)
+    return max(1, min(8, math.ceil((sms // 2) / (m.batch * groups))))
 
 
 def _timed_with_flush(fn, flush, reps):

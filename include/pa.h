@@ -165,7 +165,9 @@ pa_status pa_lse_merge(const float* workspace, int num_seqs, int num_q_heads,
  * out: [batch, num_heads, kv_lora_rank] bf16.  lse: [batch, num_heads] fp32, nullable.
  * The call runs split-KV stage 1 into `workspace`
  * (pa_decode_workspace_bytes(batch, num_heads, num_splits, kv_lora_rank) bytes,
- * splits cut as for pa_decode_splitkv from max_seq_len) and then the LSE merge.
+ * splits cut as for pa_decode_splitkv from max_seq_len) and then the LSE merge;
+ * with num_splits == 1 and `out` 16-byte aligned it writes out and lse
+ * directly and leaves the workspace untouched (it must still be passed).
  * Supported: kv_lora_rank == 512, rope_dim == 64, num_heads a multiple of 64,
  * block_size a multiple of 32.
  */

@@ -111,6 +111,7 @@ enum MlaBar {
   kMNumBars = 22
 };
 constexpr int kMlaRing = 4;   // tile descriptors passed from the producer
+constexpr int kMlaRankMax = 512;    // largest batch ranked by seq_len (B^2 comparisons)
 
 __device__ __forceinline__ uint32_t msw128(int r, int c) {
   return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
@@ -160,7 +161,8 @@ mla_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__
               const __grid_constant__ CUtensorMap c_map, const __grid_constant__ CUtensorMap cr_map,
               const int32_t* __restrict__ block_table, const int32_t* __restrict__ seq_lens,
               int max_blocks, int H, int bs, int num_blocks, float scale_log2, int S, int chunk,
-              float* __restrict__ ws, int* err) {
+              float* __restrict__ ws, __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
+              int direct, int* err) {
   using C = MlaTcCfg;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -169,8 +171,33 @@ mla_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__
 
   const uint32_t rank = tc::cluster_rank();           // 0 or 1
   const uint32_t peer = rank ^ 1u;
-  const int s = blockIdx.x >> 1, b = blockIdx.y, hg = blockIdx.z;
+  const int s = blockIdx.x >> 1, hg = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Pair row y of the grid takes the request of rank y in decreasing
+  // seq_len (ties by index), so that the longest requests are dispatched
+  // first and the last wave holds the short ones.  Every CTA ranks the whole
+  // batch itself (B^2 / 352 comparisons, in the exchange buffers, which are
+  // unused until after the cluster barrier below); batches above
+  // kMlaRankMax keep the grid order.
+  int b = blockIdx.y;
+  if (gridDim.y <= kMlaRankMax) {
+    const int nb = static_cast<int>(gridDim.y);
+    volatile int* sl = reinterpret_cast<volatile int*>(sgen + C::kOffX);
+    volatile int* pick = reinterpret_cast<volatile int*>(sgen + C::kOffBar + 8 * kMNumBars + 32);
+    for (int i = threadIdx.x; i < nb; i += blockDim.x) sl[i] = seq_lens[i];
+    __syncthreads();
+    for (int i = threadIdx.x; i < nb; i += blockDim.x) {
+      const int v = sl[i];
+      int rnk = 0;
+      for (int k = 0; k < nb; ++k) {
+        const int u = sl[k];
+        rnk += (u > v || (u == v && k < i)) ? 1 : 0;
+      }
+      if (rnk == static_cast<int>(blockIdx.y)) *pick = i;
+    }
+    __syncthreads();
+    b = *pick;
+  }
   const int seq = seq_lens[b];
   const long long a0 = static_cast<long long>(s) * chunk;
   const int t0 = static_cast<int>(a0 < seq ? a0 : seq);
@@ -375,7 +402,12 @@ mla_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__
     if (ok) ok = all_ok(tc::mbar_wait(BAR(kMFinal), 0));
     tc::tc_fence_after();
     const int head = hg * C::kH + t;
+    // One split: the output row (bf16) and LSE directly; else the split's
+    // partial row of the workspace.
     float* dst = ws + ((static_cast<int64_t>(b) * H + head) * S + s) * (C::kDv + 1);
+    uint4* orow = reinterpret_cast<uint4*>(out + (static_cast<int64_t>(b) * H + head) * C::kDv +
+                                           256 * rank);
+    const float lse_v = (ok && l > 0.f) ? (m_used + log2f(l)) * kLn2 : -CUDART_INF_F;
     if (ok) {   // warp-uniform: TMEM loads are collective
       const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
@@ -383,17 +415,33 @@ mla_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__
         uint32_t r[32];
         tc::tmem_ld32(to + c * 32, r);
         tc::tmem_wait_ld();
-        if (head < H) {
+        if (head < H && direct) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 w;
+            w.x = pack_bf16(__uint_as_float(r[v * 8 + 0]) * inv, __uint_as_float(r[v * 8 + 1]) * inv);
+            w.y = pack_bf16(__uint_as_float(r[v * 8 + 2]) * inv, __uint_as_float(r[v * 8 + 3]) * inv);
+            w.z = pack_bf16(__uint_as_float(r[v * 8 + 4]) * inv, __uint_as_float(r[v * 8 + 5]) * inv);
+            w.w = pack_bf16(__uint_as_float(r[v * 8 + 6]) * inv, __uint_as_float(r[v * 8 + 7]) * inv);
+            orow[c * 4 + v] = w;
+          }
+        } else if (head < H) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) dst[256 * rank + c * 32 + e] = __uint_as_float(r[e]) * inv;
         }
       }
-      if (head < H && rank == 0)
-        dst[C::kDv] = l > 0.f ? (m_used + log2f(l)) * kLn2 : -CUDART_INF_F;
     } else if (head < H) {
       // Nothing visible (or an aborted pair): o = 0, lse = -inf.
-      for (int e = 0; e < 256; ++e) dst[256 * rank + e] = 0.f;
-      if (rank == 0) dst[C::kDv] = -CUDART_INF_F;
+      if (direct)
+        for (int e = 0; e < 32; ++e) orow[e] = make_uint4(0, 0, 0, 0);
+      else
+        for (int e = 0; e < 256; ++e) dst[256 * rank + e] = 0.f;
+    }
+    if (head < H && rank == 0) {
+      if (!direct)
+        dst[C::kDv] = lse_v;
+      else if (lse != nullptr)
+        lse[static_cast<int64_t>(b) * H + head] = lse_v;
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------ exchange
@@ -718,9 +766,13 @@ cudaError_t launch_mla_tc(const void* q, const void* cache, const int32_t* block
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  // With one split each pair writes its output rows and LSE itself (16-byte
+  // vector stores), and the workspace and the merge are skipped.
+  const int direct = (S == 1 && (reinterpret_cast<uintptr_t>(out) & 15u) == 0) ? 1 : 0;
   e = cudaLaunchKernelEx(&cfg, mla_tc_kernel, q_map, qr_map, c_map, cr_map, block_table, seq_lens,
-                         max_blocks, H, bs, num_blocks, scale * kLog2e, S, chunk, ws, err);
-  if (e != cudaSuccess) return e;
+                         max_blocks, H, bs, num_blocks, scale * kLog2e, S, chunk, ws,
+                         static_cast<__nv_bfloat16*>(out), lse, direct, err);
+  if (e != cudaSuccess || direct) return e;
   return launch_lse_merge(ws, B * H, S, C::kDv, out, lse, stream);
 }
 

@@ -331,12 +331,14 @@ def test_mla_small_all_heads(pa):
 
 def test_mla_workload_full_size_sampled(pa):
     b = workloads.mla_decode()
-    out, lse = _mla(pa, b, 2, b.pool)
     mask = np.zeros(b.batch, np.uint8)
     mask[[0, int(np.argmax(b.seq_lens)), int(np.argmin(b.seq_lens)), 77]] = 1
     ref_o, ref_l = oracle.mla_decode(b.q, b.pool, b.block_table, b.seq_lens, b.scale,
                                      req_mask=mask)
     rows = mask.astype(bool)
-    assert_out_close(out[rows], ref_o[rows], "mla out")
-    assert_lse_close(lse[rows], ref_l[rows], "mla lse")
-    assert np.isfinite(out).all() and np.isfinite(lse).all()
+    # One split (the output written by the stage-1 kernel) and two (the merge).
+    for S in (1, 2):
+        out, lse = _mla(pa, b, S, b.pool)
+        assert_out_close(out[rows], ref_o[rows], f"mla out S={S}")
+        assert_lse_close(lse[rows], ref_l[rows], f"mla lse S={S}")
+        assert np.isfinite(out).all() and np.isfinite(lse).all()
