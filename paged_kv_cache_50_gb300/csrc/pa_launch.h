@@ -21,13 +21,7 @@ cudaError_t launch_decode_splitkv(const void* q, const void* cache, const int32_
 cudaError_t launch_lse_merge(const float* ws, int NH, int S, int dv, void* out, float* lse,
                              cudaStream_t stream);
 
-cudaError_t launch_varlen_fwd(const void* q, const void* cache, const int32_t* block_table,
-                              const int32_t* qsl, const int32_t* seq_lens, int N, int Hq, int Hkv,
-                              int d, int bs, int num_blocks, int max_blocks, int max_query_len,
-                              float scale, int causal, void* out, float* lse, int* err,
-                              cudaStream_t stream);
-
-// The same operation on tcgen05 tensor cores with TMA-gathered K/V.
+// Varlen paged attention on tcgen05 tensor cores with TMA-gathered K/V.
 cudaError_t launch_varlen_tc(const void* q, const void* cache, const int32_t* block_table,
                              const int32_t* qsl, const int32_t* seq_lens, int N, int Hq, int Hkv,
                              int d, int bs, int num_blocks, int max_blocks, int max_query_len,
@@ -39,12 +33,6 @@ cudaError_t launch_mla_tc(const void* q, const void* cache, const int32_t* block
                           const int32_t* seq_lens, int B, int H, int bs, int num_blocks,
                           int max_blocks, float scale, int S, int chunk, float* ws, void* out,
                           float* lse, int* err, cudaStream_t stream);
-
-// MLA stage 1 (warp-level mma) + merge.
-cudaError_t launch_mla_decode(const void* q, const void* cache, const int32_t* block_table,
-                              const int32_t* seq_lens, int B, int H, int bs, int num_blocks,
-                              int max_blocks, float scale, int S, int chunk, float* ws, void* out,
-                              float* lse, int* err, cudaStream_t stream);
 
 // Device address of the error word on the current device (nullptr on error).
 int* device_error_word();
