@@ -170,16 +170,17 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
-  __syncwarp();
+  __syncthreads();
   if (warp == 0) tc::tmem_alloc(tmem_slot, C::kTmemCols);
   tc::tc_fence_before();
-  // Every barrier of the cluster is initialised before any CTA multicasts.
-  if (CL > 1)
-    tc::cluster_sync();
-  else
-    __syncthreads();
-  tc::tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sgen + C::kOffBar + 8 * kNumBars);
+  // Every barrier of the cluster is initialised before any CTA multicasts:
+  // each CTA arrives on the cluster barrier now and waits for it just before
+  // its first use of a peer or of TMEM, so the Q rows and the first block ids
+  // are fetched while the peer starts up.
+  tc::cluster_arrive();
+  auto tmem_base = [&]() {
+    return *reinterpret_cast<volatile uint32_t*>(sgen + C::kOffBar + 8 * kNumBars);
+  };
   constexpr uint16_t kMask = static_cast<uint16_t>((1u << CL) - 1u);
   auto release = [&](uint32_t bar) {   // frees a K/V stage in every CTA of the cluster
     if (CL > 1)
@@ -222,6 +223,9 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(BAR(kQFull));
     }
+    tc::cluster_wait();
+    tc::tc_fence_after();
+    const uint32_t tmem = tmem_base();
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t ts = tmem + lane_base + C::col_s(x), to = tmem + lane_base + C::col_o(x);
     // TMEM loads and stores are warp-collective: every decision to skip or
@@ -380,6 +384,9 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
     }
   } else if (warp == 0) {
     // ------------------------------------------------------------ MMA issue
+    tc::cluster_wait();
+    tc::tc_fence_after();
+    const uint32_t tmem = tmem_base();
     if (lane == 0) {
       constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, C::kBN, 0, 0);
       constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, D, 0, 1);
@@ -506,6 +513,7 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
       return true;
     };
     int r0 = raw_of(0), r1 = raw_of(1), r2 = raw_of(2);   // tiles j, j+1, j+2 (raw)
+    tc::cluster_wait();
     int k_issued = 0, v_issued = 0;
     bool ok = true;
     if (ntiles > 0) { ok = issue_k(0, valid_of(0, r0)); k_issued = 1; }
@@ -531,13 +539,15 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
       for (int j = max(0, v_issued - 2); j < v_issued; ++j)
         if (!tc::mbar_wait(BAR(kVFull + (j & 1)), (j >> 1) & 1)) fail();
     }
+  } else {
+    tc::cluster_wait();   // idle warps
   }
 
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem, C::kTmemCols);
+    tc::tmem_dealloc(tmem_base(), C::kTmemCols);
   }
   // No CTA leaves while a peer may still multicast into its shared memory or
   // arrive on its barriers.
