@@ -15,6 +15,9 @@ __global__ void __launch_bounds__(256)
 reshape_and_cache_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value,
                          uint4* __restrict__ cache, const int64_t* __restrict__ slot_mapping,
                          int row_vec, int block_size, int64_t num_slots, int* err) {
+  // The attention kernel that follows may start setting up now (it waits for
+  // this kernel's completion before reading anything).
+  pdl_trigger();
   const int t = blockIdx.x;
   const int64_t slot = slot_mapping[t];
   if (slot < 0) return;

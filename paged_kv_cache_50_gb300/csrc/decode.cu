@@ -65,6 +65,8 @@ decode_splitkv_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tid4 = lane & 3;
 
+  // Every input may come from the previous kernel in the stream.
+  pdl_wait();
   const int seq = seq_lens[i];
   // Split s covers [s*chunk, (s+1)*chunk) of the request (the last split runs
   // to the end), chunk being one block-aligned size for the whole batch.
@@ -213,6 +215,8 @@ decode_splitkv_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
     }
   }
   cp_async_wait<0>();
+  // The merge may start launching (it waits for this kernel to complete).
+  pdl_trigger();
 
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
@@ -271,6 +275,7 @@ lse_merge_kernel(const float* __restrict__ ws, int S, int dv, __nv_bfloat16* __r
                  float* __restrict__ lse) {
   extern __shared__ float wsh[];   // [S] weights, then 32 floats of reduction scratch
   float* red = wsh + S;
+  pdl_wait();
   const int64_t nh = blockIdx.x;
   const float* base = ws + nh * S * static_cast<int64_t>(dv + 1);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -324,11 +329,10 @@ static cudaError_t launch_decode_t(const void* q, const void* cache, const int32
   static DeviceFlags attr_set;
   cudaError_t e = set_smem_once(kern, C::kSmemBytes, attr_set);
   if (e != cudaSuccess) return e;
-  dim3 grid(S, Hkv, N);
-  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(
-      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(cache), block_table,
-      seq_lens, max_blocks, Hq, Hkv, bs, num_blocks, scale * kLog2e, S, chunk, ws, err);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(S, Hkv, N), dim3(C::kThreads), C::kSmemBytes, stream,
+                    static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(cache),
+                    block_table, seq_lens, max_blocks, Hq, Hkv, bs, num_blocks, scale * kLog2e, S,
+                    chunk, ws, err);
 }
 
 cudaError_t launch_decode_splitkv(const void* q, const void* cache, const int32_t* block_table,
@@ -348,8 +352,8 @@ cudaError_t launch_lse_merge(const float* ws, int NH, int S, int dv, void* out, 
   static DeviceFlags attr_set;
   cudaError_t e = set_smem_once(lse_merge_kernel, 200 * 1024, attr_set);
   if (e != cudaSuccess) return e;
-  lse_merge_kernel<<<NH, 128, smem, stream>>>(ws, S, dv, static_cast<__nv_bfloat16*>(out), lse);
-  return cudaGetLastError();
+  return launch_pdl(lse_merge_kernel, dim3(NH), dim3(128), smem, stream, ws, S, dv,
+                    static_cast<__nv_bfloat16*>(out), lse);
 }
 
 }  // namespace pa
