@@ -558,24 +558,26 @@ mla_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__
           issue_s(j);
         }
       }
-      // Per tile j: S(j+2) into S buffer j & 1 once S(j) has been read from
-      // it and K(j+2) has landed, and PV(j) once P(j) is written, in
-      // whichever order they become ready.
+      // Per tile j: PV(j) once P(j) is written, and S(j+2) into S buffer
+      // j & 1 once S(j) has been read from it and K(j+2) has landed, in
+      // whichever order they become ready -- PV first when both are, since
+      // the tensor pipe runs in issue order and PV(j) frees the K stage that
+      // K(j+3) is waiting for.
       for (int j = 0; ok && j < ntiles; ++j) {
         bool s_done = j + 2 >= ntiles, pv_done = false;
         int n = 0;
         for (; n < tc::kWaitPolls && !(s_done && pv_done); ++n) {
           if (*abort_flag) break;
+          if (!pv_done && tc::mbar_try_wait(BAR(kMPFull + (j & 1)), (j >> 1) & 1)) {
+            tc::tc_fence_after();
+            issue_pv(j);
+            pv_done = true;
+          }
           if (!s_done && tc::mbar_try_wait(BAR(kMSRead + (j & 1)), (j >> 1) & 1) &&
               tc::mbar_try_wait(BAR(kMKFull + (j + 2) % C::kStages), ((j + 2) / C::kStages) & 1)) {
             tc::tc_fence_after();
             issue_s(j + 2);
             s_done = true;
-          }
-          if (!pv_done && tc::mbar_try_wait(BAR(kMPFull + (j & 1)), (j >> 1) & 1)) {
-            tc::tc_fence_after();
-            issue_pv(j);
-            pv_done = true;
           }
         }
         if (!(s_done && pv_done)) ok = false;
