@@ -329,6 +329,22 @@ def test_mla_small_all_heads(pa):
     assert pa.pa_get_device_error() == 0
 
 
+@pytest.mark.parametrize("heads,bs", [(64, 32), (256, 128), (128, 32)])
+def test_mla_head_groups_and_block_sizes(pa, heads, bs):
+    """A head count below one 128-head group (spare rows computed, never
+    stored), two head groups, and blocks of 32 and 128 tokens (a 64-token
+    tile spans two blocks, or half a block); unused pool slots hold NaN."""
+    b = workloads.make_mla_batch(f"mla_h{heads}_bs{bs}", 52, [1, 33, 64, 130, 257, 0], heads,
+                                 block_size=bs, scale=1.0 / math.sqrt(192.0))
+    pool = _poison_mla(b)
+    ref_o, ref_l = oracle.mla_decode(b.q, pool, b.block_table, b.seq_lens, b.scale)
+    for S in (1, 2):
+        out, lse = _mla(pa, b, S, pool)
+        assert_out_close(out, ref_o, f"mla H={heads} bs={bs} S={S}")
+        assert_lse_close(lse, ref_l, f"mla lse H={heads} bs={bs} S={S}")
+    assert pa.pa_get_device_error() == 0
+
+
 def test_mla_workload_full_size_sampled(pa):
     b = workloads.mla_decode()
     mask = np.zeros(b.batch, np.uint8)
