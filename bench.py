@@ -209,14 +209,41 @@ def run_e2e(pa, b, step, steps, warmup, device):
           "table": step.table, "seq": step.seq}
     h2d = sum(t.numel() * t.element_size() for t in h.values())
     d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
-    stream = torch.cuda.current_stream()
-
-    def one(k):
+    def enqueue(k):
         for name, t in h.items():
             dv[name].copy_(t, non_blocking=True)
         step.run(k)
         out_h.copy_(step.out, non_blocking=True)
         lse_h.copy_(step.lse, non_blocking=True)
+
+    # The step (input copies, the three calls, output copies) is captured once
+    # per pool copy as a CUDA graph and replayed, with the host waiting for
+    # each step's result; if capture is not possible, the same work is issued
+    # call by call.
+    for k in range(warmup):
+        enqueue(k)
+        torch.cuda.current_stream().synchronize()
+    launch = "cuda graph per step"
+    graphs = []
+    try:
+        for k in range(len(step.pools)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                enqueue(k)
+            graphs.append(g)
+        for g in graphs:
+            g.replay()
+        torch.cuda.synchronize()
+    except RuntimeError:
+        graphs, launch = [], "eager"
+        torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    def one(k):
+        if graphs:
+            graphs[k % len(graphs)].replay()
+        else:
+            enqueue(k)
         stream.synchronize()
 
     for k in range(warmup):
@@ -225,7 +252,7 @@ def run_e2e(pa, b, step, steps, warmup, device):
     for k in range(steps):
         one(k)
     dt = time.perf_counter() - t0
-    return dt, h2d, d2h
+    return dt, h2d, d2h, launch
 
 
 def cpu_baseline_sample(b, budget_s=12.0, threads=None):
@@ -464,7 +491,7 @@ def main():
     sha = kernel_source_sha(["decode.cu", "pa_common.cuh"])
     traffic = profiled_traffic("decode_splitkv_gqa_decode.md", sha)
 
-    e2e_dt, h2d, d2h = run_e2e(pa, b, step, args.steps, warmup, device)
+    e2e_dt, h2d, d2h, e2e_launch = run_e2e(pa, b, step, args.steps, warmup, device)
     e2e_value = world * kv_bytes * args.steps / e2e_dt / 1e9
 
     sec = None
@@ -490,7 +517,7 @@ def main():
                              f"{kv_bytes / 1e9:.2f} GB", "parallelism": f"replicas x{world}"},
             "clocks": clk,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+                    "d2h_bytes_per_step": d2h, "launch": e2e_launch},
             "gpu_launches": 3 * args.steps,
             "roofline": {"bound": "hbm", "kernel": "decode_splitkv_kernel<128,3>",
                          "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
