@@ -340,7 +340,7 @@ cudaError_t launch_decode_splitkv(const void* q, const void* cache, const int32_
                                   int num_blocks, int max_blocks, float scale, int S, int chunk,
                                   float* ws, int* err, cudaStream_t stream) {
   if (d == 128)
-    return launch_decode_t<128, 3>(q, cache, block_table, seq_lens, N, Hq, Hkv, bs, num_blocks,
+    return launch_decode_t<128, 2>(q, cache, block_table, seq_lens, N, Hq, Hkv, bs, num_blocks,
                                    max_blocks, scale, S, chunk, ws, err, stream);
   return launch_decode_t<64, 4>(q, cache, block_table, seq_lens, N, Hq, Hkv, bs, num_blocks,
                                 max_blocks, scale, S, chunk, ws, err, stream);
