@@ -636,7 +636,7 @@ static cudaError_t launch_varlen_tc_t(const void* q, const void* cache, const in
 }
 
 // CTAs per cluster sharing K/V tiles by multicast.
-constexpr int kVarlenCluster = 2;
+constexpr int kVarlenCluster = 1;
 
 cudaError_t launch_varlen_tc(const void* q, const void* cache, const int32_t* block_table,
                              const int32_t* qsl, const int32_t* seq_lens, int N, int Hq, int Hkv,
