@@ -627,42 +627,54 @@ mla_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__
     };
     int issued = 0;
     bool ok = true;
-    int r0 = raw_block(0), r1 = raw_block(1), r2 = raw_block(2);
-    for (int j = 0; j < ntiles; ++j) {
-      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-      const int st = j % C::kStages;
-      if (j >= C::kStages && !wait_all(BAR(kMKEmpty + st), ((j / C::kStages) - 1) & 1)) {
-        ok = false;
-        break;
+    // Raw ids of tiles j .. j+3 in rr[j % 4]: the loop is unrolled four
+    // times so that every index is a constant and a load's value is first
+    // touched three iterations after it was issued (a register rotation
+    // would wait for it at once).
+    int rr[4] = {raw_block(0), raw_block(1), raw_block(2), -1};
+    bool go = true;
+    for (int jb = 0; go && jb < ntiles; jb += 4) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = jb + u;
+        if (!go || j >= ntiles) continue;
+        if (__any_sync(0xffffffffu, *abort_flag != 0)) {
+          go = false;
+          continue;
+        }
+        const int st = j % C::kStages;
+        if (j >= C::kStages && !wait_all(BAR(kMKEmpty + st), ((j / C::kStages) - 1) & 1)) {
+          ok = false;
+          go = false;
+          continue;
+        }
+        rr[(u + 3) & 3] = raw_block(j + 3);
+        const int r0 = rr[u];
+        // The id, -1 (outside the split) or -2 (invalid id).
+        const int blk = !in_split(j) ? -1 : (r0 >= 0 && r0 < num_blocks) ? r0 : -2;
+        // Lanes 0 and 5 speak for halves 0 and 1.
+        const unsigned loaded = __ballot_sync(0xffffffffu, blk >= 0);
+        const unsigned bad = __ballot_sync(0xffffffffu, blk == -2);
+        const uint32_t mask = ((loaded >> 0) & 1u) | (((loaded >> 5) & 1u) << 1);
+        const uint32_t full = BAR(kMKFull + st);
+        if (lane == 0) {
+          if (bad != 0u) record_error(err, PA_DEVERR_BLOCK_ID);
+          ring[j % kMlaRing] = (static_cast<uint32_t>(j) << 8) | mask;
+          tc::mbar_arrive_expect_tx(full, static_cast<uint32_t>(__popc(mask)) * C::kHalfBytes);
+        }
+        __syncwarp();
+        if (blk >= 0) {
+          const uint32_t stage = sbase + C::kOffK + st * C::kStageBytes;
+          const int tok = (t0 + j * C::kBN + half * C::kBox) % bs;
+          if (box < C::kLat)
+            tc::tma_load_3d(stage + box * C::kKChunkBytes + half * (C::kBox * 128), &c_map, full,
+                            256 * static_cast<int>(rank) + 64 * box, tok, blk);
+          else
+            tc::tma_load_3d(stage + C::kLat * C::kKChunkBytes + half * (C::kBox * 64), &cr_map,
+                            full, 512 + 32 * static_cast<int>(rank), tok, blk);
+        }
+        issued = j + 1;
       }
-      const int r3 = raw_block(j + 3);
-      // The id, -1 (outside the split) or -2 (invalid id).
-      const int blk = !in_split(j) ? -1 : (r0 >= 0 && r0 < num_blocks) ? r0 : -2;
-      r0 = r1;
-      r1 = r2;
-      r2 = r3;
-      // Lanes 0 and 5 speak for halves 0 and 1.
-      const unsigned loaded = __ballot_sync(0xffffffffu, blk >= 0);
-      const unsigned bad = __ballot_sync(0xffffffffu, blk == -2);
-      const uint32_t mask = ((loaded >> 0) & 1u) | (((loaded >> 5) & 1u) << 1);
-      const uint32_t full = BAR(kMKFull + st);
-      if (lane == 0) {
-        if (bad != 0u) record_error(err, PA_DEVERR_BLOCK_ID);
-        ring[j % kMlaRing] = (static_cast<uint32_t>(j) << 8) | mask;
-        tc::mbar_arrive_expect_tx(full, static_cast<uint32_t>(__popc(mask)) * C::kHalfBytes);
-      }
-      __syncwarp();
-      if (blk >= 0) {
-        const uint32_t stage = sbase + C::kOffK + st * C::kStageBytes;
-        const int tok = (t0 + j * C::kBN + half * C::kBox) % bs;
-        if (box < C::kLat)
-          tc::tma_load_3d(stage + box * C::kKChunkBytes + half * (C::kBox * 128), &c_map, full,
-                          256 * static_cast<int>(rank) + 64 * box, tok, blk);
-        else
-          tc::tma_load_3d(stage + C::kLat * C::kKChunkBytes + half * (C::kBox * 64), &cr_map, full,
-                          512 + 32 * static_cast<int>(rank), tok, blk);
-      }
-      issued = j + 1;
     }
     if (lane == 0) {
       if (!ok) fail();
