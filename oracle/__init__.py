@@ -67,6 +67,16 @@ def _bind(path):
         fn.restype = i32
     lib.oracle_bf16_to_f64.argtypes = [P, P, i64]
     lib.oracle_bf16_to_f64.restype = None
+    lib.oracle_e4m3_decode.argtypes = [P, P, i64]
+    lib.oracle_e4m3_decode.restype = None
+    lib.oracle_e4m3_encode_f32.argtypes = [P, P, i64]
+    lib.oracle_e4m3_encode_f32.restype = None
+    lib.oracle_reshape_and_cache_fp8.argtypes = [P, P, P, P, i64, i32, i32, i32, i64,
+                                                 ctypes.c_float, ctypes.c_float]
+    lib.oracle_reshape_and_cache_fp8.restype = i32
+    lib.oracle_dequant_pool_fp8.argtypes = [P, i64, i32, i32, i32, ctypes.c_float,
+                                            ctypes.c_float, P]
+    lib.oracle_dequant_pool_fp8.restype = None
     return lib
 
 
@@ -250,3 +260,59 @@ def bf16_to_f64(bits):
     out = np.empty(b.shape, np.float64)
     lib.oracle_bf16_to_f64(_ptr(b), _ptr(out), b.size)
     return out
+
+
+# ---------------------------------------------------------------- fp8 cache
+
+def e4m3_decode(codes):
+    """Values of e4m3 codes (uint8 array) as float64 (NaN for the NaN codes)."""
+    lib = _load()
+    c = _c(codes, np.uint8)
+    out = np.empty(c.shape, np.float64)
+    lib.oracle_e4m3_decode(_ptr(c), _ptr(out), c.size)
+    return out
+
+
+def e4m3_encode(x):
+    """Nearest e4m3 codes (ties to even, saturating at +-448) of float32 values."""
+    lib = _load()
+    xs = _c(x, np.float32)
+    out = np.empty(xs.shape, np.uint8)
+    lib.oracle_e4m3_encode_f32(_ptr(xs), _ptr(out), xs.size)
+    return out
+
+
+def reshape_and_cache_fp8(key, value, pool, slot_mapping, block_size, k_scale, v_scale):
+    """Step 1 into an fp8 pool: key/value [T, Hkv, d] bf16 bits, pool
+    [nb, 2, bs, Hkv, d] uint8 e4m3 codes.  Returns the updated pool (a copy)."""
+    lib = _load()
+    k = _c(key, np.uint16)
+    v = _c(value, np.uint16)
+    out = np.array(pool, dtype=np.uint8, copy=True, order="C")
+    sm = _c(slot_mapping, np.int64)
+    T, Hkv, d = k.shape
+    nb = out.shape[0]
+    rc = lib.oracle_reshape_and_cache_fp8(_ptr(k), _ptr(v), _ptr(out), _ptr(sm), T, Hkv, d,
+                                          int(block_size), nb, float(k_scale), float(v_scale))
+    if rc != 0:
+        raise ValueError("slot outside the pool")
+    return out
+
+
+def dequant_pool_fp8(pool, k_scale, v_scale):
+    """Values of an fp8 pool [nb, 2, bs, Hkv, d]: K codes times k_scale, V
+    codes times v_scale, as float64."""
+    lib = _load()
+    p = _c(pool, np.uint8)
+    nb, two, bs, Hkv, d = p.shape
+    out = np.empty(p.shape, np.float64)
+    lib.oracle_dequant_pool_fp8(_ptr(p), nb, bs, Hkv, d, float(k_scale), float(v_scale),
+                                _ptr(out))
+    return out
+
+
+def split_partials_fp8(q, pool, block_table, seq_lens, scale, k_scale, v_scale, num_splits,
+                       max_seq_len=None, threads=None):
+    """split_partials over the values of an fp8 pool (q: bf16 bits)."""
+    return split_partials(bf16_to_f64(q), dequant_pool_fp8(pool, k_scale, v_scale), block_table,
+                          seq_lens, scale, num_splits, max_seq_len=max_seq_len, threads=threads)

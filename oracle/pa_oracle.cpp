@@ -406,6 +406,97 @@ int oracle_mla_decode_f64(const double* q, const double* pool,
 
 // Exact bf16 -> fp64 widening of n values (for callers that want the
 // oracle's view of a bf16 array).
+// ---------------------------------------------------------------- fp8 cache
+// The pages ("Triton and MLA", data flow: decode_attention_fwd always gets
+// the layer's k_scale / v_scale; "when the KV cache is BF16 the fp8 check is
+// a no-op") give only the read side: an fp8 cache entry c stands for
+// value(c) * scale.  The write side is read as its inverse: the code of a
+// new key x is the e4m3 value nearest to x / k_scale (ties to even),
+// computed in fp32 (the precision the quantising kernel works in), with
+// magnitudes past the largest finite e4m3 value (448) saturating to it.
+//
+// e4m3 (OCP FP8, "fn" variant): 1 sign bit, 4 exponent bits (bias 7), 3
+// mantissa bits; exponent 0 is subnormal (m * 2^-9); exponent 15 with
+// mantissa 7 is NaN; there is no infinity.
+
+double oracle_e4m3_value(uint8_t c) {
+  const int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  double v;
+  if (e == 15 && m == 7)
+    v = std::numeric_limits<double>::quiet_NaN();
+  else if (e == 0)
+    v = std::ldexp(static_cast<double>(m), -9);
+  else
+    v = std::ldexp(1.0 + m / 8.0, e - 7);
+  return sign ? -v : v;
+}
+
+uint8_t oracle_e4m3_encode(float x) {
+  if (std::isnan(x)) return 0x7F;
+  const uint8_t sign = std::signbit(x) ? 0x80 : 0x00;
+  const double a = std::fabs(static_cast<double>(x));
+  if (a >= 448.0) return sign | 0x7E;
+  if (a < std::ldexp(1.0, -6)) {
+    // Subnormal range: multiples of 2^-9 (m = 8 is the smallest normal).
+    const double m = std::nearbyint(a / std::ldexp(1.0, -9));
+    return sign | static_cast<uint8_t>(m);   // m <= 8 -> code 8 = 2^-6
+  }
+  int e2;
+  std::frexp(a, &e2);                  // a = f * 2^e2, f in [0.5, 1)
+  int e = e2 - 1;                      // a in [2^e, 2^(e+1))
+  double m = std::nearbyint(a / std::ldexp(1.0, e - 3));   // 8 .. 16
+  if (m >= 16.0) {
+    m = 8.0;
+    ++e;
+  }
+  const int field = e + 7;
+  if (field > 15 || (field == 15 && m - 8.0 >= 7.0)) return sign | 0x7E;
+  return sign | static_cast<uint8_t>((field << 3) | static_cast<int>(m - 8.0));
+}
+
+void oracle_e4m3_decode(const uint8_t* src, double* dst, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) dst[i] = oracle_e4m3_value(src[i]);
+}
+
+void oracle_e4m3_encode_f32(const float* src, uint8_t* dst, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) dst[i] = oracle_e4m3_encode(src[i]);
+}
+
+// Step 1 with an fp8 pool [nb][2][bs][Hkv][d] of e4m3 codes.
+int oracle_reshape_and_cache_fp8(const uint16_t* key, const uint16_t* value, uint8_t* pool,
+                                 const int64_t* slot_mapping, int64_t T, int Hkv, int d, int bs,
+                                 int64_t nb, float k_scale, float v_scale) {
+  const int64_t row = static_cast<int64_t>(Hkv) * d;
+  for (int64_t t = 0; t < T; ++t) {
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot >= nb * bs) return -1;
+    const int64_t blk = slot / bs, off = slot % bs;
+    uint8_t* kdst = pool + ((blk * 2 + 0) * bs + off) * row;
+    uint8_t* vdst = pool + ((blk * 2 + 1) * bs + off) * row;
+    for (int64_t e = 0; e < row; ++e) {
+      const float kx = static_cast<float>(widen(key[t * row + e]));
+      const float vx = static_cast<float>(widen(value[t * row + e]));
+      kdst[e] = oracle_e4m3_encode(kx / k_scale);
+      vdst[e] = oracle_e4m3_encode(vx / v_scale);
+    }
+  }
+  return 0;
+}
+
+// The pool's values: K entries value(c) * k_scale, V entries value(c) *
+// v_scale, in fp64 (exact: 4 significant bits times a float's 24).
+void oracle_dequant_pool_fp8(const uint8_t* pool, int64_t nb, int bs, int Hkv, int d,
+                             float k_scale, float v_scale, double* out) {
+  const int64_t half = static_cast<int64_t>(bs) * Hkv * d;
+  for (int64_t b = 0; b < nb; ++b)
+    for (int kv = 0; kv < 2; ++kv) {
+      const double sc = kv == 0 ? static_cast<double>(k_scale) : static_cast<double>(v_scale);
+      const int64_t base = (b * 2 + kv) * half;
+      for (int64_t e = 0; e < half; ++e) out[base + e] = oracle_e4m3_value(pool[base + e]) * sc;
+    }
+}
+
 void oracle_bf16_to_f64(const uint16_t* src, double* dst, int64_t n) {
   for (int64_t i = 0; i < n; ++i) dst[i] = widen(src[i]);
 }

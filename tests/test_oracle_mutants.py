@@ -24,6 +24,17 @@ MUTANTS = [
      "for (int e = 0; e < dv; ++e) V[p * dv + e] = widen(c[e + rope_dim]);"),
     ("cache_write_value_to_key", "std::memcpy(pool + ((blk * 2 + 1) * block_size + off) * row, value",
      "std::memcpy(pool + ((blk * 2 + 0) * block_size + off) * row, value"),
+    ("e4m3_ties_away_from_zero", "double m = std::nearbyint(a / std::ldexp(1.0, e - 3));",
+     "double m = std::round(a / std::ldexp(1.0, e - 3));"),
+    ("e4m3_overflow_to_nan", "if (a >= 448.0) return sign | 0x7E;",
+     "if (a >= 464.0) return sign | 0x7F;"),
+    ("e4m3_subnormal_step", "v = std::ldexp(static_cast<double>(m), -9);",
+     "v = std::ldexp(static_cast<double>(m), -10);"),
+    ("fp8_quantise_multiplies", "kdst[e] = oracle_e4m3_encode(kx / k_scale);",
+     "kdst[e] = oracle_e4m3_encode(kx * k_scale);"),
+    ("fp8_scales_swapped",
+     "const double sc = kv == 0 ? static_cast<double>(k_scale) : static_cast<double>(v_scale);",
+     "const double sc = kv == 0 ? static_cast<double>(v_scale) : static_cast<double>(k_scale);"),
 ]
 
 

@@ -390,3 +390,118 @@ def test_empty_request_gives_neg_inf_lse(oracle_lib):
     o, l = oracle_lib.lse_merge(part)
     assert np.isneginf(l[0]).all() and not o[0].any()
     assert np.isfinite(l[1]).all()
+
+
+# ---------------------------------------------------------------------------
+# fp8 (e4m3) cache: "Triton and MLA", data flow -- the decode kernel always
+# gets the layer's k_scale / v_scale and dequantises an fp8 cache itself.
+# The e4m3 format and its rounding are pinned against torch's float8_e4m3fn
+# (a library implementation of the OCP FP8 format), never against the oracle.
+# ---------------------------------------------------------------------------
+
+def _torch_e4m3_codes(x32):
+    return torch.from_numpy(np.ascontiguousarray(x32, np.float32)).to(
+        torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def _torch_e4m3_values(codes):
+    return torch.from_numpy(np.ascontiguousarray(codes, np.uint8)).view(
+        torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def test_fp8_decode_all_codes_match_torch(oracle_lib):
+    codes = np.arange(256, dtype=np.uint8)
+    mine, ref = oracle_lib.e4m3_decode(codes), _torch_e4m3_values(codes)
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(mine[ok], ref[ok])
+    assert mine[0x7E] == 448.0 and mine[0x01] == 2.0 ** -9   # largest, smallest
+
+
+def test_fp8_encode_matches_torch_and_ties_to_even(oracle_lib):
+    rng = np.random.default_rng(7)
+    x = (rng.standard_normal(100000) * np.exp(rng.uniform(-14, 6, 100000))).astype(np.float32)
+    x = x[np.abs(x) < 448]
+    assert np.array_equal(oracle_lib.e4m3_encode(x), _torch_e4m3_codes(x))
+    # Every finite value, and every midpoint between neighbours (a tie, which
+    # must go to the even code), with both signs.
+    vals = _torch_e4m3_values(np.arange(0x7F, dtype=np.uint8))   # 0 .. 448
+    mids = ((vals[:-1] + vals[1:]) / 2).astype(np.float32)
+    pts = np.concatenate([vals.astype(np.float32), mids])
+    pts = np.concatenate([pts, -pts])
+    assert np.array_equal(oracle_lib.e4m3_encode(pts), _torch_e4m3_codes(pts))
+    assert oracle_lib.e4m3_encode(np.array([1.0625], np.float32))[0] == 0x38   # 1.0625 -> 1.0
+
+
+def test_fp8_encode_saturates_and_keeps_signed_zero(oracle_lib):
+    x = np.array([448.0, 460.0, 479.0, 1e6, 3e38, -449.0, -1e30, 0.0, -0.0, 1e-30, -1e-30],
+                 np.float32)
+    assert list(oracle_lib.e4m3_encode(x)) == [0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0xFE,
+                                                0x00, 0x80, 0x00, 0x80]
+
+
+def test_fp8_cache_write_matches_torch_quantisation(oracle_lib):
+    b = workloads.tiny_paged()
+    ks, vs = 0.37, 0.61
+    pool0 = np.full(b.pool.shape, 0x5A, np.uint8)
+    out = oracle_lib.reshape_and_cache_fp8(b.key, b.value, pool0, b.slot_mapping, b.block_size,
+                                           ks, vs)
+    key32 = workloads.bf16_bits_to_f32(b.key)
+    val32 = workloads.bf16_bits_to_f32(b.value)
+    ref = pool0.copy()
+    s = b.slot_mapping
+    ref[s // b.block_size, 0, s % b.block_size] = _torch_e4m3_codes(key32 / np.float32(ks))
+    ref[s // b.block_size, 1, s % b.block_size] = _torch_e4m3_codes(val32 / np.float32(vs))
+    assert np.array_equal(out, ref)
+    skip = s.copy()
+    skip[0] = -1
+    out2 = oracle_lib.reshape_and_cache_fp8(b.key, b.value, pool0, skip, b.block_size, ks, vs)
+    assert np.array_equal(out2[s[0] // b.block_size, :, s[0] % b.block_size],
+                          pool0[s[0] // b.block_size, :, s[0] % b.block_size])
+
+
+def _fp8_decode_batch():
+    b = workloads.make_paged_batch("fp8", 23, [1, 17, 40, 64], [1, 1, 1, 1], 4, 2, 64, 16,
+                                   num_blocks=12)
+    rng = np.random.default_rng(5)
+    pool = rng.integers(0, 256, size=b.pool.shape, dtype=np.uint8)
+    pool[(pool & 0x7F) == 0x7F] = 0x3C        # no NaN codes
+    return b, pool
+
+
+def test_fp8_split_partials_equal_bf16_path_for_power_of_two_scales(oracle_lib):
+    # With scales 2^k every dequantised entry is exactly a bf16 value, so the
+    # fp8 path must agree exactly with the bf16 path on that bf16 pool.
+    b, pool = _fp8_decode_batch()
+    ks, vs = 0.125, 2.0
+    vals = _torch_e4m3_values(pool)
+    vals[:, 0] *= ks
+    vals[:, 1] *= vs
+    bits = workloads.f32_to_bf16_bits(vals.astype(np.float32))
+    assert np.array_equal(workloads.bf16_bits_to_f32(bits).astype(np.float64), vals)
+    q = b.q.reshape(b.num_seqs, b.num_q_heads, b.head_size)
+    p8 = oracle_lib.split_partials_fp8(q, pool, b.block_table, b.seq_lens, b.scale, ks, vs, 3)
+    p16 = oracle_lib.split_partials(q, bits, b.block_table, b.seq_lens, b.scale, 3)
+    assert np.array_equal(p8, p16)
+
+
+def test_fp8_decode_matches_torch_sdpa(oracle_lib):
+    b, pool = _fp8_decode_batch()
+    ks, vs = float(np.float32(0.37)), float(np.float32(0.61))   # scales are fp32 values
+    q = b.q.reshape(b.num_seqs, b.num_q_heads, b.head_size)
+    o, lse = oracle_lib.lse_merge(
+        oracle_lib.split_partials_fp8(q, pool, b.block_table, b.seq_lens, b.scale, ks, vs, 2))
+    vals = _torch_e4m3_values(pool)
+    g = b.num_q_heads // b.num_kv_heads
+    for i in range(b.num_seqs):
+        n = int(b.seq_lens[i])
+        pos = np.arange(n)
+        blk, off = b.block_table[i, pos // b.block_size], pos % b.block_size
+        K = torch.from_numpy(vals[blk, 0, off] * ks)          # [n, Hkv, d]
+        V = torch.from_numpy(vals[blk, 1, off] * vs)
+        qi = torch.from_numpy(workloads.bf16_bits_to_f32(q[i]).astype(np.float64))   # [Hq, d]
+        for h in range(b.num_q_heads):
+            s = (K[:, h // g] @ qi[h]) * b.scale
+            ref_o = torch.softmax(s, 0) @ V[:, h // g]
+            assert np.allclose(o[i, h], ref_o.numpy(), rtol=0, atol=1e-12)
+            assert abs(lse[i, h] - torch.logsumexp(s, 0).item()) < 1e-12
