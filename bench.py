@@ -383,8 +383,57 @@ def bench_mla(pa, device, pk, flush, reps=10):
     return res
 
 
+def device_fp8_pool(shape, seed, device):
+    """Uniformly random finite e4m3 codes (the NaN codes 0x7F / 0xFF excluded),
+    drawn on the device."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    r = torch.randint(0, 254, shape, generator=g, device=device, dtype=torch.uint8)
+    r += (r >= 0x7F).to(torch.uint8)
+    return r
+
+
+def bench_fp8_decode(pa, device, pk, flush, reps=10):
+    """Split-KV decode over an fp8 (e4m3) pool, on the GQA decode batch and the
+    long-context batch: stage 1 alone, and the whole step (quantising cache
+    write + stage 1 + merge)."""
+    res = {}
+    ks, vs = workloads.FP8_K_SCALE, workloads.FP8_V_SCALE
+    for make, seed in ((workloads.gqa_decode, 12), (workloads.long_decode, 14)):
+        b = make(with_pool=False)
+        N, hq, d = b.num_seqs, b.num_q_heads, b.head_size
+        pool = device_fp8_pool((b.num_blocks, 2, b.block_size, b.num_kv_heads, d), seed, device)
+        q = to_dev_bf16(b.q, device).view(N, hq, d)
+        key, value = to_dev_bf16(b.key, device), to_dev_bf16(b.value, device)
+        slots = to_dev(b.slot_mapping, torch.int64, device)
+        table = to_dev(b.block_table, torch.int32, device)
+        seq = to_dev(b.seq_lens, torch.int32, device)
+        mx = int(b.seq_lens.max())
+        S = pa.pa_num_kv_splits(mx, pa.pa_device_sm_count())
+        ws = pa.decode_workspace(N, hq, S, d, device=device)
+        o = torch.empty((N, hq, d), dtype=torch.bfloat16, device=device)
+        lo = torch.empty((N, hq), dtype=torch.float32, device=device)
+
+        def step():
+            pa.pa_reshape_and_cache_fp8(key, value, pool, slots, ks, vs)
+            pa.pa_decode_fp8(q, pool, table, seq, b.scale, ks, vs, ws, o, lo, mx)
+        st1 = _timed_with_flush(
+            lambda: pa.pa_decode_splitkv_fp8(q, pool, table, seq, b.scale, ks, vs, ws, mx),
+            flush, reps)
+        both = _timed_with_flush(step, flush, reps)
+        kv = b.kv_bytes() // 2                      # one byte per element
+        gbs = kv / (st1 * 1e-3) / 1e9
+        res[b.name] = {"num_splits": S, "stage1_ms": st1, "step_ms": both, "kv_bytes": kv,
+                       "stage1_gbs": gbs, "frac_of_hbm_peak": gbs / pk["hbm_gbs"],
+                       "step_gbs": kv / (both * 1e-3) / 1e9,
+                       "kernel": f"decode_splitkv_fp8_kernel<{d},{4 if d == 128 else 8}>"}
+        del pool, q, ws
+        torch.cuda.empty_cache()
+    return res
+
+
 SECONDARY = {"chunked_prefill": bench_prefill, "long_decode": bench_long_decode,
-             "mla_decode": bench_mla}
+             "mla_decode": bench_mla, "fp8_decode": bench_fp8_decode}
 
 
 def secondary(pa, device, pk):

@@ -177,6 +177,55 @@ pa_status pa_mla_decode(const void* q, const void* kv_cache, const int32_t* bloc
                         int max_seq_len, float scale, int num_splits, float* workspace, void* out,
                         float* lse, void* stream);
 
+/*
+ * fp8 KV cache.  The pool holds e4m3 codes (OCP FP8 "fn": 1 sign, 4 exponent
+ * bits with bias 7, 3 mantissa bits; largest finite 448; 0x7F / 0xFF NaN),
+ * one byte per element, in the standard layout [num_blocks, 2, block_size,
+ * num_kv_heads, head_size].  A K entry with code c stands for
+ * e4m3(c) * k_scale and a V entry for e4m3(c) * v_scale: the per-layer
+ * scales that the decode kernel always receives ("Triton and MLA", data flow,
+ * decode_attention_fwd's k_scale / v_scale).  Both scales must be finite
+ * and > 0 (else PA_ERR_INVALID).
+ */
+
+/*
+ * Step 1 with an fp8 pool: the quantising cache write.
+ *   For t < num_tokens with slot = slot_mapping[t] >= 0 and every (h, e):
+ *     kv_cache[slot / bs, 0, slot % bs, h, e] = E(key[t, h, e] / k_scale)
+ *     kv_cache[slot / bs, 1, slot % bs, h, e] = E(value[t, h, e] / v_scale)
+ *   where the quotient is the fp32 IEEE quotient of the bf16 value (widened
+ *   exactly) by the scale, and E is the e4m3 code nearest to it, ties to
+ *   even, magnitudes beyond 448 (infinities included) saturating to +-448;
+ *   NaN gives a NaN code.  Reading the write side as the inverse of the read
+ *   side is this library's reading; the pages state only the read side.
+ *   slot < 0 skips the token; a slot >= num_blocks * bs is not written and
+ *   sets PA_DEVERR_SLOT.
+ * key, value: [num_tokens, Hkv, d] bf16, 16-byte aligned.  kv_cache: fp8
+ * pool (bytes), 16-byte aligned, in-out.  Uses shape->num_kv_heads,
+ * head_size (a multiple of 16), block_size, num_blocks.  num_tokens == 0 is a
+ * no-op.
+ */
+pa_status pa_reshape_and_cache_fp8(const void* key, const void* value, void* kv_cache,
+                                   const int64_t* slot_mapping, int num_tokens,
+                                   const pa_shape* shape, float k_scale, float v_scale,
+                                   void* stream);
+
+/*
+ * Split-KV decode, stage 1, over an fp8 pool: pa_decode_splitkv with every
+ * K entry read as e4m3(c) * k_scale and every V entry as e4m3(c) * v_scale
+ * (same splits, same workspace layout and contents; merge with
+ * pa_lse_merge).  The products are taken on f16 tensor-core operands: the
+ * codes convert to f16 exactly, q is rounded bf16 -> f16 (exact for |q| in
+ * [2^-14, 65504]; larger magnitudes are not supported), and the softmax
+ * weights are rounded to f16; accumulation is fp32.
+ * q: [N, Hq, d] bf16, 4-byte aligned.  kv_cache: fp8 pool, 16-byte aligned.
+ * Supported: head_size in {64, 128}, Hq / Hkv <= 16.
+ */
+pa_status pa_decode_splitkv_fp8(const void* q, const void* kv_cache, const int32_t* block_table,
+                                const int32_t* seq_lens, const pa_shape* shape, float scale,
+                                float k_scale, float v_scale, int num_splits, int max_seq_len,
+                                float* workspace, void* stream);
+
 /* Size of the fixed device array pa_decode_noalloc keeps its split partials in. */
 #define PA_NOALLOC_WORKSPACE_BYTES (16u * 1024u * 1024u)
 

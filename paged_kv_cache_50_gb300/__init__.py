@@ -63,6 +63,8 @@ def lib() -> ctypes.CDLL:
         L.pa_decode_workspace_bytes.restype = ctypes.c_size_t
         L.pa_decode_splitkv.argtypes = [P, P, P, P, SP, f32, i32, i32, P, P]
         L.pa_lse_merge.argtypes = [P, i32, i32, i32, i32, P, P, P]
+        L.pa_reshape_and_cache_fp8.argtypes = [P, P, P, P, i32, SP, f32, f32, P]
+        L.pa_decode_splitkv_fp8.argtypes = [P, P, P, P, SP, f32, f32, f32, i32, i32, P, P]
         L.pa_mla_decode.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, f32,
                                     i32, P, P, P, P]
         L.pa_decode_noalloc.argtypes = [P, P, P, P, SP, f32, i32, i32, P, P, P]
@@ -72,7 +74,8 @@ def lib() -> ctypes.CDLL:
         L.pa_device_sm_count.argtypes = []
         L.pa_device_sm_count.restype = i32
         for name in ("pa_reshape_and_cache", "pa_varlen_fwd", "pa_decode_splitkv",
-                     "pa_lse_merge", "pa_mla_decode", "pa_get_device_error", "pa_decode_noalloc"):
+                     "pa_lse_merge", "pa_mla_decode", "pa_get_device_error", "pa_decode_noalloc",
+                     "pa_reshape_and_cache_fp8", "pa_decode_splitkv_fp8"):
             getattr(L, name).restype = st
         _lib = L
         return L
@@ -200,6 +203,57 @@ def pa_decode_splitkv(q, kv_cache, block_table, seq_lens, scale, workspace, max_
         ctypes.byref(shape), float(scale), int(workspace.shape[2]),
         _max_seq(seq_lens, max_seq_len), _dev(workspace, "workspace", torch.float32),
         _stream(stream)), "pa_decode_splitkv")
+
+
+def _codes(kv_cache: torch.Tensor) -> torch.Tensor:
+    """An fp8 pool as its bytes: uint8 codes, or float8_e4m3fn viewed as uint8."""
+    if isinstance(kv_cache, torch.Tensor) and kv_cache.dtype == torch.float8_e4m3fn:
+        return kv_cache.view(torch.uint8)
+    return kv_cache
+
+
+def pa_reshape_and_cache_fp8(key, value, kv_cache, slot_mapping, k_scale, v_scale,
+                             stream=None) -> None:
+    """Quantising cache write: key/value [T, Hkv, d] bf16 -> e4m3 codes of
+    key / k_scale and value / v_scale in the fp8 pool kv_cache
+    [nb, 2, bs, Hkv, d] (uint8 or float8_e4m3fn)."""
+    codes = _codes(kv_cache)
+    shape = _pool_shape(codes, 0, codes.shape[3], 1)
+    T = key.shape[0]
+    if tuple(key.shape) != (T, shape.num_kv_heads, shape.head_size) or value.shape != key.shape:
+        raise ValueError("key/value must be [num_tokens, num_kv_heads, head_size]")
+    if slot_mapping.shape != (T,):
+        raise ValueError("slot_mapping must be [num_tokens]")
+    _check(lib().pa_reshape_and_cache_fp8(
+        _dev(key, "key", torch.bfloat16), _dev(value, "value", torch.bfloat16),
+        _dev(codes, "kv_cache", torch.uint8), _dev(slot_mapping, "slot_mapping", torch.int64),
+        T, ctypes.byref(shape), float(k_scale), float(v_scale), _stream(stream)),
+        "pa_reshape_and_cache_fp8")
+
+
+def pa_decode_splitkv_fp8(q, kv_cache, block_table, seq_lens, scale, k_scale, v_scale,
+                          workspace, max_seq_len=None, stream=None) -> None:
+    """Split-KV stage 1 over an fp8 pool (entries = e4m3 value x k_scale or
+    v_scale): q [N, Hq, d] bf16 -> workspace [N, Hq, S, d + 1] fp32."""
+    codes = _codes(kv_cache)
+    N, hq, d = q.shape
+    if workspace.dim() != 4 or tuple(workspace.shape[:2]) != (N, hq) or workspace.shape[3] != d + 1:
+        raise ValueError("workspace must be [num_seqs, num_q_heads, num_splits, head_size + 1]")
+    shape = _pool_shape(codes, N, hq, block_table.shape[1])
+    _check(lib().pa_decode_splitkv_fp8(
+        _dev(q, "q", torch.bfloat16), _dev(codes, "kv_cache", torch.uint8),
+        _dev(block_table, "block_table", torch.int32), _dev(seq_lens, "seq_lens", torch.int32),
+        ctypes.byref(shape), float(scale), float(k_scale), float(v_scale),
+        int(workspace.shape[2]), _max_seq(seq_lens, max_seq_len),
+        _dev(workspace, "workspace", torch.float32), _stream(stream)), "pa_decode_splitkv_fp8")
+
+
+def pa_decode_fp8(q, kv_cache, block_table, seq_lens, scale, k_scale, v_scale, workspace,
+                  out=None, lse=None, max_seq_len=None, stream=None):
+    """Both split-KV stages over an fp8 pool."""
+    pa_decode_splitkv_fp8(q, kv_cache, block_table, seq_lens, scale, k_scale, v_scale,
+                          workspace, max_seq_len, stream)
+    return pa_lse_merge(workspace, out, lse, stream=stream)
 
 
 def pa_lse_merge(workspace, out=None, lse=None, return_lse=True, stream=None):

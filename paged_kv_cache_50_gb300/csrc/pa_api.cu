@@ -151,6 +151,52 @@ pa_status pa_decode_splitkv(const void* q, const void* kv_cache, const int32_t* 
       static_cast<cudaStream_t>(stream)));
 }
 
+static bool scale_ok(float x) { return x > 0.f && x <= 3.4028234663852886e38f; }
+
+pa_status pa_reshape_and_cache_fp8(const void* key, const void* value, void* kv_cache,
+                                   const int64_t* slot_mapping, int num_tokens,
+                                   const pa_shape* shape, float k_scale, float v_scale,
+                                   void* stream) {
+  if (shape == nullptr || num_tokens < 0) return PA_ERR_INVALID;
+  if (shape->num_kv_heads <= 0 || shape->head_size <= 0 || shape->block_size <= 0 ||
+      shape->block_size % 16 != 0 || shape->num_blocks <= 0)
+    return PA_ERR_INVALID;
+  if (!scale_ok(k_scale) || !scale_ok(v_scale)) return PA_ERR_INVALID;
+  if (shape->head_size % 16 != 0) return PA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PA_OK;
+  if (key == nullptr || value == nullptr || kv_cache == nullptr || slot_mapping == nullptr)
+    return PA_ERR_INVALID;
+  if (!aligned(key, 16) || !aligned(value, 16) || !aligned(kv_cache, 16) ||
+      !aligned(slot_mapping, 8))
+    return PA_ERR_INVALID;
+  return from_cuda(pa::launch_reshape_and_cache_fp8(
+      key, value, kv_cache, slot_mapping, num_tokens, shape->num_kv_heads, shape->head_size,
+      shape->block_size, shape->num_blocks, k_scale, v_scale, device_error_ptr(),
+      static_cast<cudaStream_t>(stream)));
+}
+
+pa_status pa_decode_splitkv_fp8(const void* q, const void* kv_cache, const int32_t* block_table,
+                                const int32_t* seq_lens, const pa_shape* shape, float scale,
+                                float k_scale, float v_scale, int num_splits, int max_seq_len,
+                                float* workspace, void* stream) {
+  if (!shape_ok(shape) || num_splits < 1 || num_splits > kMaxSplits || max_seq_len < 0)
+    return PA_ERR_INVALID;
+  if (!scale_ok(k_scale) || !scale_ok(v_scale)) return PA_ERR_INVALID;
+  if (shape->head_size != 64 && shape->head_size != 128) return PA_ERR_UNSUPPORTED;
+  if (shape->num_q_heads / shape->num_kv_heads > 16) return PA_ERR_UNSUPPORTED;
+  if (shape->num_seqs == 0) return PA_OK;
+  if (q == nullptr || kv_cache == nullptr || block_table == nullptr || seq_lens == nullptr ||
+      workspace == nullptr)
+    return PA_ERR_INVALID;
+  if (!aligned(q, 4) || !aligned(kv_cache, 16) || !aligned(workspace, 4)) return PA_ERR_INVALID;
+  return from_cuda(pa::launch_decode_splitkv_fp8(
+      q, kv_cache, block_table, seq_lens, shape->num_seqs, shape->num_q_heads,
+      shape->num_kv_heads, shape->head_size, shape->block_size, shape->num_blocks,
+      shape->max_blocks_per_seq, scale, k_scale, v_scale, num_splits,
+      static_cast<int>(pa::split_chunk(max_seq_len, num_splits, shape->block_size)), workspace,
+      device_error_ptr(), static_cast<cudaStream_t>(stream)));
+}
+
 pa_status pa_lse_merge(const float* workspace, int num_seqs, int num_q_heads, int num_splits,
                        int dv, void* out, float* lse, void* stream) {
   if (num_seqs < 0 || num_q_heads <= 0 || num_splits < 1 || num_splits > kMaxSplits || dv <= 0)

@@ -18,6 +18,18 @@ cudaError_t launch_decode_splitkv(const void* q, const void* cache, const int32_
                                   int num_blocks, int max_blocks, float scale, int S, int chunk,
                                   float* ws, int* err, cudaStream_t stream);
 
+// fp8 (e4m3) pool: quantising cache write and split-KV stage 1.
+cudaError_t launch_reshape_and_cache_fp8(const void* key, const void* value, void* cache,
+                                         const int64_t* slot_mapping, int num_tokens,
+                                         int num_kv_heads, int head_size, int block_size,
+                                         int num_blocks, float k_scale, float v_scale, int* err,
+                                         cudaStream_t stream);
+cudaError_t launch_decode_splitkv_fp8(const void* q, const void* cache,
+                                      const int32_t* block_table, const int32_t* seq_lens, int N,
+                                      int Hq, int Hkv, int d, int bs, int num_blocks,
+                                      int max_blocks, float scale, float k_scale, float v_scale,
+                                      int S, int chunk, float* ws, int* err, cudaStream_t stream);
+
 cudaError_t launch_lse_merge(const float* ws, int NH, int S, int dv, void* out, float* lse,
                              cudaStream_t stream);
 

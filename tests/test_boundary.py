@@ -168,3 +168,36 @@ def test_misaligned_pointers_are_rejected(pa):
     assert L.pa_reshape_and_cache(16, 24, 16, 16, 4, ctypes.byref(s), NULL) == pa.PA_ERR_INVALID
     assert L.pa_mla_decode(8, 16, 16, 16, 2, 128, 512, 64, 64, 8, 4, 256, 0.1, 2, 16, 16, NULL,
                            NULL) == pa.PA_ERR_INVALID
+
+
+def test_fp8_entry_points_reject_before_launch(pa):
+    L = pa.lib()
+    s = _shape(pa)
+    inf = float("inf")
+    for ks, vs in ((0.0, 1.0), (1.0, -2.0), (inf, 1.0), (1.0, float("nan"))):
+        assert L.pa_reshape_and_cache_fp8(16, 16, 16, 16, 4, ctypes.byref(s), ks, vs,
+                                          NULL) == pa.PA_ERR_INVALID
+        assert L.pa_decode_splitkv_fp8(16, 16, 16, 16, ctypes.byref(s), 0.1, ks, vs, 4, 64, 16,
+                                       NULL) == pa.PA_ERR_INVALID
+    # Codes move in 16-byte vectors: head sizes that are not a multiple of 16.
+    assert L.pa_reshape_and_cache_fp8(16, 16, 16, 16, 4, ctypes.byref(_shape(pa, head_size=24)),
+                                      1.0, 1.0, NULL) == pa.PA_ERR_UNSUPPORTED
+    assert L.pa_decode_splitkv_fp8(16, 16, 16, 16, ctypes.byref(_shape(pa, head_size=96)), 0.1,
+                                   1.0, 1.0, 4, 64, 16, NULL) == pa.PA_ERR_UNSUPPORTED
+    big_group = _shape(pa, num_q_heads=64, num_kv_heads=2)
+    assert L.pa_decode_splitkv_fp8(16, 16, 16, 16, ctypes.byref(big_group), 0.1, 1.0, 1.0, 4, 64,
+                                   16, NULL) == pa.PA_ERR_UNSUPPORTED
+    # Misaligned pool, null workspace, bad split counts.
+    assert L.pa_reshape_and_cache_fp8(16, 16, 24, 16, 4, ctypes.byref(s), 1.0, 1.0,
+                                      NULL) == pa.PA_ERR_INVALID
+    assert L.pa_decode_splitkv_fp8(16, 24, 16, 16, ctypes.byref(s), 0.1, 1.0, 1.0, 4, 64, 16,
+                                   NULL) == pa.PA_ERR_INVALID
+    assert L.pa_decode_splitkv_fp8(16, 16, 16, 16, ctypes.byref(s), 0.1, 1.0, 1.0, 4, 64, NULL,
+                                   NULL) == pa.PA_ERR_INVALID
+    assert L.pa_decode_splitkv_fp8(16, 16, 16, 16, ctypes.byref(s), 0.1, 1.0, 1.0, 0, 64, 16,
+                                   NULL) == pa.PA_ERR_INVALID
+    # Empty calls launch nothing.
+    assert L.pa_reshape_and_cache_fp8(NULL, NULL, NULL, NULL, 0, ctypes.byref(s), 1.0, 1.0,
+                                      NULL) == pa.PA_OK
+    assert L.pa_decode_splitkv_fp8(NULL, NULL, NULL, NULL, ctypes.byref(_shape(pa, num_seqs=0)),
+                                   0.1, 1.0, 1.0, 4, 64, NULL, NULL) == pa.PA_OK

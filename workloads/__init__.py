@@ -17,7 +17,10 @@ Recipe (the same for every workload):
     slot of each new token is slot = block_table[i][pos // bs] * bs + pos % bs
     ("Attention Backends", section "Code");
   * entries of ``block_table`` past a request's last block are -1, so a kernel
-    that read them would be caught.
+    that read them would be caught;
+  * an fp8 pool (same shape, one byte per element) is filled with uniformly
+    random finite e4m3 codes; its scales are the fixed FP8_K_SCALE and
+    FP8_V_SCALE.
 """
 
 from __future__ import annotations
@@ -199,6 +202,37 @@ def make_mla_batch(name, seed, seq_lens, num_heads, kv_lora_rank=512, rope_dim=6
         scale = 1.0 / math.sqrt(128 + rope_dim)
     return MLABatch(name, seed, num_heads, kv_lora_rank, rope_dim, block_size, nb,
                     seq_lens, table, q, pool, float(scale))
+
+
+# ---------------------------------------------------------------------------
+# fp8 (e4m3) KV cache inputs.
+# ---------------------------------------------------------------------------
+
+# Per-layer scales of the fp8 workloads: an fp8 K entry with code c stands for
+# e4m3(c) * FP8_K_SCALE, a V entry for e4m3(c) * FP8_V_SCALE.  Neither is a
+# power of two, so quantising a new key (x / scale) rounds.
+FP8_K_SCALE = float(np.float32(0.0153))
+FP8_V_SCALE = float(np.float32(0.0211))
+
+
+def e4m3_codes(rng: np.random.Generator, shape, chunk: int = 1 << 24) -> np.ndarray:
+    """Uniformly random finite e4m3 codes as uint8: each of the 254 codes other
+    than the two NaN codes (0x7F, 0xFF) is equally likely."""
+    n = int(np.prod(shape))
+    out = np.empty(n, np.uint8)
+    for a in range(0, n, chunk):
+        m = min(n, a + chunk) - a
+        r = rng.integers(0, 254, size=m, dtype=np.uint8)
+        r[r >= 0x7F] += 1
+        out[a:a + m] = r
+    return out.reshape(shape)
+
+
+def fp8_pool(b: "PagedBatch") -> np.ndarray:
+    """An fp8 pool with the shape of ``b``'s pool, [nb, 2, bs, Hkv, d] uint8,
+    filled with random finite codes drawn from ``default_rng([seed, 2])``."""
+    rng = np.random.default_rng([b.seed, 2])
+    return e4m3_codes(rng, (b.num_blocks, 2, b.block_size, b.num_kv_heads, b.head_size))
 
 
 # ---------------------------------------------------------------------------
