@@ -15,10 +15,17 @@
 //    16-token sub-blocks round-robin, each warp with its own cp.async
 //    pipeline (STAGES deep) into an XOR-swizzled shared-memory ring, so the
 //    main loop has no CTA-wide barrier;
-//  * all Hq/Hkv query heads of the kv group are the 16 rows of one
-//    mma.m16n8k16 tile, so the K/V bytes fetched once serve the whole group:
-//    S = Q K^T (16 x 16 per sub-block), online softmax in registers with quad
-//    shuffles (exp2 with the scale folded in), O += P V;
+//  * the 16 tokens of a sub-block are the M dimension of mma.m16n8k16 and
+//    the Hq/Hkv query heads of the kv group its N dimension (8 per n-tile),
+//    so the K/V bytes fetched once serve the whole group: S^T = K Q^T with K
+//    read by ldmatrix as the A operand, online softmax in registers (exp2
+//    with the scale folded in; per head over the tokens, i.e. across lanes),
+//    then O^T += V^T P^T with V^T read by ldmatrix.trans and P^T gathered by
+//    four shuffles of bf16 pairs -- d/16 MMAs per product per sub-block and
+//    d/16 x 4 output registers per n-tile;
+//  * the running max moves only when a sub-block's max exceeds it by more
+//    than 8 (log2 units), so the output rescale is rare; the next block id is
+//    loaded one iteration before its copies are issued;
 //  * the four warps' (max, sum, O) states are merged through shared memory
 //    at the end and the split's normalised partial and natural-log LSE are
 //    written to the workspace.
@@ -29,7 +36,7 @@
 
 namespace pa {
 
-template <int D, int STAGES>
+template <int D, int STAGES, int NT>
 struct DecodeCfg {
   static constexpr int kWarps = 4;
   static constexpr int kThreads = kWarps * 32;
@@ -39,8 +46,11 @@ struct DecodeCfg {
   static constexpr int kStageBytes = 2 * kTileBytes; // K + V
   static constexpr int kWarpBytes = STAGES * kStageBytes;
   static constexpr int kPipeBytes = kWarps * kWarpBytes;
-  static constexpr int kOStride = D + 4;             // padded fp32 row in the combine buffer
-  static constexpr int kCombineBytes = kWarps * (16 * kOStride + 32) * 4;
+  // Combine buffer: per warp 8*NT head rows of d floats, kOStride apart
+  // (= 4 mod 32: the fragment stores hit 32 distinct banks).
+  static constexpr int kOStride = D + 4;
+  static constexpr int kHeads = 8 * NT;
+  static constexpr int kCombineBytes = kWarps * (kHeads * kOStride + 2 * kHeads) * 4;
   static constexpr int kSmemBytes = kPipeBytes > kCombineBytes ? kPipeBytes : kCombineBytes;
 };
 
@@ -52,13 +62,15 @@ __device__ __forceinline__ uint32_t ld_u32(const __nv_bfloat16* p) {
   return *reinterpret_cast<const uint32_t*>(p);
 }
 
-template <int D, int STAGES>
+template <int D, int STAGES, int NT>
 __global__ void __launch_bounds__(128)
 decode_splitkv_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ cache,
                       const int32_t* __restrict__ block_table, const int32_t* __restrict__ seq_lens,
                       int max_blocks, int Hq, int Hkv, int bs, int num_blocks, float scale_log2,
                       int S, int chunk, float* __restrict__ ws, int* err) {
-  using C = DecodeCfg<D, STAGES>;
+  using C = DecodeCfg<D, STAGES, NT>;
+  constexpr int kK = D / 16;   // k-steps of K Q^T = d-tiles of V^T P^T
+  constexpr float kRescale = 8.f;
   extern __shared__ __align__(128) uint8_t smem[];
   const int s = blockIdx.x, kvh = blockIdx.y, i = blockIdx.z;
   const int grp = Hq / Hkv;
@@ -76,18 +88,20 @@ decode_splitkv_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
   const int nsb = (t1 - t0 + 15) >> 4;
   const int my_n = nsb > warp ? (nsb - warp + C::kWarps - 1) / C::kWarps : 0;
 
-  // Q of the kv group as the A operand: rows = the group's heads, zero-padded to 16.
-  uint32_t qf[D / 16][4];
+  // Q^T as the B operand: lane (gid, tid4) holds head nt*8 + gid (zero past
+  // the group), dimensions 16 kk + 2 tid4 + {0, 1} and + {8, 9}.
+  uint32_t qf[NT][kK][2];
   {
     const __nv_bfloat16* qb = q + (static_cast<int64_t>(i) * Hq + static_cast<int64_t>(kvh) * grp) * D;
-    const bool r0 = gid < grp, r1 = gid + 8 < grp;
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const int c0 = kk * 16 + 2 * tid4;
-      qf[kk][0] = r0 ? ld_u32(qb + gid * D + c0) : 0u;
-      qf[kk][1] = r1 ? ld_u32(qb + (gid + 8) * D + c0) : 0u;
-      qf[kk][2] = r0 ? ld_u32(qb + gid * D + c0 + 8) : 0u;
-      qf[kk][3] = r1 ? ld_u32(qb + (gid + 8) * D + c0 + 8) : 0u;
+    for (int nt = 0; nt < NT; ++nt) {
+      const int h = nt * 8 + gid;
+      const bool ok = h < grp;
+#pragma unroll
+      for (int kk = 0; kk < kK; ++kk) {
+        qf[nt][kk][0] = ok ? ld_u32(qb + h * D + kk * 16 + 2 * tid4) : 0u;
+        qf[nt][kk][1] = ok ? ld_u32(qb + h * D + kk * 16 + 8 + 2 * tid4) : 0u;
+      }
     }
   }
 
@@ -95,11 +109,19 @@ decode_splitkv_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
   const int64_t row_stride = static_cast<int64_t>(Hkv) * D;
   const int32_t* table = block_table + static_cast<int64_t>(i) * max_blocks;
 
-  auto issue = [&](int n) {
+  // Block id of the warp's n-th sub-block (loaded one iteration before its
+  // copies are issued, so the table read is off the critical path).
+  auto lookup = [&](int n) {
+    return block_at(table, (t0 + (warp + n * C::kWarps) * 16) / bs, max_blocks);
+  };
+  // Bit n % 32 of okbits: the n-th sub-block's block id was valid (at most
+  // STAGES sub-blocks are between issue and use).
+  uint32_t okbits = 0;
+  auto issue = [&](int n, int blk) {
     const int tb = t0 + (warp + n * C::kWarps) * 16;
-    const int blk = block_at(table, tb / bs, max_blocks);
     const bool ok = blk >= 0 && blk < num_blocks;
     if (!ok && lane == 0) record_error(err, PA_DEVERR_BLOCK_ID);
+    okbits = (okbits & ~(1u << (n & 31))) | (static_cast<uint32_t>(ok) << (n & 31));
     const int off = tb % bs;
     const __nv_bfloat16* kbase =
         cache + ((static_cast<int64_t>(ok ? blk : 0) * 2) * bs + off) * row_stride +
@@ -118,131 +140,159 @@ decode_splitkv_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
     }
   };
 
-  float m_r[2] = {-CUDART_INF_F, -CUDART_INF_F};
-  float l_r[2] = {0.f, 0.f};
-  float o[D / 8][4];
+  // Per lane: heads nt*8 + 2 tid4 + j (j = 0, 1) -- running max (replicated
+  // over the 8 token lanes), partial sums over the lane's tokens, and O^T.
+  float m_r[NT][2], l_r[NT][2];
+  float o[NT][kK][4];
 #pragma unroll
-  for (int nd = 0; nd < D / 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+  for (int nt = 0; nt < NT; ++nt) {
+    m_r[nt][0] = m_r[nt][1] = -CUDART_INF_F;
+    l_r[nt][0] = l_r[nt][1] = 0.f;
+#pragma unroll
+    for (int md = 0; md < kK; ++md) o[nt][md][0] = o[nt][md][1] = o[nt][md][2] = o[nt][md][3] = 0.f;
+  }
 
 #pragma unroll
   for (int n = 0; n < STAGES - 1; ++n) {
-    if (n < my_n) issue(n);
+    if (n < my_n) issue(n, lookup(n));
     cp_async_commit();
   }
+  int next_blk = STAGES - 1 < my_n ? lookup(STAGES - 1) : -1;
+
+  // Source lanes of the P^T operand: tokens 2 tid4 (srcA) and 2 tid4 + 1
+  // (srcB) hold head gid in the lane of tid4' = gid / 2, half gid % 2.
+  const int srcA = 8 * tid4 + (gid >> 1), srcB = srcA + 4;
+  const uint32_t psel = (gid & 1) ? 0x7632u : 0x5410u;
+  // ldmatrix row addresses: K as A (token lane & 15, half lane >> 4 of the
+  // k-step), V^T as A (token (lane & 7) + 8 (lane >> 4), half (lane >> 3) & 1).
+  const int k_row = lane & 15, k_half = lane >> 4;
+  const int v_row = (lane & 7) + ((lane >> 4) << 3), v_half = (lane >> 3) & 1;
 
   for (int n = 0; n < my_n; ++n) {
     cp_async_wait<STAGES - 2>();
     __syncwarp();
-    if (n + STAGES - 1 < my_n) issue(n + STAGES - 1);
+    if (n + STAGES - 1 < my_n) {
+      issue(n + STAGES - 1, next_blk);
+      if (n + STAGES < my_n) next_blk = lookup(n + STAGES);
+    }
     cp_async_commit();
 
     const int tb = t0 + (warp + n * C::kWarps) * 16;
-    const int blk = block_at(table, tb / bs, max_blocks);
-    const int lim = (blk >= 0 && blk < num_blocks) ? min(16, t1 - tb) : 0;
+    const int lim = ((okbits >> (n & 31)) & 1u) ? min(16, t1 - tb) : 0;
     const uint32_t kb = wbase + (n % STAGES) * C::kStageBytes;
     const uint32_t vb = kb + C::kTileBytes;
 
-    // S = Q K^T: 16 heads x 16 tokens.
-    float sc[2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+    // S^T = K Q^T: rows = tokens gid, gid + 8; columns = heads.  Even and
+    // odd k-steps go to separate accumulators (two MMA chains of half the
+    // length).
+    float sc[NT][4];
     {
-      const int mi = lane >> 3, rr = lane & 7;
-      const int tok = (mi >> 1) * 8 + rr;
+      float s2[NT][2][4];
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        uint32_t b0, b1, b2, b3;
-        ldmatrix_x4(kb + swz(tok, 2 * kk + (mi & 1), C::kRowBytes), b0, b1, b2, b3);
-        mma_bf16_16816(sc[0], qf[kk], b0, b1);
-        mma_bf16_16816(sc[1], qf[kk], b2, b3);
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) s2[nt][h][0] = s2[nt][h][1] = s2[nt][h][2] = s2[nt][h][3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < kK; ++kk) {
+        uint32_t a[4];
+        ldmatrix_x4(kb + swz(k_row, 2 * kk + k_half, C::kRowBytes), a[0], a[1], a[2], a[3]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          mma_bf16_16816(s2[nt][kk & 1], a, qf[nt][kk][0], qf[nt][kk][1]);
       }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[nt][e] = s2[nt][0][e] + s2[nt][1][e];
     }
 
-    // Online softmax (log2 domain, scale folded in).
-    float mx[2] = {-CUDART_INF_F, -CUDART_INF_F};
+    // Online softmax (log2 domain, scale folded in), per head over the 16
+    // tokens: two in the lane, the rest across the 8 token lanes.  The
+    // reference max moves only when a sub-block's max exceeds it by more than
+    // kRescale, so the output rescale is rare and the weights stay < 2^8.
+    const bool v0 = gid < lim, v1 = gid + 8 < lim;
+    uint32_t pb[NT][2];   // P^T operand: b0 (tokens 2 tid4, +1), b1 (+8, +9)
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+    for (int nt = 0; nt < NT; ++nt) {
+      float p[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int tok = nt * 8 + 2 * tid4 + (e & 1);
-        const float x = tok < lim ? sc[nt][e] * scale_log2 : -CUDART_INF_F;
-        sc[nt][e] = x;
-        mx[e >> 1] = fmaxf(mx[e >> 1], x);
+      for (int j = 0; j < 2; ++j) {
+        const float x0 = v0 ? sc[nt][j] * scale_log2 : -CUDART_INF_F;
+        const float x1 = v1 ? sc[nt][2 + j] * scale_log2 : -CUDART_INF_F;
+        float mx = fmaxf(x0, x1);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        if (mx > m_r[nt][j] + kRescale) {
+          const float alpha = fast_exp2(m_r[nt][j] - mx);   // 0 when m_r = -inf
+          m_r[nt][j] = mx;
+          l_r[nt][j] *= alpha;
+#pragma unroll
+          for (int md = 0; md < kK; ++md) {
+            o[nt][md][j] *= alpha;
+            o[nt][md][2 + j] *= alpha;
+          }
+        }
+        const float mu = m_r[nt][j] == -CUDART_INF_F ? 0.f : m_r[nt][j];
+        p[j] = fast_exp2(x0 - mu);
+        p[2 + j] = fast_exp2(x1 - mu);
+        l_r[nt][j] += p[j] + p[2 + j];
       }
-    float alpha[2], mu[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-      const float mn = fmaxf(m_r[r], mx[r]);
-      mu[r] = mn == -CUDART_INF_F ? 0.f : mn;
-      alpha[r] = fast_exp2(m_r[r] - mu[r]);
-      m_r[r] = mn;
-      l_r[r] *= alpha[r];
+      // S^T -> P^T: this lane's (token, head pair) values as bf16 pairs, then
+      // each lane gathers its head's four tokens.
+      const uint32_t u_lo = pack_bf16(p[0], p[1]);   // token gid, heads 2 tid4, +1
+      const uint32_t u_hi = pack_bf16(p[2], p[3]);   // token gid + 8
+      const uint32_t xa = __shfl_sync(0xffffffffu, u_lo, srcA);
+      const uint32_t xb = __shfl_sync(0xffffffffu, u_lo, srcB);
+      const uint32_t ya = __shfl_sync(0xffffffffu, u_hi, srcA);
+      const uint32_t yb = __shfl_sync(0xffffffffu, u_hi, srcB);
+      pb[nt][0] = __byte_perm(xa, xb, psel);
+      pb[nt][1] = __byte_perm(ya, yb, psel);
     }
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float p = fast_exp2(sc[nt][e] - mu[e >> 1]);
-        sc[nt][e] = p;
-        l_r[e >> 1] += p;
-      }
-#pragma unroll
-    for (int nd = 0; nd < D / 8; ++nd) {
-      o[nd][0] *= alpha[0];
-      o[nd][1] *= alpha[0];
-      o[nd][2] *= alpha[1];
-      o[nd][3] *= alpha[1];
-    }
-    uint32_t pf[4];
-    pf[0] = pack_bf16(sc[0][0], sc[0][1]);
-    pf[1] = pack_bf16(sc[0][2], sc[0][3]);
-    pf[2] = pack_bf16(sc[1][0], sc[1][1]);
-    pf[3] = pack_bf16(sc[1][2], sc[1][3]);
 
-    // O += P V.
-    {
-      const int mi = lane >> 3, rr = lane & 7;
-      const int tok = (mi & 1) * 8 + rr;
+    // O^T += V^T P^T, V^T tiles read transposed from the token-major V tile.
 #pragma unroll
-      for (int jj = 0; jj < D / 16; ++jj) {
-        uint32_t b0, b1, b2, b3;
-        ldmatrix_x4_trans(vb + swz(tok, 2 * jj + (mi >> 1), C::kRowBytes), b0, b1, b2, b3);
-        mma_bf16_16816(o[2 * jj], pf, b0, b1);
-        mma_bf16_16816(o[2 * jj + 1], pf, b2, b3);
-      }
+    for (int md = 0; md < kK; ++md) {
+      uint32_t a[4];
+      ldmatrix_x4_trans(vb + swz(v_row, 2 * md + v_half, C::kRowBytes), a[0], a[1], a[2], a[3]);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(o[nt][md], a, pb[nt][0], pb[nt][1]);
     }
   }
   cp_async_wait<0>();
   // The merge may start launching (it waits for this kernel to complete).
   pdl_trigger();
 
+  // Partial sums over the 8 token lanes.
 #pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], 1);
-    l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], 2);
-  }
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      l_r[nt][j] += __shfl_xor_sync(0xffffffffu, l_r[nt][j], 4);
+      l_r[nt][j] += __shfl_xor_sync(0xffffffffu, l_r[nt][j], 8);
+      l_r[nt][j] += __shfl_xor_sync(0xffffffffu, l_r[nt][j], 16);
+    }
 
   // Merge the four warps' states through shared memory.
   __syncthreads();
   float* cbuf = reinterpret_cast<float*>(smem);
-  float* mbuf = cbuf + C::kWarps * 16 * C::kOStride;  // [warp][16]
-  float* lbuf = mbuf + C::kWarps * 16;                // [warp][16]
-  {
-    float* ob = cbuf + warp * 16 * C::kOStride;
+  float* mbuf = cbuf + C::kWarps * C::kHeads * C::kOStride;  // [warp][kHeads]
+  float* lbuf = mbuf + C::kWarps * C::kHeads;
 #pragma unroll
-    for (int nd = 0; nd < D / 8; ++nd) {
-      const int col = nd * 8 + 2 * tid4;
-      *reinterpret_cast<float2*>(ob + gid * C::kOStride + col) = make_float2(o[nd][0], o[nd][1]);
-      *reinterpret_cast<float2*>(ob + (gid + 8) * C::kOStride + col) =
-          make_float2(o[nd][2], o[nd][3]);
-    }
-    if (tid4 == 0) {
-      mbuf[warp * 16 + gid] = m_r[0];
-      mbuf[warp * 16 + gid + 8] = m_r[1];
-      lbuf[warp * 16 + gid] = l_r[0];
-      lbuf[warp * 16 + gid + 8] = l_r[1];
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int md = 0; md < kK; ++md)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int h = nt * 8 + 2 * tid4 + (e & 1);
+        cbuf[(warp * C::kHeads + h) * C::kOStride + md * 16 + gid + 8 * (e >> 1)] = o[nt][md][e];
+      }
+    if (gid == 0) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        mbuf[warp * C::kHeads + nt * 8 + 2 * tid4 + j] = m_r[nt][j];
+        lbuf[warp * C::kHeads + nt * 8 + 2 * tid4 + j] = l_r[nt][j];
+      }
     }
   }
   __syncthreads();
@@ -250,7 +300,7 @@ decode_splitkv_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
     const int r = idx / D, e = idx % D;
     float M = -CUDART_INF_F;
 #pragma unroll
-    for (int w = 0; w < C::kWarps; ++w) M = fmaxf(M, mbuf[w * 16 + r]);
+    for (int w = 0; w < C::kWarps; ++w) M = fmaxf(M, mbuf[w * C::kHeads + r]);
     float* dst = ws + ((static_cast<int64_t>(i) * Hq + kvh * grp + r) * S + s) * (D + 1);
     if (M == -CUDART_INF_F) {
       dst[e] = 0.f;
@@ -260,9 +310,9 @@ decode_splitkv_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
     float L = 0.f, acc = 0.f;
 #pragma unroll
     for (int w = 0; w < C::kWarps; ++w) {
-      const float f = fast_exp2(mbuf[w * 16 + r] - M);
-      L += f * lbuf[w * 16 + r];
-      acc += f * cbuf[(w * 16 + r) * C::kOStride + e];
+      const float f = fast_exp2(mbuf[w * C::kHeads + r] - M);
+      L += f * lbuf[w * C::kHeads + r];
+      acc += f * cbuf[(w * C::kHeads + r) * C::kOStride + e];
     }
     dst[e] = acc / L;
     if (e == 0) dst[D] = (M + log2f(L)) * kLn2;
@@ -319,13 +369,13 @@ lse_merge_kernel(const float* __restrict__ ws, int S, int dv, __nv_bfloat16* __r
   if (lse != nullptr && tid == 0) lse[nh] = m == -CUDART_INF_F ? -CUDART_INF_F : m + logf(wsum);
 }
 
-template <int D, int STAGES>
+template <int D, int STAGES, int NT>
 static cudaError_t launch_decode_t(const void* q, const void* cache, const int32_t* block_table,
                                    const int32_t* seq_lens, int N, int Hq, int Hkv, int bs,
                                    int num_blocks, int max_blocks, float scale, int S, int chunk,
                                    float* ws, int* err, cudaStream_t stream) {
-  using C = DecodeCfg<D, STAGES>;
-  auto kern = decode_splitkv_kernel<D, STAGES>;
+  using C = DecodeCfg<D, STAGES, NT>;
+  auto kern = decode_splitkv_kernel<D, STAGES, NT>;
   static DeviceFlags attr_set;
   cudaError_t e = set_smem_once(kern, C::kSmemBytes, attr_set);
   if (e != cudaSuccess) return e;
@@ -339,11 +389,17 @@ cudaError_t launch_decode_splitkv(const void* q, const void* cache, const int32_
                                   const int32_t* seq_lens, int N, int Hq, int Hkv, int d, int bs,
                                   int num_blocks, int max_blocks, float scale, int S, int chunk,
                                   float* ws, int* err, cudaStream_t stream) {
-  if (d == 128)
-    return launch_decode_t<128, 2>(q, cache, block_table, seq_lens, N, Hq, Hkv, bs, num_blocks,
-                                   max_blocks, scale, S, chunk, ws, err, stream);
-  return launch_decode_t<64, 4>(q, cache, block_table, seq_lens, N, Hq, Hkv, bs, num_blocks,
-                                max_blocks, scale, S, chunk, ws, err, stream);
+  const bool wide = Hq / Hkv > 8;   // groups of 9..16 heads take two n-tiles
+#define PA_DECODE_LAUNCH(DD, ST, NTT)                                                          \
+  return launch_decode_t<DD, ST, NTT>(q, cache, block_table, seq_lens, N, Hq, Hkv, bs,         \
+                                      num_blocks, max_blocks, scale, S, chunk, ws, err, stream)
+  if (d == 128) {
+    if (wide) PA_DECODE_LAUNCH(128, 2, 2);
+    PA_DECODE_LAUNCH(128, 2, 1);
+  }
+  if (wide) PA_DECODE_LAUNCH(64, 4, 2);
+  PA_DECODE_LAUNCH(64, 4, 1);
+#undef PA_DECODE_LAUNCH
 }
 
 cudaError_t launch_lse_merge(const float* ws, int NH, int S, int dv, void* out, float* lse,
