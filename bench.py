@@ -568,7 +568,7 @@ def main():
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "launch": e2e_launch},
             "gpu_launches": 3 * args.steps,
-            "roofline": {"bound": "hbm", "kernel": "decode_splitkv_kernel<128,2>",
+            "roofline": {"bound": "hbm", "kernel": "decode_splitkv_kernel<128,2,1>",
                          "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
                          "algorithmic_bytes_per_launch": kv_bytes,
