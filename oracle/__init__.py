@@ -51,7 +51,7 @@ def _bind(path):
     for name in ("oracle_paged_attention_bf16", "oracle_paged_attention_f64"):
         fn = getattr(lib, name)
         fn.argtypes = [P, P, P, i32, P, P, i32, i32, i32, i32, i32, i64, f64,
-                       i32, P, P, P, i32]
+                       i32, i32, P, P, P, i32]
         fn.restype = i32
     for name in ("oracle_split_partials_bf16", "oracle_split_partials_f64"):
         fn = getattr(lib, name)
@@ -155,10 +155,11 @@ def reshape_and_cache(key, value, pool, slot_mapping, block_size):
 
 
 def paged_attention(q, pool, block_table, query_start_loc, seq_lens, scale,
-                    causal=True, row_mask=None, threads=None):
+                    causal=True, row_mask=None, threads=None, window=0):
     """Varlen paged attention.  q [T, Hq, d]; pool [nb, 2, bs, Hkv, d]
     (uint16 bf16 bits, or float64).  Returns (out [T, Hq, d], lse [T, Hq])
-    in fp64; rows not selected by ``row_mask`` are left at zero."""
+    in fp64; rows not selected by ``row_mask`` are left at zero.
+    ``window`` > 0 (causal only): a row at position p sees p - window < p' <= p."""
     lib = _load()
     kq, q = _kind(q)
     kp, pool = _kind(pool)
@@ -178,10 +179,10 @@ def paged_attention(q, pool, block_table, query_start_loc, seq_lens, scale,
     mask = None if row_mask is None else _c(row_mask, np.uint8)
     fn = lib.oracle_paged_attention_bf16 if kq == "bf16" else lib.oracle_paged_attention_f64
     rc = fn(_ptr(q), _ptr(pool), _ptr(bt), bt.shape[1], _ptr(qsl), _ptr(sl), N, Hq,
-            Hkv, d, bs, nb, float(scale), int(bool(causal)), _ptr(mask), _ptr(out),
-            _ptr(lse), threads or default_threads())
+            Hkv, d, bs, nb, float(scale), int(bool(causal)), int(window), _ptr(mask),
+            _ptr(out), _ptr(lse), threads or default_threads())
     if rc != 0:
-        raise ValueError("invalid paged-attention input (block id or lengths)")
+        raise ValueError("invalid paged-attention input (block id, lengths or window)")
     return out, lse
 
 

@@ -40,7 +40,11 @@
 //    seq_len, with C = bs * ceil(ceil(max_seq_len / S) / bs), and the last
 //    split also takes any tokens past (S-1)*C; an empty split has o = 0 and
 //    lse = -inf;
-//  * a query with nothing visible (seq_len = 0) gives o = 0, lse = -inf.
+//  * a query with nothing visible (seq_len = 0) gives o = 0, lse = -inf;
+//  * a sliding window of W positions (the pages name the parameter only, as
+//    an input of backend selection) keeps the W newest positions a causal
+//    row sees: row j at position p_j sees p_j - W < p <= p_j.  It is defined
+//    for causal attention only.
 
 #include <atomic>
 #include <cmath>
@@ -143,10 +147,11 @@ template <typename E>
 int paged_attention(const E* q, const E* pool, const int32_t* block_table,
                     int max_blocks, const int32_t* query_start_loc,
                     const int32_t* seq_lens, int N, int Hq, int Hkv, int d,
-                    int bs, int64_t nb, double scale, int causal,
+                    int bs, int64_t nb, double scale, int causal, int window,
                     const uint8_t* row_mask, double* out, double* lse,
                     int threads) {
   if (Hkv <= 0 || Hq % Hkv != 0 || bs <= 0 || d <= 0) return -1;
+  if (window < 0 || (window > 0 && !causal)) return -1;
   const int grp = Hq / Hkv;
   std::atomic<int> bad(0);
   parallel_for(static_cast<int64_t>(N) * Hkv, threads, [&](int64_t item) {
@@ -174,12 +179,14 @@ int paged_attention(const E* q, const E* pool, const int32_t* block_table,
       if (row_mask && !row_mask[j]) continue;
       const int64_t pos = ctx + (j - q0);          // absolute position of row j
       const int64_t visible = causal ? pos + 1 : seq;
+      // Sliding window: the row sees only its `window` newest positions.
+      const int64_t first = (window > 0 && visible > window) ? visible - window : 0;
       for (int r = 0; r < grp; ++r) {
         const int h = g * grp + r;
         const E* qr = q + (j * Hq + h) * d;
         for (int e = 0; e < d; ++e) qv[e] = widen(qr[e]);
-        attend(qv.data(), K.data(), V.data(), visible, d, d, scale,
-               out + (j * Hq + h) * d, lse + j * Hq + h);
+        attend(qv.data(), K.data() + first * d, V.data() + first * d, visible - first, d, d,
+               scale, out + (j * Hq + h) * d, lse + j * Hq + h);
       }
     }
   });
@@ -308,10 +315,10 @@ int oracle_paged_attention_bf16(const uint16_t* q, const uint16_t* pool,
                                 const int32_t* query_start_loc,
                                 const int32_t* seq_lens, int N, int Hq, int Hkv,
                                 int d, int bs, int64_t nb, double scale,
-                                int causal, const uint8_t* row_mask,
+                                int causal, int window, const uint8_t* row_mask,
                                 double* out, double* lse, int threads) {
   return paged_attention(q, pool, block_table, max_blocks, query_start_loc,
-                         seq_lens, N, Hq, Hkv, d, bs, nb, scale, causal,
+                         seq_lens, N, Hq, Hkv, d, bs, nb, scale, causal, window,
                          row_mask, out, lse, threads);
 }
 
@@ -321,10 +328,10 @@ int oracle_paged_attention_f64(const double* q, const double* pool,
                                const int32_t* query_start_loc,
                                const int32_t* seq_lens, int N, int Hq, int Hkv,
                                int d, int bs, int64_t nb, double scale,
-                               int causal, const uint8_t* row_mask, double* out,
-                               double* lse, int threads) {
+                               int causal, int window, const uint8_t* row_mask,
+                               double* out, double* lse, int threads) {
   return paged_attention(q, pool, block_table, max_blocks, query_start_loc,
-                         seq_lens, N, Hq, Hkv, d, bs, nb, scale, causal,
+                         seq_lens, N, Hq, Hkv, d, bs, nb, scale, causal, window,
                          row_mask, out, lse, threads);
 }
 

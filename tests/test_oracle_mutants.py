@@ -35,6 +35,10 @@ MUTANTS = [
     ("fp8_scales_swapped",
      "const double sc = kv == 0 ? static_cast<double>(k_scale) : static_cast<double>(v_scale);",
      "const double sc = kv == 0 ? static_cast<double>(v_scale) : static_cast<double>(k_scale);"),
+    ("window_one_short", "(window > 0 && visible > window) ? visible - window : 0",
+     "(window > 0 && visible > window) ? visible - window + 1 : 0"),
+    ("window_one_long", "(window > 0 && visible > window) ? visible - window : 0",
+     "(window > 0 && visible > window + 1) ? visible - window - 1 : 0"),
 ]
 
 

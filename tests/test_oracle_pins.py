@@ -505,3 +505,101 @@ def test_fp8_decode_matches_torch_sdpa(oracle_lib):
             ref_o = torch.softmax(s, 0) @ V[:, h // g]
             assert np.allclose(o[i, h], ref_o.numpy(), rtol=0, atol=1e-12)
             assert abs(lse[i, h] - torch.logsumexp(s, 0).item()) < 1e-12
+
+
+# ---------------------------------------------------------------- sliding window
+# Reading: a row at position p sees p - W < p' <= p (the W newest positions
+# a causal row sees); the pages name the parameter only.
+
+def _window_batch():
+    # Ragged lengths around the window sizes used below, queries inside and at
+    # the end of each request.
+    return workloads.make_paged_batch("window_pins", 61, [1, 9, 23, 40], [1, 5, 23, 7], 4, 2,
+                                      16, 8, num_blocks=24, scale=0.3)
+
+
+def test_window_matches_torch_sdpa_with_banded_mask(oracle_lib):
+    b = _window_batch()
+    pool = oracle_lib.reshape_and_cache(b.key, b.value, b.pool, b.slot_mapping, b.block_size)
+    P, q = _f64(pool), _f64(b.q)
+    grp = b.num_q_heads // b.num_kv_heads
+    for W in (1, 3, 8, 17):
+        out, lse = oracle_lib.paged_attention(b.q, pool, b.block_table, b.query_start_loc,
+                                              b.seq_lens, b.scale, window=W)
+        for i in range(b.num_seqs):
+            K, V = _gather(P, b.block_table[i], b.seq_lens[i], b.block_size)
+            rows = slice(b.query_start_loc[i], b.query_start_loc[i + 1])
+            qi = torch.from_numpy(q[rows]).permute(1, 0, 2)
+            Ki = torch.from_numpy(K).permute(1, 0, 2).repeat_interleave(grp, 0)
+            Vi = torch.from_numpy(V).permute(1, 0, 2).repeat_interleave(grp, 0)
+            L, S = qi.shape[1], Ki.shape[1]
+            pos = (S - L + torch.arange(L))[:, None]
+            key = torch.arange(S)[None, :]
+            mask = (key <= pos) & (key > pos - W)
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                qi, Ki, Vi, attn_mask=mask, scale=b.scale)
+            np.testing.assert_allclose(out[rows], ref.permute(1, 0, 2).numpy(), rtol=0,
+                                       atol=1e-12)
+            s = torch.einsum("hld,hsd->hls", qi, Ki) * b.scale
+            s = s.masked_fill(~mask, -math.inf)
+            np.testing.assert_allclose(lse[rows], torch.logsumexp(s, -1).T.numpy(), rtol=0,
+                                       atol=1e-12)
+
+
+def test_window_brute_force(oracle_lib):
+    b = _window_batch()
+    pool = oracle_lib.reshape_and_cache(b.key, b.value, b.pool, b.slot_mapping, b.block_size)
+    P, q = _f64(pool), _f64(b.q)
+    grp = b.num_q_heads // b.num_kv_heads
+    W = 5
+    out, lse = oracle_lib.paged_attention(b.q, pool, b.block_table, b.query_start_loc,
+                                          b.seq_lens, b.scale, window=W)
+    for i in range(b.num_seqs):
+        K, V = _gather(P, b.block_table[i], b.seq_lens[i], b.block_size)
+        q0, q1 = int(b.query_start_loc[i]), int(b.query_start_loc[i + 1])
+        for j in range(q0, q1):
+            p = int(b.seq_lens[i]) - (q1 - q0) + (j - q0)
+            lo = max(0, p - W + 1)
+            for h in range(b.num_q_heads):
+                keys = [list(K[t, h // grp]) for t in range(lo, p + 1)]
+                vals = [list(V[t, h // grp]) for t in range(lo, p + 1)]
+                o, l = bruteforce.attend(list(q[j, h]), keys, vals, b.scale)
+                np.testing.assert_allclose(out[j, h], o, rtol=0, atol=1e-12)
+                assert abs(lse[j, h] - l) < 1e-12
+
+
+def test_window_closed_forms(oracle_lib):
+    b = _window_batch()
+    pool = oracle_lib.reshape_and_cache(b.key, b.value, b.pool, b.slot_mapping, b.block_size)
+    args = (b.block_table, b.query_start_loc, b.seq_lens, b.scale)
+    full = oracle_lib.paged_attention(b.q, pool, *args)
+    # A window at least as long as every sequence changes nothing (bit-exact).
+    wide = oracle_lib.paged_attention(b.q, pool, *args, window=int(b.seq_lens.max()))
+    assert np.array_equal(full[0], wide[0]) and np.array_equal(full[1], wide[1])
+    # W = 1: each row returns its own V row exactly, lse = scale q.k.
+    P, q = _f64(pool), _f64(b.q)
+    grp = b.num_q_heads // b.num_kv_heads
+    one = oracle_lib.paged_attention(b.q, pool, *args, window=1)
+    # q = 0: the mean of the window's V rows, lse = ln(#positions in the window).
+    zq = np.zeros_like(b.q)
+    W = 6
+    zero = oracle_lib.paged_attention(zq, pool, *args, window=W)
+    for i in range(b.num_seqs):
+        K, V = _gather(P, b.block_table[i], b.seq_lens[i], b.block_size)
+        q0, q1 = int(b.query_start_loc[i]), int(b.query_start_loc[i + 1])
+        for j in range(q0, q1):
+            p = int(b.seq_lens[i]) - (q1 - q0) + (j - q0)
+            lo = max(0, p - W + 1)
+            for h in range(b.num_q_heads):
+                assert np.array_equal(one[0][j, h], V[p, h // grp])
+                assert abs(one[1][j, h] - b.scale * math.fsum(q[j, h] * K[p, h // grp])) < 1e-12
+                np.testing.assert_allclose(zero[0][j, h], V[lo:p + 1, h // grp].mean(0), rtol=0,
+                                           atol=1e-14)
+                assert abs(zero[1][j, h] - math.log(p + 1 - lo)) < 1e-14
+
+
+def test_window_is_causal_only(oracle_lib):
+    b = _window_batch()
+    with pytest.raises(ValueError):
+        oracle_lib.paged_attention(b.q, b.pool, b.block_table, b.query_start_loc, b.seq_lens,
+                                   b.scale, causal=False, window=4)
