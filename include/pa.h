@@ -59,6 +59,7 @@ typedef enum pa_status {
 #define PA_DEVERR_BLOCK_ID 1  /* a block_table entry outside [0, num_blocks) */
 #define PA_DEVERR_SLOT 2      /* a slot_mapping entry >= num_blocks * block_size */
 #define PA_DEVERR_TIMEOUT 4   /* a kernel gave up a bounded wait; its outputs are invalid */
+#define PA_DEVERR_LENGTH 8    /* a request's lengths break a call's stated precondition */
 
 /* Shape of a standard-layout paged batch. */
 typedef struct pa_shape {
@@ -108,6 +109,61 @@ pa_status pa_varlen_fwd(const void* q, const void* kv_cache, const int32_t* bloc
                         const int32_t* query_start_loc, const int32_t* seq_lens,
                         int total_q, int max_query_len, const pa_shape* shape,
                         float scale, int causal, void* out, float* lse, void* stream);
+
+/*
+ * Varlen paged attention with a sliding window: pa_varlen_fwd with causal
+ * masking in which row j at position p_j sees only the sliding_window newest
+ * positions up to its own, p_j - sliding_window < p <= p_j.  The pages name
+ * sliding_window only as an input of backend selection ("attention-backend-
+ * selection", trigger conditions); this reading (the W newest positions,
+ * the row's own included) is the library's.  sliding_window >= 1 (else
+ * PA_ERR_INVALID); a window at least as long as every sequence equals
+ * pa_varlen_fwd with causal = 1.  Other arguments as for pa_varlen_fwd.
+ */
+pa_status pa_varlen_fwd_window(const void* q, const void* kv_cache, const int32_t* block_table,
+                               const int32_t* query_start_loc, const int32_t* seq_lens,
+                               int total_q, int max_query_len, const pa_shape* shape, float scale,
+                               int sliding_window, void* out, float* lse, void* stream);
+
+/*
+ * Cascade (shared-prefix) attention ("Attention Backends", section "Cascade
+ * attention": when every running request shares its first
+ * num_common_prefix_blocks blocks, the shared part is processed once and the
+ * per-request parts separately).  The result is that of pa_varlen_fwd on the
+ * same arguments; it is computed as
+ *   pass 1: every query row of the batch against the first
+ *           num_common_prefix_blocks * block_size tokens, read once per kv
+ *           head through row 0 of block_table, without a mask, cut into
+ *           num_prefix_splits pieces -> partials in workspace slots
+ *           [0, num_prefix_splits);
+ *   pass 2: request i against its own tokens from position
+ *           num_common_prefix_blocks * block_size on (table columns from
+ *           num_common_prefix_blocks), with the call's mask -> slot
+ *           num_prefix_splits;
+ *   merge:  the pa_lse_merge of the num_prefix_splits + 1 partials -> out, lse.
+ * Preconditions: the first num_common_prefix_blocks entries of every table
+ * row are the same block ids; with causal != 0 every query lies after the
+ * prefix (seq_lens[i] - qlen_i >= num_common_prefix_blocks * block_size; a
+ * request that breaks it sets PA_DEVERR_LENGTH and its rows are invalid).
+ * workspace: pa_decode_workspace_bytes(total_q, Hq, num_prefix_splits + 1, d)
+ * bytes (fp32 [total_q, Hq, num_prefix_splits + 1, d + 1]).
+ * num_common_prefix_blocks == 0 runs pa_varlen_fwd (workspace untouched).
+ * Other arguments as for pa_varlen_fwd; head_size in {64, 128}.
+ */
+pa_status pa_cascade_fwd(const void* q, const void* kv_cache, const int32_t* block_table,
+                         const int32_t* query_start_loc, const int32_t* seq_lens, int total_q,
+                         int max_query_len, int num_common_prefix_blocks, int num_prefix_splits,
+                         const pa_shape* shape, float scale, int causal, float* workspace,
+                         void* out, float* lse, void* stream);
+
+/*
+ * A num_prefix_splits for pa_cascade_fwd: enough pieces of the prefix that
+ * pass 1 has one unit (256 packed query rows x kv head x piece) per SM, at
+ * most one per 128 prefix tokens, at least 1.  sm_count <= 0 means the
+ * current device's.
+ */
+int pa_cascade_prefix_splits(int total_q, int num_q_heads, int num_kv_heads, int prefix_tokens,
+                             int sm_count);
 
 /*
  * Split-count rule of "Triton and MLA", key-files list (_compute_num_kv_splits):

@@ -24,7 +24,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_build", "libpa.so")
 
 PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_CUDA = 0, 1, 2, 3
-PA_DEVERR_BLOCK_ID, PA_DEVERR_SLOT = 1, 2
+PA_DEVERR_BLOCK_ID, PA_DEVERR_SLOT, PA_DEVERR_TIMEOUT, PA_DEVERR_LENGTH = 1, 2, 4, 8
 
 _lock = threading.Lock()
 _lib = None
@@ -63,6 +63,11 @@ def lib() -> ctypes.CDLL:
         L.pa_decode_workspace_bytes.restype = ctypes.c_size_t
         L.pa_decode_splitkv.argtypes = [P, P, P, P, SP, f32, i32, i32, P, P]
         L.pa_lse_merge.argtypes = [P, i32, i32, i32, i32, P, P, P]
+        L.pa_varlen_fwd_window.argtypes = [P, P, P, P, P, i32, i32, SP, f32, i32, P, P, P]
+        L.pa_cascade_fwd.argtypes = [P, P, P, P, P, i32, i32, i32, i32, SP, f32, i32, P, P, P,
+                                     P]
+        L.pa_cascade_prefix_splits.argtypes = [i32, i32, i32, i32, i32]
+        L.pa_cascade_prefix_splits.restype = i32
         L.pa_reshape_and_cache_fp8.argtypes = [P, P, P, P, i32, SP, f32, f32, P]
         L.pa_decode_splitkv_fp8.argtypes = [P, P, P, P, SP, f32, f32, f32, i32, i32, P, P]
         L.pa_mla_decode.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, f32,
@@ -75,7 +80,8 @@ def lib() -> ctypes.CDLL:
         L.pa_device_sm_count.restype = i32
         for name in ("pa_reshape_and_cache", "pa_varlen_fwd", "pa_decode_splitkv",
                      "pa_lse_merge", "pa_mla_decode", "pa_get_device_error", "pa_decode_noalloc",
-                     "pa_reshape_and_cache_fp8", "pa_decode_splitkv_fp8"):
+                     "pa_reshape_and_cache_fp8", "pa_decode_splitkv_fp8", "pa_varlen_fwd_window",
+                     "pa_cascade_fwd"):
             getattr(L, name).restype = st
         _lib = L
         return L
@@ -160,6 +166,76 @@ def pa_varlen_fwd(q, kv_cache, block_table, query_start_loc, seq_lens, max_query
         _dev(seq_lens, "seq_lens", torch.int32), T, int(max_query_len), ctypes.byref(shape),
         float(scale), int(bool(causal)), _dev(out, "out", torch.bfloat16),
         _opt(lse, "lse", torch.float32), _stream(stream)), "pa_varlen_fwd")
+    return out, lse
+
+
+def pa_varlen_fwd_window(q, kv_cache, block_table, query_start_loc, seq_lens, max_query_len,
+                         scale, sliding_window, out=None, lse=None, return_lse=True, stream=None):
+    """Causal varlen paged attention in which a row at position p sees only
+    p - sliding_window < p' <= p.  Returns (out, lse) like pa_varlen_fwd."""
+    T, hq, d = q.shape
+    N = seq_lens.shape[0]
+    if query_start_loc.shape != (N + 1,):
+        raise ValueError("query_start_loc must be [num_seqs + 1]")
+    if block_table.dim() != 2 or block_table.shape[0] != N:
+        raise ValueError("block_table must be [num_seqs, max_blocks]")
+    shape = _pool_shape(kv_cache, N, hq, block_table.shape[1])
+    if d != shape.head_size:
+        raise ValueError("q head_size does not match kv_cache")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((T, hq), dtype=torch.float32, device=q.device)
+    _check(lib().pa_varlen_fwd_window(
+        _dev(q, "q", torch.bfloat16), _dev(kv_cache, "kv_cache", torch.bfloat16),
+        _dev(block_table, "block_table", torch.int32),
+        _dev(query_start_loc, "query_start_loc", torch.int32),
+        _dev(seq_lens, "seq_lens", torch.int32), T, int(max_query_len), ctypes.byref(shape),
+        float(scale), int(sliding_window), _dev(out, "out", torch.bfloat16),
+        _opt(lse, "lse", torch.float32), _stream(stream)), "pa_varlen_fwd_window")
+    return out, lse
+
+
+def pa_cascade_prefix_splits(total_q, num_q_heads, num_kv_heads, prefix_tokens, sm_count=0):
+    return int(lib().pa_cascade_prefix_splits(int(total_q), int(num_q_heads), int(num_kv_heads),
+                                              int(prefix_tokens), int(sm_count)))
+
+
+def cascade_workspace(total_q, num_q_heads, num_prefix_splits, head_size, device="cuda"):
+    """fp32 [total_q, Hq, num_prefix_splits + 1, d + 1] workspace for pa_cascade_fwd."""
+    return torch.empty((total_q, num_q_heads, num_prefix_splits + 1, head_size + 1),
+                       dtype=torch.float32, device=device)
+
+
+def pa_cascade_fwd(q, kv_cache, block_table, query_start_loc, seq_lens, max_query_len,
+                   num_common_prefix_blocks, scale, workspace, causal=True, out=None, lse=None,
+                   return_lse=True, stream=None):
+    """Cascade attention: the shared first ``num_common_prefix_blocks`` blocks
+    once for all rows, each request's own blocks separately, merged by LSE.
+    ``workspace`` [T, Hq, S1 + 1, d + 1] fp32 sets the prefix split count S1."""
+    T, hq, d = q.shape
+    N = seq_lens.shape[0]
+    if query_start_loc.shape != (N + 1,):
+        raise ValueError("query_start_loc must be [num_seqs + 1]")
+    if block_table.dim() != 2 or block_table.shape[0] != N:
+        raise ValueError("block_table must be [num_seqs, max_blocks]")
+    shape = _pool_shape(kv_cache, N, hq, block_table.shape[1])
+    if workspace.dim() != 4 or tuple(workspace.shape[:2]) != (T, hq) or \
+            workspace.shape[3] != d + 1 or workspace.shape[2] < 2:
+        raise ValueError("workspace must be [total_q, num_q_heads, num_prefix_splits + 1, d + 1]")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((T, hq), dtype=torch.float32, device=q.device)
+    _check(lib().pa_cascade_fwd(
+        _dev(q, "q", torch.bfloat16), _dev(kv_cache, "kv_cache", torch.bfloat16),
+        _dev(block_table, "block_table", torch.int32),
+        _dev(query_start_loc, "query_start_loc", torch.int32),
+        _dev(seq_lens, "seq_lens", torch.int32), T, int(max_query_len),
+        int(num_common_prefix_blocks), int(workspace.shape[2]) - 1, ctypes.byref(shape),
+        float(scale), int(bool(causal)), _dev(workspace, "workspace", torch.float32),
+        _dev(out, "out", torch.bfloat16), _opt(lse, "lse", torch.float32), _stream(stream)),
+        "pa_cascade_fwd")
     return out, lse
 
 

@@ -59,6 +59,37 @@ namespace pa {
 int* device_error_word() { return device_error_ptr(); }
 }  // namespace pa
 
+namespace {
+
+pa::VarlenLaunch varlen_launch(const void* q, const void* kv_cache, const int32_t* block_table,
+                               const int32_t* qsl, const int32_t* seq_lens, int max_query_len,
+                               const pa_shape* shape, float scale, int causal, int window,
+                               void* out, float* lse) {
+  pa::VarlenLaunch L{};
+  L.q = q;
+  L.cache = kv_cache;
+  L.block_table = block_table;
+  L.qsl = qsl;
+  L.seq_lens = seq_lens;
+  L.N = shape->num_seqs;
+  L.Hq = shape->num_q_heads;
+  L.Hkv = shape->num_kv_heads;
+  L.d = shape->head_size;
+  L.bs = shape->block_size;
+  L.num_blocks = shape->num_blocks;
+  L.max_blocks = shape->max_blocks_per_seq;
+  L.max_query_len = max_query_len;
+  L.scale = scale;
+  L.causal = causal;
+  L.window = window;
+  L.out = out;
+  L.lse = lse;
+  L.err = device_error_ptr();
+  return L;
+}
+
+}  // namespace
+
 extern "C" {
 
 pa_status pa_reshape_and_cache(const void* key, const void* value, void* kv_cache,
@@ -95,10 +126,105 @@ pa_status pa_varlen_fwd(const void* q, const void* kv_cache, const int32_t* bloc
   if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(lse, 4))
     return PA_ERR_INVALID;
   return from_cuda(pa::launch_varlen_tc(
-      q, kv_cache, block_table, query_start_loc, seq_lens, shape->num_seqs, shape->num_q_heads,
-      shape->num_kv_heads, shape->head_size, shape->block_size, shape->num_blocks,
-      shape->max_blocks_per_seq, max_query_len, scale, causal ? 1 : 0, out, lse,
-      device_error_ptr(), static_cast<cudaStream_t>(stream)));
+      varlen_launch(q, kv_cache, block_table, query_start_loc, seq_lens, max_query_len, shape,
+                    scale, causal ? 1 : 0, 0, out, lse),
+      static_cast<cudaStream_t>(stream)));
+}
+
+pa_status pa_varlen_fwd_window(const void* q, const void* kv_cache, const int32_t* block_table,
+                               const int32_t* query_start_loc, const int32_t* seq_lens,
+                               int total_q, int max_query_len, const pa_shape* shape, float scale,
+                               int sliding_window, void* out, float* lse, void* stream) {
+  if (!shape_ok(shape) || total_q < 0 || max_query_len < 0 || sliding_window < 1)
+    return PA_ERR_INVALID;
+  if (shape->head_size != 64 && shape->head_size != 128) return PA_ERR_UNSUPPORTED;
+  if (total_q == 0 || shape->num_seqs == 0 || max_query_len == 0) return PA_OK;
+  if (q == nullptr || kv_cache == nullptr || block_table == nullptr ||
+      query_start_loc == nullptr || seq_lens == nullptr || out == nullptr)
+    return PA_ERR_INVALID;
+  if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(lse, 4))
+    return PA_ERR_INVALID;
+  return from_cuda(pa::launch_varlen_tc(
+      varlen_launch(q, kv_cache, block_table, query_start_loc, seq_lens, max_query_len, shape,
+                    scale, 1, sliding_window, out, lse),
+      static_cast<cudaStream_t>(stream)));
+}
+
+int pa_cascade_prefix_splits(int total_q, int num_q_heads, int num_kv_heads,
+                             int prefix_tokens, int sm_count) {
+  if (total_q <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || prefix_tokens <= 0) return 1;
+  if (sm_count <= 0) sm_count = pa_device_sm_count();
+  if (sm_count <= 0) sm_count = 1;
+  // One CTA per (256 packed rows, kv head, split) and one CTA per SM: split
+  // the prefix until every SM has a unit, at most one split per 128 tokens.
+  const long long rows = static_cast<long long>(total_q) * (num_q_heads / num_kv_heads);
+  const long long units = ((rows + 255) / 256) * num_kv_heads;
+  long long s = (sm_count + units - 1) / units;
+  const long long by_len = (static_cast<long long>(prefix_tokens) + 127) / 128;
+  if (s > by_len) s = by_len;
+  if (s > kMaxSplits - 1) s = kMaxSplits - 1;
+  return s < 1 ? 1 : static_cast<int>(s);
+}
+
+pa_status pa_cascade_fwd(const void* q, const void* kv_cache, const int32_t* block_table,
+                         const int32_t* query_start_loc, const int32_t* seq_lens, int total_q,
+                         int max_query_len, int num_common_prefix_blocks, int num_prefix_splits,
+                         const pa_shape* shape, float scale, int causal, float* workspace,
+                         void* out, float* lse, void* stream) {
+  if (!shape_ok(shape) || total_q < 0 || max_query_len < 0 || num_common_prefix_blocks < 0 ||
+      num_common_prefix_blocks > shape->max_blocks_per_seq || num_prefix_splits < 1 ||
+      num_prefix_splits + 1 > kMaxSplits)
+    return PA_ERR_INVALID;
+  if (shape->head_size != 64 && shape->head_size != 128) return PA_ERR_UNSUPPORTED;
+  if (total_q == 0 || shape->num_seqs == 0 || max_query_len == 0) return PA_OK;
+  if (q == nullptr || kv_cache == nullptr || block_table == nullptr ||
+      query_start_loc == nullptr || seq_lens == nullptr || out == nullptr || workspace == nullptr)
+    return PA_ERR_INVALID;
+  if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
+      !aligned(workspace, 4))
+    return PA_ERR_INVALID;
+  const long long prefix_tokens =
+      static_cast<long long>(num_common_prefix_blocks) * shape->block_size;
+  const long long nh = static_cast<long long>(total_q) * shape->num_q_heads;
+  if (prefix_tokens > INT_MAX || nh > INT_MAX) return PA_ERR_INVALID;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (prefix_tokens == 0)   // nothing shared: plain varlen attention
+    return from_cuda(pa::launch_varlen_tc(
+        varlen_launch(q, kv_cache, block_table, query_start_loc, seq_lens, max_query_len, shape,
+                      scale, causal ? 1 : 0, 0, out, lse),
+        st));
+  const int slots = num_prefix_splits + 1;
+  {
+    // Pass 1: every query row of the batch against the shared prefix (read
+    // through row 0 of the table), no mask, cut into num_prefix_splits
+    // pieces: slots [0, num_prefix_splits).
+    pa::VarlenLaunch L = varlen_launch(q, kv_cache, block_table, query_start_loc, seq_lens,
+                                       max_query_len, shape, scale, 0, 0, out, lse);
+    L.virt_total_q = total_q;
+    L.virt_seq = static_cast<int>(prefix_tokens);
+    L.ws = workspace;
+    L.ws_slots = slots;
+    L.ws_slot0 = 0;
+    L.kv_splits = num_prefix_splits;
+    const long long per = (prefix_tokens + num_prefix_splits - 1) / num_prefix_splits;
+    L.kv_chunk = static_cast<int>((per + 127) / 128 * 128);
+    const cudaError_t e = pa::launch_varlen_tc(L, st);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+  }
+  // Pass 2: each request against its own blocks after the prefix, with the
+  // call's mask (positions shift alike for keys and queries): the last slot.
+  pa::VarlenLaunch L2 = varlen_launch(q, kv_cache, block_table, query_start_loc, seq_lens,
+                                      max_query_len, shape, scale, causal ? 1 : 0, 0, out, lse);
+  L2.table_col0 = num_common_prefix_blocks;
+  L2.seq_off = static_cast<int>(prefix_tokens);
+  L2.ws = workspace;
+  L2.ws_slots = slots;
+  L2.ws_slot0 = num_prefix_splits;
+  cudaError_t e = pa::launch_varlen_tc(L2, st);
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  // Merge the partials by their LSE (the split-KV stage 2).
+  return from_cuda(pa::launch_lse_merge(workspace, static_cast<int>(nh), slots,
+                                        shape->head_size, out, lse, st));
 }
 
 int pa_device_sm_count(void) {

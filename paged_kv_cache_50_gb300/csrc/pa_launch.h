@@ -34,11 +34,30 @@ cudaError_t launch_lse_merge(const float* ws, int NH, int S, int dv, void* out, 
                              cudaStream_t stream);
 
 // Varlen paged attention on tcgen05 tensor cores with TMA-gathered K/V.
-cudaError_t launch_varlen_tc(const void* q, const void* cache, const int32_t* block_table,
-                             const int32_t* qsl, const int32_t* seq_lens, int N, int Hq, int Hkv,
-                             int d, int bs, int num_blocks, int max_blocks, int max_query_len,
-                             float scale, int causal, void* out, float* lse, int* err,
-                             cudaStream_t stream);
+struct VarlenLaunch {
+  const void* q;
+  const void* cache;
+  const int32_t* block_table;
+  const int32_t* qsl;
+  const int32_t* seq_lens;
+  int N, Hq, Hkv, d, bs, num_blocks, max_blocks, max_query_len;
+  float scale;
+  int causal;
+  int window;              // > 0: sliding window of that many positions (causal)
+  void* out;               // bf16 [T, Hq, d] (unused in partial mode)
+  float* lse;              // [T, Hq], nullable (unused in partial mode)
+  int* err;
+  int table_col0 = 0;      // first table column of every request's row
+  int seq_off = 0;         // tokens skipped at the front of every request
+  int virt_total_q = 0;    // > 0: all rows [0, virt_total_q) as one request ...
+  int virt_seq = 0;        // ... over virt_seq tokens of table row 0
+  float* ws = nullptr;     // partial mode: fp32 [rows, Hq, ws_slots, d + 1]
+  int ws_slots = 0;
+  int ws_slot0 = 0;        // split s writes slot ws_slot0 + s
+  int kv_splits = 1;
+  int kv_chunk = 0;        // tokens per split, a multiple of 128
+};
+cudaError_t launch_varlen_tc(const VarlenLaunch& L, cudaStream_t stream);
 
 // MLA stage 1 on tcgen05 tensor cores + merge.
 cudaError_t launch_mla_tc(const void* q, const void* cache, const int32_t* block_table,

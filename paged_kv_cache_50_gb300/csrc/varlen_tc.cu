@@ -107,42 +107,100 @@ enum TcBar {
   kFinal = 17,
   kNumBars = 18
 };
+// Arguments of one varlen launch.  The plain call fills the first block; the
+// rest serve split-KV partials and the two passes of cascade attention.
+struct VarlenArgs {
+  const __nv_bfloat16* q;
+  const int32_t* block_table;
+  const int32_t* qsl;
+  const int32_t* seq_lens;
+  int max_blocks;   // row stride of block_table
+  int Hq, Hkv, bs, num_blocks;
+  float scale_log2;
+  int causal;
+  int window;       // > 0: sliding window (causal), row at p sees p - window < p' <= p
+  __nv_bfloat16* out;
+  float* lse;
+  int* err;
+  int table_col0;   // a request's blocks start at this column of its row
+  int seq_off;      // tokens dropped from the front of every request (seq_lens[i] - seq_off)
+  int virt_total_q; // > 0: one request made of query rows [0, virt_total_q) ...
+  int virt_seq;     // ... over virt_seq tokens of table row 0 (qsl, seq_lens unused)
+  float* ws;        // non-null: partial output, [rows][Hq][ws_slots][D + 1] fp32
+  int ws_slots, ws_slot0;
+  int kv_splits;    // context cut into kv_splits pieces of kv_chunk (a multiple of the tile)
+  int kv_chunk;
+};
+
 // After the barriers: the TMEM base address (4 B, padded to 8), the abort
 // flag (4 B, padded to 8) and a ring of 4 tile descriptors (4 B each).
 constexpr int kPieceRing = 4;
 
 template <int D, int CL>
 __global__ void __launch_bounds__(384, 1)
-varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16* __restrict__ q,
-                 const int32_t* __restrict__ block_table, const int32_t* __restrict__ qsl,
-                 const int32_t* __restrict__ seq_lens, int max_blocks, int Hq, int Hkv, int bs,
-                 int num_blocks, float scale_log2, int causal, __nv_bfloat16* __restrict__ out,
-                 float* __restrict__ lse, int* err) {
+varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ VarlenArgs a) {
   using C = TcCfg<D>;
+  const __nv_bfloat16* __restrict__ q = a.q;
+  const int32_t* __restrict__ block_table = a.block_table;
+  const int Hq = a.Hq, Hkv = a.Hkv, bs = a.bs, num_blocks = a.num_blocks;
+  const int causal = a.causal, window = a.window;
+  const float scale_log2 = a.scale_log2;
+  __nv_bfloat16* __restrict__ out = a.out;
+  float* __restrict__ lse = a.lse;
+  int* err = a.err;
+  // Usable table columns of a request's row (the row starts at column
+  // table_col0 of a max_blocks-wide table).
+  const int max_blocks = a.max_blocks - a.table_col0;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t* sgen = smem_raw + (sbase - raw);
 
   const int i = blockIdx.z, kvh = blockIdx.y;
-  const int qt = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);  // heavy tiles first
+  // blockIdx.x = split * q_tiles + (q tile counted from the last).
+  const int q_tiles = static_cast<int>(gridDim.x) / a.kv_splits;
+  const int split = static_cast<int>(blockIdx.x) / q_tiles;
+  const int qt = q_tiles - 1 - static_cast<int>(blockIdx.x) % q_tiles;  // heavy tiles first
   const int rank = CL > 1 ? static_cast<int>(tc::cluster_rank()) : 0;
   const int qt_hi = qt + rank, qt_lo = qt_hi - (CL - 1);   // the cluster's CTA tiles
   const int grp = Hq / Hkv;
-  const int q0 = qsl[i];
-  const int qlen = qsl[i + 1] - q0;
+  // A virtual request (virt_total_q > 0) is every query row of the call
+  // against one fixed context of virt_seq tokens read through table row 0.
+  const bool virt = a.virt_total_q > 0;
+  const int q0 = virt ? 0 : a.qsl[i];
+  const int qlen = virt ? a.virt_total_q : a.qsl[i + 1] - q0;
   const int rows_total = qlen * grp;
   if (qt_lo * C::kRows >= rows_total) return;   // the whole cluster is idle
   const int row0 = qt * C::kRows;               // this CTA's rows (may all be past the end)
-  const int seq = seq_lens[i];
+  const int seq = virt ? a.virt_seq : max(0, a.seq_lens[i] - a.seq_off);
   const int ctx = seq - qlen;
+  if (!virt && causal && ctx < 0 && a.seq_off > 0 && threadIdx.x == 0 && blockIdx.x == 0 &&
+      blockIdx.y == 0)
+    record_error(err, PA_DEVERR_LENGTH);   // queries inside the skipped prefix
   const int last_row = min((qt_hi + 1) * C::kRows, rows_total) - 1;   // the cluster's last row
   int kv_end = causal ? ctx + last_row / grp + 1 : seq;
   kv_end = max(0, min(kv_end, seq));
-  const int ntiles = (kv_end + C::kBN - 1) / C::kBN;
+  // Sliding window (causal only): the cluster's first row sees nothing
+  // before ctx + q_first + 1 - window, so the tiles start at that position
+  // rounded down to a tile; later rows mask their own lower bound.
+  int tbase = 0;
+  if (window > 0) {
+    const int q_first = min(qt_lo * C::kRows, rows_total - 1) / grp;
+    tbase = max(0, ctx + q_first + 1 - window) / C::kBN * C::kBN;
+  }
+  // KV split (a multiple of the tile): this CTA covers [split * kv_chunk,
+  // (split + 1) * kv_chunk) of the context, the last split to its end.
+  if (a.kv_splits > 1) {
+    const long long s0 = static_cast<long long>(split) * a.kv_chunk;
+    tbase = static_cast<int>(max(static_cast<long long>(tbase), s0));
+    if (split < a.kv_splits - 1) kv_end = static_cast<int>(min(static_cast<long long>(kv_end), s0 + a.kv_chunk));
+  }
+  tbase = min(tbase, kv_end);
+  const int ntiles = (kv_end - tbase + C::kBN - 1) / C::kBN;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int32_t* table = block_table + static_cast<int64_t>(i) * max_blocks;
+  const int32_t* table =
+      block_table + static_cast<int64_t>(virt ? 0 : i) * a.max_blocks + a.table_col0;
 
   const uint32_t bars = sbase + C::kOffBar;
   auto BAR = [&](int k) { return bars + 8u * static_cast<uint32_t>(k); };
@@ -209,6 +267,7 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
     const int64_t qoff = (static_cast<int64_t>(q0 + qi) * Hq + kvh * grp + hh) * D;
     int lim = valid ? (causal ? ctx + qi + 1 : seq) : 0;
     lim = max(0, min(lim, seq));
+    const int lo = window > 0 ? max(0, lim - window) : 0;   // first visible position
     {
       const uint4* src = reinterpret_cast<const uint4*>(q + qoff);
       const uint32_t qb = sbase + C::kOffQ + x * C::kQBytes;
@@ -238,7 +297,7 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
     float m_used = -CUDART_INF_F, l = 0.f;
     for (int j = 0; j < ntiles; ++j) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-      const int tok0 = j * C::kBN;
+      const int tok0 = tbase + j * C::kBN;
       if (!wait_warp(BAR(kSFull + x), j & 1)) break;
       tc::tc_fence_after();
       // Loaded pieces of this tile, from the producer's ring (written before
@@ -266,11 +325,11 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
           for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[c][e]);
       }
       // Mask only where some column is not visible (the diagonal tile, the
-      // end of the sequence, an unloaded piece).
-      if (!(tok0 + C::kBN <= lim && vm == (1u << (C::kBN / 16)) - 1u)) {
+      // end of the sequence, the window's start, an unloaded piece).
+      if (!(tok0 + C::kBN <= lim && tok0 >= lo && vm == (1u << (C::kBN / 16)) - 1u)) {
 #pragma unroll
         for (int col = 0; col < C::kBN; ++col) {
-          const bool vis = (tok0 + col < lim) && ((vm >> (col >> 4)) & 1u);
+          const bool vis = (tok0 + col < lim) && (tok0 + col >= lo) && ((vm >> (col >> 4)) & 1u);
           s[col] = vis ? s[col] : -CUDART_INF_F;
         }
       }
@@ -354,7 +413,29 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
     bool ok = !__any_sync(0xffffffffu, *abort_flag != 0) && ntiles > 0;
     if (ok) ok = wait_warp(BAR(kODone + x), (ntiles - 1) & 1);
     tc::tc_fence_after();
-    if (ok) {   // warp-uniform
+    // Partial mode: the row's normalised output and LSE go, in fp32, to slot
+    // ws_slot0 + split of its workspace row [ws_slots][D + 1].
+    float* wrow = a.ws == nullptr ? nullptr
+                                  : a.ws + ((qoff / D) * a.ws_slots + a.ws_slot0 + split) * (D + 1);
+    if (ok && wrow != nullptr) {   // warp-uniform
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        tc::tmem_ld32(to + c * 32, r);
+        tc::tmem_wait_ld();
+        if (valid) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) wrow[c * 32 + e] = __uint_as_float(r[e]) * inv;
+        }
+      }
+      if (valid) wrow[D] = l > 0.f ? (m_used + log2f(l)) * kLn2 : -CUDART_INF_F;
+    } else if (wrow != nullptr) {
+      if (valid) {
+        for (int c = 0; c < D; ++c) wrow[c] = 0.f;
+        wrow[D] = -CUDART_INF_F;
+      }
+    } else if (ok) {   // warp-uniform
       const float inv = l > 0.f ? 1.f / l : 0.f;
       uint4* dst = reinterpret_cast<uint4*>(out + qoff);
 #pragma unroll
@@ -462,11 +543,11 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
     const bool box_lane = lane < C::kBN / 16;
     const bool my_piece = box_lane && (pc % CL) == rank;
     auto in_range = [&](int j) -> bool {
-      return box_lane && j < ntiles && j * C::kBN + 16 * pc < kv_end;
+      return box_lane && j < ntiles && tbase + j * C::kBN + 16 * pc < kv_end;
     };
     auto raw_of = [&](int j) -> int {
       if (!in_range(j)) return -1;
-      const int idx = (j * C::kBN + 16 * pc) / bs;
+      const int idx = (tbase + j * C::kBN + 16 * pc) / bs;
       return idx < max_blocks ? __ldg(table + idx) : -1;
     };
     // The piece's block id, -1 (not visible) or -2 (invalid id).
@@ -474,7 +555,7 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16
       return !in_range(j) ? -1 : (raw >= 0 && raw < num_blocks) ? raw : -2;
     };
     auto issue = [&](int j, int blk, int which, uint32_t dst, uint32_t full) {
-      const int tok0 = j * C::kBN;
+      const int tok0 = tbase + j * C::kBN;
       const unsigned loaded = __ballot_sync(0xffffffffu, blk >= 0);
       const unsigned bad = __ballot_sync(0xffffffffu, blk == -2);
       if (lane == 0) {
@@ -592,14 +673,10 @@ bool make_kv_map(CUtensorMap* map, const void* cache, int nb, int bs, int Hkv, i
 }  // namespace
 
 template <int D, int CL>
-static cudaError_t launch_varlen_tc_t(const void* q, const void* cache, const int32_t* block_table,
-                                      const int32_t* qsl, const int32_t* seq_lens, int N, int Hq,
-                                      int Hkv, int bs, int num_blocks, int max_blocks,
-                                      int max_query_len, float scale, int causal, void* out,
-                                      float* lse, int* err, cudaStream_t stream) {
+static cudaError_t launch_varlen_tc_t(const VarlenLaunch& L, cudaStream_t stream) {
   using C = TcCfg<D>;
   CUtensorMap map;
-  if (!make_kv_map(&map, cache, num_blocks, bs, Hkv, D)) return cudaErrorInvalidValue;
+  if (!make_kv_map(&map, L.cache, L.num_blocks, L.bs, L.Hkv, D)) return cudaErrorInvalidValue;
   auto kern = varlen_tc_kernel<D, CL>;
   static DeviceFlags attr_set;
   cudaError_t e = set_smem_once(kern, C::kSmemBytes, attr_set);
@@ -615,11 +692,40 @@ static cudaError_t launch_varlen_tc_t(const void* q, const void* cache, const in
            fa.numRegs <= static_cast<int>(C::kRegSoftmax) && have >= need;
   }();
   if (!regs_ok) return cudaErrorInvalidConfiguration;
-  const long long rows = static_cast<long long>(max_query_len) * (Hq / Hkv);
+  const bool virt = L.virt_total_q > 0;
+  const long long qrows = virt ? L.virt_total_q : L.max_query_len;
+  const long long rows = qrows * (L.Hq / L.Hkv);
   long long tiles = (rows + C::kRows - 1) / C::kRows;
   tiles = (tiles + CL - 1) / CL * CL;
+  const int splits = L.kv_splits > 1 ? L.kv_splits : 1;
+  if (tiles * splits > 0x7fffffffLL) return cudaErrorInvalidValue;
+  VarlenArgs a{};
+  a.q = static_cast<const __nv_bfloat16*>(L.q);
+  a.block_table = L.block_table;
+  a.qsl = L.qsl;
+  a.seq_lens = L.seq_lens;
+  a.max_blocks = L.max_blocks;
+  a.Hq = L.Hq;
+  a.Hkv = L.Hkv;
+  a.bs = L.bs;
+  a.num_blocks = L.num_blocks;
+  a.scale_log2 = L.scale * kLog2e;
+  a.causal = L.causal;
+  a.window = L.window;
+  a.out = static_cast<__nv_bfloat16*>(L.out);
+  a.lse = L.lse;
+  a.err = L.err;
+  a.table_col0 = L.table_col0;
+  a.seq_off = L.seq_off;
+  a.virt_total_q = L.virt_total_q;
+  a.virt_seq = L.virt_seq;
+  a.ws = L.ws;
+  a.ws_slots = L.ws_slots;
+  a.ws_slot0 = L.ws_slot0;
+  a.kv_splits = splits;
+  a.kv_chunk = L.kv_chunk;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(tiles), Hkv, N);
+  cfg.gridDim = dim3(static_cast<unsigned>(tiles * splits), L.Hkv, virt ? 1 : L.N);
   cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
@@ -630,26 +736,15 @@ static cudaError_t launch_varlen_tc_t(const void* q, const void* cache, const in
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, map, static_cast<const __nv_bfloat16*>(q), block_table,
-                            qsl, seq_lens, max_blocks, Hq, Hkv, bs, num_blocks, scale * kLog2e,
-                            causal, static_cast<__nv_bfloat16*>(out), lse, err);
+  return cudaLaunchKernelEx(&cfg, kern, map, a);
 }
 
 // CTAs per cluster sharing K/V tiles by multicast.
 constexpr int kVarlenCluster = 1;
 
-cudaError_t launch_varlen_tc(const void* q, const void* cache, const int32_t* block_table,
-                             const int32_t* qsl, const int32_t* seq_lens, int N, int Hq, int Hkv,
-                             int d, int bs, int num_blocks, int max_blocks, int max_query_len,
-                             float scale, int causal, void* out, float* lse, int* err,
-                             cudaStream_t stream) {
-  if (d == 128)
-    return launch_varlen_tc_t<128, kVarlenCluster>(q, cache, block_table, qsl, seq_lens, N, Hq,
-                                                   Hkv, bs, num_blocks, max_blocks, max_query_len,
-                                                   scale, causal, out, lse, err, stream);
-  return launch_varlen_tc_t<64, kVarlenCluster>(q, cache, block_table, qsl, seq_lens, N, Hq, Hkv,
-                                                bs, num_blocks, max_blocks, max_query_len, scale,
-                                                causal, out, lse, err, stream);
+cudaError_t launch_varlen_tc(const VarlenLaunch& L, cudaStream_t stream) {
+  if (L.d == 128) return launch_varlen_tc_t<128, kVarlenCluster>(L, stream);
+  return launch_varlen_tc_t<64, kVarlenCluster>(L, stream);
 }
 
 }  // namespace pa

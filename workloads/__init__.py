@@ -204,6 +204,63 @@ def make_mla_batch(name, seed, seq_lens, num_heads, kv_lora_rank=512, rope_dim=6
                     seq_lens, table, q, pool, float(scale))
 
 
+def make_shared_prefix_batch(name, seed, prefix_blocks, suffix_lens, query_lens, num_q_heads,
+                             num_kv_heads, head_size, block_size, scale=None,
+                             with_pool=True) -> PagedBatch:
+    """A batch whose requests all begin with the same ``prefix_blocks`` blocks
+    (the same block ids in every table row: a shared system prompt) followed
+    by their own ``suffix_lens[i]`` tokens, the last ``query_lens[i]`` of which
+    are the step's new tokens.  Block ids: a seeded permutation, the first
+    ``prefix_blocks`` of it for the prefix, the rest handed out in request
+    order.  Values as in make_paged_batch."""
+    rng = np.random.default_rng(seed)
+    suffix_lens = np.asarray(suffix_lens, np.int32)
+    query_lens = np.asarray(query_lens, np.int32)
+    assert np.all(query_lens <= suffix_lens) and np.all(query_lens >= 0)
+    N = suffix_lens.shape[0]
+    seq_lens = (suffix_lens + prefix_blocks * block_size).astype(np.int32)
+    need = [(int(x) + block_size - 1) // block_size for x in suffix_lens]
+    nb = prefix_blocks + sum(need)
+    perm = rng.permutation(nb).astype(np.int32)
+    max_blocks = max(1, prefix_blocks + (max(need) if need else 0))
+    table = np.full((N, max_blocks), -1, np.int32)
+    k = prefix_blocks
+    for i, n in enumerate(need):
+        table[i, :prefix_blocks] = perm[:prefix_blocks]
+        table[i, prefix_blocks:prefix_blocks + n] = perm[k:k + n]
+        k += n
+    qsl = np.zeros(N + 1, np.int32)
+    qsl[1:] = np.cumsum(query_lens)
+    T = int(qsl[-1])
+    slots = np.empty(T, np.int64)
+    for i in range(N):
+        ctx = int(seq_lens[i] - query_lens[i])
+        for j in range(int(query_lens[i])):
+            pos = ctx + j
+            slots[qsl[i] + j] = int(table[i, pos // block_size]) * block_size + pos % block_size
+    pool = randn_bf16(rng, (nb, 2, block_size, num_kv_heads, head_size)) if with_pool else None
+    rng = np.random.default_rng([seed, 1])
+    q = randn_bf16(rng, (T, num_q_heads, head_size))
+    key = randn_bf16(rng, (T, num_kv_heads, head_size))
+    value = randn_bf16(rng, (T, num_kv_heads, head_size))
+    if scale is None:
+        scale = 1.0 / math.sqrt(head_size)
+    return PagedBatch(name, seed, num_q_heads, num_kv_heads, head_size, block_size, nb, seq_lens,
+                      query_lens, qsl, table, slots, q, key, value, pool, float(scale), True)
+
+
+def shared_prefix_decode(seed: int = 6, num_seqs: int = 64, prefix_tokens: int = 4096,
+                         lo: int = 64, hi: int = 1024, **kw) -> PagedBatch:
+    """64 decode requests (one new token each) sharing a 4096-token prompt,
+    each with its own U[64, 1024] tokens after it; 32 q / 8 kv heads, d 128,
+    block size 16."""
+    rng = np.random.default_rng(seed + 1000)
+    suf = rng.integers(lo, hi, size=num_seqs, endpoint=True).astype(np.int32)
+    return make_shared_prefix_batch(f"shared_prefix_decode_{num_seqs}req_p{prefix_tokens}",
+                                    seed, prefix_tokens // 16, suf, np.ones(num_seqs, np.int32),
+                                    32, 8, 128, 16, **kw)
+
+
 # ---------------------------------------------------------------------------
 # fp8 (e4m3) KV cache inputs.
 # ---------------------------------------------------------------------------
