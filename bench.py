@@ -432,8 +432,49 @@ def bench_fp8_decode(pa, device, pk, flush, reps=10):
     return res
 
 
+def bench_cascade(pa, device, pk, flush, reps=10):
+    """Cascade attention on 64 decode requests sharing a prompt (4096 tokens:
+    17 MB of K/V per layer, L2-resident; 32768 tokens: 134 MB, more than L2),
+    against plain split-KV decode of the same batch, which reads the prompt
+    once per request."""
+    res = {}
+    for prefix in (4096, 32768):
+        b = workloads.shared_prefix_decode(prefix_tokens=prefix, with_pool=False)
+        N, hq, d = b.num_seqs, b.num_q_heads, b.head_size
+        pool = device_pool((b.num_blocks, 2, b.block_size, b.num_kv_heads, d), 6, device)
+        q = to_dev_bf16(b.q, device)
+        table = to_dev(b.block_table, torch.int32, device)
+        qsl = to_dev(b.query_start_loc, torch.int32, device)
+        seq = to_dev(b.seq_lens, torch.int32, device)
+        P = prefix // b.block_size
+        mx = int(b.seq_lens.max())
+        sms = pa.pa_device_sm_count()
+        S = pa.pa_num_kv_splits(mx, sms)
+        ws = pa.decode_workspace(N, hq, S, d, device=device)
+        S1 = pa.pa_cascade_prefix_splits(N, hq, b.num_kv_heads, prefix, sms)
+        S2 = pa.pa_num_kv_splits(mx - prefix, sms)
+        cws = pa.cascade_workspace(N, hq, S1, S2, d, device=device)
+        o = torch.empty((N, hq, d), dtype=torch.bfloat16, device=device)
+        lo = torch.empty((N, hq), dtype=torch.float32, device=device)
+        plain = _timed_with_flush(lambda: pa.pa_decode(q.view(N, hq, d), pool, table, seq, b.scale,
+                                                       ws, o, lo, mx), flush, reps)
+        casc = _timed_with_flush(lambda: pa.pa_cascade_fwd(q, pool, table, qsl, seq, 1, P, b.scale,
+                                                           cws, S1, mx, out=o, lse=lo),
+                                 flush, reps)
+        row = b.num_kv_heads * d * 2 * 2
+        unique = (prefix + int((b.seq_lens - prefix).astype(np.int64).sum())) * row
+        res[b.name] = {"prefix_tokens": prefix, "prefix_splits": S1, "suffix_splits": S2,
+                       "cascade_ms": casc, "plain_decode_ms": plain, "speedup": plain / casc,
+                       "unique_kv_bytes": unique,
+                       "cascade_unique_gbs": unique / (casc * 1e-3) / 1e9,
+                       "plain_kv_bytes": b.kv_bytes()}
+        del pool, q, ws, cws
+        torch.cuda.empty_cache()
+    return res
+
+
 SECONDARY = {"chunked_prefill": bench_prefill, "long_decode": bench_long_decode,
-             "mla_decode": bench_mla, "fp8_decode": bench_fp8_decode}
+             "mla_decode": bench_mla, "fp8_decode": bench_fp8_decode, "cascade": bench_cascade}
 
 
 def secondary(pa, device, pk):

@@ -132,29 +132,35 @@ pa_status pa_varlen_fwd_window(const void* q, const void* kv_cache, const int32_
  * per-request parts separately).  The result is that of pa_varlen_fwd on the
  * same arguments; it is computed as
  *   pass 1: every query row of the batch against the first
- *           num_common_prefix_blocks * block_size tokens, read once per kv
+ *           P = num_common_prefix_blocks * block_size tokens, read once per kv
  *           head through row 0 of block_table, without a mask, cut into
- *           num_prefix_splits pieces -> partials in workspace slots
- *           [0, num_prefix_splits);
- *   pass 2: request i against its own tokens from position
- *           num_common_prefix_blocks * block_size on (table columns from
- *           num_common_prefix_blocks), with the call's mask -> slot
- *           num_prefix_splits;
- *   merge:  the pa_lse_merge of the num_prefix_splits + 1 partials -> out, lse.
+ *           num_prefix_splits pieces of whole 128-token tiles -> workspace
+ *           slots [0, num_prefix_splits);
+ *   pass 2: request i against its own tokens from position P on (table
+ *           columns from num_common_prefix_blocks), with the call's mask, cut
+ *           into num_suffix_splits pieces as pa_decode_splitkv cuts a batch
+ *           whose longest sequence is max_seq_len - P -> slots
+ *           [num_prefix_splits, num_prefix_splits + num_suffix_splits).  A
+ *           batch of one query per request (total_q == num_seqs,
+ *           max_query_len == 1) runs this pass on the split-KV decode kernel;
+ *   merge:  the pa_lse_merge of all the slots -> out, lse.
  * Preconditions: the first num_common_prefix_blocks entries of every table
  * row are the same block ids; with causal != 0 every query lies after the
- * prefix (seq_lens[i] - qlen_i >= num_common_prefix_blocks * block_size; a
- * request that breaks it sets PA_DEVERR_LENGTH and its rows are invalid).
- * workspace: pa_decode_workspace_bytes(total_q, Hq, num_prefix_splits + 1, d)
- * bytes (fp32 [total_q, Hq, num_prefix_splits + 1, d + 1]).
+ * prefix (seq_lens[i] - qlen_i >= P; a request that breaks it sets
+ * PA_DEVERR_LENGTH and its rows are invalid).  max_seq_len >= every
+ * seq_lens[i] (sizes the suffix pieces; a smaller value costs speed, never
+ * correctness).
+ * workspace: pa_decode_workspace_bytes(total_q, Hq, num_prefix_splits +
+ * num_suffix_splits, d) bytes (fp32 [total_q, Hq, slots, d + 1]).
  * num_common_prefix_blocks == 0 runs pa_varlen_fwd (workspace untouched).
- * Other arguments as for pa_varlen_fwd; head_size in {64, 128}.
+ * Other arguments as for pa_varlen_fwd; head_size in {64, 128}, Hq / Hkv <= 16.
  */
 pa_status pa_cascade_fwd(const void* q, const void* kv_cache, const int32_t* block_table,
                          const int32_t* query_start_loc, const int32_t* seq_lens, int total_q,
-                         int max_query_len, int num_common_prefix_blocks, int num_prefix_splits,
-                         const pa_shape* shape, float scale, int causal, float* workspace,
-                         void* out, float* lse, void* stream);
+                         int max_query_len, int max_seq_len, int num_common_prefix_blocks,
+                         int num_prefix_splits, int num_suffix_splits, const pa_shape* shape,
+                         float scale, int causal, float* workspace, void* out, float* lse,
+                         void* stream);
 
 /*
  * A num_prefix_splits for pa_cascade_fwd: enough pieces of the prefix that

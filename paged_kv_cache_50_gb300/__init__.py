@@ -64,8 +64,8 @@ def lib() -> ctypes.CDLL:
         L.pa_decode_splitkv.argtypes = [P, P, P, P, SP, f32, i32, i32, P, P]
         L.pa_lse_merge.argtypes = [P, i32, i32, i32, i32, P, P, P]
         L.pa_varlen_fwd_window.argtypes = [P, P, P, P, P, i32, i32, SP, f32, i32, P, P, P]
-        L.pa_cascade_fwd.argtypes = [P, P, P, P, P, i32, i32, i32, i32, SP, f32, i32, P, P, P,
-                                     P]
+        L.pa_cascade_fwd.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, SP, f32, i32,
+                                     P, P, P, P]
         L.pa_cascade_prefix_splits.argtypes = [i32, i32, i32, i32, i32]
         L.pa_cascade_prefix_splits.restype = i32
         L.pa_reshape_and_cache_fp8.argtypes = [P, P, P, P, i32, SP, f32, f32, P]
@@ -201,18 +201,21 @@ def pa_cascade_prefix_splits(total_q, num_q_heads, num_kv_heads, prefix_tokens, 
                                               int(prefix_tokens), int(sm_count)))
 
 
-def cascade_workspace(total_q, num_q_heads, num_prefix_splits, head_size, device="cuda"):
-    """fp32 [total_q, Hq, num_prefix_splits + 1, d + 1] workspace for pa_cascade_fwd."""
-    return torch.empty((total_q, num_q_heads, num_prefix_splits + 1, head_size + 1),
-                       dtype=torch.float32, device=device)
+def cascade_workspace(total_q, num_q_heads, num_prefix_splits, num_suffix_splits, head_size,
+                      device="cuda"):
+    """fp32 [total_q, Hq, S1 + S2, d + 1] workspace for pa_cascade_fwd."""
+    return torch.empty((total_q, num_q_heads, num_prefix_splits + num_suffix_splits,
+                        head_size + 1), dtype=torch.float32, device=device)
 
 
 def pa_cascade_fwd(q, kv_cache, block_table, query_start_loc, seq_lens, max_query_len,
-                   num_common_prefix_blocks, scale, workspace, causal=True, out=None, lse=None,
-                   return_lse=True, stream=None):
+                   num_common_prefix_blocks, scale, workspace, num_prefix_splits,
+                   max_seq_len=None, causal=True, out=None, lse=None, return_lse=True,
+                   stream=None):
     """Cascade attention: the shared first ``num_common_prefix_blocks`` blocks
-    once for all rows, each request's own blocks separately, merged by LSE.
-    ``workspace`` [T, Hq, S1 + 1, d + 1] fp32 sets the prefix split count S1."""
+    once for all rows (``num_prefix_splits`` pieces), each request's own
+    blocks separately (the workspace's remaining slots), merged by LSE.
+    ``workspace`` is [T, Hq, S1 + S2, d + 1] fp32 (see cascade_workspace)."""
     T, hq, d = q.shape
     N = seq_lens.shape[0]
     if query_start_loc.shape != (N + 1,):
@@ -221,21 +224,22 @@ def pa_cascade_fwd(q, kv_cache, block_table, query_start_loc, seq_lens, max_quer
         raise ValueError("block_table must be [num_seqs, max_blocks]")
     shape = _pool_shape(kv_cache, N, hq, block_table.shape[1])
     if workspace.dim() != 4 or tuple(workspace.shape[:2]) != (T, hq) or \
-            workspace.shape[3] != d + 1 or workspace.shape[2] < 2:
-        raise ValueError("workspace must be [total_q, num_q_heads, num_prefix_splits + 1, d + 1]")
+            workspace.shape[3] != d + 1 or workspace.shape[2] <= int(num_prefix_splits):
+        raise ValueError("workspace must be [total_q, num_q_heads, S1 + S2, d + 1] with S2 >= 1")
     if out is None:
         out = torch.empty_like(q)
     if lse is None and return_lse:
         lse = torch.empty((T, hq), dtype=torch.float32, device=q.device)
+    s1 = int(num_prefix_splits)
     _check(lib().pa_cascade_fwd(
         _dev(q, "q", torch.bfloat16), _dev(kv_cache, "kv_cache", torch.bfloat16),
         _dev(block_table, "block_table", torch.int32),
         _dev(query_start_loc, "query_start_loc", torch.int32),
         _dev(seq_lens, "seq_lens", torch.int32), T, int(max_query_len),
-        int(num_common_prefix_blocks), int(workspace.shape[2]) - 1, ctypes.byref(shape),
-        float(scale), int(bool(causal)), _dev(workspace, "workspace", torch.float32),
-        _dev(out, "out", torch.bfloat16), _opt(lse, "lse", torch.float32), _stream(stream)),
-        "pa_cascade_fwd")
+        _max_seq(seq_lens, max_seq_len), int(num_common_prefix_blocks), s1,
+        int(workspace.shape[2]) - s1, ctypes.byref(shape), float(scale), int(bool(causal)),
+        _dev(workspace, "workspace", torch.float32), _dev(out, "out", torch.bfloat16),
+        _opt(lse, "lse", torch.float32), _stream(stream)), "pa_cascade_fwd")
     return out, lse
 
 

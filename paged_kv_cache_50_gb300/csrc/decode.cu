@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(128)
 decode_splitkv_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ cache,
                       const int32_t* __restrict__ block_table, const int32_t* __restrict__ seq_lens,
                       int max_blocks, int Hq, int Hkv, int bs, int num_blocks, float scale_log2,
-                      int S, int chunk, float* __restrict__ ws, int* err) {
+                      int S, int chunk, float* __restrict__ ws, int* err, DecodeExt ext) {
   using C = DecodeCfg<D, STAGES, NT>;
   constexpr int kK = D / 16;   // k-steps of K Q^T = d-tiles of V^T P^T
   constexpr float kRescale = 8.f;
@@ -79,7 +79,9 @@ decode_splitkv_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
 
   // Every input may come from the previous kernel in the stream.
   pdl_wait();
-  const int seq = seq_lens[i];
+  // ext.seq_off tokens at the front of every request are skipped (their
+  // blocks are the first ext.table_col0 columns of the table row).
+  const int seq = max(0, seq_lens[i] - ext.seq_off);
   // Split s covers [s*chunk, (s+1)*chunk) of the request (the last split runs
   // to the end), chunk being one block-aligned size for the whole batch.
   const long long a0 = static_cast<long long>(s) * chunk;
@@ -107,12 +109,13 @@ decode_splitkv_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
 
   const uint32_t wbase = smem_u32(smem) + warp * C::kWarpBytes;
   const int64_t row_stride = static_cast<int64_t>(Hkv) * D;
-  const int32_t* table = block_table + static_cast<int64_t>(i) * max_blocks;
+  const int32_t* table = block_table + static_cast<int64_t>(i) * max_blocks + ext.table_col0;
+  const int cols = max_blocks - ext.table_col0;
 
   // Block id of the warp's n-th sub-block (loaded one iteration before its
   // copies are issued, so the table read is off the critical path).
   auto lookup = [&](int n) {
-    return block_at(table, (t0 + (warp + n * C::kWarps) * 16) / bs, max_blocks);
+    return block_at(table, (t0 + (warp + n * C::kWarps) * 16) / bs, cols);
   };
   // Bit n % 32 of okbits: the n-th sub-block's block id was valid (at most
   // STAGES sub-blocks are between issue and use).
@@ -301,7 +304,8 @@ decode_splitkv_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
     float M = -CUDART_INF_F;
 #pragma unroll
     for (int w = 0; w < C::kWarps; ++w) M = fmaxf(M, mbuf[w * C::kHeads + r]);
-    float* dst = ws + ((static_cast<int64_t>(i) * Hq + kvh * grp + r) * S + s) * (D + 1);
+    float* dst =
+        ws + ((static_cast<int64_t>(i) * Hq + kvh * grp + r) * ext.ws_slots + ext.ws_slot0 + s) * (D + 1);
     if (M == -CUDART_INF_F) {
       dst[e] = 0.f;
       if (e == 0) dst[D] = -CUDART_INF_F;
@@ -373,7 +377,8 @@ template <int D, int STAGES, int NT>
 static cudaError_t launch_decode_t(const void* q, const void* cache, const int32_t* block_table,
                                    const int32_t* seq_lens, int N, int Hq, int Hkv, int bs,
                                    int num_blocks, int max_blocks, float scale, int S, int chunk,
-                                   float* ws, int* err, cudaStream_t stream) {
+                                   float* ws, int* err, const DecodeExt& ext,
+                                   cudaStream_t stream) {
   using C = DecodeCfg<D, STAGES, NT>;
   auto kern = decode_splitkv_kernel<D, STAGES, NT>;
   static DeviceFlags attr_set;
@@ -382,17 +387,19 @@ static cudaError_t launch_decode_t(const void* q, const void* cache, const int32
   return launch_pdl(kern, dim3(S, Hkv, N), dim3(C::kThreads), C::kSmemBytes, stream,
                     static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(cache),
                     block_table, seq_lens, max_blocks, Hq, Hkv, bs, num_blocks, scale * kLog2e, S,
-                    chunk, ws, err);
+                    chunk, ws, err, ext);
 }
 
 cudaError_t launch_decode_splitkv(const void* q, const void* cache, const int32_t* block_table,
                                   const int32_t* seq_lens, int N, int Hq, int Hkv, int d, int bs,
                                   int num_blocks, int max_blocks, float scale, int S, int chunk,
-                                  float* ws, int* err, cudaStream_t stream) {
+                                  float* ws, int* err, cudaStream_t stream, const DecodeExt* ext) {
+  const DecodeExt plain{0, 0, S, 0};
+  const DecodeExt& x = ext != nullptr ? *ext : plain;
   const bool wide = Hq / Hkv > 8;   // groups of 9..16 heads take two n-tiles
 #define PA_DECODE_LAUNCH(DD, ST, NTT)                                                          \
   return launch_decode_t<DD, ST, NTT>(q, cache, block_table, seq_lens, N, Hq, Hkv, bs,         \
-                                      num_blocks, max_blocks, scale, S, chunk, ws, err, stream)
+                                      num_blocks, max_blocks, scale, S, chunk, ws, err, x, stream)
   if (d == 128) {
     if (wide) PA_DECODE_LAUNCH(128, 2, 2);
     PA_DECODE_LAUNCH(128, 2, 1);

@@ -4,6 +4,7 @@
 // is a diagnostic).
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <climits>
 #include <cstdint>
 #include <mutex>
@@ -168,14 +169,17 @@ int pa_cascade_prefix_splits(int total_q, int num_q_heads, int num_kv_heads,
 
 pa_status pa_cascade_fwd(const void* q, const void* kv_cache, const int32_t* block_table,
                          const int32_t* query_start_loc, const int32_t* seq_lens, int total_q,
-                         int max_query_len, int num_common_prefix_blocks, int num_prefix_splits,
-                         const pa_shape* shape, float scale, int causal, float* workspace,
-                         void* out, float* lse, void* stream) {
-  if (!shape_ok(shape) || total_q < 0 || max_query_len < 0 || num_common_prefix_blocks < 0 ||
-      num_common_prefix_blocks > shape->max_blocks_per_seq || num_prefix_splits < 1 ||
-      num_prefix_splits + 1 > kMaxSplits)
+                         int max_query_len, int max_seq_len, int num_common_prefix_blocks,
+                         int num_prefix_splits, int num_suffix_splits, const pa_shape* shape,
+                         float scale, int causal, float* workspace, void* out, float* lse,
+                         void* stream) {
+  if (!shape_ok(shape) || total_q < 0 || max_query_len < 0 || max_seq_len < 0 ||
+      num_common_prefix_blocks < 0 || num_common_prefix_blocks > shape->max_blocks_per_seq ||
+      num_prefix_splits < 1 || num_suffix_splits < 1 ||
+      num_prefix_splits + num_suffix_splits > kMaxSplits)
     return PA_ERR_INVALID;
   if (shape->head_size != 64 && shape->head_size != 128) return PA_ERR_UNSUPPORTED;
+  if (shape->num_q_heads / shape->num_kv_heads > 16) return PA_ERR_UNSUPPORTED;
   if (total_q == 0 || shape->num_seqs == 0 || max_query_len == 0) return PA_OK;
   if (q == nullptr || kv_cache == nullptr || block_table == nullptr ||
       query_start_loc == nullptr || seq_lens == nullptr || out == nullptr || workspace == nullptr)
@@ -193,7 +197,7 @@ pa_status pa_cascade_fwd(const void* q, const void* kv_cache, const int32_t* blo
         varlen_launch(q, kv_cache, block_table, query_start_loc, seq_lens, max_query_len, shape,
                       scale, causal ? 1 : 0, 0, out, lse),
         st));
-  const int slots = num_prefix_splits + 1;
+  const int slots = num_prefix_splits + num_suffix_splits;
   {
     // Pass 1: every query row of the batch against the shared prefix (read
     // through row 0 of the table), no mask, cut into num_prefix_splits
@@ -208,20 +212,37 @@ pa_status pa_cascade_fwd(const void* q, const void* kv_cache, const int32_t* blo
     L.kv_splits = num_prefix_splits;
     const long long per = (prefix_tokens + num_prefix_splits - 1) / num_prefix_splits;
     L.kv_chunk = static_cast<int>((per + 127) / 128 * 128);
-    const cudaError_t e = pa::launch_varlen_tc(L, st);
-    if (e != cudaSuccess) return PA_ERR_CUDA;
+    if (pa::launch_varlen_tc(L, st) != cudaSuccess) return PA_ERR_CUDA;
   }
-  // Pass 2: each request against its own blocks after the prefix, with the
-  // call's mask (positions shift alike for keys and queries): the last slot.
-  pa::VarlenLaunch L2 = varlen_launch(q, kv_cache, block_table, query_start_loc, seq_lens,
-                                      max_query_len, shape, scale, causal ? 1 : 0, 0, out, lse);
-  L2.table_col0 = num_common_prefix_blocks;
-  L2.seq_off = static_cast<int>(prefix_tokens);
-  L2.ws = workspace;
-  L2.ws_slots = slots;
-  L2.ws_slot0 = num_prefix_splits;
-  cudaError_t e = pa::launch_varlen_tc(L2, st);
-  if (e != cudaSuccess) return PA_ERR_CUDA;
+  // Pass 2: each request against its own blocks after the prefix (positions
+  // shift alike for keys and queries, so the call's mask is kept), cut into
+  // num_suffix_splits pieces: slots [num_prefix_splits, slots).  A batch of
+  // one query per request takes the split-KV decode kernel.
+  const int suffix_max = static_cast<int>(std::max(0LL, max_seq_len - prefix_tokens));
+  if (max_query_len == 1 && total_q == shape->num_seqs) {
+    const pa::DecodeExt ext{num_common_prefix_blocks, static_cast<int>(prefix_tokens), slots,
+                            num_prefix_splits};
+    if (pa::launch_decode_splitkv(
+            q, kv_cache, block_table, seq_lens, shape->num_seqs, shape->num_q_heads,
+            shape->num_kv_heads, shape->head_size, shape->block_size, shape->num_blocks,
+            shape->max_blocks_per_seq, scale, num_suffix_splits,
+            static_cast<int>(pa::split_chunk(suffix_max, num_suffix_splits, shape->block_size)),
+            workspace, device_error_ptr(), st, &ext) != cudaSuccess)
+      return PA_ERR_CUDA;
+  } else {
+    pa::VarlenLaunch L2 = varlen_launch(q, kv_cache, block_table, query_start_loc, seq_lens,
+                                        max_query_len, shape, scale, causal ? 1 : 0, 0, out, lse);
+    L2.table_col0 = num_common_prefix_blocks;
+    L2.seq_off = static_cast<int>(prefix_tokens);
+    L2.ws = workspace;
+    L2.ws_slots = slots;
+    L2.ws_slot0 = num_prefix_splits;
+    L2.kv_splits = num_suffix_splits;
+    const long long per = (static_cast<long long>(suffix_max) + num_suffix_splits - 1) /
+                          num_suffix_splits;
+    L2.kv_chunk = static_cast<int>(std::max(128LL, (per + 127) / 128 * 128));
+    if (pa::launch_varlen_tc(L2, st) != cudaSuccess) return PA_ERR_CUDA;
+  }
   // Merge the partials by their LSE (the split-KV stage 2).
   return from_cuda(pa::launch_lse_merge(workspace, static_cast<int>(nh), slots,
                                         shape->head_size, out, lse, st));

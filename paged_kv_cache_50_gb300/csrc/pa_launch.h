@@ -12,11 +12,25 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* c
                                      int num_kv_heads, int head_size, int block_size,
                                      int num_blocks, int* err, cudaStream_t stream);
 
+// Offsets of a split-KV stage-1 launch that serves part of a larger
+// computation (the suffix pass of cascade attention): every request skips its
+// first seq_off tokens, whose blocks are the first table_col0 columns of its
+// row, and split s writes slot ws_slot0 + s of a workspace with ws_slots
+// slots per (request, head).
+struct DecodeExt {
+  int table_col0;
+  int seq_off;
+  int ws_slots;
+  int ws_slot0;
+};
+
 // Split-KV stage 1; `chunk` = tokens per split (split_chunk in pa_common.cuh).
+// ext == nullptr: no offsets, S slots.
 cudaError_t launch_decode_splitkv(const void* q, const void* cache, const int32_t* block_table,
                                   const int32_t* seq_lens, int N, int Hq, int Hkv, int d, int bs,
                                   int num_blocks, int max_blocks, float scale, int S, int chunk,
-                                  float* ws, int* err, cudaStream_t stream);
+                                  float* ws, int* err, cudaStream_t stream,
+                                  const DecodeExt* ext = nullptr);
 
 // fp8 (e4m3) pool: quantising cache write and split-KV stage 1.
 cudaError_t launch_reshape_and_cache_fp8(const void* key, const void* value, void* cache,

@@ -136,21 +136,26 @@ struct VarlenArgs {
 // flag (4 B, padded to 8) and a ring of 4 tile descriptors (4 B each).
 constexpr int kPieceRing = 4;
 
-template <int D, int CL>
+// EXT = false compiles the plain call (no window, split, offsets, virtual
+// request or partial output: those fields are ignored).
+template <int D, int CL, bool EXT>
 __global__ void __launch_bounds__(384, 1)
 varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ VarlenArgs a) {
   using C = TcCfg<D>;
   const __nv_bfloat16* __restrict__ q = a.q;
   const int32_t* __restrict__ block_table = a.block_table;
   const int Hq = a.Hq, Hkv = a.Hkv, bs = a.bs, num_blocks = a.num_blocks;
-  const int causal = a.causal, window = a.window;
+  const int causal = a.causal, window = EXT ? a.window : 0;
+  const int table_col0 = EXT ? a.table_col0 : 0, seq_off = EXT ? a.seq_off : 0;
+  const int kv_splits = EXT ? a.kv_splits : 1;
+  float* const ws = EXT ? a.ws : nullptr;
   const float scale_log2 = a.scale_log2;
   __nv_bfloat16* __restrict__ out = a.out;
   float* __restrict__ lse = a.lse;
   int* err = a.err;
   // Usable table columns of a request's row (the row starts at column
   // table_col0 of a max_blocks-wide table).
-  const int max_blocks = a.max_blocks - a.table_col0;
+  const int max_blocks = a.max_blocks - table_col0;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -158,23 +163,24 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
 
   const int i = blockIdx.z, kvh = blockIdx.y;
   // blockIdx.x = split * q_tiles + (q tile counted from the last).
-  const int q_tiles = static_cast<int>(gridDim.x) / a.kv_splits;
-  const int split = static_cast<int>(blockIdx.x) / q_tiles;
-  const int qt = q_tiles - 1 - static_cast<int>(blockIdx.x) % q_tiles;  // heavy tiles first
+  const int q_tiles = static_cast<int>(gridDim.x) / kv_splits;
+  const int split = EXT ? static_cast<int>(blockIdx.x) / q_tiles : 0;
+  const int qt = EXT ? q_tiles - 1 - static_cast<int>(blockIdx.x) % q_tiles
+                     : static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);  // heavy tiles first
   const int rank = CL > 1 ? static_cast<int>(tc::cluster_rank()) : 0;
   const int qt_hi = qt + rank, qt_lo = qt_hi - (CL - 1);   // the cluster's CTA tiles
   const int grp = Hq / Hkv;
   // A virtual request (virt_total_q > 0) is every query row of the call
   // against one fixed context of virt_seq tokens read through table row 0.
-  const bool virt = a.virt_total_q > 0;
+  const bool virt = EXT && a.virt_total_q > 0;
   const int q0 = virt ? 0 : a.qsl[i];
   const int qlen = virt ? a.virt_total_q : a.qsl[i + 1] - q0;
   const int rows_total = qlen * grp;
   if (qt_lo * C::kRows >= rows_total) return;   // the whole cluster is idle
   const int row0 = qt * C::kRows;               // this CTA's rows (may all be past the end)
-  const int seq = virt ? a.virt_seq : max(0, a.seq_lens[i] - a.seq_off);
+  const int seq = virt ? a.virt_seq : max(0, a.seq_lens[i] - seq_off);
   const int ctx = seq - qlen;
-  if (!virt && causal && ctx < 0 && a.seq_off > 0 && threadIdx.x == 0 && blockIdx.x == 0 &&
+  if (EXT && !virt && causal && ctx < 0 && seq_off > 0 && threadIdx.x == 0 && blockIdx.x == 0 &&
       blockIdx.y == 0)
     record_error(err, PA_DEVERR_LENGTH);   // queries inside the skipped prefix
   const int last_row = min((qt_hi + 1) * C::kRows, rows_total) - 1;   // the cluster's last row
@@ -190,17 +196,17 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
   }
   // KV split (a multiple of the tile): this CTA covers [split * kv_chunk,
   // (split + 1) * kv_chunk) of the context, the last split to its end.
-  if (a.kv_splits > 1) {
+  if (kv_splits > 1) {
     const long long s0 = static_cast<long long>(split) * a.kv_chunk;
     tbase = static_cast<int>(max(static_cast<long long>(tbase), s0));
-    if (split < a.kv_splits - 1) kv_end = static_cast<int>(min(static_cast<long long>(kv_end), s0 + a.kv_chunk));
+    if (split < kv_splits - 1) kv_end = static_cast<int>(min(static_cast<long long>(kv_end), s0 + a.kv_chunk));
   }
   tbase = min(tbase, kv_end);
   const int ntiles = (kv_end - tbase + C::kBN - 1) / C::kBN;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int32_t* table =
-      block_table + static_cast<int64_t>(virt ? 0 : i) * a.max_blocks + a.table_col0;
+      block_table + static_cast<int64_t>(virt ? 0 : i) * a.max_blocks + table_col0;
 
   const uint32_t bars = sbase + C::kOffBar;
   auto BAR = [&](int k) { return bars + 8u * static_cast<uint32_t>(k); };
@@ -415,8 +421,8 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
     tc::tc_fence_after();
     // Partial mode: the row's normalised output and LSE go, in fp32, to slot
     // ws_slot0 + split of its workspace row [ws_slots][D + 1].
-    float* wrow = a.ws == nullptr ? nullptr
-                                  : a.ws + ((qoff / D) * a.ws_slots + a.ws_slot0 + split) * (D + 1);
+    float* wrow = ws == nullptr ? nullptr
+                                : ws + ((qoff / D) * a.ws_slots + a.ws_slot0 + split) * (D + 1);
     if (ok && wrow != nullptr) {   // warp-uniform
       const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
@@ -672,12 +678,12 @@ bool make_kv_map(CUtensorMap* map, const void* cache, int nb, int bs, int Hkv, i
 
 }  // namespace
 
-template <int D, int CL>
+template <int D, int CL, bool EXT>
 static cudaError_t launch_varlen_tc_t(const VarlenLaunch& L, cudaStream_t stream) {
   using C = TcCfg<D>;
   CUtensorMap map;
   if (!make_kv_map(&map, L.cache, L.num_blocks, L.bs, L.Hkv, D)) return cudaErrorInvalidValue;
-  auto kern = varlen_tc_kernel<D, CL>;
+  auto kern = varlen_tc_kernel<D, CL, EXT>;
   static DeviceFlags attr_set;
   cudaError_t e = set_smem_once(kern, C::kSmemBytes, attr_set);
   if (e != cudaSuccess) return e;
@@ -743,8 +749,13 @@ static cudaError_t launch_varlen_tc_t(const VarlenLaunch& L, cudaStream_t stream
 constexpr int kVarlenCluster = 1;
 
 cudaError_t launch_varlen_tc(const VarlenLaunch& L, cudaStream_t stream) {
-  if (L.d == 128) return launch_varlen_tc_t<128, kVarlenCluster>(L, stream);
-  return launch_varlen_tc_t<64, kVarlenCluster>(L, stream);
+  const bool ext = L.window > 0 || L.kv_splits > 1 || L.ws != nullptr || L.virt_total_q > 0 ||
+                   L.table_col0 != 0 || L.seq_off != 0;
+  if (L.d == 128)
+    return ext ? launch_varlen_tc_t<128, kVarlenCluster, true>(L, stream)
+               : launch_varlen_tc_t<128, kVarlenCluster, false>(L, stream);
+  return ext ? launch_varlen_tc_t<64, kVarlenCluster, true>(L, stream)
+             : launch_varlen_tc_t<64, kVarlenCluster, false>(L, stream);
 }
 
 }  // namespace pa

@@ -103,11 +103,11 @@ def test_window_chunked_prefill_full_size_sampled(pa):
 # Cascade attention
 # ---------------------------------------------------------------------------
 
-def _cascade(pa, d, P, S1, causal=True):
+def _cascade(pa, d, P, S1, S2=1, causal=True):
     b = d.b
-    ws = pa.cascade_workspace(b.num_tokens, b.num_q_heads, S1, b.head_size)
+    ws = pa.cascade_workspace(b.num_tokens, b.num_q_heads, S1, S2, b.head_size)
     out, lse = pa.pa_cascade_fwd(d.q, d.pool, d.table, d.qsl, d.seq, int(b.query_lens.max()), P,
-                                 b.scale, ws, causal=causal)
+                                 b.scale, ws, S1, causal=causal)
     o, l = _np(out, lse)
     return o, l, ws.cpu().numpy()
 
@@ -129,10 +129,10 @@ def test_cascade_equals_plain_attention(pa, name):
     pool = d.ref_pool()
     ref_o, ref_l = oracle.paged_attention(b.q, pool, b.block_table, b.query_start_loc,
                                           b.seq_lens, b.scale)
-    for S1 in (1, 3):
-        out, lse, ws = _cascade(pa, d, P, S1)
-        assert_out_close(out, ref_o, f"{name} cascade S1={S1}")
-        assert_lse_close(lse, ref_l, f"{name} cascade S1={S1} lse")
+    for S1, S2 in ((1, 1), (3, 1), (2, 5)):
+        out, lse, ws = _cascade(pa, d, P, S1, S2)
+        assert_out_close(out, ref_o, f"{name} cascade S1={S1} S2={S2}")
+        assert_lse_close(lse, ref_l, f"{name} cascade S1={S1} S2={S2} lse")
     assert pa.pa_get_device_error() == 0
 
 
@@ -183,7 +183,7 @@ def test_cascade_non_causal_and_no_prefix(pa):
     pool = d.ref_pool()
     ref_o, ref_l = oracle.paged_attention(b.q, pool, b.block_table, b.query_start_loc,
                                           b.seq_lens, b.scale, causal=False)
-    out, lse, _ = _cascade(pa, d, P, 2, causal=False)
+    out, lse, _ = _cascade(pa, d, P, 2, 2, causal=False)
     assert_out_close(out, ref_o, "non-causal cascade")
     assert_lse_close(lse, ref_l, "non-causal cascade lse")
     # No shared prefix: the plain path.
@@ -197,11 +197,13 @@ def test_cascade_non_causal_and_no_prefix(pa):
 def test_cascade_query_inside_prefix_is_flagged(pa):
     # A request whose new tokens start inside the shared blocks breaks the
     # precondition: the call flags it (and its rows are not checked).
-    b = workloads.make_shared_prefix_batch("inside", 45, 4, [10, 40], [1, 1], 8, 2, 128, 16)
+    b = workloads.make_shared_prefix_batch("inside", 45, 4, [10, 40], [2, 2], 8, 2, 128, 16)
     d = Dev(pa, b)
     assert pa.pa_get_device_error() == 0
-    ws = pa.cascade_workspace(2, 8, 1, 128)
-    pa.pa_cascade_fwd(d.q, d.pool, d.table, d.qsl, d.seq, 1, 5, b.scale, ws)   # 5 > 4 shared
+    # Two queries per request, so the varlen suffix pass (which checks) runs.
+    ws = pa.cascade_workspace(b.num_tokens, 8, 1, 1, 128)
+    pa.pa_cascade_fwd(d.q, d.pool, d.table, d.qsl, d.seq, int(b.query_lens.max()), 5, b.scale,
+                      ws, 1)   # 5 > 4 shared blocks
     torch.cuda.synchronize()
     assert pa.pa_get_device_error() & pa.PA_DEVERR_LENGTH
 
@@ -211,7 +213,8 @@ def test_cascade_shared_prefix_decode_full_size_sampled(pa):
     d = Dev(pa, b, poison=False)
     P = 4096 // 16
     S1 = pa.pa_cascade_prefix_splits(b.num_tokens, b.num_q_heads, b.num_kv_heads, 4096)
-    out, lse, _ = _cascade(pa, d, P, S1)
+    S2 = pa.pa_num_kv_splits(int(b.seq_lens.max()) - 4096)
+    out, lse, _ = _cascade(pa, d, P, S1, S2)
     mask = np.zeros(b.num_tokens, np.uint8)
     mask[[0, 7, 31, 63]] = 1
     ref_o, ref_l = oracle.paged_attention(b.q, d.ref_pool(), b.block_table, b.query_start_loc,
