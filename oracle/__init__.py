@@ -48,6 +48,8 @@ def _bind(path):
     i32, i64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double
     lib.oracle_reshape_and_cache.argtypes = [P, P, P, P, i64, i32, i32, i32, i64]
     lib.oracle_reshape_and_cache.restype = i32
+    lib.oracle_mla_cache_write.argtypes = [P, P, P, P, i64, i32, i32, i32, i64]
+    lib.oracle_mla_cache_write.restype = i32
     for name in ("oracle_paged_attention_bf16", "oracle_paged_attention_f64"):
         fn = getattr(lib, name)
         fn.argtypes = [P, P, P, i32, P, P, i32, i32, i32, i32, i32, i64, f64,
@@ -149,6 +151,24 @@ def reshape_and_cache(key, value, pool, slot_mapping, block_size):
     nb = out.shape[0]
     rc = lib.oracle_reshape_and_cache(_ptr(key), _ptr(value), _ptr(out), _ptr(slots),
                                       T, Hkv, d, block_size, nb)
+    if rc != 0:
+        raise ValueError("slot outside the pool")
+    return out
+
+
+def mla_cache_write(kv_c, k_pe, pool, slot_mapping, block_size):
+    """Returns a copy of the MLA pool ([nb, bs, R + P] uint16) with each new
+    token's kv_c ([T, R]) and k_pe ([T, P]) written at ``slot_mapping`` [T]."""
+    lib = _load()
+    kv_c = _c(kv_c, np.uint16)
+    k_pe = _c(k_pe, np.uint16)
+    out = np.array(pool, dtype=np.uint16, copy=True, order="C")
+    slots = _c(slot_mapping, np.int64)
+    T, R = kv_c.shape
+    P = k_pe.shape[1]
+    assert out.shape[2] == R + P and k_pe.shape[0] == T
+    rc = lib.oracle_mla_cache_write(_ptr(kv_c), _ptr(k_pe), _ptr(out), _ptr(slots), T, R, P,
+                                    int(block_size), out.shape[0])
     if rc != 0:
         raise ValueError("slot outside the pool")
     return out

@@ -307,6 +307,27 @@ int oracle_reshape_and_cache(const uint16_t* key, const uint16_t* value,
   return 0;
 }
 
+// The MLA cache write: a new token's cache entry is its compressed latent
+// kv_c followed by its rotary key part k_pe, one kv_lora_rank + rope_dim
+// vector per token, no K/V halves ("Triton and MLA": the cache holds the
+// concatenation [kv_c (kv_lora_rank), k_pe (qk_rope_head_dim)]; its shape is
+// (num_blocks, block_size, head_size)).  slot < 0 skips the token.
+int oracle_mla_cache_write(const uint16_t* kv_c, const uint16_t* k_pe, uint16_t* pool,
+                           const int64_t* slot_mapping, int64_t num_tokens, int kv_lora_rank,
+                           int rope_dim, int block_size, int64_t num_blocks) {
+  const int64_t width = static_cast<int64_t>(kv_lora_rank) + rope_dim;
+  for (int64_t t = 0; t < num_tokens; ++t) {
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    const int64_t blk = slot / block_size, off = slot % block_size;
+    if (blk >= num_blocks) return -1;
+    uint16_t* dst = pool + (blk * block_size + off) * width;
+    std::memcpy(dst, kv_c + t * kv_lora_rank, sizeof(uint16_t) * kv_lora_rank);
+    std::memcpy(dst + kv_lora_rank, k_pe + t * rope_dim, sizeof(uint16_t) * rope_dim);
+  }
+  return 0;
+}
+
 // Step 2 of the contract (varlen paged attention), bf16 inputs.
 // q [T][Hq][d], pool [nb][2][bs][Hkv][d], out [T][Hq][d] fp64,
 // lse [T][Hq] fp64 natural log.  row_mask (nullable, [T]) selects rows.

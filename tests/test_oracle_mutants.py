@@ -35,6 +35,10 @@ MUTANTS = [
     ("fp8_scales_swapped",
      "const double sc = kv == 0 ? static_cast<double>(k_scale) : static_cast<double>(v_scale);",
      "const double sc = kv == 0 ? static_cast<double>(v_scale) : static_cast<double>(k_scale);"),
+    ("mla_write_rope_first", "std::memcpy(dst + kv_lora_rank, k_pe + t * rope_dim",
+     "std::memcpy(dst + 0, k_pe + t * rope_dim"),
+    ("mla_write_row_stride", "uint16_t* dst = pool + (blk * block_size + off) * width;",
+     "uint16_t* dst = pool + (blk * block_size + off) * kv_lora_rank;"),
     ("window_one_short", "(window > 0 && visible > window) ? visible - window : 0",
      "(window > 0 && visible > window) ? visible - window + 1 : 0"),
     ("window_one_long", "(window > 0 && visible > window) ? visible - window : 0",

@@ -603,3 +603,40 @@ def test_window_is_causal_only(oracle_lib):
     with pytest.raises(ValueError):
         oracle_lib.paged_attention(b.q, b.pool, b.block_table, b.query_start_loc, b.seq_lens,
                                    b.scale, causal=False, window=4)
+
+
+# ---------------------------------------------------------------- MLA cache write
+
+def test_mla_cache_write_matches_numpy_scatter(oracle_lib):
+    m = workloads.make_mla_batch("mla_w", 71, [1, 64, 65, 130], 4, block_size=64)
+    kv_c, k_pe, slots = workloads.mla_new_tokens(m)
+    out = oracle_lib.mla_cache_write(kv_c, k_pe, m.pool, slots, m.block_size)
+    ref = m.pool.copy()
+    ref[slots // 64, slots % 64, :512] = kv_c
+    ref[slots // 64, slots % 64, 512:] = k_pe
+    assert np.array_equal(out, ref)
+    skip = slots.copy()
+    skip[2] = -1
+    out2 = oracle_lib.mla_cache_write(kv_c, k_pe, m.pool, skip, m.block_size)
+    assert np.array_equal(out2[slots[2] // 64, slots[2] % 64], m.pool[slots[2] // 64,
+                                                                      slots[2] % 64])
+    bad = slots.copy()
+    bad[0] = m.num_blocks * 64
+    with pytest.raises(ValueError):
+        oracle_lib.mla_cache_write(kv_c, k_pe, m.pool, bad, m.block_size)
+
+
+def test_mla_cache_write_then_decode_of_one_token(oracle_lib):
+    # A request of length 1 whose only token is the one just written: the MLA
+    # output is that token's kv_c exactly (the value is the first 512 entries
+    # of the row) and the LSE is scale * q . [kv_c | k_pe].
+    m = workloads.make_mla_batch("mla_w1", 72, [1, 1, 40], 2, block_size=64)
+    kv_c, k_pe, slots = workloads.mla_new_tokens(m)
+    pool = oracle_lib.mla_cache_write(kv_c, k_pe, m.pool, slots, m.block_size)
+    o, l = oracle_lib.mla_decode(m.q, pool, m.block_table, m.seq_lens, m.scale)
+    row = np.concatenate([_f64(kv_c), _f64(k_pe)], axis=1)
+    q = _f64(m.q)
+    for i in (0, 1):
+        for h in range(2):
+            assert np.array_equal(o[i, h], row[i, :512])
+            assert abs(l[i, h] - m.scale * math.fsum(q[i, h] * row[i])) < 1e-12

@@ -204,6 +204,25 @@ def make_mla_batch(name, seed, seq_lens, num_heads, kv_lora_rank=512, rope_dim=6
                     seq_lens, table, q, pool, float(scale))
 
 
+def mla_new_tokens(m: "MLABatch", seed_offset: int = 2):
+    """The decode step's new latent entries of an MLA batch: for each request
+    the token at position seq_len - 1, with kv_c [B, kv_lora_rank] and k_pe
+    [B, rope_dim] drawn as N(0, 1) bf16 bits from default_rng([seed, 2]) and
+    slot = block_table[i][pos // bs] * bs + pos % bs (requests of length 0
+    get slot -1)."""
+    rng = np.random.default_rng([m.seed, seed_offset])
+    B = m.batch
+    kv_c = randn_bf16(rng, (B, m.kv_lora_rank))
+    k_pe = randn_bf16(rng, (B, m.rope_dim))
+    slots = np.full(B, -1, np.int64)
+    for i in range(B):
+        n = int(m.seq_lens[i])
+        if n > 0:
+            pos = n - 1
+            slots[i] = int(m.block_table[i, pos // m.block_size]) * m.block_size + pos % m.block_size
+    return kv_c, k_pe, slots
+
+
 def make_shared_prefix_batch(name, seed, prefix_blocks, suffix_lens, query_lens, num_q_heads,
                              num_kv_heads, head_size, block_size, scale=None,
                              with_pool=True) -> PagedBatch:
