@@ -372,12 +372,19 @@ def bench_mla(pa, device, pk, flush, reps=10):
     ms = _timed_with_flush(lambda: pa.pa_mla_decode(q, pool, table, seq, m.scale, ws, o, lo,
                                                     max_seq_len=mx),
                            flush, reps)
+    # The step's cache write of the 128 new latent rows, timed alone.
+    kv_c, k_pe, slots = workloads.mla_new_tokens(m)
+    d_kv_c, d_k_pe = to_dev_bf16(kv_c, device), to_dev_bf16(k_pe, device)
+    d_slots = to_dev(slots, torch.int64, device)
+    write_ms = _timed_with_flush(lambda: pa.pa_mla_cache_write(d_kv_c, d_k_pe, pool, d_slots),
+                                 flush, reps)
     gbs = m.kv_bytes() / (ms * 1e-3) / 1e9
     flops = int(m.seq_lens.astype(np.int64).sum()) * m.num_heads * 2 * (
         m.kv_lora_rank + m.rope_dim + m.kv_lora_rank)
     res = {"workload": m.name, "num_splits": S, "ms": ms, "kv_bytes": m.kv_bytes(),
                          "gbs": gbs, "frac_of_hbm_peak": gbs / pk["hbm_gbs"],
-                         "tflops": flops / (ms * 1e-3) / 1e12}
+                         "tflops": flops / (ms * 1e-3) / 1e12,
+                         "cache_write_us": write_ms * 1e3, "cache_write_tokens": int(m.batch)}
     del pool, q, ws
     torch.cuda.empty_cache()
     return res

@@ -288,6 +288,23 @@ pa_status pa_decode_splitkv_fp8(const void* q, const void* kv_cache, const int32
                                 float k_scale, float v_scale, int num_splits, int max_seq_len,
                                 float* workspace, void* stream);
 
+/*
+ * The MLA cache write, the step before pa_mla_decode ("Triton and MLA": the
+ * cache stores one vector per token, the compressed latent kv_c followed by
+ * the rotary key part k_pe; its shape is (num_blocks, block_size, head_size)).
+ *   For t < num_tokens with slot = slot_mapping[t] >= 0:
+ *     kv_cache[slot / bs, slot % bs, 0:kv_lora_rank] = kv_c[t, :]
+ *     kv_cache[slot / bs, slot % bs, kv_lora_rank:]  = k_pe[t, :]
+ *   A bit copy.  slot < 0 skips the token; a slot >= num_blocks * bs is not
+ *   written and sets PA_DEVERR_SLOT.
+ * kv_c: [num_tokens, kv_lora_rank] bf16; k_pe: [num_tokens, rope_dim] bf16;
+ * kv_cache: [num_blocks, block_size, kv_lora_rank + rope_dim] bf16, in-out.
+ * All 16-byte aligned.  Supported: kv_lora_rank and rope_dim multiples of 8.
+ */
+pa_status pa_mla_cache_write(const void* kv_c, const void* k_pe, void* kv_cache,
+                             const int64_t* slot_mapping, int num_tokens, int kv_lora_rank,
+                             int rope_dim, int block_size, int num_blocks, void* stream);
+
 /* Size of the fixed device array pa_decode_noalloc keeps its split partials in. */
 #define PA_NOALLOC_WORKSPACE_BYTES (16u * 1024u * 1024u)
 

@@ -69,6 +69,7 @@ def lib() -> ctypes.CDLL:
         L.pa_cascade_prefix_splits.argtypes = [i32, i32, i32, i32, i32]
         L.pa_cascade_prefix_splits.restype = i32
         L.pa_reshape_and_cache_fp8.argtypes = [P, P, P, P, i32, SP, f32, f32, P]
+        L.pa_mla_cache_write.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, P]
         L.pa_decode_splitkv_fp8.argtypes = [P, P, P, P, SP, f32, f32, f32, i32, i32, P, P]
         L.pa_mla_decode.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, f32,
                                     i32, P, P, P, P]
@@ -81,7 +82,7 @@ def lib() -> ctypes.CDLL:
         for name in ("pa_reshape_and_cache", "pa_varlen_fwd", "pa_decode_splitkv",
                      "pa_lse_merge", "pa_mla_decode", "pa_get_device_error", "pa_decode_noalloc",
                      "pa_reshape_and_cache_fp8", "pa_decode_splitkv_fp8", "pa_varlen_fwd_window",
-                     "pa_cascade_fwd"):
+                     "pa_cascade_fwd", "pa_mla_cache_write"):
             getattr(L, name).restype = st
         _lib = L
         return L
@@ -140,6 +141,24 @@ def pa_reshape_and_cache(key, value, kv_cache, slot_mapping, stream=None) -> Non
         _dev(key, "key", torch.bfloat16), _dev(value, "value", torch.bfloat16),
         _dev(kv_cache, "kv_cache", torch.bfloat16), _dev(slot_mapping, "slot_mapping", torch.int64),
         T, ctypes.byref(shape), _stream(stream)), "pa_reshape_and_cache")
+
+
+def pa_mla_cache_write(kv_c, k_pe, kv_cache, slot_mapping, stream=None) -> None:
+    """Writes [kv_c | k_pe] ([T, R], [T, P] bf16) into the MLA pool
+    [nb, bs, R + P] at slot_mapping [T] int64."""
+    if kv_cache.dim() != 3:
+        raise ValueError("kv_cache must be [num_blocks, block_size, kv_lora_rank + rope_dim]")
+    nb, bs, w = kv_cache.shape
+    T, R = kv_c.shape
+    if k_pe.dim() != 2 or k_pe.shape[0] != T or R + k_pe.shape[1] != w:
+        raise ValueError("kv_c [T, R] and k_pe [T, P] must fill a cache row of R + P")
+    if slot_mapping.shape != (T,):
+        raise ValueError("slot_mapping must be [num_tokens]")
+    _check(lib().pa_mla_cache_write(
+        _dev(kv_c, "kv_c", torch.bfloat16), _dev(k_pe, "k_pe", torch.bfloat16),
+        _dev(kv_cache, "kv_cache", torch.bfloat16),
+        _dev(slot_mapping, "slot_mapping", torch.int64), T, R, int(k_pe.shape[1]), bs, nb,
+        _stream(stream)), "pa_mla_cache_write")
 
 
 def pa_varlen_fwd(q, kv_cache, block_table, query_start_loc, seq_lens, max_query_len, scale,

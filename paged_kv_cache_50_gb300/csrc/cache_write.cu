@@ -123,4 +123,41 @@ cudaError_t launch_reshape_and_cache_fp8(const void* key, const void* value, voi
   return cudaGetLastError();
 }
 
+// The MLA cache write ("Triton and MLA": the cache holds one vector per token,
+// [kv_c (kv_lora_rank) | k_pe (rope_dim)], in a [num_blocks, block_size,
+// kv_lora_rank + rope_dim] pool).  One warp per token copies the two parts in
+// 16-byte vectors into the row at slot_mapping.
+__global__ void __launch_bounds__(128)
+mla_cache_write_kernel(const uint4* __restrict__ kv_c, const uint4* __restrict__ k_pe,
+                       uint4* __restrict__ cache, const int64_t* __restrict__ slot_mapping,
+                       int num_tokens, int c_vec, int pe_vec, int64_t num_slots, int* err) {
+  pdl_trigger();
+  const int t = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (t >= num_tokens) return;
+  const int64_t slot = slot_mapping[t];
+  if (slot < 0) return;
+  if (slot >= num_slots) {
+    if (lane == 0) record_error(err, PA_DEVERR_SLOT);
+    return;
+  }
+  const int row_vec = c_vec + pe_vec;
+  uint4* dst = cache + slot * row_vec;   // slot = block * block_size + offset
+  const uint4* src_c = kv_c + static_cast<int64_t>(t) * c_vec;
+  const uint4* src_pe = k_pe + static_cast<int64_t>(t) * pe_vec;
+  for (int c = lane; c < row_vec; c += 32)
+    dst[c] = c < c_vec ? __ldcs(src_c + c) : __ldcs(src_pe + (c - c_vec));
+}
+
+cudaError_t launch_mla_cache_write(const void* kv_c, const void* k_pe, void* cache,
+                                   const int64_t* slot_mapping, int num_tokens, int kv_lora_rank,
+                                   int rope_dim, int block_size, int num_blocks, int* err,
+                                   cudaStream_t stream) {
+  const int blocks = (num_tokens + 3) / 4;
+  mla_cache_write_kernel<<<blocks, 128, 0, stream>>>(
+      static_cast<const uint4*>(kv_c), static_cast<const uint4*>(k_pe),
+      static_cast<uint4*>(cache), slot_mapping, num_tokens, kv_lora_rank / 8, rope_dim / 8,
+      static_cast<int64_t>(num_blocks) * block_size, err);
+  return cudaGetLastError();
+}
+
 }  // namespace pa

@@ -114,6 +114,26 @@ pa_status pa_reshape_and_cache(const void* key, const void* value, void* kv_cach
                                                 static_cast<cudaStream_t>(stream)));
 }
 
+pa_status pa_mla_cache_write(const void* kv_c, const void* k_pe, void* kv_cache,
+                             const int64_t* slot_mapping, int num_tokens, int kv_lora_rank,
+                             int rope_dim, int block_size, int num_blocks, void* stream) {
+  if (num_tokens < 0 || kv_lora_rank <= 0 || rope_dim < 0 || block_size <= 0 ||
+      block_size % 16 != 0 || num_blocks <= 0)
+    return PA_ERR_INVALID;
+  if (kv_lora_rank % 8 != 0 || rope_dim % 8 != 0) return PA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PA_OK;
+  if (kv_c == nullptr || (k_pe == nullptr && rope_dim > 0) || kv_cache == nullptr ||
+      slot_mapping == nullptr)
+    return PA_ERR_INVALID;
+  if (!aligned(kv_c, 16) || !aligned(k_pe, 16) || !aligned(kv_cache, 16) ||
+      !aligned(slot_mapping, 8))
+    return PA_ERR_INVALID;
+  return from_cuda(pa::launch_mla_cache_write(kv_c, k_pe, kv_cache, slot_mapping, num_tokens,
+                                              kv_lora_rank, rope_dim, block_size, num_blocks,
+                                              device_error_ptr(),
+                                              static_cast<cudaStream_t>(stream)));
+}
+
 pa_status pa_varlen_fwd(const void* q, const void* kv_cache, const int32_t* block_table,
                         const int32_t* query_start_loc, const int32_t* seq_lens, int total_q,
                         int max_query_len, const pa_shape* shape, float scale, int causal,

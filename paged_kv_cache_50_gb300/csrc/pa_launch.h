@@ -32,6 +32,12 @@ cudaError_t launch_decode_splitkv(const void* q, const void* cache, const int32_
                                   float* ws, int* err, cudaStream_t stream,
                                   const DecodeExt* ext = nullptr);
 
+// MLA cache write: [kv_c | k_pe] rows of a [nb, bs, kv_lora_rank + rope_dim] pool.
+cudaError_t launch_mla_cache_write(const void* kv_c, const void* k_pe, void* cache,
+                                   const int64_t* slot_mapping, int num_tokens, int kv_lora_rank,
+                                   int rope_dim, int block_size, int num_blocks, int* err,
+                                   cudaStream_t stream);
+
 // fp8 (e4m3) pool: quantising cache write and split-KV stage 1.
 cudaError_t launch_reshape_and_cache_fp8(const void* key, const void* value, void* cache,
                                          const int64_t* slot_mapping, int num_tokens,

@@ -201,3 +201,36 @@ def test_fp8_entry_points_reject_before_launch(pa):
                                       NULL) == pa.PA_OK
     assert L.pa_decode_splitkv_fp8(NULL, NULL, NULL, NULL, ctypes.byref(_shape(pa, num_seqs=0)),
                                    0.1, 1.0, 1.0, 4, 64, NULL, NULL) == pa.PA_OK
+
+
+def test_mla_cache_write_rejects(pa):
+    L = pa.lib()
+    assert L.pa_mla_cache_write(16, 16, 16, 16, 4, 512, 64, 24, 8, NULL) == pa.PA_ERR_INVALID
+    assert L.pa_mla_cache_write(16, 16, 16, 16, 4, 500, 64, 64, 8, NULL) == pa.PA_ERR_UNSUPPORTED
+    assert L.pa_mla_cache_write(16, 16, 24, 16, 4, 512, 64, 64, 8, NULL) == pa.PA_ERR_INVALID
+    assert L.pa_mla_cache_write(NULL, 16, 16, 16, 4, 512, 64, 64, 8, NULL) == pa.PA_ERR_INVALID
+    assert L.pa_mla_cache_write(NULL, NULL, NULL, NULL, 0, 512, 64, 64, 8, NULL) == pa.PA_OK
+
+
+def test_window_and_cascade_reject(pa):
+    L = pa.lib()
+    s = _shape(pa)
+    assert L.pa_varlen_fwd_window(16, 16, 16, 16, 16, 4, 2, ctypes.byref(s), 0.1, 0, 16, NULL,
+                                  NULL) == pa.PA_ERR_INVALID          # window < 1
+    assert L.pa_varlen_fwd_window(16, 16, 16, 16, 16, 4, 2, ctypes.byref(_shape(pa, head_size=96)),
+                                  0.1, 8, 16, NULL, NULL) == pa.PA_ERR_UNSUPPORTED
+    args = [16, 16, 16, 16, 16, 4, 2, 64]
+    # num_common_prefix_blocks past the table, zero splits, too many splits.
+    assert L.pa_cascade_fwd(*args, 5, 1, 1, ctypes.byref(s), 0.1, 1, 16, 16, NULL,
+                            NULL) == pa.PA_ERR_INVALID
+    assert L.pa_cascade_fwd(*args, 2, 0, 1, ctypes.byref(s), 0.1, 1, 16, 16, NULL,
+                            NULL) == pa.PA_ERR_INVALID
+    assert L.pa_cascade_fwd(*args, 2, 1, 0, ctypes.byref(s), 0.1, 1, 16, 16, NULL,
+                            NULL) == pa.PA_ERR_INVALID
+    assert L.pa_cascade_fwd(*args, 2, 10000, 10000, ctypes.byref(s), 0.1, 1, 16, 16, NULL,
+                            NULL) == pa.PA_ERR_INVALID
+    assert L.pa_cascade_fwd(*args, 2, 1, 1, ctypes.byref(s), 0.1, 1, NULL, 16, NULL,
+                            NULL) == pa.PA_ERR_INVALID          # no workspace
+    assert pa.pa_cascade_prefix_splits(64, 32, 8, 4096, 152) == 19
+    assert pa.pa_cascade_prefix_splits(64, 32, 8, 128, 152) == 1   # one tile of prefix
+    assert pa.pa_cascade_prefix_splits(0, 32, 8, 4096, 152) == 1

@@ -358,3 +358,46 @@ def test_mla_workload_full_size_sampled(pa):
         assert_out_close(out[rows], ref_o[rows], f"mla out S={S}")
         assert_lse_close(lse[rows], ref_l[rows], f"mla lse S={S}")
         assert np.isfinite(out).all() and np.isfinite(lse).all()
+
+
+# ---------------------------------------------------------------------------
+# MLA cache write
+# ---------------------------------------------------------------------------
+
+def test_mla_cache_write_then_decode(pa):
+    """The step's new latent rows land bit-exactly (whole pool compared), and
+    the MLA decode over the written pool matches the oracle's."""
+    b = workloads.make_mla_batch("mla_write", 53, [1, 63, 64, 65, 700, 0], 128,
+                                 scale=1.0 / math.sqrt(192.0))
+    kv_c, k_pe, slots = workloads.mla_new_tokens(b)
+    pool = _poison_mla(b)
+    d_pool = to_dev_bf16(pool)
+    pa.pa_mla_cache_write(to_dev_bf16(kv_c), to_dev_bf16(k_pe), d_pool,
+                          to_dev(slots, torch.int64))
+    ref_pool = oracle.mla_cache_write(kv_c, k_pe, pool, slots, b.block_size)
+    assert np.array_equal(bf16_bits(d_pool), ref_pool)
+    assert pa.pa_get_device_error() == 0
+    ref_o, ref_l = oracle.mla_decode(b.q, ref_pool, b.block_table, b.seq_lens, b.scale)
+    ws = pa.decode_workspace(b.batch, b.num_heads, 2, b.kv_lora_rank)
+    out, lse = pa.pa_mla_decode(to_dev_bf16(b.q), d_pool, to_dev(b.block_table, torch.int32),
+                                to_dev(b.seq_lens, torch.int32), b.scale, ws)
+    torch.cuda.synchronize()
+    assert_out_close(bf16_to_f64(out), ref_o, "mla after write")
+    assert_lse_close(lse.cpu().numpy().astype(np.float64), ref_l, "mla lse after write")
+
+
+def test_mla_cache_write_skip_out_of_range_and_full_workload(pa):
+    b = workloads.mla_decode()
+    kv_c, k_pe, slots = workloads.mla_new_tokens(b)
+    slots = slots.copy()
+    slots[5] = -1
+    slots[9] = b.num_blocks * b.block_size + 7      # outside the pool: flagged, not written
+    d_pool = to_dev_bf16(b.pool)
+    pa.pa_mla_cache_write(to_dev_bf16(kv_c), to_dev_bf16(k_pe), d_pool,
+                          to_dev(slots, torch.int64))
+    assert pa.pa_get_device_error() == pa.PA_DEVERR_SLOT
+    keep = slots.copy()
+    keep[9] = -1
+    ref_pool = oracle.mla_cache_write(kv_c, k_pe, b.pool, keep, b.block_size)
+    assert np.array_equal(bf16_bits(d_pool), ref_pool)
+    assert pa.pa_get_device_error() == 0
