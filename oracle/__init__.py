@@ -49,6 +49,11 @@ def _bind(path):
     lib.oracle_reshape_and_cache.argtypes = [P, P, P, P, i64, i32, i32, i32, i64]
     lib.oracle_reshape_and_cache.restype = i32
     lib.oracle_mla_cache_write.argtypes = [P, P, P, P, i64, i32, i32, i32, i64]
+    lib.oracle_mla_prefill.argtypes = [P, P, P, P, i32, P, P, i32, i32, i32, i32, i32, i32,
+                                       i32, i64, f64, i32, i32, P, P, P, P, i32]
+    lib.oracle_mla_prefill.restype = i32
+    lib.oracle_round_bf16.argtypes = [P, P, i64]
+    lib.oracle_round_bf16.restype = None
     lib.oracle_mla_cache_write.restype = i32
     for name in ("oracle_paged_attention_bf16", "oracle_paged_attention_f64"):
         fn = getattr(lib, name)
@@ -171,6 +176,49 @@ def mla_cache_write(kv_c, k_pe, pool, slot_mapping, block_size):
                                     int(block_size), out.shape[0])
     if rc != 0:
         raise ValueError("slot outside the pool")
+    return out
+
+
+def mla_prefill(q, pool, w_kv_b, block_table, query_start_loc, seq_lens, scale, causal=True,
+                round_kv=True, head_mask=None, row_mask=None, threads=None):
+    """MLA prefill, multi-head formulation.  q [T, H, dn + dr], pool
+    [nb, bs, R + dr], w_kv_b [H, dn + dv, R] (bf16 bits).  Each head's key is
+    [w_kv_b[h, :dn] c | k_pe], its value w_kv_b[h, dn:] c (rounded to bf16
+    with ``round_kv``).  Returns (out [T, H, dv], lse [T, H]) in fp64; rows or
+    heads not selected by the masks are left at zero."""
+    lib = _load()
+    q = _c(q, np.uint16)
+    pool = _c(pool, np.uint16)
+    w = _c(w_kv_b, np.uint16)
+    bt = _c(block_table, np.int32)
+    qsl = _c(query_start_loc, np.int32)
+    sl = _c(seq_lens, np.int32)
+    T, H, dk = q.shape
+    nb, bs, width = pool.shape
+    Hw, wrow, R = w.shape
+    assert Hw == H
+    dr = width - R
+    dn = dk - dr
+    dv = wrow - dn
+    out = np.zeros((T, H, dv), np.float64)
+    lse = np.full((T, H), -np.inf, np.float64)
+    hm = None if head_mask is None else _c(head_mask, np.uint8)
+    rm = None if row_mask is None else _c(row_mask, np.uint8)
+    rc = lib.oracle_mla_prefill(_ptr(q), _ptr(pool), _ptr(w), _ptr(bt), bt.shape[1], _ptr(qsl),
+                                _ptr(sl), sl.shape[0], H, R, dr, dn, dv, bs, nb, float(scale),
+                                int(bool(causal)), int(bool(round_kv)), _ptr(hm), _ptr(rm),
+                                _ptr(out), _ptr(lse), threads or default_threads())
+    if rc != 0:
+        raise ValueError("invalid MLA prefill input")
+    return out, lse
+
+
+def round_bf16(x):
+    """Nearest bf16 values (ties to even) of float64 values, as float64."""
+    lib = _load()
+    xs = _c(x, np.float64)
+    out = np.empty(xs.shape, np.float64)
+    lib.oracle_round_bf16(_ptr(xs), _ptr(out), xs.size)
     return out
 
 

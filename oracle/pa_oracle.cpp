@@ -281,9 +281,103 @@ int mla_decode(const E* q, const E* pool, const int32_t* block_table,
   return bad ? -1 : 0;
 }
 
+// Nearest bf16 value of x (ties to even), in double: 8 significant bits.
+double round_bf16(double x) {
+  if (x == 0.0 || !std::isfinite(x)) return x;
+  int e = std::ilogb(x);
+  if (e < -126) e = -126;                        // bf16 subnormals: spacing 2^-133
+  const double ulp = std::ldexp(1.0, e - 7);
+  return std::nearbyint(x / ulp) * ulp;          // default rounding: to nearest even
+}
+
+// MLA prefill in the multi-head formulation ("Attention Backends", section
+// "Latent attention is a different cache, not just a different kernel":
+// prefill and decode use different formulations of the same mathematics;
+// "AttentionBackend: attention backend abstraction layer": the MLA impl's
+// entry points are forward_mqa for decode and forward_mha).  The cache holds [c | k_pe] per token (c: kv_lora_rank R,
+// k_pe: rope_dim); the model's kv_b_proj weight w [H][dn + dv][R] expands c
+// per head h into a key part k_nope = w[h][0:dn] c and a value
+// v = w[h][dn:dn+dv] c.  Head h's key is [k_nope | k_pe] (dn + rope_dim),
+// its value v; queries are [q_nope (dn) | q_pe (rope_dim)] per head.  With
+// round_kv the expanded k_nope and v are rounded to bf16 (the dtype of the
+// projection's output) before attention.  Causal alignment as in varlen.
+template <typename E>
+int mla_prefill(const E* q, const E* pool, const E* w, const int32_t* block_table,
+                int max_blocks, const int32_t* qsl, const int32_t* seq_lens, int N, int H,
+                int R, int dr, int dn, int dv, int bs, int64_t nb, double scale, int causal,
+                int round_kv, const uint8_t* head_mask, const uint8_t* row_mask, double* out,
+                double* lse, int threads) {
+  if (bs <= 0 || R <= 0 || dn <= 0 || dv <= 0 || dr < 0) return -1;
+  const int dk = dn + dr, wrow = dn + dv;
+  std::atomic<int> bad(0);
+  parallel_for(static_cast<int64_t>(N) * H, threads, [&](int64_t item) {
+    const int i = static_cast<int>(item / H), h = static_cast<int>(item % H);
+    if (head_mask && !head_mask[h]) return;
+    const int64_t q0 = qsl[i], q1 = qsl[i + 1], seq = seq_lens[i], qlen = q1 - q0;
+    if (qlen <= 0) return;
+    if (qlen > seq) {
+      bad = 1;
+      return;
+    }
+    bool any = row_mask == nullptr;
+    for (int64_t j = q0; j < q1 && !any; ++j) any = row_mask[j] != 0;
+    if (!any) return;
+    std::vector<double> C(static_cast<size_t>(R)), K(static_cast<size_t>(seq) * dk),
+        V(static_cast<size_t>(seq) * dv), qv(dk);
+    const int32_t* row = block_table + static_cast<int64_t>(i) * max_blocks;
+    const E* wh = w + static_cast<int64_t>(h) * wrow * R;
+    for (int64_t p = 0; p < seq; ++p) {
+      const int64_t blk = row[p / bs];
+      if (blk < 0 || blk >= nb) {
+        bad = 1;
+        return;
+      }
+      const E* c = pool + (blk * bs + p % bs) * (R + dr);
+      for (int r = 0; r < R; ++r) C[r] = widen(c[r]);
+      for (int e = 0; e < wrow; ++e) {
+        double acc = 0.0;
+        for (int r = 0; r < R; ++r) acc += widen(wh[static_cast<int64_t>(e) * R + r]) * C[r];
+        if (round_kv) acc = round_bf16(acc);
+        if (e < dn)
+          K[p * dk + e] = acc;
+        else
+          V[p * dv + (e - dn)] = acc;
+      }
+      for (int e = 0; e < dr; ++e) K[p * dk + dn + e] = widen(c[R + e]);
+    }
+    const int64_t ctx = seq - qlen;
+    for (int64_t j = q0; j < q1; ++j) {
+      if (row_mask && !row_mask[j]) continue;
+      const int64_t visible = causal ? ctx + (j - q0) + 1 : seq;
+      for (int e = 0; e < dk; ++e) qv[e] = widen(q[(j * H + h) * dk + e]);
+      attend(qv.data(), K.data(), V.data(), visible, dk, dv, scale, out + (j * H + h) * dv,
+             lse + j * H + h);
+    }
+  });
+  return bad ? -1 : 0;
+}
+
 }  // namespace
 
 extern "C" {
+
+// MLA prefill (multi-head formulation), bf16 inputs: q [T][H][dn + dr],
+// pool [nb][bs][R + dr], w [H][dn + dv][R]; out [T][H][dv], lse [T][H] fp64.
+// head_mask ([H]) and row_mask ([T]) are nullable selections.
+int oracle_mla_prefill(const uint16_t* q, const uint16_t* pool, const uint16_t* w,
+                       const int32_t* block_table, int max_blocks, const int32_t* qsl,
+                       const int32_t* seq_lens, int N, int H, int R, int dr, int dn, int dv,
+                       int bs, int64_t nb, double scale, int causal, int round_kv,
+                       const uint8_t* head_mask, const uint8_t* row_mask, double* out,
+                       double* lse, int threads) {
+  return mla_prefill(q, pool, w, block_table, max_blocks, qsl, seq_lens, N, H, R, dr, dn, dv, bs,
+                     nb, scale, causal, round_kv, head_mask, row_mask, out, lse, threads);
+}
+
+// Nearest bf16 values (ties to even) of n doubles, as doubles.
+void oracle_round_bf16(const double* src, double* dst, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) dst[i] = round_bf16(src[i]);
+}
 
 // Step 1 of the paged-kernel contract: for every token t with
 // slot = slot_mapping[t] >= 0, copy key[t] / value[t] ([Hkv][d] each) into

@@ -39,6 +39,11 @@ MUTANTS = [
      "std::memcpy(dst + 0, k_pe + t * rope_dim"),
     ("mla_write_row_stride", "uint16_t* dst = pool + (blk * block_size + off) * width;",
      "uint16_t* dst = pool + (blk * block_size + off) * kv_lora_rank;"),
+    ("mla_prefill_unrounded", "if (round_kv) acc = round_bf16(acc);", ""),
+    ("mla_prefill_rope_from_latent", "K[p * dk + dn + e] = widen(c[R + e]);",
+     "K[p * dk + dn + e] = widen(c[e]);"),
+    ("mla_prefill_weight_transposed", "widen(wh[static_cast<int64_t>(e) * R + r])",
+     "widen(wh[static_cast<int64_t>(r) * wrow + e])"),
     ("window_one_short", "(window > 0 && visible > window) ? visible - window : 0",
      "(window > 0 && visible > window) ? visible - window + 1 : 0"),
     ("window_one_long", "(window > 0 && visible > window) ? visible - window : 0",

@@ -640,3 +640,115 @@ def test_mla_cache_write_then_decode_of_one_token(oracle_lib):
         for h in range(2):
             assert np.array_equal(o[i, h], row[i, :512])
             assert abs(l[i, h] - m.scale * math.fsum(q[i, h] * row[i])) < 1e-12
+
+
+# ---------------------------------------------------------------- MLA prefill
+# Multi-head formulation: each head's key is [w_kv_b[h, :dn] c | k_pe], its
+# value w_kv_b[h, dn:] c, the expanded parts rounded to bf16 (the dtype of the
+# projection's output).
+
+def _mla_prefill_tiny(oracle_lib):
+    """A ragged prefill batch (causal rows inside and at the end of each
+    request) with its new latent rows already written."""
+    b = workloads.make_mla_prefill_batch("mla_pf", 81, [20, 9, 37], [5, 9, 1], 3,
+                                         kv_lora_rank=16, rope_dim=8, qk_nope_dim=8, v_dim=6,
+                                         block_size=16)
+    pool = oracle_lib.mla_cache_write(b.kv_c, b.k_pe, b.pool, b.slot_mapping, b.block_size)
+    return b, pool
+
+
+def _py_round_bf16(x):
+    """Nearest bf16 value of a float (8 significant bits, ties to even),
+    written independently of the oracle's."""
+    if x == 0.0:
+        return x
+    m, e = math.frexp(x)                 # x = m * 2^e, 0.5 <= |m| < 1
+    scaled = m * 256.0                   # 8 significant bits above the point
+    r = round(scaled)                    # Python rounds halves to even
+    return math.ldexp(r, e - 8)
+
+
+def test_round_bf16_matches_torch_on_float32_values(oracle_lib):
+    rng = np.random.default_rng(3)
+    x = (rng.standard_normal(20000) * np.exp(rng.uniform(-20, 20, 20000))).astype(np.float32)
+    ties = np.array([1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -(1.0 + 2.0 ** -8), 3.0 + 2.0 ** -7],
+                    np.float32)
+    x = np.concatenate([x, ties]).astype(np.float64)
+    mine = oracle_lib.round_bf16(x)
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(mine, ref)
+    assert all(_py_round_bf16(v) == r for v, r in zip(x[-4:], mine[-4:]))
+
+
+def test_mla_prefill_matches_bruteforce(oracle_lib):
+    b, pool = _mla_prefill_tiny(oracle_lib)
+    out, lse = oracle_lib.mla_prefill(b.q, pool, b.w_kv_b, b.block_table, b.query_start_loc,
+                                      b.seq_lens, b.scale)
+    P, q, W = _f64(pool), _f64(b.q), _f64(b.w_kv_b)
+    R, dn = b.kv_lora_rank, b.qk_nope_dim
+    for i in range(b.num_seqs):
+        n = int(b.seq_lens[i])
+        rows = [P[b.block_table[i][p // 16], p % 16] for p in range(n)]
+        q0, q1 = int(b.query_start_loc[i]), int(b.query_start_loc[i + 1])
+        for h in range(b.num_heads):
+            keys, vals = [], []
+            for r in rows:
+                c = list(r[:R])
+                kn = [_py_round_bf16(math.fsum(W[h, e, k] * c[k] for k in range(R)))
+                      for e in range(dn)]
+                v = [_py_round_bf16(math.fsum(W[h, dn + e, k] * c[k] for k in range(R)))
+                     for e in range(b.v_dim)]
+                keys.append(kn + list(r[R:]))
+                vals.append(v)
+            for j in range(q0, q1):
+                vis = n - (q1 - q0) + (j - q0) + 1
+                o, l = bruteforce.attend(list(q[j, h]), keys[:vis], vals[:vis], b.scale)
+                np.testing.assert_allclose(out[j, h], o, rtol=0, atol=1e-12)
+                assert abs(lse[j, h] - l) < 1e-12
+
+
+def test_mla_prefill_equals_absorbed_formulation(oracle_lib):
+    # "The same mathematics" in the decode formulation: q_abs = [W_UK^T q_nope
+    # | q_pe] against the latent rows themselves (one shared kv head, key =
+    # whole row, value = its first R entries), then o = W_UV o_latent.  Exact
+    # (unrounded) expansion on the prefill side.
+    b, pool = _mla_prefill_tiny(oracle_lib)
+    out, lse = oracle_lib.mla_prefill(b.q, pool, b.w_kv_b, b.block_table, b.query_start_loc,
+                                      b.seq_lens, b.scale, round_kv=False)
+    P, q, W = _f64(pool), _f64(b.q), _f64(b.w_kv_b)
+    R, dn, dr = b.kv_lora_rank, b.qk_nope_dim, b.rope_dim
+    q_abs = np.concatenate([np.einsum("her,the->thr", W[:, :dn], q[:, :, :dn]), q[:, :, dn:]],
+                           axis=2)                                   # [T, H, R + dr]
+    std = np.stack([P, P], axis=1)[:, :, :, None, :]                 # [nb, 2, bs, 1, R + dr]
+    o_lat, l_abs = oracle_lib.paged_attention(q_abs, std, b.block_table, b.query_start_loc,
+                                              b.seq_lens, b.scale)
+    o_abs = np.einsum("hvr,thr->thv", W[:, dn:], o_lat[:, :, :R])
+    np.testing.assert_allclose(out, o_abs, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, l_abs, rtol=0, atol=1e-12)
+
+
+def test_mla_prefill_matches_torch_sdpa(oracle_lib):
+    b, pool = _mla_prefill_tiny(oracle_lib)
+    out, lse = oracle_lib.mla_prefill(b.q, pool, b.w_kv_b, b.block_table, b.query_start_loc,
+                                      b.seq_lens, b.scale, round_kv=False)
+    P, q, W = _f64(pool), _f64(b.q), _f64(b.w_kv_b)
+    R, dn = b.kv_lora_rank, b.qk_nope_dim
+    for i in range(b.num_seqs):
+        n = int(b.seq_lens[i])
+        pos = np.arange(n)
+        rows = torch.from_numpy(P[b.block_table[i, pos // 16], pos % 16])        # [n, R + dr]
+        Wt = torch.from_numpy(W)
+        K = torch.cat([torch.einsum("her,nr->hne", Wt[:, :dn], rows[:, :R]),
+                       rows[None, :, R:].expand(b.num_heads, n, -1)], -1)     # [H, n, dk]
+        V = torch.einsum("hvr,nr->hnv", Wt[:, dn:], rows[:, :R])               # [H, n, dv]
+        q0, q1 = int(b.query_start_loc[i]), int(b.query_start_loc[i + 1])
+        qi = torch.from_numpy(q[q0:q1]).permute(1, 0, 2)                       # [H, L, dk]
+        L = q1 - q0
+        mask = torch.arange(n)[None, :] <= (n - L + torch.arange(L))[:, None]
+        ref = torch.nn.functional.scaled_dot_product_attention(qi, K, V, attn_mask=mask,
+                                                               scale=b.scale)
+        np.testing.assert_allclose(out[q0:q1], ref.permute(1, 0, 2).numpy(), rtol=0, atol=1e-12)
+        s = torch.einsum("hld,hnd->hln", qi, K) * b.scale
+        s = s.masked_fill(~mask, -math.inf)
+        np.testing.assert_allclose(lse[q0:q1], torch.logsumexp(s, -1).T.numpy(), rtol=0,
+                                   atol=1e-12)

@@ -223,6 +223,104 @@ def mla_new_tokens(m: "MLABatch", seed_offset: int = 2):
     return kv_c, k_pe, slots
 
 
+@dataclass
+class MLAPrefillBatch:
+    """One prefill step of the MLA workload in the multi-head formulation:
+    latent pool [nb, bs, R + dr], per-head queries [T, H, dn + dr], the
+    kv_b_proj weight [H, dn + dv, R], and the step's new latent rows."""
+    name: str
+    seed: int
+    num_heads: int
+    kv_lora_rank: int
+    rope_dim: int
+    qk_nope_dim: int
+    v_dim: int
+    block_size: int
+    num_blocks: int
+    seq_lens: np.ndarray          # int32 [N]
+    query_lens: np.ndarray        # int32 [N]
+    query_start_loc: np.ndarray   # int32 [N + 1]
+    block_table: np.ndarray       # int32 [N, max_blocks], -1 past the end
+    slot_mapping: np.ndarray      # int64 [T]
+    q: np.ndarray                 # uint16 [T, H, dn + dr]
+    kv_c: np.ndarray              # uint16 [T, R]  (new latent rows)
+    k_pe: np.ndarray              # uint16 [T, dr]
+    w_kv_b: np.ndarray            # uint16 [H, dn + dv, R]
+    pool: np.ndarray              # uint16 [nb, bs, R + dr] BEFORE the write
+    scale: float
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.seq_lens.shape[0])
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.query_start_loc[-1])
+
+    def causal_flops(self) -> int:
+        """2 * (dn + dr + dv) * H * sum_i(qlen_i * ctx_i + qlen_i (qlen_i + 1) / 2)."""
+        ql = self.query_lens.astype(np.int64)
+        ctx = self.seq_lens.astype(np.int64) - ql
+        pairs = int((ql * ctx + ql * (ql + 1) // 2).sum())
+        return 2 * (self.qk_nope_dim + self.rope_dim + self.v_dim) * self.num_heads * pairs
+
+    def expand_flops(self) -> int:
+        """2 * R * H * (dn + dv) per context token (the kv_b_proj expansion)."""
+        return (2 * self.kv_lora_rank * self.num_heads * (self.qk_nope_dim + self.v_dim) *
+                int(self.seq_lens.astype(np.int64).sum()))
+
+
+def make_mla_prefill_batch(name, seed, seq_lens, query_lens, num_heads, kv_lora_rank=512,
+                           rope_dim=64, qk_nope_dim=128, v_dim=128, block_size=64,
+                           with_pool=True, scale=None) -> MLAPrefillBatch:
+    """Latent pool and queries N(0, 1) bf16; kv_b_proj weight N(0, 1/R) bf16
+    (so the expanded keys and values are of unit scale); new tokens are the
+    last query_lens[i] positions of each request, their slots as in
+    make_paged_batch."""
+    rng = np.random.default_rng(seed)
+    seq_lens = np.asarray(seq_lens, np.int32)
+    query_lens = np.asarray(query_lens, np.int32)
+    assert np.all(query_lens <= seq_lens) and np.all(query_lens >= 0)
+    N = seq_lens.shape[0]
+    qsl = np.zeros(N + 1, np.int32)
+    qsl[1:] = np.cumsum(query_lens)
+    table, nb = _assign_blocks(rng, seq_lens, block_size)
+    T = int(qsl[-1])
+    slots = np.empty(T, np.int64)
+    for i in range(N):
+        ctx = int(seq_lens[i] - query_lens[i])
+        for j in range(int(query_lens[i])):
+            pos = ctx + j
+            slots[qsl[i] + j] = int(table[i, pos // block_size]) * block_size + pos % block_size
+    width = kv_lora_rank + rope_dim
+    pool = randn_bf16(rng, (nb, block_size, width)) if with_pool else None
+    rng = np.random.default_rng([seed, 1])
+    q = randn_bf16(rng, (T, num_heads, qk_nope_dim + rope_dim))
+    kv_c = randn_bf16(rng, (T, kv_lora_rank))
+    k_pe = randn_bf16(rng, (T, rope_dim))
+    wr = np.random.default_rng([seed, 3])
+    w = (wr.standard_normal((num_heads, qk_nope_dim + v_dim, kv_lora_rank), dtype=np.float32) /
+         np.float32(math.sqrt(kv_lora_rank)))
+    w_kv_b = f32_to_bf16_bits(w)
+    if scale is None:
+        scale = 1.0 / math.sqrt(qk_nope_dim + rope_dim)
+    return MLAPrefillBatch(name, seed, num_heads, kv_lora_rank, rope_dim, qk_nope_dim, v_dim,
+                           block_size, nb, seq_lens, query_lens, qsl, table, slots, q, kv_c,
+                           k_pe, w_kv_b, pool, float(scale))
+
+
+def mla_prefill(seed: int = 7, num_seqs: int = 8, qlo: int = 256, qhi: int = 2048,
+                clo: int = 0, chi: int = 4096, **kw) -> MLAPrefillBatch:
+    """DeepSeek-V3 MLA chunked prefill: 8 requests, new tokens U[256, 2048],
+    cached prefix U[0, 4096], 128 heads, latent 512 + rope 64, q/k nope 128,
+    v 128, block size 64, scale 1/sqrt(192)."""
+    rng = np.random.default_rng(seed + 1000)
+    ql = rng.integers(qlo, qhi, size=num_seqs, endpoint=True).astype(np.int32)
+    ctx = rng.integers(clo, chi, size=num_seqs, endpoint=True).astype(np.int32)
+    return make_mla_prefill_batch(f"mla_prefill_{num_seqs}req_128h", seed, ctx + ql, ql, 128,
+                                  **kw)
+
+
 def make_shared_prefix_batch(name, seed, prefix_blocks, suffix_lens, query_lens, num_q_heads,
                              num_kv_heads, head_size, block_size, scale=None,
                              with_pool=True) -> PagedBatch:
