@@ -390,6 +390,44 @@ def bench_mla(pa, device, pk, flush, reps=10):
     return res
 
 
+def bench_mla_prefill(pa, device, pk, flush, reps=10):
+    """MLA chunked prefill, multi-head formulation (DeepSeek-V3 shape): the
+    kv_b_proj expansion of every context token and the attention over the
+    expanded keys and values, timed together and apart."""
+    m = workloads.mla_prefill(with_pool=False)
+    pool = device_pool((m.num_blocks, m.block_size, m.kv_lora_rank + m.rope_dim), 7, device)
+    q = to_dev_bf16(m.q, device)
+    w = to_dev_bf16(m.w_kv_b, device)
+    table = to_dev(m.block_table, torch.int32, device)
+    qsl = to_dev(m.query_start_loc, torch.int32, device)
+    seq = to_dev(m.seq_lens, torch.int32, device)
+    S = int(m.seq_lens.max())
+    mq = int(m.query_lens.max())
+    ws = torch.empty(pa.pa_mla_prefill_workspace_bytes(m.num_seqs, S, m.num_heads),
+                     dtype=torch.uint8, device=device)
+    out = torch.empty((m.num_tokens, m.num_heads, 128), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((m.num_tokens, m.num_heads), dtype=torch.float32, device=device)
+    kv_elems = m.num_seqs * S * m.num_heads
+    k_ws = ws[:kv_elems * 192 * 2].view(torch.bfloat16).view(m.num_seqs, S, m.num_heads, 192)
+    v_ws = ws[kv_elems * 192 * 2:kv_elems * 320 * 2].view(torch.bfloat16).view(
+        m.num_seqs, S, m.num_heads, 128)
+    total = _timed_with_flush(lambda: pa.pa_mla_prefill(q, pool, w, table, qsl, seq, mq, m.scale,
+                                                        ws, S, out=out, lse=lse), flush, reps)
+    expand = _timed_with_flush(lambda: pa.pa_mla_expand_kv(pool, w, table, seq, k_ws, v_ws),
+                               flush, reps)
+    attn = total - expand
+    ef, af = m.expand_flops(), m.causal_flops()
+    res = {"workload": m.name, "ms": total, "expand_ms": expand, "attention_ms": attn,
+           "expand_tflops": ef / (expand * 1e-3) / 1e12,
+           "attention_tflops": af / (attn * 1e-3) / 1e12,
+           "tflops": (ef + af) / (total * 1e-3) / 1e12,
+           "frac_of_bf16_peak": (ef + af) / (total * 1e-3) / 1e12 / pk["bf16_tflops"],
+           "expanded_bytes": kv_elems * 320 * 2}
+    del pool, q, w, ws
+    torch.cuda.empty_cache()
+    return res
+
+
 def device_fp8_pool(shape, seed, device):
     """Uniformly random finite e4m3 codes (the NaN codes 0x7F / 0xFF excluded),
     drawn on the device."""
@@ -481,7 +519,8 @@ def bench_cascade(pa, device, pk, flush, reps=10):
 
 
 SECONDARY = {"chunked_prefill": bench_prefill, "long_decode": bench_long_decode,
-             "mla_decode": bench_mla, "fp8_decode": bench_fp8_decode, "cascade": bench_cascade}
+             "mla_decode": bench_mla, "fp8_decode": bench_fp8_decode, "cascade": bench_cascade,
+             "mla_prefill": bench_mla_prefill}
 
 
 def secondary(pa, device, pk):

@@ -305,6 +305,54 @@ pa_status pa_mla_cache_write(const void* kv_c, const void* k_pe, void* kv_cache,
                              const int64_t* slot_mapping, int num_tokens, int kv_lora_rank,
                              int rope_dim, int block_size, int num_blocks, void* stream);
 
+/*
+ * MLA prefill, multi-head formulation ("Attention Backends", section "Latent
+ * attention is a different cache, not just a different kernel": prefill and
+ * decode use different formulations of the same mathematics;
+ * "AttentionBackend: attention backend abstraction layer": forward_mha).
+ * Widths are DeepSeek-V3's: kv_lora_rank 512, rope_dim 64, qk_nope 128,
+ * v 128 (the cache row is 576 wide, the query 192, the output 128).
+ *
+ * pa_mla_expand_kv -- step 1: for every request i and context token
+ * t < seq_lens[i], with c = kv_cache[block_table[i][t / bs]][t % bs]:
+ *   k_ws[i][t][h][0:128]   = bf16(w_kv_b[h][0:128] . c[0:512])
+ *   k_ws[i][t][h][128:192] = c[512:576]                       (k_pe)
+ *   v_ws[i][t][h][0:128]   = bf16(w_kv_b[h][128:256] . c[0:512])
+ * fp32 accumulation, round to nearest even; entries for t >= seq_lens[i] are
+ * not written.  w_kv_b: the model's kv_b_proj weight [num_heads][256][512]
+ * bf16.  k_ws: [num_seqs][max_seq_len][num_heads][192] bf16, v_ws:
+ * [num_seqs][max_seq_len][num_heads][128] bf16 (together
+ * pa_mla_prefill_workspace_bytes bytes).  max_seq_len >= every seq_lens[i]
+ * (a shorter one is the caller's error: tokens past it are not expanded).
+ * A block id outside [0, num_blocks) sets PA_DEVERR_BLOCK_ID and its tokens
+ * expand as zero latents.  All pointers 16-byte aligned.
+ */
+size_t pa_mla_prefill_workspace_bytes(int num_seqs, int max_seq_len, int num_heads);
+pa_status pa_mla_expand_kv(const void* kv_cache, const void* w_kv_b, const int32_t* block_table,
+                           const int32_t* seq_lens, int num_seqs, int num_heads, int block_size,
+                           int num_blocks, int max_blocks_per_seq, int max_seq_len, void* k_ws,
+                           void* v_ws, void* stream);
+
+/*
+ * pa_mla_prefill -- the whole forward_mha step: pa_mla_expand_kv into the
+ * workspace (k_ws first, then v_ws, together pa_mla_prefill_workspace_bytes(
+ * num_seqs, max_seq_len, num_heads) bytes), then varlen attention with
+ * per-head keys [k_nope | k_pe] (192) and values v (128):
+ *   out[j, h, :] = softmax(scale * q[j, h, :] . K_h[p] for visible p) . V_h
+ *   lse[j, h]    = ln sum_p exp(scale * q[j, h, :] . K_h[p])
+ * with visibility as in pa_varlen_fwd (causal: bottom-right aligned).
+ * q: [total_q, num_heads, 192] bf16 ([q_nope | q_pe]); out: [total_q,
+ * num_heads, 128] bf16; lse: [total_q, num_heads] fp32, nullable.
+ * query_start_loc, seq_lens, max_query_len as for pa_varlen_fwd; the new
+ * tokens must already be in kv_cache (pa_mla_cache_write).
+ */
+pa_status pa_mla_prefill(const void* q, const void* kv_cache, const void* w_kv_b,
+                         const int32_t* block_table, const int32_t* query_start_loc,
+                         const int32_t* seq_lens, int total_q, int max_query_len, int num_seqs,
+                         int num_heads, int block_size, int num_blocks, int max_blocks_per_seq,
+                         int max_seq_len, float scale, int causal, void* workspace, void* out,
+                         float* lse, void* stream);
+
 /* Size of the fixed device array pa_decode_noalloc keeps its split partials in. */
 #define PA_NOALLOC_WORKSPACE_BYTES (16u * 1024u * 1024u)
 

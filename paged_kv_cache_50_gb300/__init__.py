@@ -70,6 +70,11 @@ def lib() -> ctypes.CDLL:
         L.pa_cascade_prefix_splits.restype = i32
         L.pa_reshape_and_cache_fp8.argtypes = [P, P, P, P, i32, SP, f32, f32, P]
         L.pa_mla_cache_write.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, P]
+        L.pa_mla_prefill_workspace_bytes.argtypes = [i32, i32, i32]
+        L.pa_mla_prefill_workspace_bytes.restype = ctypes.c_size_t
+        L.pa_mla_expand_kv.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, P, P, P]
+        L.pa_mla_prefill.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32,
+                                     f32, i32, P, P, P, P]
         L.pa_decode_splitkv_fp8.argtypes = [P, P, P, P, SP, f32, f32, f32, i32, i32, P, P]
         L.pa_mla_decode.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, f32,
                                     i32, P, P, P, P]
@@ -82,7 +87,8 @@ def lib() -> ctypes.CDLL:
         for name in ("pa_reshape_and_cache", "pa_varlen_fwd", "pa_decode_splitkv",
                      "pa_lse_merge", "pa_mla_decode", "pa_get_device_error", "pa_decode_noalloc",
                      "pa_reshape_and_cache_fp8", "pa_decode_splitkv_fp8", "pa_varlen_fwd_window",
-                     "pa_cascade_fwd", "pa_mla_cache_write"):
+                     "pa_cascade_fwd", "pa_mla_cache_write", "pa_mla_expand_kv",
+                     "pa_mla_prefill"):
             getattr(L, name).restype = st
         _lib = L
         return L
@@ -159,6 +165,68 @@ def pa_mla_cache_write(kv_c, k_pe, kv_cache, slot_mapping, stream=None) -> None:
         _dev(kv_cache, "kv_cache", torch.bfloat16),
         _dev(slot_mapping, "slot_mapping", torch.int64), T, R, int(k_pe.shape[1]), bs, nb,
         _stream(stream)), "pa_mla_cache_write")
+
+
+def mla_prefill_workspace(num_seqs, max_seq_len, num_heads, device="cuda"):
+    """(k_ws [N, S, H, 192], v_ws [N, S, H, 128]) bf16 for the MLA prefill."""
+    k = torch.empty((num_seqs, max_seq_len, num_heads, 192), dtype=torch.bfloat16, device=device)
+    v = torch.empty((num_seqs, max_seq_len, num_heads, 128), dtype=torch.bfloat16, device=device)
+    return k, v
+
+
+def pa_mla_expand_kv(kv_cache, w_kv_b, block_table, seq_lens, k_ws, v_ws, stream=None) -> None:
+    """MLA prefill step 1: per head [W_UK c | k_pe] and W_UV c of every context
+    token into k_ws [N, S, H, 192] / v_ws [N, S, H, 128] (S = max_seq_len)."""
+    nb, bs, w = kv_cache.shape
+    H = w_kv_b.shape[0]
+    N, S = k_ws.shape[0], k_ws.shape[1]
+    if tuple(w_kv_b.shape) != (H, 256, 512) or w != 576:
+        raise ValueError("w_kv_b must be [H, 256, 512] and kv_cache [nb, bs, 576]")
+    if tuple(k_ws.shape) != (N, S, H, 192) or tuple(v_ws.shape) != (N, S, H, 128):
+        raise ValueError("k_ws must be [N, S, H, 192] and v_ws [N, S, H, 128]")
+    _check(lib().pa_mla_expand_kv(
+        _dev(kv_cache, "kv_cache", torch.bfloat16), _dev(w_kv_b, "w_kv_b", torch.bfloat16),
+        _dev(block_table, "block_table", torch.int32), _dev(seq_lens, "seq_lens", torch.int32),
+        N, H, bs, nb, int(block_table.shape[1]), S, _dev(k_ws, "k_ws", torch.bfloat16),
+        _dev(v_ws, "v_ws", torch.bfloat16), _stream(stream)), "pa_mla_expand_kv")
+
+
+def pa_mla_prefill_workspace_bytes(num_seqs, max_seq_len, num_heads) -> int:
+    return int(lib().pa_mla_prefill_workspace_bytes(int(num_seqs), int(max_seq_len),
+                                                    int(num_heads)))
+
+
+def pa_mla_prefill(q, kv_cache, w_kv_b, block_table, query_start_loc, seq_lens, max_query_len,
+                   scale, workspace, max_seq_len=None, causal=True, out=None, lse=None,
+                   return_lse=True, stream=None):
+    """MLA prefill (forward_mha): q [T, H, 192] against each request's latent
+    context expanded through w_kv_b [H, 256, 512] -> (out [T, H, 128] bf16,
+    lse [T, H] fp32).  ``workspace``: a uint8 tensor of at least
+    pa_mla_prefill_workspace_bytes(N, max_seq_len, H) bytes."""
+    T, H, dk = q.shape
+    N = seq_lens.shape[0]
+    nb, bs, w = kv_cache.shape
+    if dk != 192 or w != 576 or tuple(w_kv_b.shape) != (H, 256, 512):
+        raise ValueError("q [T, H, 192], kv_cache [nb, bs, 576], w_kv_b [H, 256, 512] expected")
+    if query_start_loc.shape != (N + 1,) or block_table.dim() != 2 or block_table.shape[0] != N:
+        raise ValueError("query_start_loc [N + 1] and block_table [N, max_blocks] expected")
+    S = _max_seq(seq_lens, max_seq_len)
+    need = pa_mla_prefill_workspace_bytes(N, S, H)
+    if workspace.dtype != torch.uint8 or workspace.numel() < need:
+        raise ValueError(f"workspace must be a uint8 tensor of at least {need} bytes")
+    if out is None:
+        out = torch.empty((T, H, 128), dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
+    _check(lib().pa_mla_prefill(
+        _dev(q, "q", torch.bfloat16), _dev(kv_cache, "kv_cache", torch.bfloat16),
+        _dev(w_kv_b, "w_kv_b", torch.bfloat16), _dev(block_table, "block_table", torch.int32),
+        _dev(query_start_loc, "query_start_loc", torch.int32),
+        _dev(seq_lens, "seq_lens", torch.int32), T, int(max_query_len), N, H, bs, nb,
+        int(block_table.shape[1]), S, float(scale), int(bool(causal)),
+        _dev(workspace, "workspace", torch.uint8), _dev(out, "out", torch.bfloat16),
+        _opt(lse, "lse", torch.float32), _stream(stream)), "pa_mla_prefill")
+    return out, lse
 
 
 def pa_varlen_fwd(q, kv_cache, block_table, query_start_loc, seq_lens, max_query_len, scale,

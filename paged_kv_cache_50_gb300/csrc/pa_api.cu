@@ -134,6 +134,89 @@ pa_status pa_mla_cache_write(const void* kv_c, const void* k_pe, void* kv_cache,
                                               static_cast<cudaStream_t>(stream)));
 }
 
+size_t pa_mla_prefill_workspace_bytes(int num_seqs, int max_seq_len, int num_heads) {
+  if (num_seqs < 0 || max_seq_len < 0 || num_heads <= 0) return 0;
+  return static_cast<size_t>(num_seqs) * max_seq_len * num_heads * (192 + 128) * 2;
+}
+
+static bool mla_prefill_shape_ok(int num_seqs, int num_heads, int block_size, int num_blocks,
+                                 int max_blocks_per_seq, int max_seq_len) {
+  return num_seqs >= 0 && num_seqs <= kMaxGridYZ && num_heads > 0 && num_heads <= kMaxGridYZ &&
+         block_size > 0 && block_size % 16 == 0 && num_blocks > 0 && max_blocks_per_seq > 0 &&
+         max_seq_len >= 0;
+}
+
+pa_status pa_mla_expand_kv(const void* kv_cache, const void* w_kv_b, const int32_t* block_table,
+                           const int32_t* seq_lens, int num_seqs, int num_heads, int block_size,
+                           int num_blocks, int max_blocks_per_seq, int max_seq_len, void* k_ws,
+                           void* v_ws, void* stream) {
+  if (!mla_prefill_shape_ok(num_seqs, num_heads, block_size, num_blocks, max_blocks_per_seq,
+                            max_seq_len))
+    return PA_ERR_INVALID;
+  if (num_seqs == 0 || max_seq_len == 0) return PA_OK;
+  if (kv_cache == nullptr || w_kv_b == nullptr || block_table == nullptr ||
+      seq_lens == nullptr || k_ws == nullptr || v_ws == nullptr)
+    return PA_ERR_INVALID;
+  if (!aligned(kv_cache, 16) || !aligned(w_kv_b, 16) || !aligned(k_ws, 16) || !aligned(v_ws, 16))
+    return PA_ERR_INVALID;
+  return from_cuda(pa::launch_mla_expand(kv_cache, w_kv_b, block_table, seq_lens, num_seqs,
+                                         num_heads, block_size, num_blocks, max_blocks_per_seq,
+                                         max_seq_len, max_seq_len, k_ws, v_ws,
+                                         device_error_ptr(), static_cast<cudaStream_t>(stream)));
+}
+
+pa_status pa_mla_prefill(const void* q, const void* kv_cache, const void* w_kv_b,
+                         const int32_t* block_table, const int32_t* query_start_loc,
+                         const int32_t* seq_lens, int total_q, int max_query_len, int num_seqs,
+                         int num_heads, int block_size, int num_blocks, int max_blocks_per_seq,
+                         int max_seq_len, float scale, int causal, void* workspace, void* out,
+                         float* lse, void* stream) {
+  if (!mla_prefill_shape_ok(num_seqs, num_heads, block_size, num_blocks, max_blocks_per_seq,
+                            max_seq_len) ||
+      total_q < 0 || max_query_len < 0)
+    return PA_ERR_INVALID;
+  if (total_q == 0 || num_seqs == 0 || max_query_len == 0) return PA_OK;
+  if (q == nullptr || kv_cache == nullptr || w_kv_b == nullptr || block_table == nullptr ||
+      query_start_loc == nullptr || seq_lens == nullptr || workspace == nullptr || out == nullptr)
+    return PA_ERR_INVALID;
+  if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(w_kv_b, 16) ||
+      !aligned(workspace, 16) || !aligned(out, 16) || !aligned(lse, 4))
+    return PA_ERR_INVALID;
+  const long long rows = static_cast<long long>(num_seqs) * max_seq_len;
+  if (rows * num_heads > INT_MAX) return PA_ERR_INVALID;   // 3-D map row coordinate
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* k_ws = static_cast<uint8_t*>(workspace);
+  uint8_t* v_ws = k_ws + rows * num_heads * 192 * 2;
+  if (pa::launch_mla_expand(kv_cache, w_kv_b, block_table, seq_lens, num_seqs, num_heads,
+                            block_size, num_blocks, max_blocks_per_seq, max_seq_len, max_seq_len,
+                            k_ws, v_ws, device_error_ptr(), st) != cudaSuccess)
+    return PA_ERR_CUDA;
+  pa::VarlenLaunch L{};
+  L.q = q;
+  L.cache = kv_cache;
+  L.block_table = block_table;
+  L.qsl = query_start_loc;
+  L.seq_lens = seq_lens;
+  L.N = num_seqs;
+  L.Hq = num_heads;
+  L.Hkv = num_heads;
+  L.d = 192;
+  L.bs = block_size;
+  L.num_blocks = num_blocks;
+  L.max_blocks = max_blocks_per_seq;
+  L.max_query_len = max_query_len;
+  L.scale = scale;
+  L.causal = causal ? 1 : 0;
+  L.window = 0;
+  L.out = out;
+  L.lse = lse;
+  L.err = device_error_ptr();
+  L.mla_k = k_ws;
+  L.mla_v = v_ws;
+  L.mla_s_max = max_seq_len;
+  return from_cuda(pa::launch_varlen_tc(L, st));
+}
+
 pa_status pa_varlen_fwd(const void* q, const void* kv_cache, const int32_t* block_table,
                         const int32_t* query_start_loc, const int32_t* seq_lens, int total_q,
                         int max_query_len, const pa_shape* shape, float scale, int causal,

@@ -38,6 +38,14 @@ cudaError_t launch_mla_cache_write(const void* kv_c, const void* k_pe, void* cac
                                    int rope_dim, int block_size, int num_blocks, int* err,
                                    cudaStream_t stream);
 
+// MLA prefill, step 1: expand every context token's latent through kv_b_proj
+// into K_ws [N][s_max][H][192] = [k_nope | k_pe] and V_ws [N][s_max][H][128]
+// (bf16).  Fixed widths: kv_lora_rank 512, rope 64, nope 128, v 128.
+cudaError_t launch_mla_expand(const void* pool, const void* w_kv_b, const int32_t* block_table,
+                              const int32_t* seq_lens, int N, int H, int bs, int num_blocks,
+                              int max_blocks, int max_seq_len, int s_max, void* k_ws, void* v_ws,
+                              int* err, cudaStream_t stream);
+
 // fp8 (e4m3) pool: quantising cache write and split-KV stage 1.
 cudaError_t launch_reshape_and_cache_fp8(const void* key, const void* value, void* cache,
                                          const int64_t* slot_mapping, int num_tokens,
@@ -76,6 +84,12 @@ struct VarlenLaunch {
   int ws_slot0 = 0;        // split s writes slot ws_slot0 + s
   int kv_splits = 1;
   int kv_chunk = 0;        // tokens per split, a multiple of 128
+  // MLA prefill attention: keys [N * mla_s_max][Hkv][192] and values
+  // [N * mla_s_max][Hkv][128] (the expanded workspaces) instead of the pool;
+  // q is [T][Hkv][192], out [T][Hkv][128], one q head per kv head.
+  const void* mla_k = nullptr;
+  const void* mla_v = nullptr;
+  int mla_s_max = 0;
 };
 cudaError_t launch_varlen_tc(const VarlenLaunch& L, cudaStream_t stream);
 

@@ -35,8 +35,11 @@
 // them to all; a stage is released cluster-wide by a multicast tcgen05.commit.
 //
 // Shared memory (128-byte swizzled, 1024-byte aligned atoms):
-//   Q    2 tiles x [D/64 halves][128 rows][128 B]
-//   K, V 2 stages each x [D/64 halves][128 tokens][128 B]
+//   Q    2 tiles x [DK/64 halves][128 rows][128 B]
+//   K    2 stages x [DK/64 halves][BN tokens][128 B]
+//   V    2 stages x [DV/64 halves][BN tokens][128 B]
+// (DK = DV = d and BN = 128 for the standard pool; DK = 192, DV = 128 and
+// BN = 64 for the MLA prefill, whose queries and keys are [nope | rope].)
 // TMEM (512 columns): S_0/P_0 at 0, S_1/P_1 at 128, O_0 at 256, O_1 at 384.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -50,18 +53,22 @@
 
 namespace pa {
 
-template <int D>
+// DK: width of queries and keys; DV: width of values and outputs; BN: tokens
+// per K/V tile.
+template <int DK, int DV, int BN>
 struct TcCfg {
   static constexpr int kBM = 128;                     // rows per Q tile
   static constexpr int kRows = 2 * kBM;               // packed rows per CTA
-  static constexpr int kBN = 128;                     // tokens per K/V tile
-  static constexpr int kHalves = D / 64;              // 128-byte column groups of a row
-  static constexpr int kQBytes = kBM * D * 2;         // one Q tile
-  static constexpr int kTileBytes = kBN * D * 2;      // one K (or V) tile
+  static constexpr int kBN = BN;                      // tokens per K/V tile
+  static constexpr int kHalvesK = DK / 64;            // 128-byte column groups of a key row
+  static constexpr int kHalvesV = DV / 64;            // ... of a value row
+  static constexpr int kQBytes = kBM * DK * 2;        // one Q tile
+  static constexpr int kKBytes = kBN * DK * 2;        // one K tile
+  static constexpr int kVBytes = kBN * DV * 2;        // one V tile
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = 2 * kQBytes;
-  static constexpr int kOffV = kOffK + 2 * kTileBytes;
-  static constexpr int kOffBar = kOffV + 2 * kTileBytes;
+  static constexpr int kOffV = kOffK + 2 * kKBytes;
+  static constexpr int kOffBar = kOffV + 2 * kVBytes;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;   // barriers + alignment slack
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kThreads = 384;
@@ -126,10 +133,11 @@ struct VarlenArgs {
   int seq_off;      // tokens dropped from the front of every request (seq_lens[i] - seq_off)
   int virt_total_q; // > 0: one request made of query rows [0, virt_total_q) ...
   int virt_seq;     // ... over virt_seq tokens of table row 0 (qsl, seq_lens unused)
-  float* ws;        // non-null: partial output, [rows][Hq][ws_slots][D + 1] fp32
+  float* ws;        // non-null: partial output, [rows][Hq][ws_slots][DV + 1] fp32
   int ws_slots, ws_slot0;
   int kv_splits;    // context cut into kv_splits pieces of kv_chunk (a multiple of the tile)
   int kv_chunk;
+  int mla_s_max;    // MLA mode: token rows per request in the expanded workspaces
 };
 
 // After the barriers: the TMEM base address (4 B, padded to 8), the abort
@@ -138,10 +146,14 @@ constexpr int kPieceRing = 4;
 
 // EXT = false compiles the plain call (no window, split, offsets, virtual
 // request or partial output: those fields are ignored).
-template <int D, int CL, bool EXT>
+// MLA = true: keys and values come from the contiguous expanded workspaces
+// of the MLA prefill (k_map over [N * s_max][H][DK], v_map over
+// [N * s_max][H][DV]) instead of the paged pool; no block table.
+template <int DK, int DV, int BN, int CL, bool EXT, bool MLA>
 __global__ void __launch_bounds__(384, 1)
-varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ VarlenArgs a) {
-  using C = TcCfg<D>;
+varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap v_map,
+                 const __grid_constant__ VarlenArgs a) {
+  using C = TcCfg<DK, DV, BN>;
   const __nv_bfloat16* __restrict__ q = a.q;
   const int32_t* __restrict__ block_table = a.block_table;
   const int Hq = a.Hq, Hkv = a.Hkv, bs = a.bs, num_blocks = a.num_blocks;
@@ -270,7 +282,8 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
     const bool valid = pr < rows_total;
     const int qi = valid ? pr / grp : 0;
     const int hh = valid ? pr % grp : 0;
-    const int64_t qoff = (static_cast<int64_t>(q0 + qi) * Hq + kvh * grp + hh) * D;
+    const int64_t qrow = static_cast<int64_t>(q0 + qi) * Hq + kvh * grp + hh;
+    const int64_t qoff = qrow * DK;
     int lim = valid ? (causal ? ctx + qi + 1 : seq) : 0;
     lim = max(0, min(lim, seq));
     const int lo = window > 0 ? max(0, lim - window) : 0;   // first visible position
@@ -278,7 +291,7 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
       const uint4* src = reinterpret_cast<const uint4*>(q + qoff);
       const uint32_t qb = sbase + C::kOffQ + x * C::kQBytes;
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
+      for (int c = 0; c < DK / 8; ++c) {
         uint4 v = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
         const uint32_t dst = qb + (c >> 3) * (C::kBM * 128) + sw128(t, c & 7);
         asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v.x), "r"(v.y),
@@ -360,7 +373,7 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
       // S_x(j) has landed, hence PV_x(j-1) too: O_x may be rescaled now.
       if (__any_sync(0xffffffffu, need) && j > 0) {
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < DV / 32; ++c) {
           uint32_t r[32];
           tc::tmem_ld32(to + c * 32, r);
           tc::tmem_wait_ld();
@@ -375,12 +388,13 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
       // before P_0(j) is published; PV_1(j) is issued after PV_0(j).
       if (x == 0) {
         const int tok = tok0 + t;
-        const bool row_ok = tok < seq && ((vm >> (t >> 4)) & 1u);
+        // Threads past the tile's kBN rows own no V row.
+        const bool row_ok = t >= C::kBN || (tok < seq && ((vm >> (t >> 4)) & 1u));
         if (!row_ok) {
           if (!tc::mbar_wait(BAR(kVFull + (j & 1)), (j >> 1) & 1)) fail();
-          const uint32_t vbase = sbase + C::kOffV + (j & 1) * C::kTileBytes;
+          const uint32_t vbase = sbase + C::kOffV + (j & 1) * C::kVBytes;
 #pragma unroll
-          for (int h = 0; h < C::kHalves; ++h)
+          for (int h = 0; h < C::kHalvesV; ++h)
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
               const uint32_t dst = vbase + h * (C::kBN * 128) + sw128(t, c);
@@ -420,13 +434,13 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
     if (ok) ok = wait_warp(BAR(kODone + x), (ntiles - 1) & 1);
     tc::tc_fence_after();
     // Partial mode: the row's normalised output and LSE go, in fp32, to slot
-    // ws_slot0 + split of its workspace row [ws_slots][D + 1].
+    // ws_slot0 + split of its workspace row [ws_slots][DV + 1].
     float* wrow = ws == nullptr ? nullptr
-                                : ws + ((qoff / D) * a.ws_slots + a.ws_slot0 + split) * (D + 1);
+                                : ws + (qrow * a.ws_slots + a.ws_slot0 + split) * (DV + 1);
     if (ok && wrow != nullptr) {   // warp-uniform
       const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < DV / 32; ++c) {
         uint32_t r[32];
         tc::tmem_ld32(to + c * 32, r);
         tc::tmem_wait_ld();
@@ -435,17 +449,17 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
           for (int e = 0; e < 32; ++e) wrow[c * 32 + e] = __uint_as_float(r[e]) * inv;
         }
       }
-      if (valid) wrow[D] = l > 0.f ? (m_used + log2f(l)) * kLn2 : -CUDART_INF_F;
+      if (valid) wrow[DV] = l > 0.f ? (m_used + log2f(l)) * kLn2 : -CUDART_INF_F;
     } else if (wrow != nullptr) {
       if (valid) {
-        for (int c = 0; c < D; ++c) wrow[c] = 0.f;
-        wrow[D] = -CUDART_INF_F;
+        for (int c = 0; c < DV; ++c) wrow[c] = 0.f;
+        wrow[DV] = -CUDART_INF_F;
       }
     } else if (ok) {   // warp-uniform
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint4* dst = reinterpret_cast<uint4*>(out + qoff);
+      uint4* dst = reinterpret_cast<uint4*>(out + qrow * DV);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < DV / 32; ++c) {
         uint32_t r[32];
         tc::tmem_ld32(to + c * 32, r);
         tc::tmem_wait_ld();
@@ -462,12 +476,12 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
         }
       }
       if (valid && lse != nullptr)
-        lse[qoff / D] = l > 0.f ? (m_used + log2f(l)) * kLn2 : -CUDART_INF_F;
+        lse[qrow] = l > 0.f ? (m_used + log2f(l)) * kLn2 : -CUDART_INF_F;
     } else if (valid) {
       // Nothing visible (or an aborted CTA): o = 0, lse = -inf.
-      uint4* dst = reinterpret_cast<uint4*>(out + qoff);
-      for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
-      if (lse != nullptr) lse[qoff / D] = -CUDART_INF_F;
+      uint4* dst = reinterpret_cast<uint4*>(out + qrow * DV);
+      for (int c = 0; c < DV / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+      if (lse != nullptr) lse[qrow] = -CUDART_INF_F;
     }
   } else if (warp == 0) {
     // ------------------------------------------------------------ MMA issue
@@ -476,15 +490,15 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
     const uint32_t tmem = tmem_base();
     if (lane == 0) {
       constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, C::kBN, 0, 0);
-      constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, D, 0, 1);
+      constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, DV, 0, 1);
       bool ok = ntiles == 0 || tc::mbar_wait(BAR(kQFull), 0);
       if (!ok) fail();
       // S_x(j) = Q_x K(j)^T into the S columns of tile x.
       auto issue_s = [&](int xq, int j) {
         const uint32_t qs = sbase + C::kOffQ + xq * C::kQBytes;
-        const uint32_t ks = sbase + C::kOffK + (j & 1) * C::kTileBytes;
+        const uint32_t ks = sbase + C::kOffK + (j & 1) * C::kKBytes;
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
+        for (int k = 0; k < DK / 16; ++k) {
           const uint32_t off = (k >> 2) * (C::kBM * 128) + (k & 3) * 32;
           const uint32_t koff = (k >> 2) * (C::kBN * 128) + (k & 3) * 32;
           tc::mma_bf16_ss(tmem + C::col_s(xq), tc::smem_desc_sw128(qs + off, 16, 1024),
@@ -495,7 +509,7 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
       // O_x += P_x(j) V(j) over the 16-token steps [k0, k0 + 4); P_x is read
       // from TMEM, 8 columns (16 bf16) per step.
       auto issue_pv = [&](int xq, int j, int k0) {
-        const uint32_t vs = sbase + C::kOffV + (j & 1) * C::kTileBytes;
+        const uint32_t vs = sbase + C::kOffV + (j & 1) * C::kVBytes;
 #pragma unroll
         for (int k = k0; k < k0 + C::kBN / 32; ++k)
           tc::mma_bf16_ts(tmem + C::col_o(xq), tmem + C::col_s(xq) + k * 8,
@@ -544,7 +558,10 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
     // 64-column half), multicast to the whole cluster.  Every CTA expects
     // the bytes of all loaded pieces on its own barrier.  V(j) goes out before
     // K(j+2) (PV(j) needs it first) and reuses K(j)'s block ids.
-    if (lane == 0) tc::tma_prefetch_desc(&kv_map);
+    if (lane == 0) {
+      tc::tma_prefetch_desc(&kv_map);
+      if (MLA) tc::tma_prefetch_desc(&v_map);
+    }
     const int pc = lane;
     const bool box_lane = lane < C::kBN / 16;
     const bool my_piece = box_lane && (pc % CL) == rank;
@@ -553,6 +570,7 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
     };
     auto raw_of = [&](int j) -> int {
       if (!in_range(j)) return -1;
+      if (MLA) return 0;   // contiguous workspace: every in-range piece is loaded
       const int idx = (tbase + j * C::kBN + 16 * pc) / bs;
       return idx < max_blocks ? __ldg(table + idx) : -1;
     };
@@ -568,12 +586,20 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
         if (bad != 0u && which == 0 && rank == 0) record_error(err, PA_DEVERR_BLOCK_ID);
         if (which == 0) piece_ring[j % kPieceRing] = (static_cast<uint32_t>(j) << 8) | (loaded & 0xffu);
         tc::mbar_arrive_expect_tx(
-            full, static_cast<uint32_t>(__popc(loaded)) * C::kHalves * C::kPieceBytes);
+            full, static_cast<uint32_t>(__popc(loaded)) *
+                      static_cast<uint32_t>(which == 0 ? C::kHalvesK : C::kHalvesV) * C::kPieceBytes);
       }
       __syncwarp();
-      if (my_piece && blk >= 0) {
+      if (MLA && my_piece && blk >= 0) {
+        // Token row (request i, position tok0 + 16 pc) of the workspace.
+        const int row = static_cast<int>(static_cast<long long>(i) * a.mla_s_max + tok0 + 16 * pc);
+        const int halves = which == 0 ? C::kHalvesK : C::kHalvesV;
+        for (int h = 0; h < halves; ++h)
+          tc::tma_load_3d(dst + h * (C::kBN * 128) + pc * C::kPieceBytes,
+                          which == 0 ? &kv_map : &v_map, full, h * 64, kvh, row);
+      } else if (!MLA && my_piece && blk >= 0) {
 #pragma unroll
-        for (int h = 0; h < C::kHalves; ++h) {
+        for (int h = 0; h < C::kHalvesK; ++h) {
           const uint32_t d = dst + h * (C::kBN * 128) + pc * C::kPieceBytes;
           if (CL > 1)
             tc::tma_load_5d_mc(d, &kv_map, full, kMask, h * 64, kvh, (tok0 + 16 * pc) % bs, which,
@@ -590,13 +616,13 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
     auto issue_k = [&](int j, int blk) -> bool {
       const int st = j & 1;
       if (j >= 2 && !wait_all(BAR(kKEmpty + st), ((j >> 1) - 1) & 1)) return false;
-      issue(j, blk, 0, sbase + C::kOffK + st * C::kTileBytes, BAR(kKFull + st));
+      issue(j, blk, 0, sbase + C::kOffK + st * C::kKBytes, BAR(kKFull + st));
       return true;
     };
     auto issue_v = [&](int j, int blk) -> bool {
       const int st = j & 1;
       if (j >= 2 && !wait_all(BAR(kVEmpty + st), ((j >> 1) - 1) & 1)) return false;
-      issue(j, blk, 1, sbase + C::kOffV + st * C::kTileBytes, BAR(kVFull + st));
+      issue(j, blk, 1, sbase + C::kOffV + st * C::kVBytes, BAR(kVFull + st));
       return true;
     };
     int r0 = raw_of(0), r1 = raw_of(1), r2 = raw_of(2);   // tiles j, j+1, j+2 (raw)
@@ -678,12 +704,35 @@ bool make_kv_map(CUtensorMap* map, const void* cache, int nb, int bs, int Hkv, i
 
 }  // namespace
 
-template <int D, int CL, bool EXT>
+// MLA prefill workspaces [rows][H][width] viewed 3-D (innermost first):
+// 64-column x 1-head x 16-token boxes, 128-byte swizzle.
+bool make_ws_map(CUtensorMap* map, const void* ws, long long rows, int H, int width) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(width), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(width) * 2,
+                                 static_cast<cuuint64_t>(width) * 2 * H};
+  const cuuint32_t box[3] = {64, 1, 16};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ws), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int DK, int DV, int BN, int CL, bool EXT, bool MLA>
 static cudaError_t launch_varlen_tc_t(const VarlenLaunch& L, cudaStream_t stream) {
-  using C = TcCfg<D>;
-  CUtensorMap map;
-  if (!make_kv_map(&map, L.cache, L.num_blocks, L.bs, L.Hkv, D)) return cudaErrorInvalidValue;
-  auto kern = varlen_tc_kernel<D, CL, EXT>;
+  using C = TcCfg<DK, DV, BN>;
+  CUtensorMap map, vmap;
+  if (MLA) {
+    const long long rows = static_cast<long long>(L.N) * L.mla_s_max;
+    if (!make_ws_map(&map, L.mla_k, rows, L.Hkv, DK) || !make_ws_map(&vmap, L.mla_v, rows, L.Hkv, DV))
+      return cudaErrorInvalidValue;
+  } else {
+    if (!make_kv_map(&map, L.cache, L.num_blocks, L.bs, L.Hkv, DK)) return cudaErrorInvalidValue;
+    vmap = map;
+  }
+  auto kern = varlen_tc_kernel<DK, DV, BN, CL, EXT, MLA>;
   static DeviceFlags attr_set;
   cudaError_t e = set_smem_once(kern, C::kSmemBytes, attr_set);
   if (e != cudaSuccess) return e;
@@ -730,6 +779,7 @@ static cudaError_t launch_varlen_tc_t(const VarlenLaunch& L, cudaStream_t stream
   a.ws_slot0 = L.ws_slot0;
   a.kv_splits = splits;
   a.kv_chunk = L.kv_chunk;
+  a.mla_s_max = L.mla_s_max;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(tiles * splits), L.Hkv, virt ? 1 : L.N);
   cfg.blockDim = dim3(C::kThreads);
@@ -742,20 +792,22 @@ static cudaError_t launch_varlen_tc_t(const VarlenLaunch& L, cudaStream_t stream
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, map, a);
+  return cudaLaunchKernelEx(&cfg, kern, map, vmap, a);
 }
 
 // CTAs per cluster sharing K/V tiles by multicast.
 constexpr int kVarlenCluster = 1;
 
 cudaError_t launch_varlen_tc(const VarlenLaunch& L, cudaStream_t stream) {
+  if (L.mla_k != nullptr)   // MLA prefill attention: [nope | rope] keys, 128-wide values
+    return launch_varlen_tc_t<192, 128, 64, kVarlenCluster, false, true>(L, stream);
   const bool ext = L.window > 0 || L.kv_splits > 1 || L.ws != nullptr || L.virt_total_q > 0 ||
                    L.table_col0 != 0 || L.seq_off != 0;
   if (L.d == 128)
-    return ext ? launch_varlen_tc_t<128, kVarlenCluster, true>(L, stream)
-               : launch_varlen_tc_t<128, kVarlenCluster, false>(L, stream);
-  return ext ? launch_varlen_tc_t<64, kVarlenCluster, true>(L, stream)
-             : launch_varlen_tc_t<64, kVarlenCluster, false>(L, stream);
+    return ext ? launch_varlen_tc_t<128, 128, 128, kVarlenCluster, true, false>(L, stream)
+               : launch_varlen_tc_t<128, 128, 128, kVarlenCluster, false, false>(L, stream);
+  return ext ? launch_varlen_tc_t<64, 64, 128, kVarlenCluster, true, false>(L, stream)
+             : launch_varlen_tc_t<64, 64, 128, kVarlenCluster, false, false>(L, stream);
 }
 
 }  // namespace pa
