@@ -76,41 +76,49 @@ namespace pa {
 struct MlaTcCfg {
   static constexpr int kDk = 576, kDv = 512, kH = 128, kBN = 64, kBox = 32;
   static constexpr int kLat = 4;                           // latent chunks per CTA
-  static constexpr int kQChunkBytes = kH * 128;            // 16 KB
   static constexpr int kQRopeBytes = kH * 64;              // 8 KB
   static constexpr int kKChunkBytes = kBN * 128;           // 8 KB
   static constexpr int kKRopeBytes = kBN * 64;             // 4 KB
   static constexpr int kStageBytes = kLat * kKChunkBytes + kKRopeBytes;   // 36 KB
-  static constexpr int kStages = 3;
+  static constexpr int kStages = 4;
   static constexpr int kHalfBytes = kBox * (kLat * 128 + 64);           // 18 KB per 32 tokens
   static constexpr int kXBytes = kH * 9 * 16;              // 18 KB per buffer
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffQr = kLat * kQChunkBytes;       // 64 KB
-  static constexpr int kOffK = kOffQr + kQRopeBytes;       // 72 KB
-  static constexpr int kOffX = kOffK + kStages * kStageBytes;   // 180 KB
-  static constexpr int kOffBar = kOffX + 2 * kXBytes;      // 216 KB
-  static constexpr int kSmemBytes = kOffBar + 256 + 1024;
+  static constexpr int kOffQr = 0;
+  static constexpr int kOffK = kQRopeBytes;                // 8 KB
+  static constexpr int kPBytes = kH * 128;                 // P tile: [128 heads][64 tokens] bf16
+  static constexpr int kOffX = kOffK + kStages * kStageBytes;   // 152 KB
+  static constexpr int kOffP = kOffX + 2 * kXBytes;        // 188 KB
+  static constexpr int kOffBar = kOffP + 2 * kPBytes;      // 220 KB
+  static constexpr int kBarBlock = 320;                    // barriers, TMEM slot, flags, ring
+  static constexpr int kSmemBytes = kOffBar + kBarBlock + 1024;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColP = 128;
+  static constexpr uint32_t kColQ = 128;                   // query latent half, bf16 pairs
   static constexpr uint32_t kColO = 256;
   static constexpr int kThreads = 352;
 };
 
 enum MlaBar {
   kMQFull = 0,
-  kMKFull = 1,    // [3]
-  kMKEmpty = 4,   // [3]
-  kMSFull = 7,    // [2]
-  kMXFull = 9,    // [2] the peer's partial scores have arrived in buffer b
-  kMXEmpty = 11,  // [2] the peer has consumed buffer b of the scores this CTA sent
-  kMPFull = 13,   // [2] P buffer b written
-  kMPDone = 15,   // [2] PV of P buffer b completed
-  kMFinal = 17,
-  kMXRead = 18,   // [2] the softmax warps have read exchange buffer b
-  kMSRead = 20,   // [2] the softmax and exchange warps have read S buffer b
-  kMNumBars = 22
+  kMKFull = 1,                              // [kStages]
+  kMKEmpty = kMKFull + MlaTcCfg::kStages,   // [kStages]
+  kMSFull = kMKEmpty + MlaTcCfg::kStages,   // [2]
+  kMXFull = kMSFull + 2,    // [2] the peer's partial scores have arrived in buffer b
+  kMXEmpty = kMXFull + 2,   // [2] the peer has consumed buffer b of the scores this CTA sent
+  kMPFull = kMXEmpty + 2,   // [2] P buffer b written
+  kMPDone = kMPFull + 2,    // [2] PV of P buffer b completed
+  kMFinal = kMPDone + 2,
+  kMXRead = kMFinal + 1,    // [2] the softmax warps have read exchange buffer b
+  kMSRead = kMXRead + 2,    // [2] the softmax and exchange warps have read S buffer b
+  kMNumBars = kMSRead + 2
 };
-constexpr int kMlaRing = 4;   // tile descriptors passed from the producer
+// Block layout after the barriers: TMEM slot (+0), abort flag (+8),
+// descriptor ring (+16, kMlaRing words), rank pick (+16 + 4 * kMlaRing).
+static_assert(8 * kMNumBars + 16 + 4 * 8 + 4 <= MlaTcCfg::kBarBlock,
+              "MLA barrier block overflows its reservation");
+// Tile descriptors passed from the producer: it runs up to kStages tiles
+// ahead of the consumers, so the ring must hold more entries than that.
+constexpr int kMlaRing = 8;
+static_assert(kMlaRing > MlaTcCfg::kStages, "descriptor ring shorter than the producer's lead");
 constexpr int kMlaRankMax = 512;    // largest batch ranked by seq_len (B^2 comparisons)
 
 __device__ __forceinline__ uint32_t msw128(int r, int c) {
@@ -157,7 +165,7 @@ __device__ __forceinline__ float dequant(int q, float unit, float bias_unit) {
 }
 
 __global__ void __launch_bounds__(352, 1)
-mla_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap qr_map,
+mla_tc_kernel(const __nv_bfloat16* __restrict__ q, const __grid_constant__ CUtensorMap qr_map,
               const __grid_constant__ CUtensorMap c_map, const __grid_constant__ CUtensorMap cr_map,
               const int32_t* __restrict__ block_table, const int32_t* __restrict__ seq_lens,
               int max_blocks, int H, int bs, int num_blocks, float scale_log2, int S, int chunk,
@@ -183,7 +191,8 @@ mla_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__
   if (gridDim.y <= kMlaRankMax) {
     const int nb = static_cast<int>(gridDim.y);
     volatile int* sl = reinterpret_cast<volatile int*>(sgen + C::kOffX);
-    volatile int* pick = reinterpret_cast<volatile int*>(sgen + C::kOffBar + 8 * kMNumBars + 32);
+    volatile int* pick =
+        reinterpret_cast<volatile int*>(sgen + C::kOffBar + 8 * kMNumBars + 16 + 4 * kMlaRing);
     for (int i = threadIdx.x; i < nb; i += blockDim.x) sl[i] = seq_lens[i];
     __syncthreads();
     for (int i = threadIdx.x; i < nb; i += blockDim.x) {
@@ -213,7 +222,9 @@ mla_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__
       reinterpret_cast<volatile uint32_t*>(sgen + C::kOffBar + 8 * kMNumBars + 16);
 
   if (threadIdx.x == 0) {
-    tc::mbar_init(BAR(kMQFull), 1);
+    // The query: 128 softmax threads store its latent half in TMEM, the
+    // producer's rope box lands by TMA.
+    tc::mbar_init(BAR(kMQFull), 129);
     for (int k = 0; k < C::kStages; ++k) {
       tc::mbar_init(BAR(kMKFull + k), 1);
       tc::mbar_init(BAR(kMKEmpty + k), 1);
@@ -259,6 +270,30 @@ mla_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__
       if (!w) fail();
       return w;
     };
+    {
+      // Head t's latent half of the query, [256 r, 256 r + 256), as the A
+      // operand of the score MMAs: TMEM lane t, two bf16 per column (the
+      // lower index in the low half).
+      const int head = hg * C::kH + t;
+      const uint4* src = reinterpret_cast<const uint4*>(
+          q + (static_cast<int64_t>(b) * H + (head < H ? head : 0)) * C::kDk + 256 * rank);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const uint4 x = head < H ? __ldg(src + c * 8 + v) : make_uint4(0, 0, 0, 0);
+          r[4 * v] = x.x;
+          r[4 * v + 1] = x.y;
+          r[4 * v + 2] = x.z;
+          r[4 * v + 3] = x.w;
+        }
+        tc::tmem_st32(tmem + lane_base + C::kColQ + c * 32, r);
+      }
+      tc::tmem_wait_st();
+      tc::tc_fence_before();
+      tc::mbar_arrive(BAR(kMQFull));
+    }
     float m_used = -CUDART_INF_F, l = 0.f;
     for (int j = 0; j < ntiles; ++j) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
@@ -370,30 +405,32 @@ mla_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__
                          : "memory");
         tc::fence_proxy_async_smem();
       }
-      // P = exp2(s * scale_log2 - m_used), bf16 pairs into P buffer `buf`,
-      // once PV(j-2) has read it.
+      // P = exp2(s * scale_log2 - m_used) as bf16, row t of shared-memory
+      // P buffer `buf` (128-byte swizzle, the A operand of PV), once PV(j-2)
+      // has read it.  Keeping P out of TMEM lets S(j+2) reuse the S buffer
+      // as soon as S(j) has been read.
       if (j >= 2 && !all_ok(tc::mbar_wait(BAR(kMPDone + buf), ((j >> 1) - 1) & 1))) break;
-      tc::tc_fence_after();
-      const uint32_t tp = tmem + lane_base + C::kColP + 32u * buf;
       {
+        const uint32_t pb = sbase + C::kOffP + buf * C::kPBytes;
         float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t pk[16];
+        for (int c = 0; c < 8; ++c) {
+          uint32_t pk[4];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int c = h * 16 + e;
-            const float p0 = mex2(fmaf(sc[2 * c], scale_log2, -mu));
-            const float p1 = mex2(fmaf(sc[2 * c + 1], scale_log2, -mu));
-            l8[e & 7] += p0 + p1;
+          for (int e = 0; e < 4; ++e) {
+            const float p0 = mex2(fmaf(sc[8 * c + 2 * e], scale_log2, -mu));
+            const float p1 = mex2(fmaf(sc[8 * c + 2 * e + 1], scale_log2, -mu));
+            l8[(2 * e) & 7] += p0;
+            l8[(2 * e + 1) & 7] += p1;
             pk[e] = pack_bf16(p0, p1);
           }
-          tc::tmem_st16(tp + h * 16, pk);
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(pb + msw128(t, c)),
+                       "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3])
+                       : "memory");
         }
         l = l * alpha + (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
       }
-      tc::tmem_wait_st();
-      tc::tc_fence_before();
+      tc::fence_proxy_async_smem();
       tc::mbar_arrive(BAR(kMPFull + buf));
     }
     // ------------------------------------------------------------ epilogue
@@ -514,9 +551,11 @@ mla_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__
     if (lane == 0) {
       constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, C::kBN, 0, 0);
       constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, 256, 0, 1);
-      const uint32_t qs = sbase + C::kOffQ, qr = sbase + C::kOffQr;
-      // S(j) = Q_r K_r(j)^T into S buffer j & 1: 4 latent chunks x 4 K-steps
-      // (128-byte swizzle) and the rope half, 2 K-steps (64-byte swizzle).
+      const uint32_t qr = sbase + C::kOffQr;
+      // S(j) = Q_r K_r(j)^T into S buffer j & 1: the latent half with A from
+      // TMEM (16 K-steps of 8 columns) against the 4 latent chunks of the
+      // stage (128-byte swizzle), then the rope half from shared memory
+      // (2 K-steps, 64-byte swizzle).
       auto issue_s = [&](int j) {
         const uint32_t ks = sbase + C::kOffK + (j % C::kStages) * C::kStageBytes;
         const uint32_t d = tmem + 64u * (j & 1);
@@ -524,7 +563,7 @@ mla_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__
         for (int c = 0; c < C::kLat; ++c)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            tc::mma_bf16_ss(d, tc::smem_desc_sw128(qs + c * C::kQChunkBytes + kk * 32, 16, 1024),
+            tc::mma_bf16_ts(d, tmem + C::kColQ + (c * 4 + kk) * 8,
                             tc::smem_desc_sw128(ks + c * C::kKChunkBytes + kk * 32, 16, 1024),
                             idesc_s, (c > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
@@ -537,14 +576,15 @@ mla_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__
       auto wait_k = [&](int j) {
         return tc::mbar_wait(BAR(kMKFull + j % C::kStages), (j / C::kStages) & 1);
       };
-      // O_r += P(j) V_r(j): P from TMEM (8 columns = 16 tokens per K-step),
-      // V_r = the 4 latent chunks of the stage, N = 256.
+      // O_r += P(j) V_r(j): P from shared-memory buffer j & 1 (K-major,
+      // 32 bytes = 16 tokens per K-step), V_r = the 4 latent chunks of the
+      // stage, N = 256.
       auto issue_pv = [&](int j) {
         const uint32_t vs = sbase + C::kOffK + (j % C::kStages) * C::kStageBytes;
-        const uint32_t pa = tmem + C::kColP + 32u * (j & 1);
+        const uint32_t pa = sbase + C::kOffP + (j & 1) * C::kPBytes;
 #pragma unroll
         for (int k = 0; k < C::kBN / 16; ++k)
-          tc::mma_bf16_ts(tmem + C::kColO, pa + k * 8,
+          tc::mma_bf16_ss(tmem + C::kColO, tc::smem_desc_sw128(pa + k * 32, 16, 1024),
                           tc::smem_desc_sw128(vs + k * 16 * 128, C::kKChunkBytes, 1024), idesc_o,
                           (j > 0 || k > 0) ? 1u : 0u);
         tc::mma_commit(BAR(kMPDone + (j & 1)));
@@ -562,7 +602,7 @@ mla_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__
       // j & 1 once S(j) has been read from it and K(j+2) has landed, in
       // whichever order they become ready -- PV first when both are, since
       // the tensor pipe runs in issue order and PV(j) frees the K stage that
-      // K(j+3) is waiting for.
+      // a later K load is waiting for.
       for (int j = 0; ok && j < ntiles; ++j) {
         bool s_done = j + 2 >= ntiles, pv_done = false;
         int n = 0;
@@ -591,24 +631,16 @@ mla_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__
     // Lane i < 10 owns box i % 5 (latent chunk 0-3, or the rope half) of the
     // 32-token half i / 5 of every tile.
     if (lane == 0) {
-      tc::tma_prefetch_desc(&q_map);
       tc::tma_prefetch_desc(&qr_map);
       tc::tma_prefetch_desc(&c_map);
       tc::tma_prefetch_desc(&cr_map);
     }
     const int half = lane / 5, box = lane % 5;
     const bool box_lane = lane < 10;
-    if (ntiles > 0) {
-      if (lane == 0)
-        tc::mbar_arrive_expect_tx(BAR(kMQFull), C::kLat * C::kQChunkBytes + C::kQRopeBytes);
-      __syncwarp();
-      const int row = b * H + hg * C::kH;
-      if (lane < C::kLat)
-        tc::tma_load_2d_(sbase + C::kOffQ + lane * C::kQChunkBytes, &q_map, BAR(kMQFull),
-                         256 * static_cast<int>(rank) + 64 * lane, row);
-      else if (lane == C::kLat)
-        tc::tma_load_2d_(sbase + C::kOffQr, &qr_map, BAR(kMQFull), 512 + 32 * static_cast<int>(rank),
-                         row);
+    if (ntiles > 0 && lane == 0) {
+      tc::mbar_arrive_expect_tx(BAR(kMQFull), C::kQRopeBytes);
+      tc::tma_load_2d_(sbase + C::kOffQr, &qr_map, BAR(kMQFull), 512 + 32 * static_cast<int>(rank),
+                       b * H + hg * C::kH);
     }
     // Half `half` of tile j lies inside the split iff its first token does.
     auto in_split = [&](int j) -> bool {
@@ -745,14 +777,12 @@ cudaError_t launch_mla_tc(const void* q, const void* cache, const int32_t* block
   using C = MlaTcCfg;
   // Query [B*H rows][576]: 64-column latent boxes and 32-column rope boxes of
   // 128 heads.  Cache [nb][bs][576]: the same boxes over 32 tokens.
-  CUtensorMap q_map, qr_map, c_map, cr_map;
+  CUtensorMap qr_map, c_map, cr_map;
   {
     const cuuint64_t dims[2] = {C::kDk, static_cast<cuuint64_t>(B) * H};
     const cuuint64_t strides[1] = {C::kDk * 2};
-    const cuuint32_t box[2] = {64, C::kH};
     const cuuint32_t box_r[2] = {32, C::kH};
-    if (!encode(&q_map, q, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode(&qr_map, q, 2, dims, strides, box_r, CU_TENSOR_MAP_SWIZZLE_64B))
+    if (!encode(&qr_map, q, 2, dims, strides, box_r, CU_TENSOR_MAP_SWIZZLE_64B))
       return cudaErrorInvalidValue;
   }
   {
@@ -783,7 +813,8 @@ cudaError_t launch_mla_tc(const void* q, const void* cache, const int32_t* block
   // With one split each pair writes its output rows and LSE itself (16-byte
   // vector stores), and the workspace and the merge are skipped.
   const int direct = (S == 1 && (reinterpret_cast<uintptr_t>(out) & 15u) == 0) ? 1 : 0;
-  e = cudaLaunchKernelEx(&cfg, mla_tc_kernel, q_map, qr_map, c_map, cr_map, block_table, seq_lens,
+  e = cudaLaunchKernelEx(&cfg, mla_tc_kernel, static_cast<const __nv_bfloat16*>(q), qr_map, c_map,
+                         cr_map, block_table, seq_lens,
                          max_blocks, H, bs, num_blocks, scale * kLog2e, S, chunk, ws,
                          static_cast<__nv_bfloat16*>(out), lse, direct, err);
   if (e != cudaSuccess || direct) return e;
