@@ -9,7 +9,7 @@
 // One (split, request, group of 128 heads) is computed by a cluster of two
 // CTAs.  The 128 heads form the M = 128 rows of every MMA.  A 128 x 576 query
 // (144 KB) and a 128 x 512 fp32 output (all 512 TMEM columns) do not fit one
-// CTA next to a K tile and the scores, so the pair splits both:
+// CTA next to a K ring and the scores, so the pair splits both:
 //   * the contraction: CTA r holds the query / key columns of latent chunks
 //     [256r, 256r + 256) and rope half [512 + 32r, 512 + 32r + 32); it computes
 //     the partial scores S_r(j) = Q_r K_r(j)^T of a 64-token tile (N = 64);
@@ -26,9 +26,11 @@
 // largest scores, which dominate the LSE).  CTA r then holds
 // S = S_r + decode(S_peer) and runs the online softmax on it; each CTA's
 // output half and row sum come from its own P, so each half is normalised
-// consistently.  P goes
-// to its own TMEM buffer and PV takes it from there, so the next scores can
-// be computed into the S buffer as soon as the S of the tile has been read.
+// consistently.  The query's latent half is the A operand of the score MMAs
+// straight from TMEM (so shared memory holds only its 8 KB rope part and a
+// four-stage K ring), and P goes to a shared-memory buffer that PV reads as
+// its A operand, so the next scores can be computed into the S buffer as
+// soon as the S of the tile has been read.
 //
 // 352 threads per CTA:
 //   warps 0-3  softmax: thread t owns head t = TMEM lane t;
@@ -40,7 +42,7 @@
 //              (and K(j+2) has landed), PV(j) as soon as P(j) is written,
 //              whichever comes first, so the scores of the next tiles are
 //              computed while the softmax works on the current one;
-//   warp 9     TMA producer: its query columns once, then per 64-token tile
+//   warp 9     TMA producer: the query's rope half once, then per 64-token tile
 //              two 32-token halves (each inside one cache block, since
 //              block_size % 32 == 0) of 4 latent boxes (64 columns) and one
 //              rope box (32 columns), through the block table;
@@ -52,15 +54,15 @@
 // (exact: P keeps the older reference max).
 //
 // Shared memory per CTA (1024-byte aligned regions):
-//   Q     4 latent chunks [128 heads][128 B] (128-byte swizzle) + rope half
-//         [128 heads][64 B] (64-byte swizzle)                         72 KB
-//   K/V   3 stages x (4 latent chunks [64 tokens][128 B] + rope half
-//         [64 tokens][64 B])                                          108 KB
+//   Qr    rope half of the query [128 heads][64 B] (64-byte swizzle)    8 KB
+//   K/V   4 stages x (4 latent chunks [64 tokens][128 B] + rope half
+//         [64 tokens][64 B])                                          144 KB
 //   X     2 buffers of the peer's partial scores, [9 chunks][128 heads]
 //         [16 B]: 8 chunks of 8 int16 scores, then the row's exponent E, so
 //         that one warp-wide store or load covers 512 contiguous bytes 36 KB
-// TMEM: S buffers at columns 0 and 64, P buffers (bf16 pairs) at 128 and 160,
-// O half at columns 256-511.
+//   P     2 buffers [128 heads][64 tokens] bf16 (128-byte swizzle)     32 KB
+// TMEM: S buffers at columns 0 and 64, the query's latent half (bf16 pairs)
+// at 128-255, O half at columns 256-511.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math_constants.h>
