@@ -131,6 +131,23 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(values, dist=None, device=None):
+    """Element-wise maximum of this rank's timings (a list of floats) over the
+    process group -- the slowest replica sets the job's time; unchanged on a
+    single process."""
+    if dist is None:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def replica_rate(world, bytes_per_step, steps, seconds):
+    """Whole-job GB/s of `world` replicas that each moved bytes_per_step per
+    step for `steps` steps in `seconds` (the slowest rank's time)."""
+    return world * bytes_per_step * steps / seconds / 1e9
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -616,19 +633,17 @@ def main():
         dist.barrier()
     clk = clocks.stop()
     total_ms = t_start.elapsed_time(t_end)
-    if dist is not None:
-        t = torch.tensor([total_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    ms_per_step = total_ms / args.steps
-    value = world * kv_bytes * args.steps / (total_ms * 1e-3) / 1e9
     dec_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
     achieved = kv_bytes / (dec_ms * 1e-3) / 1e9
     sha = kernel_source_sha(["decode.cu", "pa_common.cuh"])
     traffic = profiled_traffic("decode_splitkv_gqa_decode.md", sha)
 
     e2e_dt, h2d, d2h, e2e_launch = run_e2e(pa, b, step, args.steps, warmup, device)
-    e2e_value = world * kv_bytes * args.steps / e2e_dt / 1e9
+    # The job's times are the slowest replica's.
+    total_ms, e2e_dt = max_over_ranks([total_ms, e2e_dt], dist, device)
+    ms_per_step = total_ms / args.steps
+    value = replica_rate(world, kv_bytes, args.steps, total_ms * 1e-3)
+    e2e_value = replica_rate(world, kv_bytes, args.steps, e2e_dt)
 
     sec = None
     if not args.no_secondary and rank == 0:
