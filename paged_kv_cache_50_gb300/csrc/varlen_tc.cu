@@ -54,9 +54,10 @@
 namespace pa {
 
 // DK: width of queries and keys; DV: width of values and outputs; BN: tokens
-// per K/V tile.
-template <int DK, int DV, int BN>
+// per K/V tile; VST: V stages (2, or 1 where two do not fit).
+template <int DK, int DV, int BN, int VST = 2>
 struct TcCfg {
+  static constexpr int kVStages = VST;
   static constexpr int kBM = 128;                     // rows per Q tile
   static constexpr int kRows = 2 * kBM;               // packed rows per CTA
   static constexpr int kBN = BN;                      // tokens per K/V tile
@@ -68,7 +69,7 @@ struct TcCfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = 2 * kQBytes;
   static constexpr int kOffV = kOffK + 2 * kKBytes;
-  static constexpr int kOffBar = kOffV + 2 * kVBytes;
+  static constexpr int kOffBar = kOffV + VST * kVBytes;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;   // barriers + alignment slack
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kThreads = 384;
@@ -149,11 +150,11 @@ constexpr int kPieceRing = 4;
 // MLA = true: keys and values come from the contiguous expanded workspaces
 // of the MLA prefill (k_map over [N * s_max][H][DK], v_map over
 // [N * s_max][H][DV]) instead of the paged pool; no block table.
-template <int DK, int DV, int BN, int CL, bool EXT, bool MLA>
+template <int DK, int DV, int BN, int VST, int CL, bool EXT, bool MLA>
 __global__ void __launch_bounds__(384, 1)
 varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap v_map,
                  const __grid_constant__ VarlenArgs a) {
-  using C = TcCfg<DK, DV, BN>;
+  using C = TcCfg<DK, DV, BN, VST>;
   const __nv_bfloat16* __restrict__ q = a.q;
   const int32_t* __restrict__ block_table = a.block_table;
   const int Hq = a.Hq, Hkv = a.Hkv, bs = a.bs, num_blocks = a.num_blocks;
@@ -391,8 +392,8 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
         // Threads past the tile's kBN rows own no V row.
         const bool row_ok = t >= C::kBN || (tok < seq && ((vm >> (t >> 4)) & 1u));
         if (!row_ok) {
-          if (!tc::mbar_wait(BAR(kVFull + (j & 1)), (j >> 1) & 1)) fail();
-          const uint32_t vbase = sbase + C::kOffV + (j & 1) * C::kVBytes;
+          if (!tc::mbar_wait(BAR(kVFull + j % C::kVStages), (j / C::kVStages) & 1)) fail();
+          const uint32_t vbase = sbase + C::kOffV + (j % C::kVStages) * C::kVBytes;
 #pragma unroll
           for (int h = 0; h < C::kHalvesV; ++h)
 #pragma unroll
@@ -509,7 +510,7 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
       // O_x += P_x(j) V(j) over the 16-token steps [k0, k0 + 4); P_x is read
       // from TMEM, 8 columns (16 bf16) per step.
       auto issue_pv = [&](int xq, int j, int k0) {
-        const uint32_t vs = sbase + C::kOffV + (j & 1) * C::kVBytes;
+        const uint32_t vs = sbase + C::kOffV + (j % C::kVStages) * C::kVBytes;
 #pragma unroll
         for (int k = k0; k < k0 + C::kBN / 32; ++k)
           tc::mma_bf16_ts(tmem + C::col_o(xq), tmem + C::col_s(xq) + k * 8,
@@ -529,7 +530,7 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
       for (int j = 0; ok && j < ntiles; ++j) {
         if (*abort_flag) { ok = false; break; }
         const bool more = j + 1 < ntiles;
-        if (!tc::mbar_wait(BAR(kVFull + (j & 1)), (j >> 1) & 1)) { ok = false; break; }
+        if (!tc::mbar_wait(BAR(kVFull + j % C::kVStages), (j / C::kVStages) & 1)) { ok = false; break; }
         if (more && !wait_k(j + 1)) { ok = false; break; }
         for (int xq = 0; xq < 2 && ok; ++xq) {
           if (!tc::mbar_wait(BAR(kPLo + xq), j & 1)) { ok = false; break; }
@@ -542,7 +543,7 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
           if (more) issue_s(xq, j + 1);
         }
         if (!ok) break;
-        release(BAR(kVEmpty + (j & 1)));
+        release(BAR(kVEmpty + j % C::kVStages));
         if (more) release(BAR(kKEmpty + ((j + 1) & 1)));
       }
       if (!ok && !*abort_flag) fail();
@@ -620,9 +621,10 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
       return true;
     };
     auto issue_v = [&](int j, int blk) -> bool {
-      const int st = j & 1;
-      if (j >= 2 && !wait_all(BAR(kVEmpty + st), ((j >> 1) - 1) & 1)) return false;
-      issue(j, blk, 1, sbase + C::kOffV + st * C::kVBytes, BAR(kVFull + st));
+      const int vst = j % C::kVStages;
+      if (j >= C::kVStages && !wait_all(BAR(kVEmpty + vst), ((j / C::kVStages) - 1) & 1))
+        return false;
+      issue(j, blk, 1, sbase + C::kOffV + vst * C::kVBytes, BAR(kVFull + vst));
       return true;
     };
     int r0 = raw_of(0), r1 = raw_of(1), r2 = raw_of(2);   // tiles j, j+1, j+2 (raw)
@@ -649,8 +651,8 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
       // No copy may still be landing when the CTA exits.
       for (int j = max(0, k_issued - 2); j < k_issued; ++j)
         if (!tc::mbar_wait(BAR(kKFull + (j & 1)), (j >> 1) & 1)) fail();
-      for (int j = max(0, v_issued - 2); j < v_issued; ++j)
-        if (!tc::mbar_wait(BAR(kVFull + (j & 1)), (j >> 1) & 1)) fail();
+      for (int j = max(0, v_issued - C::kVStages); j < v_issued; ++j)
+        if (!tc::mbar_wait(BAR(kVFull + j % C::kVStages), (j / C::kVStages) & 1)) fail();
     }
   } else {
     tc::cluster_wait();   // idle warps
@@ -720,9 +722,9 @@ bool make_ws_map(CUtensorMap* map, const void* ws, long long rows, int H, int wi
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int DK, int DV, int BN, int CL, bool EXT, bool MLA>
+template <int DK, int DV, int BN, int VST, int CL, bool EXT, bool MLA>
 static cudaError_t launch_varlen_tc_t(const VarlenLaunch& L, cudaStream_t stream) {
-  using C = TcCfg<DK, DV, BN>;
+  using C = TcCfg<DK, DV, BN, VST>;
   CUtensorMap map, vmap;
   if (MLA) {
     const long long rows = static_cast<long long>(L.N) * L.mla_s_max;
@@ -732,7 +734,7 @@ static cudaError_t launch_varlen_tc_t(const VarlenLaunch& L, cudaStream_t stream
     if (!make_kv_map(&map, L.cache, L.num_blocks, L.bs, L.Hkv, DK)) return cudaErrorInvalidValue;
     vmap = map;
   }
-  auto kern = varlen_tc_kernel<DK, DV, BN, CL, EXT, MLA>;
+  auto kern = varlen_tc_kernel<DK, DV, BN, VST, CL, EXT, MLA>;
   static DeviceFlags attr_set;
   cudaError_t e = set_smem_once(kern, C::kSmemBytes, attr_set);
   if (e != cudaSuccess) return e;
@@ -800,14 +802,14 @@ constexpr int kVarlenCluster = 1;
 
 cudaError_t launch_varlen_tc(const VarlenLaunch& L, cudaStream_t stream) {
   if (L.mla_k != nullptr)   // MLA prefill attention: [nope | rope] keys, 128-wide values
-    return launch_varlen_tc_t<192, 128, 64, kVarlenCluster, false, true>(L, stream);
+    return launch_varlen_tc_t<192, 128, 128, 1, kVarlenCluster, false, true>(L, stream);
   const bool ext = L.window > 0 || L.kv_splits > 1 || L.ws != nullptr || L.virt_total_q > 0 ||
                    L.table_col0 != 0 || L.seq_off != 0;
   if (L.d == 128)
-    return ext ? launch_varlen_tc_t<128, 128, 128, kVarlenCluster, true, false>(L, stream)
-               : launch_varlen_tc_t<128, 128, 128, kVarlenCluster, false, false>(L, stream);
-  return ext ? launch_varlen_tc_t<64, 64, 128, kVarlenCluster, true, false>(L, stream)
-             : launch_varlen_tc_t<64, 64, 128, kVarlenCluster, false, false>(L, stream);
+    return ext ? launch_varlen_tc_t<128, 128, 128, 2, kVarlenCluster, true, false>(L, stream)
+               : launch_varlen_tc_t<128, 128, 128, 2, kVarlenCluster, false, false>(L, stream);
+  return ext ? launch_varlen_tc_t<64, 64, 128, 2, kVarlenCluster, true, false>(L, stream)
+             : launch_varlen_tc_t<64, 64, 128, 2, kVarlenCluster, false, false>(L, stream);
 }
 
 }  // namespace pa
