@@ -17,7 +17,9 @@
 // request).  The chunk's 128 latent rows (128 KB, eight 64-column 128-byte
 // swizzled slabs) are gathered once through the block table with TMA and
 // stay resident; each head's 256 x 512 weight slice streams through a
-// two-stage ring of 64-column slabs (32 KB).  One thread issues
+// three-stage ring of 64-column slabs (32 KB each; two stages left the L2
+// latency of a slab exposed: a slab feeds only 512 cycles of MMAs).  One
+// thread issues
 // D[128 x 256] = C W_h^T (M = 128 tokens, N = dn + dv = 256, K = 512) into one
 // of two 256-column TMEM buffers, so the epilogue of head h (four warps, one
 // token row per thread: TMEM -> bf16 -> global) overlaps the MMAs of head
@@ -44,7 +46,7 @@ struct MlaExpCfg {
   static constexpr int kABytes = kM * kR * 2;           // 128 KB
   static constexpr int kASlab = kM * 128;               // 16 KB
   static constexpr int kWSlab = kN * 128;               // 32 KB
-  static constexpr int kWStages = 2;
+  static constexpr int kWStages = 3;
   static constexpr int kOffA = 0;
   static constexpr int kOffW = kABytes;
   static constexpr int kOffBar = kOffW + kWStages * kWSlab;
@@ -54,13 +56,13 @@ struct MlaExpCfg {
 };
 
 enum MlaExpBar {
-  kEAFull = 0,     // the latent tile has landed
-  kEWFull = 1,     // [2] weight slab stage
-  kEWEmpty = 3,    // [2]
-  kEDFull = 5,     // [2] head accumulator buffer complete
-  kEDEmpty = 7,    // [2] buffer read out by the epilogue
-  kEFinal = 9,
-  kENumBars = 10
+  kEAFull = 0,                                 // the latent tile has landed
+  kEWFull = 1,                                 // [kWStages] weight slab stage
+  kEWEmpty = kEWFull + MlaExpCfg::kWStages,    // [kWStages]
+  kEDFull = kEWEmpty + MlaExpCfg::kWStages,    // [2] head accumulator buffer complete
+  kEDEmpty = kEDFull + 2,                      // [2] buffer read out by the epilogue
+  kEFinal = kEDEmpty + 2,
+  kENumBars = kEFinal + 1
 };
 
 __global__ void __launch_bounds__(192, 1)
@@ -95,9 +97,11 @@ mla_expand_kernel(const __grid_constant__ CUtensorMap lat_map,
 
   if (threadIdx.x == 0) {
     tc::mbar_init(BAR(kEAFull), 1);
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < C::kWStages; ++b) {
       tc::mbar_init(BAR(kEWFull + b), 1);
       tc::mbar_init(BAR(kEWEmpty + b), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
       tc::mbar_init(BAR(kEDFull + b), 1);
       tc::mbar_init(BAR(kEDEmpty + b), 128);
     }
@@ -143,13 +147,14 @@ mla_expand_kernel(const __grid_constant__ CUtensorMap lat_map,
         tc::tma_load_3d(sbase + C::kOffA + k * C::kASlab + p * 16 * 128, &lat_map, BAR(kEAFull),
                         k * 64, tok % bs, blk);
     }
-    // Weight slabs through the two-stage ring.
+    // Weight slabs through the three-stage ring.
     if (lane == 0) {
       int issued = 0;
       for (int n = 0; n < n_slabs; ++n) {
         if (*abort_flag) break;
-        const int st = n & 1;
-        if (n >= 2 && !tc::mbar_wait(BAR(kEWEmpty + st), ((n >> 1) - 1) & 1)) {
+        const int st = n % C::kWStages;
+        if (n >= C::kWStages &&
+            !tc::mbar_wait(BAR(kEWEmpty + st), ((n / C::kWStages) - 1) & 1)) {
           fail();
           break;
         }
@@ -161,8 +166,8 @@ mla_expand_kernel(const __grid_constant__ CUtensorMap lat_map,
       }
       // No copy may still be landing when the CTA exits.
       if (!tc::mbar_wait(BAR(kEAFull), 0)) fail();
-      for (int n = max(0, issued - 2); n < issued; ++n)
-        if (!tc::mbar_wait(BAR(kEWFull + (n & 1)), (n >> 1) & 1)) fail();
+      for (int n = max(0, issued - C::kWStages); n < issued; ++n)
+        if (!tc::mbar_wait(BAR(kEWFull + n % C::kWStages), (n / C::kWStages) & 1)) fail();
     }
   } else if (warp == 0) {
     // ------------------------------------------------------------ MMA issue
@@ -201,8 +206,8 @@ mla_expand_kernel(const __grid_constant__ CUtensorMap lat_map,
         }
         tc::tc_fence_after();
         for (int k = 0; k < C::kSlabs; ++k) {
-          const int n = j * C::kSlabs + k, st = n & 1;
-          if (*abort_flag || !tc::mbar_wait(BAR(kEWFull + st), (n >> 1) & 1)) {
+          const int n = j * C::kSlabs + k, st = n % C::kWStages;
+          if (*abort_flag || !tc::mbar_wait(BAR(kEWFull + st), (n / C::kWStages) & 1)) {
             fail();
             ok = false;
             break;
