@@ -83,6 +83,8 @@ def test_mla_expand_matches_oracle(pa, heads, bs):
     pool = _written_pool(b)
     S = int(b.seq_lens.max())
     k_ws, v_ws = pa.mla_prefill_workspace(b.num_seqs, S, heads)
+    k_ws.zero_()   # rows past each sequence are not written; keep them finite for the copy
+    v_ws.zero_()
     pa.pa_mla_expand_kv(to_dev_bf16(pool), to_dev_bf16(b.w_kv_b), to_dev(b.block_table, torch.int32),
                         to_dev(b.seq_lens, torch.int32), k_ws, v_ws)
     torch.cuda.synchronize()
