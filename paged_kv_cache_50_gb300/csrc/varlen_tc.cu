@@ -101,6 +101,22 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Packed fp32 pairs (one instruction for two lanes' worth of work, each
+// half rounded as its scalar counterpart): (x, y) = (a0 b + c, a1 b + c) and
+// (x, y) += (a0, a1).
+__device__ __forceinline__ void ffma2(float& x, float& y, float a0, float a1, float b, float c) {
+  asm("{\n.reg .b64 a, b, c, d;\nmov.b64 a, {%2, %3};\nmov.b64 b, {%4, %4};\n"
+      "mov.b64 c, {%5, %5};\nfma.rn.f32x2 d, a, b, c;\nmov.b64 {%0, %1}, d;\n}"
+      : "=f"(x), "=f"(y)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+__device__ __forceinline__ void fadd2(float& x, float& y, float a0, float a1) {
+  asm("{\n.reg .b64 a, b;\nmov.b64 a, {%0, %1};\nmov.b64 b, {%2, %3};\n"
+      "add.rn.f32x2 a, a, b;\nmov.b64 {%0, %1}, a;\n}"
+      : "+f"(x), "+f"(y)
+      : "f"(a0), "f"(a1));
+}
+
 // Barriers; pairs are indexed by stage (j & 1) or by Q tile x.
 enum TcBar {
   kQFull = 0,
@@ -408,6 +424,7 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
       // columns of the S row, published in two halves (tokens 0-63, 64-127)
       // so that the first half of PV_x(j) runs while the second is computed.
       {
+        // Row sums in eight partial sums, four packed pairs.
         float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c16 = 0; c16 < C::kBN / 32; ++c16) {
@@ -415,9 +432,11 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int c = c16 * 16 + e;
-            const float p0 = ex2(fmaf(s[2 * c], scale_log2, -mu));
-            const float p1 = ex2(fmaf(s[2 * c + 1], scale_log2, -mu));
-            l8[e & 7] += p0 + p1;
+            float x0, x1;
+            ffma2(x0, x1, s[2 * c], s[2 * c + 1], scale_log2, -mu);
+            const float p0 = ex2(x0);
+            const float p1 = ex2(x1);
+            fadd2(l8[2 * (e & 3)], l8[2 * (e & 3) + 1], p0, p1);
             pk[e] = pack_bf16(p0, p1);
           }
           tc::tmem_st16(ts + c16 * 16, pk);
