@@ -325,7 +325,8 @@ pa_status pa_mla_cache_write(const void* kv_c, const void* k_pe, void* kv_cache,
  * pa_mla_prefill_workspace_bytes bytes).  max_seq_len >= every seq_lens[i]
  * (a shorter one is the caller's error: tokens past it are not expanded).
  * A block id outside [0, num_blocks) sets PA_DEVERR_BLOCK_ID and its tokens
- * expand as zero latents.  All pointers 16-byte aligned.
+ * expand as zero latents.  k_ws and v_ws 32-byte aligned (rows are written
+ * with 32-byte stores), the other pointers 16-byte aligned.
  */
 size_t pa_mla_prefill_workspace_bytes(int num_seqs, int max_seq_len, int num_heads);
 pa_status pa_mla_expand_kv(const void* kv_cache, const void* w_kv_b, const int32_t* block_table,
@@ -344,7 +345,8 @@ pa_status pa_mla_expand_kv(const void* kv_cache, const void* w_kv_b, const int32
  * q: [total_q, num_heads, 192] bf16 ([q_nope | q_pe]); out: [total_q,
  * num_heads, 128] bf16; lse: [total_q, num_heads] fp32, nullable.
  * query_start_loc, seq_lens, max_query_len as for pa_varlen_fwd; the new
- * tokens must already be in kv_cache (pa_mla_cache_write).
+ * tokens must already be in kv_cache (pa_mla_cache_write).  workspace
+ * 32-byte aligned; q, kv_cache, w_kv_b and out 16-byte aligned.
  */
 pa_status pa_mla_prefill(const void* q, const void* kv_cache, const void* w_kv_b,
                          const int32_t* block_table, const int32_t* query_start_loc,

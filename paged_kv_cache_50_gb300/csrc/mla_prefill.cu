@@ -23,7 +23,9 @@
 // D[128 x 256] = C W_h^T (M = 128 tokens, N = dn + dv = 256, K = 512) into one
 // of two 256-column TMEM buffers, so the epilogue of head h (four warps, one
 // token row per thread: TMEM -> bf16 -> global) overlaps the MMAs of head
-// h + 1.
+// h + 1.  The epilogue writes each row with 32-byte stores: a warp's store
+// touches 32 rows (one per thread), and whole sectors halve the store
+// transactions against 16-byte ones.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -64,6 +66,13 @@ enum MlaExpBar {
   kEFinal = kEDEmpty + 2,
   kENumBars = kEFinal + 1
 };
+
+// 32 bytes to global memory in one store (32-byte aligned address).
+__device__ __forceinline__ void st_global_v8(uint32_t* p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+               "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
 
 __global__ void __launch_bounds__(192, 1)
 mla_expand_kernel(const __grid_constant__ CUtensorMap lat_map,
@@ -253,29 +262,41 @@ mla_expand_kernel(const __grid_constant__ CUtensorMap lat_map,
         break;
       }
       tc::tc_fence_after();
-      uint4* kdst = reinterpret_cast<uint4*>(k_ws + (tok * H + h) * (C::kDn + C::kDr));
-      uint4* vdst = reinterpret_cast<uint4*>(v_ws + (tok * H + h) * C::kDv);
+      // 32-byte stores (one whole sector each): the thread's row is 384 bytes
+      // of K (k_nope | k_pe) and 256 of V, both 32-byte aligned.
+      uint32_t* kdst = reinterpret_cast<uint32_t*>(k_ws + (tok * H + h) * (C::kDn + C::kDr));
+      uint32_t* vdst = reinterpret_cast<uint32_t*>(v_ws + (tok * H + h) * C::kDv);
 #pragma unroll
-      for (int c = 0; c < C::kN / 32; ++c) {
-        uint32_t r[32];
-        tc::tmem_ld32(tmem + lane_base + b * 256 + c * 32, r);
+      for (int c2 = 0; c2 < C::kN / 64; ++c2) {
+        uint32_t r[2][32];
+        tc::tmem_ld32(tmem + lane_base + b * 256 + c2 * 64, r[0]);
+        tc::tmem_ld32(tmem + lane_base + b * 256 + c2 * 64 + 32, r[1]);
         tc::tmem_wait_ld();
         if (valid) {
-          uint4* dst = c < C::kDn / 32 ? kdst + c * 4 : vdst + (c - C::kDn / 32) * 4;
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 w;
-            w.x = pack_bf16(__uint_as_float(r[v * 8 + 0]), __uint_as_float(r[v * 8 + 1]));
-            w.y = pack_bf16(__uint_as_float(r[v * 8 + 2]), __uint_as_float(r[v * 8 + 3]));
-            w.z = pack_bf16(__uint_as_float(r[v * 8 + 4]), __uint_as_float(r[v * 8 + 5]));
-            w.w = pack_bf16(__uint_as_float(r[v * 8 + 6]), __uint_as_float(r[v * 8 + 7]));
-            dst[v] = w;
+          for (int u = 0; u < 2; ++u) {
+            const int c = 2 * c2 + u;   // 32 columns: 64 bytes of bf16
+            uint32_t* dst = c < C::kDn / 32 ? kdst + c * 16 : vdst + (c - C::kDn / 32) * 16;
+#pragma unroll
+            for (int v = 0; v < 2; ++v) {
+              uint32_t w[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                w[e] = pack_bf16(__uint_as_float(r[u][v * 16 + 2 * e]),
+                                 __uint_as_float(r[u][v * 16 + 2 * e + 1]));
+              st_global_v8(dst + v * 8, w);
+            }
           }
         }
       }
       if (valid) {
 #pragma unroll
-        for (int c = 0; c < C::kDr / 8; ++c) kdst[C::kDn / 8 + c] = kpe[c];
+        for (int c = 0; c < C::kDr / 16; ++c) {
+          const uint32_t w[8] = {kpe[2 * c].x, kpe[2 * c].y, kpe[2 * c].z, kpe[2 * c].w,
+                                 kpe[2 * c + 1].x, kpe[2 * c + 1].y, kpe[2 * c + 1].z,
+                                 kpe[2 * c + 1].w};
+          st_global_v8(kdst + C::kDn / 2 + c * 8, w);
+        }
       }
       tc::tc_fence_before();
       tc::mbar_arrive(BAR(kEDEmpty + b));
@@ -340,7 +361,6 @@ bool make_weight_map(CUtensorMap* map, const void* w, int H) {
 // Heads per CTA of the expansion: a CTA reuses its resident latent tile for
 // this many heads' weight slices.
 constexpr int kMlaExpandHeads = 16;
-
 cudaError_t launch_mla_expand(const void* pool, const void* w_kv_b, const int32_t* block_table,
                               const int32_t* seq_lens, int N, int H, int bs, int num_blocks,
                               int max_blocks, int max_seq_len, int s_max, void* k_ws, void* v_ws,

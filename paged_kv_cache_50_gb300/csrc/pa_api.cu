@@ -157,7 +157,8 @@ pa_status pa_mla_expand_kv(const void* kv_cache, const void* w_kv_b, const int32
   if (kv_cache == nullptr || w_kv_b == nullptr || block_table == nullptr ||
       seq_lens == nullptr || k_ws == nullptr || v_ws == nullptr)
     return PA_ERR_INVALID;
-  if (!aligned(kv_cache, 16) || !aligned(w_kv_b, 16) || !aligned(k_ws, 16) || !aligned(v_ws, 16))
+  // The expansion writes its rows with 32-byte stores.
+  if (!aligned(kv_cache, 16) || !aligned(w_kv_b, 16) || !aligned(k_ws, 32) || !aligned(v_ws, 32))
     return PA_ERR_INVALID;
   return from_cuda(pa::launch_mla_expand(kv_cache, w_kv_b, block_table, seq_lens, num_seqs,
                                          num_heads, block_size, num_blocks, max_blocks_per_seq,
@@ -180,7 +181,7 @@ pa_status pa_mla_prefill(const void* q, const void* kv_cache, const void* w_kv_b
       query_start_loc == nullptr || seq_lens == nullptr || workspace == nullptr || out == nullptr)
     return PA_ERR_INVALID;
   if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(w_kv_b, 16) ||
-      !aligned(workspace, 16) || !aligned(out, 16) || !aligned(lse, 4))
+      !aligned(workspace, 32) || !aligned(out, 16) || !aligned(lse, 4))
     return PA_ERR_INVALID;
   const long long rows = static_cast<long long>(num_seqs) * max_seq_len;
   if (rows * num_heads > INT_MAX) return PA_ERR_INVALID;   // 3-D map row coordinate

@@ -212,6 +212,18 @@ def test_mla_cache_write_rejects(pa):
     assert L.pa_mla_cache_write(NULL, NULL, NULL, NULL, 0, 512, 64, 64, 8, NULL) == pa.PA_OK
 
 
+def test_mla_prefill_workspace_alignment(pa):
+    # The expansion writes workspace rows with 32-byte stores: 16-byte
+    # aligned workspaces are refused before anything is launched.
+    L = pa.lib()
+    assert L.pa_mla_expand_kv(16, 16, 16, 16, 2, 16, 64, 8, 4, 100, 48, 64, NULL) == \
+        pa.PA_ERR_INVALID
+    assert L.pa_mla_expand_kv(16, 16, 16, 16, 2, 16, 64, 8, 4, 100, 64, 80, NULL) == \
+        pa.PA_ERR_INVALID
+    assert L.pa_mla_prefill(16, 16, 16, 16, 16, 16, 8, 4, 2, 16, 64, 8, 4, 100, 0.1, 1, 48, 16,
+                            NULL, NULL) == pa.PA_ERR_INVALID
+
+
 def test_window_and_cascade_reject(pa):
     L = pa.lib()
     s = _shape(pa)
