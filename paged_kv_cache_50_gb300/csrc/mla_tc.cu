@@ -160,11 +160,6 @@ __device__ __forceinline__ uint32_t pack_q16(float lo, float hi, float mul) {
   return (static_cast<uint32_t>(a) & 0xffffu) | (static_cast<uint32_t>(b) << 16);
 }
 
-// The signed 16-bit value q times `unit`, exactly (|q| < 2^15, unit a power
-// of two).
-__device__ __forceinline__ float dequant(int q, float unit, float bias_unit) {
-  return fmaf(__int_as_float(kRoundBiasBits + q), unit, -bias_unit);
-}
 
 __global__ void __launch_bounds__(352, 1)
 mla_tc_kernel(const __nv_bfloat16* __restrict__ q, const __grid_constant__ CUtensorMap qr_map,
@@ -335,9 +330,15 @@ mla_tc_kernel(const __nv_bfloat16* __restrict__ q, const __grid_constant__ CUten
                        : "memory");
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
+            // The pair's two int16 values q times `unit`, exactly (|q| <
+            // 2^15, unit a power of two): the float with bits bias + q is
+            // 1.5 * 2^23 + q, so (that * unit - bias_unit) = q * unit.  Then
+            // added to this CTA's partial scores; both steps as packed pairs.
             const int lo = static_cast<int>(v[e] << 16) >> 16, hi = static_cast<int>(v[e]) >> 16;
-            sc[8 * c + 2 * e] += dequant(lo, unit, bias_unit);
-            sc[8 * c + 2 * e + 1] += dequant(hi, unit, bias_unit);
+            float d0, d1;
+            ffma2(d0, d1, __int_as_float(kRoundBiasBits + lo), __int_as_float(kRoundBiasBits + hi),
+                  unit, -bias_unit);
+            fadd2(sc[8 * c + 2 * e], sc[8 * c + 2 * e + 1], d0, d1);
           }
         }
       }
@@ -420,10 +421,11 @@ mla_tc_kernel(const __nv_bfloat16* __restrict__ q, const __grid_constant__ CUten
           uint32_t pk[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float p0 = mex2(fmaf(sc[8 * c + 2 * e], scale_log2, -mu));
-            const float p1 = mex2(fmaf(sc[8 * c + 2 * e + 1], scale_log2, -mu));
-            l8[(2 * e) & 7] += p0;
-            l8[(2 * e + 1) & 7] += p1;
+            float x0, x1;
+            ffma2(x0, x1, sc[8 * c + 2 * e], sc[8 * c + 2 * e + 1], scale_log2, -mu);
+            const float p0 = mex2(x0);
+            const float p1 = mex2(x1);
+            fadd2(l8[2 * e], l8[2 * e + 1], p0, p1);
             pk[e] = pack_bf16(p0, p1);
           }
           asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(pb + msw128(t, c)),

@@ -141,6 +141,22 @@ inline long long split_chunk(int max_seq_len, int S, int bs) {
   return ((per + bs - 1) / bs) * bs;
 }
 
+// Packed fp32 pairs (sm_100 and later: one instruction does the work of two,
+// each half rounded as its scalar counterpart): (x, y) = (a0 b + c, a1 b + c)
+// and (x, y) += (a0, a1).
+__device__ __forceinline__ void ffma2(float& x, float& y, float a0, float a1, float b, float c) {
+  asm("{\n.reg .b64 a, b, c, d;\nmov.b64 a, {%2, %3};\nmov.b64 b, {%4, %4};\n"
+      "mov.b64 c, {%5, %5};\nfma.rn.f32x2 d, a, b, c;\nmov.b64 {%0, %1}, d;\n}"
+      : "=f"(x), "=f"(y)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+__device__ __forceinline__ void fadd2(float& x, float& y, float a0, float a1) {
+  asm("{\n.reg .b64 a, b;\nmov.b64 a, {%0, %1};\nmov.b64 b, {%2, %3};\n"
+      "add.rn.f32x2 a, a, b;\nmov.b64 {%0, %1}, a;\n}"
+      : "+f"(x), "+f"(y)
+      : "f"(a0), "f"(a1));
+}
+
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 

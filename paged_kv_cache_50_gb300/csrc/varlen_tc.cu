@@ -101,22 +101,6 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Packed fp32 pairs (one instruction for two lanes' worth of work, each
-// half rounded as its scalar counterpart): (x, y) = (a0 b + c, a1 b + c) and
-// (x, y) += (a0, a1).
-__device__ __forceinline__ void ffma2(float& x, float& y, float a0, float a1, float b, float c) {
-  asm("{\n.reg .b64 a, b, c, d;\nmov.b64 a, {%2, %3};\nmov.b64 b, {%4, %4};\n"
-      "mov.b64 c, {%5, %5};\nfma.rn.f32x2 d, a, b, c;\nmov.b64 {%0, %1}, d;\n}"
-      : "=f"(x), "=f"(y)
-      : "f"(a0), "f"(a1), "f"(b), "f"(c));
-}
-__device__ __forceinline__ void fadd2(float& x, float& y, float a0, float a1) {
-  asm("{\n.reg .b64 a, b;\nmov.b64 a, {%0, %1};\nmov.b64 b, {%2, %3};\n"
-      "add.rn.f32x2 a, a, b;\nmov.b64 {%0, %1}, a;\n}"
-      : "+f"(x), "+f"(y)
-      : "f"(a0), "f"(a1));
-}
-
 // Barriers; pairs are indexed by stage (j & 1) or by Q tile x.
 enum TcBar {
   kQFull = 0,
