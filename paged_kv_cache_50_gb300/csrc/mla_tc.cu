@@ -151,15 +151,18 @@ __device__ __forceinline__ uint32_t xoff(int t, int c) {
 constexpr float kRoundBias = 12582912.0f;       // 1.5 * 2^23
 constexpr int kRoundBiasBits = 0x4B400000;
 
-// x * mul rounded to the nearest int16 (saturating), two per 32-bit word.
+// x * mul rounded to the nearest integer q (nearest even), two per 32-bit
+// word as int16, for |x * mul| < 2^15.  The float bias + q has q in its low
+// 16 bits (two's complement: the bias's own low 16 bits are zero), so one
+// byte permute packs the pair; only +32768 (a value just under 2^15 rounded
+// up) falls outside int16 and is clamped to 32767.
 __device__ __forceinline__ uint32_t pack_q16(float lo, float hi, float mul) {
-  int a = __float_as_int(fmaf(lo, mul, kRoundBias)) - kRoundBiasBits;
-  int b = __float_as_int(fmaf(hi, mul, kRoundBias)) - kRoundBiasBits;
-  a = min(max(a, -32767), 32767);
-  b = min(max(b, -32767), 32767);
-  return (static_cast<uint32_t>(a) & 0xffffu) | (static_cast<uint32_t>(b) << 16);
+  float a, b;
+  ffma2(a, b, lo, hi, mul, kRoundBias);
+  a = fminf(a, kRoundBias + 32767.f);
+  b = fminf(b, kRoundBias + 32767.f);
+  return __byte_perm(__float_as_uint(a), __float_as_uint(b), 0x5410);
 }
-
 
 __global__ void __launch_bounds__(352, 1)
 mla_tc_kernel(const __nv_bfloat16* __restrict__ q, const __grid_constant__ CUtensorMap qr_map,
@@ -520,13 +523,24 @@ mla_tc_kernel(const __nv_bfloat16* __restrict__ q, const __grid_constant__ CUten
       tc::mbar_arrive(BAR(kMSRead + buf));
       const int nvis = min(C::kBN, t1 - (t0 + j * C::kBN));
       float v[C::kBN];
-      float amax = 0.f;
 #pragma unroll
-      for (int e = 0; e < C::kBN; ++e) {
-        const bool vis = e < nvis && ((vm >> (e >> 5)) & 1u);
-        v[e] = vis ? __uint_as_float(r[e >> 5][e & 31]) : 0.f;
-        amax = fmaxf(amax, fabsf(v[e]));
+      for (int e = 0; e < C::kBN; ++e) v[e] = __uint_as_float(r[e >> 5][e & 31]);
+      if (nvis < C::kBN || vm != 0x3u) {
+#pragma unroll
+        for (int e = 0; e < C::kBN; ++e) {
+          const bool vis = e < nvis && ((vm >> (e >> 5)) & 1u);
+          v[e] = vis ? v[e] : 0.f;
+        }
       }
+      float a8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) a8[k] = fmaxf(fabsf(v[k]), fabsf(v[8 + k]));
+#pragma unroll
+      for (int e = 16; e < C::kBN; e += 16)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) a8[k] = mmax3(a8[k], fabsf(v[e + k]), fabsf(v[e + 8 + k]));
+      const float amax = mmax3(mmax3(a8[0], a8[1], a8[2]), mmax3(a8[3], a8[4], a8[5]),
+                               fmaxf(a8[6], a8[7]));
       // E with max |v| < 2^E (E = -100 for an all-zero row), and 2^(15 - E).
       const int ebits = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu);
       const int e_row = ebits == 0 ? -100 : min(ebits - 126, 127);
