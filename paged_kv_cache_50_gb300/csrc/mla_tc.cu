@@ -144,23 +144,22 @@ __device__ __forceinline__ uint32_t xoff(int t, int c) {
   return static_cast<uint32_t>(c * 2048 + t * 16);
 }
 
-// Integer <-> float conversions through the 1.5 * 2^23 bias: adding it to a
-// float of magnitude below 2^22 rounds to an integer (nearest even) held in
-// the low mantissa bits, and the reverse subtraction is exact.  This keeps
-// the exchange on the FMA / integer pipes.
-constexpr float kRoundBias = 12582912.0f;       // 1.5 * 2^23
-constexpr int kRoundBiasBits = 0x4B400000;
-
-// x * mul rounded to the nearest integer q (nearest even), two per 32-bit
-// word as int16, for |x * mul| < 2^15.  The float bias + q has q in its low
-// 16 bits (two's complement: the bias's own low 16 bits are zero), so one
-// byte permute packs the pair; only +32768 (a value just under 2^15 rounded
-// up) falls outside int16 and is clamped to 32767.
+// The exchange's 16-bit fixed point, offset binary: a partial score x with
+// |x| < 2^E travels as u = q + 32768, q = x * 2^(15-E) rounded to the
+// nearest integer (nearest even; +32768 clamped to 32767), two per 32-bit
+// word.  Integer <-> float conversions go through a bias, which keeps the
+// exchange on the FMA and integer pipes: x * 2^(15-E) + (1.5 * 2^23 + 32768),
+// rounded once by the FMA, is the float 1.5 * 2^23 + u, whose bits are
+// 0x4B40 << 16 | u for 0 <= u < 2^16.  One byte permute packs a pair's low
+// halves; the receiver rebuilds each float with one byte permute and
+// subtracts the bias exactly.
+constexpr float kXBias = 12615680.0f;   // 1.5 * 2^23 + 32768
+constexpr uint32_t kXBiasHi = 0x4B40u;  // upper 16 bits of the float 1.5 * 2^23 + u
 __device__ __forceinline__ uint32_t pack_q16(float lo, float hi, float mul) {
   float a, b;
-  ffma2(a, b, lo, hi, mul, kRoundBias);
-  a = fminf(a, kRoundBias + 32767.f);
-  b = fminf(b, kRoundBias + 32767.f);
+  ffma2(a, b, lo, hi, mul, kXBias);
+  a = fminf(a, kXBias + 32767.f);
+  b = fminf(b, kXBias + 32767.f);
   return __byte_perm(__float_as_uint(a), __float_as_uint(b), 0x5410);
 }
 
@@ -323,7 +322,7 @@ mla_tc_kernel(const __nv_bfloat16* __restrict__ q, const __grid_constant__ CUten
         int e_row;
         asm volatile("ld.shared.b32 %0, [%1];" : "=r"(e_row) : "r"(xb + xoff(t, 8)) : "memory");
         const float unit = __uint_as_float(static_cast<uint32_t>(112 + e_row) << 23);  // 2^(E-15)
-        const float bias_unit = kRoundBias * unit;
+        const float bias_unit = kXBias * unit;   // exact: kXBias < 2^24
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           uint32_t v[4];
@@ -333,14 +332,13 @@ mla_tc_kernel(const __nv_bfloat16* __restrict__ q, const __grid_constant__ CUten
                        : "memory");
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            // The pair's two int16 values q times `unit`, exactly (|q| <
-            // 2^15, unit a power of two): the float with bits bias + q is
-            // 1.5 * 2^23 + q, so (that * unit - bias_unit) = q * unit.  Then
-            // added to this CTA's partial scores; both steps as packed pairs.
-            const int lo = static_cast<int>(v[e] << 16) >> 16, hi = static_cast<int>(v[e]) >> 16;
+            // The pair's two values q times `unit`, exactly (unit a power of
+            // two): (1.5 * 2^23 + u) * unit - bias_unit = (u - 32768) * unit.
+            // Then added to this CTA's partial scores; both steps as packed
+            // pairs.
             float d0, d1;
-            ffma2(d0, d1, __int_as_float(kRoundBiasBits + lo), __int_as_float(kRoundBiasBits + hi),
-                  unit, -bias_unit);
+            ffma2(d0, d1, __uint_as_float(__byte_perm(v[e], kXBiasHi, 0x5410)),
+                  __uint_as_float(__byte_perm(v[e], kXBiasHi, 0x5432)), unit, -bias_unit);
             fadd2(sc[8 * c + 2 * e], sc[8 * c + 2 * e + 1], d0, d1);
           }
         }
