@@ -8,12 +8,14 @@
 // CTA = (256 packed rows as two Q tiles of 128, kv head, request); a packed
 // row is one (query row, q head of the kv group) pair, so the Hq/Hkv heads
 // sharing a kv head share every K/V tile.  Warp roles (384 threads):
-//   warp 0     MMA issue (one thread): S_x(j) = Q_x K(j)^T, then
-//              O_x += P_x(j) V(j) with the A operand (P) read from TMEM;
+//   warp 0     MMA issue (one thread; with MLA keys warp 2 too, one thread
+//              per Q tile): S_x(j) = Q_x K(j)^T, then O_x += P_x(j) V(j)
+//              with the A operand (P) read from TMEM;
 //   warp 1     K/V producer: per 16-token piece of a cache block one TMA box
-//              per 64-column half, through the block table;
-//   warps 2-3  idle (they complete the first warpgroup, which hands its
-//              registers to the softmax warpgroups);
+//              per 64-column half of K and one box for both halves of V,
+//              through the block table;
+//   warps 2-3  idle otherwise (they complete the first warpgroup, which
+//              hands its registers to the softmax warpgroups);
 //   warps 4-7 / 8-11  two softmax warpgroups, one per Q tile: thread t of a
 //              group owns row t of its tile = TMEM lane t.  Per 128-token K/V
 //              tile it reads its S row from TMEM, masks (causal,
@@ -23,10 +25,12 @@
 // The MMA and producer warps have the lowest warp ids: each shares its
 // scheduler with two busy softmax warps, and the low ids keep them from being
 // starved of issue slots.
-// The two Q tiles interleave on the tensor core: PV_0(j), S_0(j+1),
-// PV_1(j), S_1(j+1), ... so each softmax warpgroup works on one tile while
-// the MMAs of the other proceed.  The tensor pipe runs in issue order, so
-// once S_x(j) has landed PV_x(j-1) has too: the softmax may rescale O_x (TMEM
+// The two Q tiles interleave on the tensor core (PV_0(j), S_0(j+1), PV_1(j),
+// S_1(j+1), ... from one thread; with two issuers each tile's PV_x(j) and
+// S_x(j+1) as soon as P_x(j) is written), so each softmax warpgroup works on
+// one tile while the MMAs of the other proceed.  The tensor pipe runs in
+// issue order and S_x(j) follows PV_x(j-1) from the same thread, so once
+// S_x(j) has landed PV_x(j-1) has too: the softmax may rescale O_x (TMEM
 // load, scale, store) without another wait; it does so only when a row's
 // running max grows by more than 2^8 (P keeps the older reference max
 // otherwise, which keeps O / l exact).
@@ -37,7 +41,8 @@
 // Shared memory (128-byte swizzled, 1024-byte aligned atoms):
 //   Q    2 tiles x [DK/64 halves][128 rows][128 B]
 //   K    2 stages x [DK/64 halves][BN tokens][128 B]
-//   V    2 stages x [DV/64 halves][BN tokens][128 B]
+//   V    VST stages x [BN/16 pieces][DV/64 halves][16 tokens][128 B] (the MLA
+//        workspaces: [DV/64 halves][BN tokens][128 B])
 // (DK = DV = d and BN = 128 for the standard pool; DK = 192, DV = 128 and
 // BN = 64 for the MLA prefill, whose queries and keys are [nope | rope].)
 // TMEM (512 columns): S_0/P_0 at 0, S_1/P_1 at 128, O_0 at 256, O_1 at 384.
@@ -155,6 +160,16 @@ __global__ void __launch_bounds__(384, 1)
 varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap v_map,
                  const __grid_constant__ VarlenArgs a) {
   using C = TcCfg<DK, DV, BN, VST>;
+  // Standard pool: a V piece (16 tokens, both halves) is one TMA box, laid
+  // out [half][16 tokens][128 B]; TMA issue, not bandwidth, is what the
+  // producer spends its time on, so V takes half the boxes of K.
+  constexpr bool kVm = !MLA;
+  constexpr uint32_t kVPiece = C::kHalvesV * C::kPieceBytes;
+  // MMA issue by one thread per Q tile (measured faster for the MLA shape:
+  // 192-wide keys, one V stage) or by one thread for both (faster for the
+  // standard pool).
+  constexpr bool kTwoIssuers = MLA;
+  constexpr uint32_t kIssuers = kTwoIssuers ? 2 : 1;
   const __nv_bfloat16* __restrict__ q = a.q;
   const int32_t* __restrict__ block_table = a.block_table;
   const int Hq = a.Hq, Hkv = a.Hkv, bs = a.bs, num_blocks = a.num_blocks;
@@ -235,15 +250,16 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
     tc::mbar_init(BAR(kQFull), C::kRows);
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(BAR(kKFull + b), 1);
-      tc::mbar_init(BAR(kKEmpty + b), CL);   // released by every CTA of the cluster
+      // Released by every issuing thread of every CTA of the cluster.
+      tc::mbar_init(BAR(kKEmpty + b), kIssuers * CL);
       tc::mbar_init(BAR(kVFull + b), 1);
-      tc::mbar_init(BAR(kVEmpty + b), CL);
+      tc::mbar_init(BAR(kVEmpty + b), kIssuers * CL);
       tc::mbar_init(BAR(kSFull + b), 1);
       tc::mbar_init(BAR(kPLo + b), C::kBM);
       tc::mbar_init(BAR(kPHi + b), C::kBM);
       tc::mbar_init(BAR(kODone + b), 1);
     }
-    tc::mbar_init(BAR(kFinal), 1);
+    tc::mbar_init(BAR(kFinal), kIssuers);
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
@@ -385,9 +401,10 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
       }
       // V rows that must contribute nothing: past seq_len (stale or unset
       // cache contents) or in pieces that were not loaded.  Zeroed once the
-      // tile's V has landed, by the first warpgroup (one row per thread),
-      // before P_0(j) is published; PV_1(j) is issued after PV_0(j).
-      if (x == 0) {
+      // tile's V has landed (one row per thread) by both warpgroups, each
+      // before it publishes its own P: PV_0(j) and PV_1(j) go out in either
+      // order.  Both write zeros, so the overlap is harmless.
+      {
         const int tok = tok0 + t;
         // Threads past the tile's kBN rows own no V row.
         const bool row_ok = t >= C::kBN || (tok < seq && ((vm >> (t >> 4)) & 1u));
@@ -398,11 +415,13 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
           for (int h = 0; h < C::kHalvesV; ++h)
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-              const uint32_t dst = vbase + h * (C::kBN * 128) + sw128(t, c);
+              const uint32_t dst =
+                  kVm ? vbase + (t >> 4) * kVPiece + h * C::kPieceBytes + sw128(t & 15, c)
+                      : vbase + h * (C::kBN * 128) + sw128(t, c);
               asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(dst), "r"(0u) : "memory");
             }
+          tc::fence_proxy_async_smem();   // before this thread's P arrival
         }
-        tc::fence_proxy_async_smem();
       }
       // P = exp2(s * scale_log2 - m_used) as bf16 pairs over the first 64
       // columns of the S row, published in two halves (tokens 0-63, 64-127)
@@ -487,7 +506,7 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
       for (int c = 0; c < DV / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
       if (lse != nullptr) lse[qrow] = -CUDART_INF_F;
     }
-  } else if (warp == 0) {
+  } else if (warp == 0 || (kTwoIssuers && warp == 2)) {
     // ------------------------------------------------------------ MMA issue
     tc::cluster_wait();
     tc::tc_fence_after();
@@ -517,25 +536,33 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
 #pragma unroll
         for (int k = k0; k < k0 + C::kBN / 32; ++k)
           tc::mma_bf16_ts(tmem + C::col_o(xq), tmem + C::col_s(xq) + k * 8,
-                          tc::smem_desc_sw128(vs + k * 16 * 128, C::kBN * 128, 1024), idesc_o,
+                          kVm ? tc::smem_desc_sw128(vs + k * kVPiece, C::kPieceBytes, 1024)
+                              : tc::smem_desc_sw128(vs + k * 16 * 128, C::kBN * 128, 1024),
+                          idesc_o,
                           (j > 0 || k > 0) ? 1u : 0u);
       };
       auto wait_k = [&](int j) { return tc::mbar_wait(BAR(kKFull + (j & 1)), (j >> 1) & 1); };
-      if (ok && ntiles > 0) {
-        ok = wait_k(0);
-        if (ok) {
-          tc::tc_fence_after();
-          issue_s(0, 0);
-          issue_s(1, 0);
-          release(BAR(kKEmpty + 0));
+      if (kTwoIssuers) {
+        // Each Q tile has its own issuing thread (warp 0: tile 0, warp 2:
+        // tile 1).  A thread blocks while the tensor pipe's queue is full, so
+        // with one thread for both tiles P_0(j+1), long written, can wait
+        // behind tile 1's batch; with two, each tile's PV and next S go out
+        // as soon as its own P is ready.  tcgen05.commit tracks the issuing
+        // thread's own MMAs, so each thread releases the K and V stages for
+        // its tile (the empty barriers count both threads).
+        const int xq = warp == 0 ? 0 : 1;
+        if (ok && ntiles > 0) {
+          ok = wait_k(0);
+          if (ok) {
+            tc::tc_fence_after();
+            issue_s(xq, 0);
+            release(BAR(kKEmpty + 0));
+          }
         }
-      }
-      for (int j = 0; ok && j < ntiles; ++j) {
-        if (*abort_flag) { ok = false; break; }
-        const bool more = j + 1 < ntiles;
-        if (!tc::mbar_wait(BAR(kVFull + j % C::kVStages), (j / C::kVStages) & 1)) { ok = false; break; }
-        if (more && !wait_k(j + 1)) { ok = false; break; }
-        for (int xq = 0; xq < 2 && ok; ++xq) {
+        for (int j = 0; ok && j < ntiles; ++j) {
+          if (*abort_flag) { ok = false; break; }
+          const bool more = j + 1 < ntiles;
+          if (!tc::mbar_wait(BAR(kVFull + j % C::kVStages), (j / C::kVStages) & 1)) { ok = false; break; }
           if (!tc::mbar_wait(BAR(kPLo + xq), j & 1)) { ok = false; break; }
           tc::tc_fence_after();
           issue_pv(xq, j, 0);
@@ -543,11 +570,43 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
           tc::tc_fence_after();
           issue_pv(xq, j, C::kBN / 32);
           tc::mma_commit(BAR(kODone + xq));
+          // K(j+1) only now: PV_x(j) does not need it.
+          if (more && !wait_k(j + 1)) { ok = false; break; }
+          tc::tc_fence_after();
           if (more) issue_s(xq, j + 1);
+          release(BAR(kVEmpty + j % C::kVStages));
+          if (more) release(BAR(kKEmpty + ((j + 1) & 1)));
         }
-        if (!ok) break;
-        release(BAR(kVEmpty + j % C::kVStages));
-        if (more) release(BAR(kKEmpty + ((j + 1) & 1)));
+      } else {
+        // One thread for both tiles: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1).
+        if (ok && ntiles > 0) {
+          ok = wait_k(0);
+          if (ok) {
+            tc::tc_fence_after();
+            issue_s(0, 0);
+            issue_s(1, 0);
+            release(BAR(kKEmpty + 0));
+          }
+        }
+        for (int j = 0; ok && j < ntiles; ++j) {
+          if (*abort_flag) { ok = false; break; }
+          const bool more = j + 1 < ntiles;
+          if (!tc::mbar_wait(BAR(kVFull + j % C::kVStages), (j / C::kVStages) & 1)) { ok = false; break; }
+          if (more && !wait_k(j + 1)) { ok = false; break; }
+          for (int xq = 0; xq < 2 && ok; ++xq) {
+            if (!tc::mbar_wait(BAR(kPLo + xq), j & 1)) { ok = false; break; }
+            tc::tc_fence_after();
+            issue_pv(xq, j, 0);
+            if (!tc::mbar_wait(BAR(kPHi + xq), j & 1)) { ok = false; break; }
+            tc::tc_fence_after();
+            issue_pv(xq, j, C::kBN / 32);
+            tc::mma_commit(BAR(kODone + xq));
+            if (more) issue_s(xq, j + 1);
+          }
+          if (!ok) break;
+          release(BAR(kVEmpty + j % C::kVStages));
+          if (more) release(BAR(kKEmpty + ((j + 1) & 1)));
+        }
       }
       if (!ok && !*abort_flag) fail();
       // Everything issued has completed before TMEM is released.
@@ -564,7 +623,7 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
     // K(j+2) (PV(j) needs it first) and reuses K(j)'s block ids.
     if (lane == 0) {
       tc::tma_prefetch_desc(&kv_map);
-      if (MLA) tc::tma_prefetch_desc(&v_map);
+      tc::tma_prefetch_desc(&v_map);
     }
     const int pc = lane;
     const bool box_lane = lane < C::kBN / 16;
@@ -601,6 +660,14 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
         for (int h = 0; h < halves; ++h)
           tc::tma_load_3d(dst + h * (C::kBN * 128) + pc * C::kPieceBytes,
                           which == 0 ? &kv_map : &v_map, full, h * 64, kvh, row);
+      } else if (!MLA && my_piece && blk >= 0 && which == 1) {
+        // V: both halves of the piece in one box (tensor map coordinates:
+        // column 0, token, half 0, head, 2 * block + 1).
+        const uint32_t d = dst + pc * kVPiece;
+        if (CL > 1)
+          tc::tma_load_5d_mc(d, &v_map, full, kMask, 0, (tok0 + 16 * pc) % bs, 0, kvh, 2 * blk + 1);
+        else
+          tc::tma_load_5d(d, &v_map, full, 0, (tok0 + 16 * pc) % bs, 0, kvh, 2 * blk + 1);
       } else if (!MLA && my_piece && blk >= 0) {
 #pragma unroll
         for (int h = 0; h < C::kHalvesK; ++h) {
@@ -707,6 +774,25 @@ bool make_kv_map(CUtensorMap* map, const void* cache, int nb, int bs, int Hkv, i
   return r == CUDA_SUCCESS;
 }
 
+// The V half of the same pool viewed 5-D so that one box holds a 16-token
+// piece's 64-column halves as consecutive 128-byte-swizzled [16][128 B]
+// tiles: dims (innermost first) 64 columns, bs tokens, d/64 halves, Hkv
+// heads, 2 nb (kv index + 2 * block); box 64 x 16 x d/64 x 1 x 1.
+bool make_v_map(CUtensorMap* map, const void* cache, int nb, int bs, int Hkv, int d) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[5] = {64, static_cast<cuuint64_t>(bs), static_cast<cuuint64_t>(d / 64),
+                              static_cast<cuuint64_t>(Hkv), 2 * static_cast<cuuint64_t>(nb)};
+  const cuuint64_t row = static_cast<cuuint64_t>(d) * 2;
+  const cuuint64_t strides[4] = {row * Hkv, 128, row, row * Hkv * bs};
+  const cuuint32_t box[5] = {64, 16, static_cast<cuuint32_t>(d / 64), 1, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(cache), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 // MLA prefill workspaces [rows][H][width] viewed 3-D (innermost first):
@@ -734,8 +820,11 @@ static cudaError_t launch_varlen_tc_t(const VarlenLaunch& L, cudaStream_t stream
     if (!make_ws_map(&map, L.mla_k, rows, L.Hkv, DK) || !make_ws_map(&vmap, L.mla_v, rows, L.Hkv, DV))
       return cudaErrorInvalidValue;
   } else {
-    if (!make_kv_map(&map, L.cache, L.num_blocks, L.bs, L.Hkv, DK)) return cudaErrorInvalidValue;
-    vmap = map;
+    // TMA coordinates are 32-bit: 2 * block + 1 must fit.
+    if (2LL * L.num_blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    if (!make_kv_map(&map, L.cache, L.num_blocks, L.bs, L.Hkv, DK) ||
+        !make_v_map(&vmap, L.cache, L.num_blocks, L.bs, L.Hkv, DV))
+      return cudaErrorInvalidValue;
   }
   auto kern = varlen_tc_kernel<DK, DV, BN, VST, CL, EXT, MLA>;
   static DeviceFlags attr_set;
