@@ -29,8 +29,6 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
-#include <mutex>
-
 #include "pa_common.cuh"
 #include "pa_launch.h"
 #include "tc_common.cuh"
@@ -315,24 +313,10 @@ mla_expand_kernel(const __grid_constant__ CUtensorMap lat_map,
 
 namespace {
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn_mla() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult qr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &qr) == cudaSuccess &&
-        qr == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
 // Latent pool [nb][bs][576] viewed 3-D (innermost first): 64-column x
 // 16-token boxes, 128-byte swizzle.
 bool make_latent_map(CUtensorMap* map, const void* pool, int nb, int bs) {
-  auto fn = encode_fn_mla();
+  auto fn = tensor_map_encoder();
   if (fn == nullptr) return false;
   const cuuint64_t dims[3] = {576, static_cast<cuuint64_t>(bs), static_cast<cuuint64_t>(nb)};
   const cuuint64_t strides[2] = {576 * 2, static_cast<cuuint64_t>(bs) * 576 * 2};
@@ -345,7 +329,7 @@ bool make_latent_map(CUtensorMap* map, const void* pool, int nb, int bs) {
 
 // kv_b_proj weight [H * 256][512] viewed 2-D: 64-column x 256-row boxes.
 bool make_weight_map(CUtensorMap* map, const void* w, int H) {
-  auto fn = encode_fn_mla();
+  auto fn = tensor_map_encoder();
   if (fn == nullptr) return false;
   const cuuint64_t dims[2] = {512, static_cast<cuuint64_t>(H) * 256};
   const cuuint64_t strides[1] = {512 * 2};

@@ -67,8 +67,6 @@
 #include <cudaTypedefs.h>
 #include <math_constants.h>
 
-#include <mutex>
-
 #include "pa_common.cuh"
 #include "pa_launch.h"
 #include "tc_common.cuh"
@@ -760,23 +758,9 @@ mla_tc_kernel(const __nv_bfloat16* __restrict__ q, const __grid_constant__ CUten
 
 namespace {
 
-PFN_cuTensorMapEncodeTiled_v12000 mla_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult qr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &qr) == cudaSuccess &&
-        qr == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
 bool encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
             const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swz) {
-  auto fn = mla_encode_fn();
+  auto fn = tensor_map_encoder();
   if (fn == nullptr) return false;
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides,

@@ -2,10 +2,16 @@
 // C-ABI entry points.  Each returns the launch's cudaError_t.
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace pa {
+
+// The driver's cuTensorMapEncodeTiled, looked up once through the runtime
+// (nullptr if the driver does not provide it).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* cache,
                                      const int64_t* slot_mapping, int num_tokens,

@@ -50,8 +50,6 @@
 #include <cudaTypedefs.h>
 #include <math_constants.h>
 
-#include <mutex>
-
 #include "pa_common.cuh"
 #include "pa_launch.h"
 #include "tc_common.cuh"
@@ -743,24 +741,10 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
 
 namespace {
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult qr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &qr) == cudaSuccess &&
-        qr == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
 // 5-D view of the standard pool [nb][2][bs][Hkv][d] (innermost first) with a
 // 64-element x 1 head x 16 token box and 128-byte swizzle.
 bool make_kv_map(CUtensorMap* map, const void* cache, int nb, int bs, int Hkv, int d) {
-  auto fn = encode_fn();
+  auto fn = tensor_map_encoder();
   if (fn == nullptr) return false;
   const cuuint64_t dims[5] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(Hkv),
                               static_cast<cuuint64_t>(bs), 2, static_cast<cuuint64_t>(nb)};
@@ -779,7 +763,7 @@ bool make_kv_map(CUtensorMap* map, const void* cache, int nb, int bs, int Hkv, i
 // tiles: dims (innermost first) 64 columns, bs tokens, d/64 halves, Hkv
 // heads, 2 nb (kv index + 2 * block); box 64 x 16 x d/64 x 1 x 1.
 bool make_v_map(CUtensorMap* map, const void* cache, int nb, int bs, int Hkv, int d) {
-  auto fn = encode_fn();
+  auto fn = tensor_map_encoder();
   if (fn == nullptr) return false;
   const cuuint64_t dims[5] = {64, static_cast<cuuint64_t>(bs), static_cast<cuuint64_t>(d / 64),
                               static_cast<cuuint64_t>(Hkv), 2 * static_cast<cuuint64_t>(nb)};
@@ -798,7 +782,7 @@ bool make_v_map(CUtensorMap* map, const void* cache, int nb, int bs, int Hkv, in
 // MLA prefill workspaces [rows][H][width] viewed 3-D (innermost first):
 // 64-column x 1-head x 16-token boxes, 128-byte swizzle.
 bool make_ws_map(CUtensorMap* map, const void* ws, long long rows, int H, int width) {
-  auto fn = encode_fn();
+  auto fn = tensor_map_encoder();
   if (fn == nullptr) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(width), static_cast<cuuint64_t>(H),
                               static_cast<cuuint64_t>(rows)};
