@@ -209,29 +209,46 @@ class DecodeStep:
 def run_e2e(pa, b, step, steps, warmup, device):
     """Same step through the public API with the step's inputs in pinned host
     memory: H2D copies of q / new K,V / slot_mapping / block_table / seq_lens,
-    the three calls, and a D2H read of out + lse, every step."""
+    the three calls, and a D2H read of out + lse, every step.  As a serving
+    loop would, the host enqueues step k + 1 before it waits for step k's
+    result, so the GPU does not idle while the host waits; each step's result
+    lands in its own pinned buffer, which the host has waited for before that
+    buffer is written again."""
     N, hq, d = b.num_seqs, b.num_q_heads, b.head_size
-    h = {
-        "q": torch.from_numpy(b.q.view(np.int16)).view(torch.bfloat16).reshape(N, hq, d)
-        .pin_memory(),
-        "key": torch.from_numpy(b.key.view(np.int16)).view(torch.bfloat16).pin_memory(),
-        "value": torch.from_numpy(b.value.view(np.int16)).view(torch.bfloat16).pin_memory(),
-        "slots": torch.from_numpy(b.slot_mapping).pin_memory(),
-        "table": torch.from_numpy(b.block_table).pin_memory(),
-        "seq": torch.from_numpy(b.seq_lens).pin_memory(),
-    }
-    out_h = torch.empty((N, hq, d), dtype=torch.bfloat16).pin_memory()
-    lse_h = torch.empty((N, hq), dtype=torch.float32).pin_memory()
-    dv = {"q": step.q, "key": step.key, "value": step.value, "slots": step.slots,
-          "table": step.table, "seq": step.seq}
-    h2d = sum(t.numel() * t.element_size() for t in h.values())
-    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+    # The step's inputs travel as one packed transfer and its results as
+    # another, as a serving loop would batch them: q, the new K and V, slots,
+    # block table and lengths at 256-byte-aligned offsets of one pinned
+    # buffer, copied into one device buffer of which the library's arguments
+    # are views; out and LSE likewise in one device buffer, read back whole.
+    parts = [("q", b.q.view(np.int16), torch.bfloat16, (N, hq, d)),
+             ("key", b.key.view(np.int16), torch.bfloat16, b.key.shape),
+             ("value", b.value.view(np.int16), torch.bfloat16, b.value.shape),
+             ("slots", b.slot_mapping, torch.int64, b.slot_mapping.shape),
+             ("table", b.block_table, torch.int32, b.block_table.shape),
+             ("seq", b.seq_lens, torch.int32, b.seq_lens.shape)]
+    align = lambda x: (x + 255) // 256 * 256
+    offs, total = {}, 0
+    for name, arr, _, _ in parts:
+        offs[name] = total
+        total = align(total + arr.nbytes)
+    hbuf = torch.empty(total, dtype=torch.uint8).pin_memory()
+    dbuf = torch.empty(total, dtype=torch.uint8, device=device)
+    for name, arr, dt, shape in parts:
+        o = offs[name]
+        hbuf[o:o + arr.nbytes].copy_(torch.from_numpy(np.ascontiguousarray(arr).view(np.uint8).reshape(-1)))
+        setattr(step, name, dbuf[o:o + arr.nbytes].view(dt).view(*shape))
+    o_bytes, l_bytes = N * hq * d * 2, N * hq * 4
+    obuf = torch.empty(align(o_bytes) + l_bytes, dtype=torch.uint8, device=device)
+    step.out = obuf[:o_bytes].view(torch.bfloat16).view(N, hq, d)
+    step.lse = obuf[align(o_bytes):].view(torch.float32).view(N, hq)
+    nbuf = len(step.pools)
+    res_h = [torch.empty(obuf.numel(), dtype=torch.uint8).pin_memory() for _ in range(nbuf)]
+    h2d, d2h = total, obuf.numel()
+
     def enqueue(k):
-        for name, t in h.items():
-            dv[name].copy_(t, non_blocking=True)
+        dbuf.copy_(hbuf, non_blocking=True)
         step.run(k)
-        out_h.copy_(step.out, non_blocking=True)
-        lse_h.copy_(step.lse, non_blocking=True)
+        res_h[k % nbuf].copy_(obuf, non_blocking=True)
 
     # The step (input copies, the three calls, output copies) is captured once
     # per pool copy as a CUDA graph and replayed, with the host waiting for
@@ -255,21 +272,26 @@ def run_e2e(pa, b, step, steps, warmup, device):
         graphs, launch = [], "eager"
         torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
+    done = [torch.cuda.Event() for _ in range(nbuf)]
 
-    def one(k):
-        if graphs:
-            graphs[k % len(graphs)].replay()
-        else:
-            enqueue(k)
-        stream.synchronize()
+    def run(n):
+        # Step k is enqueued, then the host waits for step k - 1's result.
+        for k in range(n):
+            if graphs:
+                graphs[k % nbuf].replay()
+            else:
+                enqueue(k)
+            done[k % nbuf].record(stream)
+            if k >= 1:
+                done[(k - 1) % nbuf].synchronize()
+        done[(n - 1) % nbuf].synchronize()
 
-    for k in range(warmup):
-        one(k)
+    run(warmup)
     t0 = time.perf_counter()
-    for k in range(steps):
-        one(k)
+    run(steps)
     dt = time.perf_counter() - t0
-    return dt, h2d, d2h, launch
+    return dt, h2d, d2h, (launch + ", one packed copy each way, step k+1 enqueued before "
+                          "the host waits for step k's result")
 
 
 def cpu_baseline_sample(b, budget_s=12.0, threads=None):
