@@ -261,12 +261,15 @@ def test_decode_long_context_full_size_sampled(pa):
     assert pa.pa_get_device_error() == 0
 
 
-def test_lse_merge_random_partials(pa):
-    rng = np.random.default_rng(41)
-    N, H, S, dv = 5, 7, 13, 128
+# (S, dv): one split, a group of splits that fills a warp and one past it,
+# hundreds of splits; value widths of the standard pool and of MLA.
+@pytest.mark.parametrize("S,dv", [(13, 128), (1, 64), (32, 512), (33, 128), (300, 64)])
+def test_lse_merge_random_partials(pa, S, dv):
+    rng = np.random.default_rng(41 + S)
+    N, H = 5, 7                                   # 35 heads: not a multiple of 4
     part = rng.standard_normal((N, H, S, dv + 1)).astype(np.float32)
     part[..., -1] *= 4.0
-    part[0, 0, 3:, -1] = -np.inf                  # some empty splits
+    part[0, 0, S // 4:, -1] = -np.inf             # some empty splits (all but the first, S = 1..3)
     part[1, 2, :, -1] = -np.inf                   # all empty
     part[..., :-1][np.isneginf(part[..., -1])] = 0.0
     ws = torch.from_numpy(part).cuda()
