@@ -65,13 +65,6 @@ enum MlaExpBar {
   kENumBars = kEFinal + 1
 };
 
-// 32 bytes to global memory in one store (32-byte aligned address).
-__device__ __forceinline__ void st_global_v8(uint32_t* p, const uint32_t (&w)[8]) {
-  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
-               "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
-               : "memory");
-}
-
 __global__ void __launch_bounds__(192, 1)
 mla_expand_kernel(const __grid_constant__ CUtensorMap lat_map,
                   const __grid_constant__ CUtensorMap w_map,

@@ -141,6 +141,14 @@ inline long long split_chunk(int max_seq_len, int S, int bs) {
   return ((per + bs - 1) / bs) * bs;
 }
 
+// 32 bytes to global memory in one store (sm_100 and later; 32-byte aligned
+// address): a whole sector where a warp's store covers one row per thread.
+__device__ __forceinline__ void st_global_v8(uint32_t* p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+               "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 // Packed fp32 pairs (sm_100 and later: one instruction does the work of two,
 // each half rounded as its scalar counterpart): (x, y) = (a0 b + c, a1 b + c)
 // and (x, y) += (a0, a1).

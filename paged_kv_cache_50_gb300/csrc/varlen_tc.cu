@@ -478,22 +478,35 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
       }
     } else if (ok) {   // warp-uniform
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint4* dst = reinterpret_cast<uint4*>(out + qrow * DV);
+      // A warp's store covers 32 rows (one per thread): 32-byte stores write
+      // whole sectors where `out` is 32-byte aligned (rows are multiples of
+      // 32 bytes), 16-byte ones otherwise.
+      const bool a32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
+      uint32_t* dst = reinterpret_cast<uint32_t*>(out + qrow * DV);
 #pragma unroll
-      for (int c = 0; c < DV / 32; ++c) {
-        uint32_t r[32];
-        tc::tmem_ld32(to + c * 32, r);
+      for (int c2 = 0; c2 < DV / 64; ++c2) {
+        uint32_t r[2][32];
+        tc::tmem_ld32(to + c2 * 64, r[0]);
+        tc::tmem_ld32(to + c2 * 64 + 32, r[1]);
         tc::tmem_wait_ld();
         if (valid) {
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 w;
-            w.x = pack_bf16(__uint_as_float(r[v * 8 + 0]) * inv, __uint_as_float(r[v * 8 + 1]) * inv);
-            w.y = pack_bf16(__uint_as_float(r[v * 8 + 2]) * inv, __uint_as_float(r[v * 8 + 3]) * inv);
-            w.z = pack_bf16(__uint_as_float(r[v * 8 + 4]) * inv, __uint_as_float(r[v * 8 + 5]) * inv);
-            w.w = pack_bf16(__uint_as_float(r[v * 8 + 6]) * inv, __uint_as_float(r[v * 8 + 7]) * inv);
-            dst[c * 4 + v] = w;
-          }
+          for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int v = 0; v < 2; ++v) {
+              uint32_t w[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                w[e] = pack_bf16(__uint_as_float(r[u][v * 16 + 2 * e]) * inv,
+                                 __uint_as_float(r[u][v * 16 + 2 * e + 1]) * inv);
+              uint32_t* p = dst + (c2 * 2 + u) * 16 + v * 8;
+              if (a32) {
+                st_global_v8(p, w);
+              } else {
+                reinterpret_cast<uint4*>(p)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                reinterpret_cast<uint4*>(p)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+              }
+            }
         }
       }
       if (valid && lse != nullptr)
