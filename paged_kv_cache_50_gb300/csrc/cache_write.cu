@@ -15,6 +15,9 @@ __global__ void __launch_bounds__(256)
 reshape_and_cache_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value,
                          uint4* __restrict__ cache, const int64_t* __restrict__ slot_mapping,
                          int row_vec, int block_size, int64_t num_slots, int* err) {
+  // Launched with launch_pdl: wait for the previous kernel in the stream
+  // (which may still read the pool or produce these inputs) to complete.
+  pdl_wait();
   // The attention kernel that follows may start setting up now (it waits for
   // this kernel's completion before reading anything).
   pdl_trigger();
@@ -45,11 +48,10 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* c
   const int row_vec = num_kv_heads * head_size / 8;  // 16-byte vectors per row
   int threads = ((row_vec + 31) / 32) * 32;
   if (threads > 256) threads = 256;
-  reshape_and_cache_kernel<<<num_tokens, threads, 0, stream>>>(
-      static_cast<const uint4*>(key), static_cast<const uint4*>(value),
-      static_cast<uint4*>(cache), slot_mapping, row_vec, block_size,
-      static_cast<int64_t>(num_blocks) * block_size, err);
-  return cudaGetLastError();
+  return launch_pdl(reshape_and_cache_kernel, dim3(num_tokens), dim3(threads), 0, stream,
+                    static_cast<const uint4*>(key), static_cast<const uint4*>(value),
+                    static_cast<uint4*>(cache), slot_mapping, row_vec, block_size,
+                    static_cast<int64_t>(num_blocks) * block_size, err);
 }
 
 // The same step with an fp8 pool of e4m3 codes, [num_blocks, 2, block_size,
@@ -86,6 +88,7 @@ reshape_and_cache_fp8_kernel(const uint4* __restrict__ key, const uint4* __restr
                              uint4* __restrict__ cache, const int64_t* __restrict__ slot_mapping,
                              int row_vec, int block_size, int64_t num_slots, float k_scale,
                              float v_scale, int* err) {
+  pdl_wait();
   pdl_trigger();
   const int t = blockIdx.x;
   const int64_t slot = slot_mapping[t];
@@ -116,11 +119,10 @@ cudaError_t launch_reshape_and_cache_fp8(const void* key, const void* value, voi
   const int row_vec = num_kv_heads * head_size / 16;  // 16-byte vectors of codes per row
   int threads = ((row_vec + 31) / 32) * 32;
   if (threads > 256) threads = 256;
-  reshape_and_cache_fp8_kernel<<<num_tokens, threads, 0, stream>>>(
-      static_cast<const uint4*>(key), static_cast<const uint4*>(value),
-      static_cast<uint4*>(cache), slot_mapping, row_vec, block_size,
-      static_cast<int64_t>(num_blocks) * block_size, k_scale, v_scale, err);
-  return cudaGetLastError();
+  return launch_pdl(reshape_and_cache_fp8_kernel, dim3(num_tokens), dim3(threads), 0, stream,
+                    static_cast<const uint4*>(key), static_cast<const uint4*>(value),
+                    static_cast<uint4*>(cache), slot_mapping, row_vec, block_size,
+                    static_cast<int64_t>(num_blocks) * block_size, k_scale, v_scale, err);
 }
 
 // The MLA cache write ("Triton and MLA": the cache holds one vector per token,
@@ -131,6 +133,7 @@ __global__ void __launch_bounds__(128)
 mla_cache_write_kernel(const uint4* __restrict__ kv_c, const uint4* __restrict__ k_pe,
                        uint4* __restrict__ cache, const int64_t* __restrict__ slot_mapping,
                        int num_tokens, int c_vec, int pe_vec, int64_t num_slots, int* err) {
+  pdl_wait();
   pdl_trigger();
   const int t = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (t >= num_tokens) return;
@@ -153,11 +156,10 @@ cudaError_t launch_mla_cache_write(const void* kv_c, const void* k_pe, void* cac
                                    int rope_dim, int block_size, int num_blocks, int* err,
                                    cudaStream_t stream) {
   const int blocks = (num_tokens + 3) / 4;
-  mla_cache_write_kernel<<<blocks, 128, 0, stream>>>(
-      static_cast<const uint4*>(kv_c), static_cast<const uint4*>(k_pe),
-      static_cast<uint4*>(cache), slot_mapping, num_tokens, kv_lora_rank / 8, rope_dim / 8,
-      static_cast<int64_t>(num_blocks) * block_size, err);
-  return cudaGetLastError();
+  return launch_pdl(mla_cache_write_kernel, dim3(blocks), dim3(128), 0, stream,
+                    static_cast<const uint4*>(kv_c), static_cast<const uint4*>(k_pe),
+                    static_cast<uint4*>(cache), slot_mapping, num_tokens, kv_lora_rank / 8,
+                    rope_dim / 8, static_cast<int64_t>(num_blocks) * block_size, err);
 }
 
 }  // namespace pa

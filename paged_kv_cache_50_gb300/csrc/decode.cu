@@ -1,5 +1,5 @@
-// Split-KV decode (stage 1) and the LSE merge (stage 2) for the standard
-// paged layout [num_blocks, 2, block_size, Hkv, d].
+// Split-KV decode, stage 1, for the standard paged layout
+// [num_blocks, 2, block_size, Hkv, d] (stage 2, the LSE merge, is merge.cu).
 //
 // Method: "Chapter 1: attention backends" (zero-to-sglang), section 3.1 --
 // a decode query has too little parallelism, so the context is split along
@@ -323,56 +323,6 @@ decode_splitkv_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
   }
 }
 
-// Stage 2: one CTA per (request, head); weights exp(lse_s - M) in shared memory.
-__global__ void __launch_bounds__(128)
-lse_merge_kernel(const float* __restrict__ ws, int S, int dv, __nv_bfloat16* __restrict__ out,
-                 float* __restrict__ lse) {
-  extern __shared__ float wsh[];   // [S] weights, then 32 floats of reduction scratch
-  float* red = wsh + S;
-  pdl_wait();
-  const int64_t nh = blockIdx.x;
-  const float* base = ws + nh * S * static_cast<int64_t>(dv + 1);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-
-  float m = -CUDART_INF_F;
-  for (int s = tid; s < S; s += blockDim.x) m = fmaxf(m, base[static_cast<int64_t>(s) * (dv + 1) + dv]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if (lane == 0) red[warp] = m;
-  __syncthreads();
-  m = red[0];
-  for (int w = 1; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, red[w]);
-  __syncthreads();
-
-  float wsum = 0.f;
-  for (int s = tid; s < S; s += blockDim.x) {
-    const float l = base[static_cast<int64_t>(s) * (dv + 1) + dv];
-    const float w = (m == -CUDART_INF_F || l == -CUDART_INF_F) ? 0.f : expf(l - m);
-    wsh[s] = w;
-    wsum += w;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
-  if (lane == 0) red[8 + warp] = wsum;
-  __syncthreads();
-  wsum = 0.f;
-  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) wsum += red[8 + w];
-
-  const float inv = m == -CUDART_INF_F ? 0.f : 1.f / wsum;
-  for (int e = tid; e < dv; e += blockDim.x) {
-    float acc = 0.f;
-    int s = 0;
-    for (; s + 4 <= S; s += 4) {
-      const float* p = base + static_cast<int64_t>(s) * (dv + 1) + e;
-      const float v0 = p[0], v1 = p[dv + 1], v2 = p[2 * (dv + 1)], v3 = p[3 * (dv + 1)];
-      acc += wsh[s] * v0 + wsh[s + 1] * v1 + wsh[s + 2] * v2 + wsh[s + 3] * v3;
-    }
-    for (; s < S; ++s) acc += wsh[s] * base[static_cast<int64_t>(s) * (dv + 1) + e];
-    out[nh * dv + e] = __float2bfloat16_rn(acc * inv);
-  }
-  if (lse != nullptr && tid == 0) lse[nh] = m == -CUDART_INF_F ? -CUDART_INF_F : m + logf(wsum);
-}
-
 template <int D, int STAGES, int NT>
 static cudaError_t launch_decode_t(const void* q, const void* cache, const int32_t* block_table,
                                    const int32_t* seq_lens, int N, int Hq, int Hkv, int bs,
@@ -407,16 +357,6 @@ cudaError_t launch_decode_splitkv(const void* q, const void* cache, const int32_
   if (wide) PA_DECODE_LAUNCH(64, 4, 2);
   PA_DECODE_LAUNCH(64, 4, 1);
 #undef PA_DECODE_LAUNCH
-}
-
-cudaError_t launch_lse_merge(const float* ws, int NH, int S, int dv, void* out, float* lse,
-                             cudaStream_t stream) {
-  const size_t smem = (static_cast<size_t>(S) + 32) * sizeof(float);
-  static DeviceFlags attr_set;
-  cudaError_t e = set_smem_once(lse_merge_kernel, 200 * 1024, attr_set);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(lse_merge_kernel, dim3(NH), dim3(128), smem, stream, ws, S, dv,
-                    static_cast<__nv_bfloat16*>(out), lse);
 }
 
 }  // namespace pa

@@ -261,9 +261,12 @@ def test_decode_long_context_full_size_sampled(pa):
     assert pa.pa_get_device_error() == 0
 
 
-# (S, dv): one split, a group of splits that fills a warp and one past it,
-# hundreds of splits; value widths of the standard pool and of MLA.
-@pytest.mark.parametrize("S,dv", [(13, 128), (1, 64), (32, 512), (33, 128), (300, 64)])
+# (S, dv): one split, the warp-per-head merge at and below its split limits
+# (8 and 16 at dv 128, 32 at dv 64) and one past them, a group of splits that
+# fills a warp and one past it, hundreds of splits; value widths of the
+# standard pool and of MLA.
+@pytest.mark.parametrize("S,dv", [(13, 128), (1, 64), (8, 128), (16, 128), (17, 128), (32, 64),
+                                  (33, 64), (32, 512), (33, 128), (300, 64)])
 def test_lse_merge_random_partials(pa, S, dv):
     rng = np.random.default_rng(41 + S)
     N, H = 5, 7                                   # 35 heads: not a multiple of 4
