@@ -140,8 +140,19 @@ decode_splitkv_fp8_kernel(const __nv_bfloat16* __restrict__ q, const uint8_t* __
   const int gid = lane >> 2, tid4 = lane & 3;
 
   pdl_wait();
-  const int seq = seq_lens[i];
   const long long a0 = static_cast<long long>(s) * chunk;
+  const int32_t* table = block_table + static_cast<int64_t>(i) * max_blocks;
+  // Block ids of the warp's first STAGES sub-blocks, read together with
+  // seq_len (they do not depend on it when the split is not empty, which
+  // then starts at a0); ids of sub-blocks the split does not have are never
+  // used.
+  int first_blk[STAGES];
+#pragma unroll
+  for (int n = 0; n < STAGES; ++n) {
+    const long long col = (a0 + (warp + n * C::kWarps) * 16) / bs;
+    first_blk[n] = col < max_blocks ? block_at(table, static_cast<int>(col), max_blocks) : -1;
+  }
+  const int seq = seq_lens[i];
   const int t0 = static_cast<int>(a0 < seq ? a0 : seq);
   const int t1 = (s == S - 1) ? seq : static_cast<int>(a0 + chunk < seq ? a0 + chunk : seq);
   const int nsb = (t1 - t0 + 15) >> 4;
@@ -167,7 +178,6 @@ decode_splitkv_fp8_kernel(const __nv_bfloat16* __restrict__ q, const uint8_t* __
 
   const uint32_t wbase = smem_u32(smem) + warp * C::kWarpBytes;
   const int64_t row_stride = static_cast<int64_t>(Hkv) * D;  // bytes per token row
-  const int32_t* table = block_table + static_cast<int64_t>(i) * max_blocks;
 
   // Block id of the warp's n-th sub-block (loaded one iteration before its
   // copies are issued, so the table read is off the critical path).
@@ -213,10 +223,10 @@ decode_splitkv_fp8_kernel(const __nv_bfloat16* __restrict__ q, const uint8_t* __
 
 #pragma unroll
   for (int n = 0; n < STAGES - 1; ++n) {
-    if (n < my_n) issue(n, lookup(n));
+    if (n < my_n) issue(n, first_blk[n]);
     cp_async_commit();
   }
-  int next_blk = STAGES - 1 < my_n ? lookup(STAGES - 1) : -1;
+  int next_blk = STAGES - 1 < my_n ? first_blk[STAGES - 1] : -1;
 
   // Source lanes of the P^T operand: tokens 2 tid4 (srcA) and 2 tid4 + 1
   // (srcB) hold head gid in the lane of tid4' = gid / 2, half gid % 2.
