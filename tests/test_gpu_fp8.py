@@ -11,6 +11,8 @@ NaN code 0x7F, so a kernel that read anything outside a request's first
 seq_len tokens would produce NaN and fail.
 """
 
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -208,6 +210,46 @@ def test_fp8_decode_gqa_workload_all_requests(pa):
         empty = np.isneginf(part[..., -1])
         assert not ws[..., :-1][empty].any()
         assert_out_close(ws[..., :-1][~empty], part[..., :-1][~empty], f"fp8 split o S={S}")
+    assert pa.pa_get_device_error() == 0
+
+
+def test_fp8_decode_long_context_full_size_sampled(pa):
+    """The long-context batch (8 x 131072 tokens, 64 q / 8 kv heads) over an
+    fp8 pool at the split count the bench times: the step's 8 new rows are
+    quantised bit-exactly, and two sampled requests match the oracle, which
+    runs on those requests' blocks only (the whole pool in fp64 would take
+    17 GB)."""
+    b = workloads.long_decode(with_pool=False)
+    d = Dev8(pa, b, poison=False)
+    sms = pa.pa_device_sm_count()
+    S = min(math.ceil(131072 / 512), 2 * sms)
+    assert pa.pa_num_kv_splits(131072, sms) == S
+    out, lse, _ = d.decode(pa, S)
+    bs = b.block_size
+    s = b.slot_mapping
+    # Expected codes of the new rows: the oracle's write into a small pool,
+    # one block per request, at the same offsets.
+    small = np.zeros((b.num_seqs, 2, bs, b.num_kv_heads, b.head_size), np.uint8)
+    small = oracle.reshape_and_cache_fp8(b.key, b.value, small,
+                                         np.arange(b.num_seqs) * bs + s % bs, bs, KS, VS)
+    rows = d.pool.view(torch.uint8)[torch.from_numpy(s // bs).cuda(), :,
+                                    torch.from_numpy(s % bs).cuda()].cpu().numpy()
+    assert np.array_equal(rows, small[np.arange(b.num_seqs), :, s % bs])
+    q = _decode_q(b)
+    for r in (0, 5):
+        n = int(b.seq_lens[r])
+        blocks = b.block_table[r, :(n + bs - 1) // bs]
+        sub = oracle.reshape_and_cache_fp8(b.key[r:r + 1], b.value[r:r + 1],
+                                           d.host_pool_before[blocks], np.array([n - 1]), bs,
+                                           KS, VS)
+        table = np.arange(len(blocks), dtype=np.int32)[None, :]
+        part = oracle.split_partials_fp8(q[r:r + 1], sub, table, b.seq_lens[r:r + 1], b.scale,
+                                         KS, VS, 1)
+        ref_o, ref_l = oracle.lse_merge(part)
+        assert_out_close(out[r:r + 1], ref_o, f"fp8 long decode out, request {r}")
+        assert_lse_close(lse[r:r + 1], ref_l, f"fp8 long decode lse, request {r}")
+        del sub, part
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
     assert pa.pa_get_device_error() == 0
 
 
