@@ -86,20 +86,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint
       : "memory");
 }
 
-// 5-D tiled tensor load delivered to the same shared-memory offset in every
-// CTA of the cluster named in `mask`; each receiving CTA counts the bytes on
-// its own barrier at offset `bar`.
-__device__ __forceinline__ void tma_load_5d_mc(uint32_t dst, const void* tmap, uint32_t bar,
-                                               uint16_t mask, int c0, int c1, int c2, int c3,
-                                               int c4) {
-  asm volatile(
-      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
-      "r"(bar), "h"(mask)
-      : "memory");
-}
-
 // Cluster-scope variants for barriers that a peer CTA of the cluster
 // signals (remote arrivals, st.async transactions): the wait acquires at
 // cluster scope.
@@ -240,15 +226,6 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
-// The same, arriving once on the barrier at offset `bar` of every CTA in `mask`.
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
-      "h"(mask)
       : "memory");
 }
 

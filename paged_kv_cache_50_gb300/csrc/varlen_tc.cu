@@ -34,9 +34,6 @@
 // load, scale, store) without another wait; it does so only when a row's
 // running max grows by more than 2^8 (P keeps the older reference max
 // otherwise, which keeps O / l exact).
-// Clusters of CL CTAs (consecutive q tiles of one request and kv head) share
-// every K/V tile: each CTA gathers 1/CL of the boxes and the TMA multicasts
-// them to all; a stage is released cluster-wide by a multicast tcgen05.commit.
 //
 // Shared memory (128-byte swizzled, 1024-byte aligned atoms):
 //   Q    2 tiles x [DK/64 halves][128 rows][128 B]
@@ -153,7 +150,7 @@ constexpr int kPieceRing = 4;
 // MLA = true: keys and values come from the contiguous expanded workspaces
 // of the MLA prefill (k_map over [N * s_max][H][DK], v_map over
 // [N * s_max][H][DV]) instead of the paged pool; no block table.
-template <int DK, int DV, int BN, int VST, int CL, bool EXT, bool MLA>
+template <int DK, int DV, int BN, int VST, bool EXT, bool MLA>
 __global__ void __launch_bounds__(384, 1)
 varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap v_map,
                  const __grid_constant__ VarlenArgs a) {
@@ -193,8 +190,6 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
   const int split = EXT ? static_cast<int>(blockIdx.x) / q_tiles : 0;
   const int qt = EXT ? q_tiles - 1 - static_cast<int>(blockIdx.x) % q_tiles
                      : static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);  // heavy tiles first
-  const int rank = CL > 1 ? static_cast<int>(tc::cluster_rank()) : 0;
-  const int qt_hi = qt + rank, qt_lo = qt_hi - (CL - 1);   // the cluster's CTA tiles
   const int grp = Hq / Hkv;
   // A virtual request (virt_total_q > 0) is every query row of the call
   // against one fixed context of virt_seq tokens read through table row 0.
@@ -202,22 +197,22 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
   const int q0 = virt ? 0 : a.qsl[i];
   const int qlen = virt ? a.virt_total_q : a.qsl[i + 1] - q0;
   const int rows_total = qlen * grp;
-  if (qt_lo * C::kRows >= rows_total) return;   // the whole cluster is idle
+  if (qt * C::kRows >= rows_total) return;      // nothing to do
   const int row0 = qt * C::kRows;               // this CTA's rows (may all be past the end)
   const int seq = virt ? a.virt_seq : max(0, a.seq_lens[i] - seq_off);
   const int ctx = seq - qlen;
   if (EXT && !virt && causal && ctx < 0 && seq_off > 0 && threadIdx.x == 0 && blockIdx.x == 0 &&
       blockIdx.y == 0)
     record_error(err, PA_DEVERR_LENGTH);   // queries inside the skipped prefix
-  const int last_row = min((qt_hi + 1) * C::kRows, rows_total) - 1;   // the cluster's last row
+  const int last_row = min((qt + 1) * C::kRows, rows_total) - 1;   // this CTA's last row
   int kv_end = causal ? ctx + last_row / grp + 1 : seq;
   kv_end = max(0, min(kv_end, seq));
-  // Sliding window (causal only): the cluster's first row sees nothing
+  // Sliding window (causal only): the CTA's first row sees nothing
   // before ctx + q_first + 1 - window, so the tiles start at that position
   // rounded down to a tile; later rows mask their own lower bound.
   int tbase = 0;
   if (window > 0) {
-    const int q_first = min(qt_lo * C::kRows, rows_total - 1) / grp;
+    const int q_first = min(qt * C::kRows, rows_total - 1) / grp;
     tbase = max(0, ctx + q_first + 1 - window) / C::kBN * C::kBN;
   }
   // KV split (a multiple of the tile): this CTA covers [split * kv_chunk,
@@ -248,10 +243,10 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
     tc::mbar_init(BAR(kQFull), C::kRows);
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(BAR(kKFull + b), 1);
-      // Released by every issuing thread of every CTA of the cluster.
-      tc::mbar_init(BAR(kKEmpty + b), kIssuers * CL);
+      // Released by every issuing thread.
+      tc::mbar_init(BAR(kKEmpty + b), kIssuers);
       tc::mbar_init(BAR(kVFull + b), 1);
-      tc::mbar_init(BAR(kVEmpty + b), kIssuers * CL);
+      tc::mbar_init(BAR(kVEmpty + b), kIssuers);
       tc::mbar_init(BAR(kSFull + b), 1);
       tc::mbar_init(BAR(kPLo + b), C::kBM);
       tc::mbar_init(BAR(kPHi + b), C::kBM);
@@ -264,21 +259,15 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
   __syncthreads();
   if (warp == 0) tc::tmem_alloc(tmem_slot, C::kTmemCols);
   tc::tc_fence_before();
-  // Every barrier of the cluster is initialised before any CTA multicasts:
-  // each CTA arrives on the cluster barrier now and waits for it just before
-  // its first use of a peer or of TMEM, so the Q rows and the first block ids
-  // are fetched while the peer starts up.
+  // The launch is a cluster of one CTA, so the cluster barrier is a split
+  // barrier of this CTA: every thread arrives now and waits just before its
+  // first use of TMEM, and the Q rows and the first block ids are fetched
+  // while the TMEM allocation completes.
   tc::cluster_arrive();
   auto tmem_base = [&]() {
     return *reinterpret_cast<volatile uint32_t*>(sgen + C::kOffBar + 8 * kNumBars);
   };
-  constexpr uint16_t kMask = static_cast<uint16_t>((1u << CL) - 1u);
-  auto release = [&](uint32_t bar) {   // frees a K/V stage in every CTA of the cluster
-    if (CL > 1)
-      tc::mma_commit_mc(bar, kMask);
-    else
-      tc::mma_commit(bar);
-  };
+  auto release = [&](uint32_t bar) { tc::mma_commit(bar); };   // frees a K/V stage
   auto fail = [&]() {
     record_error(err, PA_DEVERR_TIMEOUT);
     *abort_flag = 1;
@@ -628,9 +617,9 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
     // ------------------------------------------------------------ K/V producer
     // Lane p looks after the tile's 16-token piece p: its block id (loaded
     // three tiles ahead and validated only when used, so the load's latency
-    // never stalls an issue) and, if p % CL is this CTA's rank, its TMA boxes (one per
-    // 64-column half), multicast to the whole cluster.  Every CTA expects
-    // the bytes of all loaded pieces on its own barrier.  V(j) goes out before
+    // never stalls an issue) and its TMA boxes (one per 64-column half of K,
+    // one for both halves of V).  The barrier expects the bytes of all loaded
+    // pieces.  V(j) goes out before
     // K(j+2) (PV(j) needs it first) and reuses K(j)'s block ids.
     if (lane == 0) {
       tc::tma_prefetch_desc(&kv_map);
@@ -638,7 +627,7 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
     }
     const int pc = lane;
     const bool box_lane = lane < C::kBN / 16;
-    const bool my_piece = box_lane && (pc % CL) == rank;
+    const bool my_piece = box_lane;
     auto in_range = [&](int j) -> bool {
       return box_lane && j < ntiles && tbase + j * C::kBN + 16 * pc < kv_end;
     };
@@ -657,7 +646,7 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
       const unsigned loaded = __ballot_sync(0xffffffffu, blk >= 0);
       const unsigned bad = __ballot_sync(0xffffffffu, blk == -2);
       if (lane == 0) {
-        if (bad != 0u && which == 0 && rank == 0) record_error(err, PA_DEVERR_BLOCK_ID);
+        if (bad != 0u && which == 0) record_error(err, PA_DEVERR_BLOCK_ID);
         if (which == 0) piece_ring[j % kPieceRing] = (static_cast<uint32_t>(j) << 8) | (loaded & 0xffu);
         tc::mbar_arrive_expect_tx(
             full, static_cast<uint32_t>(__popc(loaded)) *
@@ -674,20 +663,13 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
       } else if (!MLA && my_piece && blk >= 0 && which == 1) {
         // V: both halves of the piece in one box (tensor map coordinates:
         // column 0, token, half 0, head, 2 * block + 1).
-        const uint32_t d = dst + pc * kVPiece;
-        if (CL > 1)
-          tc::tma_load_5d_mc(d, &v_map, full, kMask, 0, (tok0 + 16 * pc) % bs, 0, kvh, 2 * blk + 1);
-        else
-          tc::tma_load_5d(d, &v_map, full, 0, (tok0 + 16 * pc) % bs, 0, kvh, 2 * blk + 1);
+        tc::tma_load_5d(dst + pc * kVPiece, &v_map, full, 0, (tok0 + 16 * pc) % bs, 0, kvh,
+                        2 * blk + 1);
       } else if (!MLA && my_piece && blk >= 0) {
 #pragma unroll
         for (int h = 0; h < C::kHalvesK; ++h) {
-          const uint32_t d = dst + h * (C::kBN * 128) + pc * C::kPieceBytes;
-          if (CL > 1)
-            tc::tma_load_5d_mc(d, &kv_map, full, kMask, h * 64, kvh, (tok0 + 16 * pc) % bs, which,
-                               blk);
-          else
-            tc::tma_load_5d(d, &kv_map, full, h * 64, kvh, (tok0 + 16 * pc) % bs, which, blk);
+          tc::tma_load_5d(dst + h * (C::kBN * 128) + pc * C::kPieceBytes, &kv_map, full, h * 64, kvh,
+                          (tok0 + 16 * pc) % bs, which, blk);
         }
       }
     };
@@ -745,9 +727,6 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem_base(), C::kTmemCols);
   }
-  // No CTA leaves while a peer may still multicast into its shared memory or
-  // arrive on its barriers.
-  if (CL > 1) tc::cluster_sync();
 }
 
 // ---------------------------------------------------------------- host side
@@ -808,7 +787,7 @@ bool make_ws_map(CUtensorMap* map, const void* ws, long long rows, int H, int wi
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int DK, int DV, int BN, int VST, int CL, bool EXT, bool MLA>
+template <int DK, int DV, int BN, int VST, bool EXT, bool MLA>
 static cudaError_t launch_varlen_tc_t(const VarlenLaunch& L, cudaStream_t stream) {
   using C = TcCfg<DK, DV, BN, VST>;
   CUtensorMap map, vmap;
@@ -823,7 +802,7 @@ static cudaError_t launch_varlen_tc_t(const VarlenLaunch& L, cudaStream_t stream
         !make_v_map(&vmap, L.cache, L.num_blocks, L.bs, L.Hkv, DV))
       return cudaErrorInvalidValue;
   }
-  auto kern = varlen_tc_kernel<DK, DV, BN, VST, CL, EXT, MLA>;
+  auto kern = varlen_tc_kernel<DK, DV, BN, VST, EXT, MLA>;
   static DeviceFlags attr_set;
   cudaError_t e = set_smem_once(kern, C::kSmemBytes, attr_set);
   if (e != cudaSuccess) return e;
@@ -842,7 +821,6 @@ static cudaError_t launch_varlen_tc_t(const VarlenLaunch& L, cudaStream_t stream
   const long long qrows = virt ? L.virt_total_q : L.max_query_len;
   const long long rows = qrows * (L.Hq / L.Hkv);
   long long tiles = (rows + C::kRows - 1) / C::kRows;
-  tiles = (tiles + CL - 1) / CL * CL;
   const int splits = L.kv_splits > 1 ? L.kv_splits : 1;
   if (tiles * splits > 0x7fffffffLL) return cudaErrorInvalidValue;
   VarlenArgs a{};
@@ -876,9 +854,10 @@ static cudaError_t launch_varlen_tc_t(const VarlenLaunch& L, cudaStream_t stream
   cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
+  // A cluster of one CTA (the kernel's start-up uses the cluster barrier).
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.x = 1;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
@@ -886,19 +865,16 @@ static cudaError_t launch_varlen_tc_t(const VarlenLaunch& L, cudaStream_t stream
   return cudaLaunchKernelEx(&cfg, kern, map, vmap, a);
 }
 
-// CTAs per cluster sharing K/V tiles by multicast.
-constexpr int kVarlenCluster = 1;
-
 cudaError_t launch_varlen_tc(const VarlenLaunch& L, cudaStream_t stream) {
   if (L.mla_k != nullptr)   // MLA prefill attention: [nope | rope] keys, 128-wide values
-    return launch_varlen_tc_t<192, 128, 128, 1, kVarlenCluster, false, true>(L, stream);
+    return launch_varlen_tc_t<192, 128, 128, 1, false, true>(L, stream);
   const bool ext = L.window > 0 || L.kv_splits > 1 || L.ws != nullptr || L.virt_total_q > 0 ||
                    L.table_col0 != 0 || L.seq_off != 0;
   if (L.d == 128)
-    return ext ? launch_varlen_tc_t<128, 128, 128, 2, kVarlenCluster, true, false>(L, stream)
-               : launch_varlen_tc_t<128, 128, 128, 2, kVarlenCluster, false, false>(L, stream);
-  return ext ? launch_varlen_tc_t<64, 64, 128, 2, kVarlenCluster, true, false>(L, stream)
-             : launch_varlen_tc_t<64, 64, 128, 2, kVarlenCluster, false, false>(L, stream);
+    return ext ? launch_varlen_tc_t<128, 128, 128, 2, true, false>(L, stream)
+               : launch_varlen_tc_t<128, 128, 128, 2, false, false>(L, stream);
+  return ext ? launch_varlen_tc_t<64, 64, 128, 2, true, false>(L, stream)
+             : launch_varlen_tc_t<64, 64, 128, 2, false, false>(L, stream);
 }
 
 }  // namespace pa
