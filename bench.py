@@ -131,6 +131,80 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+class NvmlClockSampler:
+    """SM clock and throttle reasons polled through NVML from a host thread
+    every ~0.5 ms, so that samples land inside a timed region of a few
+    milliseconds; the device is matched to the CUDA device by UUID.  Falls
+    back to ClockSampler (nvidia-smi, 10 ms) where NVML cannot be loaded."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device_index: int):
+        import ctypes
+        import threading
+        self.ct, self.threading = ctypes, threading
+        self.dev = device_index
+        self.samples = []            # (perf_counter, sm MHz, reason bits)
+        self.windows = []            # (t0, t1) of timed regions
+        self.fallback = None
+        self.nvml = self.handle = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            h = ctypes.c_void_p()
+            uuid = str(getattr(torch.cuda.get_device_properties(device_index), "uuid", ""))
+            ok = False
+            if uuid:
+                ok = nv.nvmlDeviceGetHandleByUUID(("GPU-" + uuid).encode(), ctypes.byref(h)) == 0
+            if not ok and nv.nvmlDeviceGetHandleByIndex_v2(device_index, ctypes.byref(h)) != 0:
+                raise OSError("no NVML handle")
+            self.nvml, self.handle = nv, h
+            mx = ctypes.c_uint()
+            self.max_mhz = float(mx.value) if nv.nvmlDeviceGetMaxClockInfo(
+                h, 1, ctypes.byref(mx)) == 0 else None
+            self._reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        except (OSError, AttributeError):
+            self.fallback = ClockSampler(device_index)
+
+    def _poll(self):
+        ct, nv, h = self.ct, self.nvml, self.handle
+        clk, rs = ct.c_uint(), ct.c_ulonglong()
+        while not self._stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ct.byref(clk)) == 0:
+                r = rs.value if self._reasons(h, ct.byref(rs)) == 0 else 0
+                self.samples.append((time.perf_counter(), float(clk.value), int(r)))
+            time.sleep(0.0005)
+
+    def start(self):
+        if self.fallback is not None:
+            return self.fallback.start()
+        self._stop = self.threading.Event()
+        self._thread = self.threading.Thread(target=self._poll, daemon=True)
+        self._thread.start()
+        while not self.samples and self._thread.is_alive():
+            time.sleep(0.001)
+
+    def mark(self, t0, t1):
+        self.windows.append((t0, t1))
+
+    def stop(self):
+        if self.fallback is not None:
+            return self.fallback.stop()
+        self._stop.set()
+        self._thread.join()
+        inside = [x for x in self.samples if any(a <= x[0] <= b for a, b in self.windows)]
+        use = inside or self.samples
+        reasons = sorted({name for _, _, r in use for bit, name in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(x[1] for x in use) if use else None,
+                "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(use),
+                "samples_in_timed_regions": len(inside), "timed_regions": len(self.windows),
+                "how": "NVML from a host thread every ~0.5 ms; the median over samples taken "
+                       "inside the timed regions (all samples if none landed)"}
+
+
 def max_over_ranks(values, dist=None, device=None):
     """Element-wise maximum of this rank's timings (a list of floats) over the
     process group -- the slowest replica sets the job's time; unchanged on a
@@ -162,12 +236,6 @@ def to_dev_bf16(bits, device):
 
 def to_dev(a, dtype, device):
     return torch.from_numpy(np.ascontiguousarray(a)).to(device=device, dtype=dtype)
-
-
-def device_pool(shape, seed, device):
-    g = torch.Generator(device=device)
-    g.manual_seed(seed)
-    return torch.randn(shape, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
 
 
 # ---------------------------------------------------------------------------
@@ -325,14 +393,20 @@ def run_e2e(pa, b, step, steps, warmup, device):
 
 
 def cpu_baseline_sample(b, budget_s=12.0, threads=None):
-    """The oracle, as it stands, on a bounded sample of the decode batch:
-    whole requests in order until ~budget_s of CPU work.  Returns
-    (GB/s of KV processed, threads, sample description)."""
+    """The oracle, as it stands, on a bounded sample of the decode batch: the
+    whole batch once (which is also the reference of the headline's parity
+    pass), then groups of requests in order until ~budget_s of CPU work.
+    Returns (GB/s of KV processed, threads, sample description, (out, lse)
+    of the whole batch)."""
     import oracle
     threads = threads or (os.cpu_count() or 1)
     pool = oracle.reshape_and_cache(b.key, b.value, b.pool, b.slot_mapping, b.block_size)
-    done_bytes, elapsed, n = 0, 0.0, 0
     per_tok = b.num_kv_heads * b.head_size * 2 * 2
+    t0 = time.perf_counter()
+    ref = oracle.paged_attention(b.q, pool, b.block_table, b.query_start_loc, b.seq_lens, b.scale,
+                                 threads=threads)
+    elapsed = time.perf_counter() - t0
+    done_bytes, n = int(b.seq_lens.astype(np.int64).sum()) * per_tok, b.num_seqs
     group = max(1, threads)
     while elapsed < budget_s:
         # A group of requests per call (so the oracle's threads have work),
@@ -348,12 +422,21 @@ def cpu_baseline_sample(b, budget_s=12.0, threads=None):
         n += len(grp)
     return done_bytes / elapsed / 1e9, threads, (
         f"oracle decode attention (fp64, paged gather + softmax), {n} request-decodes cycling "
-        f"through the {b.num_seqs}-request GQA decode batch, {elapsed:.1f} s of {threads} threads")
+        f"through the {b.num_seqs}-request GQA decode batch, {elapsed:.1f} s of {threads} "
+        "threads"), ref
 
 
 # ---------------------------------------------------------------------------
-# Secondary workloads (kernels timed alone, events on the launch stream).
+# Secondary workloads: every other named configuration, its kernels timed
+# alone (CUDA events on the launch stream, median of >= 50 launches), each
+# line with its seed, one parity pass against the oracle on the same seeded
+# inputs (the rows / requests it names), the oracle's own rate on that
+# sample, and the roofline of its dominant kernel.
 # ---------------------------------------------------------------------------
+
+SECONDARY_REPS = 50
+OUT_ATOL, LSE_ATOL = 1e-2, 1e-3
+
 
 def time_events(fn, reps, warmup=3):
     for _ in range(warmup):
@@ -392,13 +475,145 @@ def l2_flusher(device):
     return lambda: buf.fill_(1)
 
 
-def bench_prefill(pa, device, pk, flush, reps=10):
-    """Chunked prefill: the varlen kernel on its own."""
-    b = workloads.chunked_prefill(with_pool=False)
-    pool = device_pool((b.num_blocks, 2, b.block_size, b.num_kv_heads, b.head_size), 3, device)
+def _timed_with_flush(fn, flush, reps):
+    """Median of reps event-timed launches, L2 flushed before each."""
+    for _ in range(3):
+        flush()
+        fn()
+    times = []
+    for _ in range(reps):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    return statistics.median(times)
+
+
+def _bf16_ulp(x):
+    ax = np.maximum(np.abs(x), np.finfo(np.float32).tiny)
+    return np.exp2(np.floor(np.log2(ax)) - 7)
+
+
+def parity(got_o, ref_o, got_l, ref_l, checked):
+    """Max abs errors of a parity pass and whether every element met the
+    tolerance: bf16 outputs within max(1e-2, one bf16 ulp of the oracle
+    value), LSE within 1e-3 (and -inf exactly where the oracle's is)."""
+    got_o, ref_o = np.asarray(got_o, np.float64), np.asarray(ref_o, np.float64)
+    got_l, ref_l = np.asarray(got_l, np.float64), np.asarray(ref_l, np.float64)
+    eo = np.abs(got_o - ref_o)
+    bad_o = int((eo > np.maximum(OUT_ATOL, _bf16_ulp(ref_o))).sum()) + int(
+        (~np.isfinite(got_o)).sum())
+    fin = np.isfinite(ref_l)
+    el = np.abs(got_l[fin] - ref_l[fin])
+    bad_l = int((el > LSE_ATOL).sum()) + int((np.isneginf(got_l) != np.isneginf(ref_l)).sum())
+    return {"max_abs_out_err": float(eo.max()) if eo.size else 0.0,
+            "max_abs_lse_err": float(el.max()) if el.size else 0.0,
+            "out_beyond_tol": bad_o, "lse_beyond_tol": bad_l, "pass": bad_o == 0 and bad_l == 0,
+            "checked": checked,
+            "tolerance": "out: max(1e-2, 1 bf16 ulp of the oracle value); lse: 1e-3"}
+
+
+def _timed_oracle(fn):
+    t0 = time.perf_counter()
+    r = fn()
+    return r, time.perf_counter() - t0
+
+
+def cpu_line(rate, unit, seconds, threads, sample):
+    return {"value": rate, "unit": unit, "cores": threads, "kind": "oracle",
+            "sample": f"{sample}; {seconds:.2f} s of {threads} threads"}
+
+
+def roofline(bound, achieved, pk, unit, kernel, algo, traffic=None):
+    if bound == "hbm":
+        peak, src = pk["hbm_gbs"], "MEASURED_PEAKS hbm_gbs"
+    else:
+        peak, src = pk["bf16_tflops"], "MEASURED_PEAKS bf16_tflops (burst)"
+    if pk["source"] != "measured":
+        src = "fallback"
+    return {"bound": bound, "kernel": kernel, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "traffic": traffic, "algorithmic_per_launch": algo,
+            "peak_source": src + (" (of measured)" if pk["source"] == "measured" else
+                                  " (of fallback)")}
+
+
+def sub_pool(pool, block_table, seq_lens, reqs):
+    """The blocks of requests ``reqs`` gathered into a small pool, with a
+    table that numbers them 0, 1, ... in request order: the oracle then runs
+    on those requests alone (the whole pool in fp64 can take tens of GB)."""
+    bs = pool.shape[2] if pool.ndim == 5 else pool.shape[1]
+    ids = [block_table[r, :(int(seq_lens[r]) + bs - 1) // bs] for r in reqs]
+    width = max(1, max(len(x) for x in ids))
+    table = np.full((len(reqs), width), -1, np.int32)
+    k = 0
+    for i, x in enumerate(ids):
+        table[i, :len(x)] = np.arange(k, k + len(x), dtype=np.int32)
+        k += len(x)
+    return pool[np.concatenate(ids)], table
+
+
+def _new_slots(table, seq_lens, reqs, bs):
+    """Slots of each request's newest token (position seq_len - 1) in the
+    small pool of sub_pool."""
+    return np.array([int(table[k, (int(seq_lens[r]) - 1) // bs]) * bs + (int(seq_lens[r]) - 1) % bs
+                     for k, r in enumerate(reqs)], np.int64)
+
+
+def _last_rows(b):
+    return b.query_start_loc[1:] - 1
+
+
+def bench_tiny(pa, device, pk, flush, reps=SECONDARY_REPS, check=True):
+    """The tiny paged-attention batch: the whole step (cache write + varlen
+    attention with LSE), launch-bound; timed warm (everything fits in L2)."""
+    b = workloads.tiny_paged()
+    pool = to_dev_bf16(b.pool, device)
+    q, key, val = (to_dev_bf16(x, device) for x in (b.q, b.key, b.value))
+    slots = to_dev(b.slot_mapping, torch.int64, device)
+    table = to_dev(b.block_table, torch.int32, device)
+    qsl = to_dev(b.query_start_loc, torch.int32, device)
+    seq = to_dev(b.seq_lens, torch.int32, device)
+    out = torch.empty_like(q)
+    lse = torch.empty((b.num_tokens, b.num_q_heads), dtype=torch.float32, device=device)
+    mq = int(b.query_lens.max())
+
+    def step():
+        pa.pa_reshape_and_cache(key, val, pool, slots)
+        pa.pa_varlen_fwd(q, pool, table, qsl, seq, mq, b.scale, out=out, lse=lse)
+    ms = time_events(step, reps)
+    tf = b.causal_flops() / (ms * 1e-3) / 1e12
+    res = {"workload": b.name, "seed": b.seed, "kernels": "reshape_and_cache + varlen_tc_kernel",
+           "ms": ms, "reps": reps, "tflops": tf, "causal_flops": b.causal_flops(),
+           "l2": "warm (the whole batch is 170 KB)",
+           "note": "launch-bound: 7 query rows; the time is two kernel launches"}
+    if check:
+        import oracle
+        ref_pool = oracle.reshape_and_cache(b.key, b.value, b.pool, b.slot_mapping, b.block_size)
+        (ro, rl), dt = _timed_oracle(lambda: oracle.paged_attention(
+            b.q, ref_pool, b.block_table, b.query_start_loc, b.seq_lens, b.scale))
+        res["parity"] = parity(out.float().cpu().numpy(), ro, lse.cpu().numpy(), rl,
+                               "all 7 rows x 4 heads")
+        res["parity"]["cache_write_bit_exact"] = bool(np.array_equal(
+            pool.view(torch.int16).cpu().numpy().view(np.uint16), ref_pool))
+        res["cpu_baseline"] = cpu_line(b.causal_flops() / dt / 1e12, "TFLOP/s", dt,
+                                       oracle.default_threads(),
+                                       "oracle varlen attention over the whole tiny batch")
+    return res
+
+
+def bench_prefill(pa, device, pk, flush, reps=SECONDARY_REPS, check=True):
+    """Chunked prefill: the varlen kernel on its own, L2 flushed before each
+    launch."""
+    b = workloads.chunked_prefill()
+    pool = to_dev_bf16(b.pool, device)
     q = to_dev_bf16(b.q, device)
-    table, qsl = to_dev(b.block_table, torch.int32, device), to_dev(b.query_start_loc,
-                                                                     torch.int32, device)
+    pa.pa_reshape_and_cache(to_dev_bf16(b.key, device), to_dev_bf16(b.value, device), pool,
+                            to_dev(b.slot_mapping, torch.int64, device))
+    table = to_dev(b.block_table, torch.int32, device)
+    qsl = to_dev(b.query_start_loc, torch.int32, device)
     seq = to_dev(b.seq_lens, torch.int32, device)
     out = torch.empty_like(q)
     lse = torch.empty((b.num_tokens, b.num_q_heads), dtype=torch.float32, device=device)
@@ -409,21 +624,62 @@ def bench_prefill(pa, device, pk, flush, reps=10):
     ms = _timed_with_flush(prefill, flush, reps)
     warm = time_events(prefill, reps)
     tf = b.causal_flops() / (ms * 1e-3) / 1e12
-    res = {"workload": b.name, "kernel": "varlen_fwd", "ms": ms, "warm_ms": warm,
-                              "tflops": tf, "causal_flops": b.causal_flops(),
-                              "frac_of_bf16_peak": tf / pk["bf16_tflops"],
-                              "peak": "bf16_tflops (measured burst)" if pk["source"] == "measured"
-                              else "fallback"}
+    res = {"workload": b.name, "seed": b.seed, "kernel": "varlen_tc_kernel", "ms": ms,
+           "warm_ms": warm, "reps": reps, "tflops": tf, "causal_flops": b.causal_flops(),
+           "frac_of_bf16_peak": tf / pk["bf16_tflops"],
+           "l2": "flushed (256 MB write) before each launch",
+           "roofline": roofline("tensor", tf, pk, "TFLOP/s", "varlen_tc_kernel",
+                                b.causal_flops())}
+    if check:
+        import oracle
+        prefill()
+        torch.cuda.synchronize()
+        rng = np.random.default_rng(1003)
+        mask = np.zeros(b.num_tokens, np.uint8)
+        for i in range(b.num_seqs):
+            a, e = int(b.query_start_loc[i]), int(b.query_start_loc[i + 1])
+            mask[[a, e - 1]] = 1
+            mask[rng.integers(a, e, size=2)] = 1
+        rows = mask.astype(bool)
+        ref_pool = oracle.reshape_and_cache(b.key, b.value, b.pool, b.slot_mapping, b.block_size)
+        (ro, rl), dt = _timed_oracle(lambda: oracle.paged_attention(
+            b.q, ref_pool, b.block_table, b.query_start_loc, b.seq_lens, b.scale, row_mask=mask))
+        res["parity"] = parity(out.float().cpu().numpy()[rows], ro[rows],
+                               lse.cpu().numpy()[rows], rl[rows],
+                               f"{int(rows.sum())} rows (first, last and 2 random of each "
+                               f"request) x {b.num_q_heads} heads")
+        # Causal-visible flops of the sampled rows.
+        pos = np.concatenate([np.arange(int(b.seq_lens[i] - b.query_lens[i]), int(b.seq_lens[i]))
+                              for i in range(b.num_seqs)])
+        fl = 4 * b.head_size * b.num_q_heads * int((pos[rows] + 1).sum())
+        res["cpu_baseline"] = cpu_line(fl / dt / 1e12, "TFLOP/s", dt, oracle.default_threads(),
+                                       f"oracle varlen attention on the {int(rows.sum())} "
+                                       "sampled rows")
     del pool, q, out
     torch.cuda.empty_cache()
     return res
 
 
-def bench_long_decode(pa, device, pk, flush, reps=10):
-    """Long-context split-KV decode (8 x 131072)."""
-    b = workloads.long_decode(with_pool=False)
-    pool = device_pool((b.num_blocks, 2, b.block_size, b.num_kv_heads, b.head_size), 4, device)
+def _decode_check(b, out, lse, reqs, ref_fn, unit_bytes):
+    """Parity of decode outputs on requests ``reqs`` and the oracle's rate
+    on them: ref_fn() -> (out, lse) of those requests, in order."""
+    import oracle
+    (ro, rl), dt = _timed_oracle(ref_fn)
+    par = parity(out.float().cpu().numpy()[reqs], ro, lse.cpu().numpy()[reqs], rl,
+                 f"requests {[int(r) for r in reqs]} (all heads)")
+    done = int(b.seq_lens[reqs].astype(np.int64).sum()) * unit_bytes
+    return par, cpu_line(done / dt / 1e9, "GB/s", dt, oracle.default_threads(),
+                         f"oracle decode on the {len(reqs)} checked requests")
+
+
+def bench_long_decode(pa, device, pk, flush, reps=SECONDARY_REPS, check=True):
+    """Long-context split-KV decode (8 x 131072): stage 1, and stage 1 +
+    merge, cycling through two pool copies."""
+    b = workloads.long_decode()
     N, hq, d = b.num_seqs, b.num_q_heads, b.head_size
+    pool = to_dev_bf16(b.pool, device)
+    pa.pa_reshape_and_cache(to_dev_bf16(b.key, device), to_dev_bf16(b.value, device), pool,
+                            to_dev(b.slot_mapping, torch.int64, device))
     q = to_dev_bf16(b.q, device).view(N, hq, d)
     table, seq = to_dev(b.block_table, torch.int32, device), to_dev(b.seq_lens, torch.int32,
                                                                     device)
@@ -439,60 +695,104 @@ def bench_long_decode(pa, device, pk, flush, reps=10):
     both = _timed_rotating([lambda p=p: pa.pa_decode(q, p, table, seq, b.scale, ws, o, lo, 131072)
                             for p in pools], reps)
     gbs = b.kv_bytes() / (st1 * 1e-3) / 1e9
-    res = {"workload": b.name, "num_splits": S, "stage1_ms": st1, "stage1_warm_ms": warm,
-                          "decode_plus_merge_ms": both, "kv_bytes": b.kv_bytes(),
-                          "stage1_gbs": gbs, "frac_of_hbm_peak": gbs / pk["hbm_gbs"],
-                          "step_gbs": b.kv_bytes() / (both * 1e-3) / 1e9,
-                          "l2": "2 rotating pool copies"}
+    sha = kernel_source_sha(["decode.cu", "pa_common.cuh"])
+    res = {"workload": b.name, "seed": b.seed, "num_splits": S, "stage1_ms": st1,
+           "stage1_warm_ms": warm, "reps": reps, "decode_plus_merge_ms": both,
+           "kv_bytes": b.kv_bytes(), "stage1_gbs": gbs, "frac_of_hbm_peak": gbs / pk["hbm_gbs"],
+           "step_gbs": b.kv_bytes() / (both * 1e-3) / 1e9, "l2": "2 rotating pool copies",
+           "roofline": roofline("hbm", gbs, pk, "GB/s", "decode_splitkv_kernel", b.kv_bytes(),
+                                profiled_traffic("decode_splitkv_long_decode.md", sha))}
+    if check:
+        import oracle
+        pa.pa_decode(q, pools[0], table, seq, b.scale, ws, o, lo, 131072)
+        torch.cuda.synchronize()
+        reqs = np.array([0, 5])
+
+        def ref():
+            sp, st = sub_pool(b.pool, b.block_table, b.seq_lens, reqs)
+            sp = oracle.reshape_and_cache(b.key[reqs], b.value[reqs], sp,
+                                          _new_slots(st, b.seq_lens, reqs, b.block_size),
+                                          b.block_size)
+            return oracle.paged_attention(b.q[_last_rows(b)[reqs]], sp, st,
+                                          np.arange(len(reqs) + 1, dtype=np.int32),
+                                          b.seq_lens[reqs], b.scale)
+        res["parity"], res["cpu_baseline"] = _decode_check(b, o, lo, reqs, ref,
+                                                           b.num_kv_heads * d * 2 * 2)
     del pool, pools, q, ws
     torch.cuda.empty_cache()
     return res
 
 
-def bench_mla(pa, device, pk, flush, reps=10):
-    """MLA latent decode (DeepSeek-V3 shape)."""
-    m = workloads.mla_decode(with_pool=False)
-    pool = device_pool((m.num_blocks, m.block_size, m.kv_lora_rank + m.rope_dim), 5, device)
+def bench_mla(pa, device, pk, flush, reps=SECONDARY_REPS, check=True):
+    """MLA latent decode (DeepSeek-V3 shape), split count from the library's
+    planner, cycling through two pool copies; the step's cache write of the
+    128 new latent rows timed alone."""
+    m = workloads.mla_decode()
+    pool = to_dev_bf16(m.pool, device)
     q = to_dev_bf16(m.q, device)
     table, seq = to_dev(m.block_table, torch.int32, device), to_dev(m.seq_lens, torch.int32,
                                                                     device)
-    S = mla_splits(m, pa.pa_device_sm_count())
+    mx = int(m.seq_lens.max())
+    S = pa.pa_mla_num_kv_splits(m.batch, m.num_heads, mx, pa.pa_device_sm_count())
     ws = pa.decode_workspace(m.batch, m.num_heads, S, m.kv_lora_rank, device=device)
     o = torch.empty((m.batch, m.num_heads, m.kv_lora_rank), dtype=torch.bfloat16, device=device)
     lo = torch.empty((m.batch, m.num_heads), dtype=torch.float32, device=device)
-    mx = int(m.seq_lens.max())
     pools = [pool, pool.clone()]
     mla = [lambda p=p: pa.pa_mla_decode(q, p, table, seq, m.scale, ws, o, lo, max_seq_len=mx)
            for p in pools]
     ms = _timed_rotating(mla, reps)
     warm = time_events(mla[0], reps)
-    # The step's cache write of the 128 new latent rows, timed alone.
     kv_c, k_pe, slots = workloads.mla_new_tokens(m)
     d_kv_c, d_k_pe = to_dev_bf16(kv_c, device), to_dev_bf16(k_pe, device)
     d_slots = to_dev(slots, torch.int64, device)
-    write_ms = _timed_with_flush(lambda: pa.pa_mla_cache_write(d_kv_c, d_k_pe, pool, d_slots),
+    scratch = pools[1]
+    write_ms = _timed_with_flush(lambda: pa.pa_mla_cache_write(d_kv_c, d_k_pe, scratch, d_slots),
                                  flush, reps)
     gbs = m.kv_bytes() / (ms * 1e-3) / 1e9
     flops = int(m.seq_lens.astype(np.int64).sum()) * m.num_heads * 2 * (
         m.kv_lora_rank + m.rope_dim + m.kv_lora_rank)
-    res = {"workload": m.name, "num_splits": S, "ms": ms, "warm_ms": warm, "kv_bytes": m.kv_bytes(),
-                         "gbs": gbs, "frac_of_hbm_peak": gbs / pk["hbm_gbs"],
-                         "tflops": flops / (ms * 1e-3) / 1e12,
-                         "cache_write_us": write_ms * 1e3, "cache_write_tokens": int(m.batch),
-                         "l2": "2 rotating pool copies (cache write: L2 flushed)"}
+    sha = kernel_source_sha(["mla_tc.cu", "tc_common.cuh"])
+    res = {"workload": m.name, "seed": m.seed, "num_splits": S,
+           "splits_from": "pa_mla_num_kv_splits", "ms": ms, "warm_ms": warm, "reps": reps,
+           "kv_bytes": m.kv_bytes(), "gbs": gbs, "frac_of_hbm_peak": gbs / pk["hbm_gbs"],
+           "tflops": flops / (ms * 1e-3) / 1e12,
+           "cache_write_us": write_ms * 1e3, "cache_write_tokens": int(m.batch),
+           "l2": "2 rotating pool copies (cache write: L2 flushed)",
+           "roofline": roofline("hbm", gbs, pk, "GB/s", "mla_tc_kernel", m.kv_bytes(),
+                                profiled_traffic("mla_tc_mla_decode.md", sha))}
+    if check:
+        import oracle
+        mla[0]()
+        torch.cuda.synchronize()
+        order = np.argsort(m.seq_lens, kind="stable")
+        rng = np.random.default_rng(1005)
+        pick = set(order[:2].tolist()) | set(order[-2:].tolist()) | set(
+            rng.choice(m.batch, 4, replace=False).tolist())
+        reqs = np.array(sorted(pick))
+        mask = np.zeros(m.batch, np.uint8)
+        mask[reqs] = 1
+
+        def ref():
+            ro, rl = oracle.mla_decode(m.q, m.pool, m.block_table, m.seq_lens, m.scale,
+                                       req_mask=mask)
+            return ro[reqs], rl[reqs]
+        res["parity"], res["cpu_baseline"] = _decode_check(
+            m, o, lo, reqs, ref, (m.kv_lora_rank + m.rope_dim) * 2)
     del pool, pools, q, ws
     torch.cuda.empty_cache()
     return res
 
 
-def bench_mla_prefill(pa, device, pk, flush, reps=10):
+def bench_mla_prefill(pa, device, pk, flush, reps=SECONDARY_REPS, check=True):
     """MLA chunked prefill, multi-head formulation (DeepSeek-V3 shape): the
     kv_b_proj expansion of every context token and the attention over the
     expanded keys and values, timed together and apart."""
-    m = workloads.mla_prefill(with_pool=False)
-    pool = device_pool((m.num_blocks, m.block_size, m.kv_lora_rank + m.rope_dim), 7, device)
+    m = workloads.mla_prefill()
+    pool = to_dev_bf16(m.pool, device)
+    pa.pa_mla_cache_write(to_dev_bf16(m.kv_c, device), to_dev_bf16(m.k_pe, device), pool,
+                          to_dev(m.slot_mapping, torch.int64, device))
     q = to_dev_bf16(m.q, device)
-    w = to_dev_bf16(m.w_kv_b, device)
+    wt = to_dev_bf16(m.w_kv_b, device)
     table = to_dev(m.block_table, torch.int32, device)
     qsl = to_dev(m.query_start_loc, torch.int32, device)
     seq = to_dev(m.seq_lens, torch.int32, device)
@@ -506,34 +806,55 @@ def bench_mla_prefill(pa, device, pk, flush, reps=10):
     k_ws = ws[:kv_elems * 192 * 2].view(torch.bfloat16).view(m.num_seqs, S, m.num_heads, 192)
     v_ws = ws[kv_elems * 192 * 2:kv_elems * 320 * 2].view(torch.bfloat16).view(
         m.num_seqs, S, m.num_heads, 128)
-    call = lambda: pa.pa_mla_prefill(q, pool, w, table, qsl, seq, mq, m.scale, ws, S, out=out,
-                                     lse=lse)
+
+    def call():
+        pa.pa_mla_prefill(q, pool, wt, table, qsl, seq, mq, m.scale, ws, S, out=out, lse=lse)
     total = _timed_with_flush(call, flush, reps)
     warm = time_events(call, reps)
-    expand = _timed_with_flush(lambda: pa.pa_mla_expand_kv(pool, w, table, seq, k_ws, v_ws),
+    expand = _timed_with_flush(lambda: pa.pa_mla_expand_kv(pool, wt, table, seq, k_ws, v_ws),
                                flush, reps)
     attn = total - expand
     ef, af = m.expand_flops(), m.causal_flops()
-    res = {"workload": m.name, "ms": total, "warm_ms": warm, "expand_ms": expand,
-           "attention_ms": attn,
+    tf = (ef + af) / (total * 1e-3) / 1e12
+    res = {"workload": m.name, "seed": m.seed, "ms": total, "warm_ms": warm, "reps": reps,
+           "expand_ms": expand, "attention_ms": attn,
            "expand_tflops": ef / (expand * 1e-3) / 1e12,
            "attention_tflops": af / (attn * 1e-3) / 1e12,
-           "tflops": (ef + af) / (total * 1e-3) / 1e12,
-           "frac_of_bf16_peak": (ef + af) / (total * 1e-3) / 1e12 / pk["bf16_tflops"],
-           "expanded_bytes": kv_elems * 320 * 2}
-    del pool, q, w, ws
+           "tflops": tf, "frac_of_bf16_peak": tf / pk["bf16_tflops"],
+           "expanded_bytes": kv_elems * 320 * 2,
+           "l2": "flushed (256 MB write) before each launch",
+           "roofline": roofline("tensor", tf, pk, "TFLOP/s",
+                                "mla_expand_kernel + varlen_tc_kernel", ef + af)}
+    if check:
+        import oracle
+        call()
+        torch.cuda.synchronize()
+        ref_pool = oracle.mla_cache_write(m.kv_c, m.k_pe, m.pool, m.slot_mapping, m.block_size)
+        rng = np.random.default_rng(1007)
+        rows = np.zeros(m.num_tokens, np.uint8)
+        for i in range(m.num_seqs):
+            a, e = int(m.query_start_loc[i]), int(m.query_start_loc[i + 1])
+            rows[[a, e - 1]] = 1
+            rows[rng.integers(a, e)] = 1
+        heads = np.zeros(m.num_heads, np.uint8)
+        heads[rng.choice(m.num_heads, 8, replace=False)] = 1
+        (ro, rl), dt = _timed_oracle(lambda: oracle.mla_prefill(
+            m.q, ref_pool, m.w_kv_b, m.block_table, m.query_start_loc, m.seq_lens, m.scale,
+            head_mask=heads, row_mask=rows))
+        r, h = rows.astype(bool), heads.astype(bool)
+        res["parity"] = parity(out.float().cpu().numpy()[r][:, h], ro[r][:, h],
+                               lse.cpu().numpy()[r][:, h], rl[r][:, h],
+                               f"{int(r.sum())} rows x {int(h.sum())} heads")
+        pos = np.concatenate([np.arange(int(m.seq_lens[i] - m.query_lens[i]), int(m.seq_lens[i]))
+                              for i in range(m.num_seqs)])
+        fl = 2 * (192 + 128) * int(h.sum()) * int((pos[r] + 1).sum())
+        res["cpu_baseline"] = cpu_line(fl / dt / 1e12, "TFLOP/s", dt, oracle.default_threads(),
+                                       "oracle MLA prefill on the checked rows x heads "
+                                       "(rate counts their causal-visible attention flops; the "
+                                       "oracle's time also holds its kv_b_proj expansion)")
+    del pool, q, wt, ws
     torch.cuda.empty_cache()
     return res
-
-
-def device_fp8_pool(shape, seed, device):
-    """Uniformly random finite e4m3 codes (the NaN codes 0x7F / 0xFF excluded),
-    drawn on the device."""
-    g = torch.Generator(device=device)
-    g.manual_seed(seed)
-    r = torch.randint(0, 254, shape, generator=g, device=device, dtype=torch.uint8)
-    r += (r >= 0x7F).to(torch.uint8)
-    return r
 
 
 def fp8_kernel_name(d, grp):
@@ -544,16 +865,17 @@ def fp8_kernel_name(d, grp):
     return f"decode_splitkv_fp8_kernel<{d},{stages},{2 if wide else 1}>"
 
 
-def bench_fp8_decode(pa, device, pk, flush, reps=10):
+def bench_fp8_decode(pa, device, pk, flush, reps=SECONDARY_REPS, check=True):
     """Split-KV decode over an fp8 (e4m3) pool, on the GQA decode batch and the
     long-context batch: stage 1 alone, and the whole step (quantising cache
     write + stage 1 + merge)."""
     res = {}
     ks, vs = workloads.FP8_K_SCALE, workloads.FP8_V_SCALE
-    for make, seed in ((workloads.gqa_decode, 12), (workloads.long_decode, 14)):
+    for make in (workloads.gqa_decode, workloads.long_decode):
         b = make(with_pool=False)
         N, hq, d = b.num_seqs, b.num_q_heads, b.head_size
-        pool = device_fp8_pool((b.num_blocks, 2, b.block_size, b.num_kv_heads, d), seed, device)
+        host_pool = workloads.fp8_pool(b)
+        pool = torch.from_numpy(host_pool).to(device)
         q = to_dev_bf16(b.q, device).view(N, hq, d)
         key, value = to_dev_bf16(b.key, device), to_dev_bf16(b.value, device)
         slots = to_dev(b.slot_mapping, torch.int64, device)
@@ -564,7 +886,6 @@ def bench_fp8_decode(pa, device, pk, flush, reps=10):
         ws = pa.decode_workspace(N, hq, S, d, device=device)
         o = torch.empty((N, hq, d), dtype=torch.bfloat16, device=device)
         lo = torch.empty((N, hq), dtype=torch.float32, device=device)
-
         pools = [pool, pool.clone()]
 
         def step(p):
@@ -577,27 +898,50 @@ def bench_fp8_decode(pa, device, pk, flush, reps=10):
         both = _timed_rotating([lambda p=p: step(p) for p in pools], reps)
         kv = b.kv_bytes() // 2                      # one byte per element
         gbs = kv / (st1 * 1e-3) / 1e9
-        res[b.name] = {"num_splits": S, "stage1_ms": st1, "stage1_warm_ms": warm,
-                       "step_ms": both, "kv_bytes": kv,
-                       "stage1_gbs": gbs, "frac_of_hbm_peak": gbs / pk["hbm_gbs"],
-                       "step_gbs": kv / (both * 1e-3) / 1e9,
-                       "kernel": fp8_kernel_name(d, b.num_q_heads // b.num_kv_heads),
-                       "l2": "2 rotating pool copies"}
-        del pool, pools, q, ws
+        kname = fp8_kernel_name(d, b.num_q_heads // b.num_kv_heads)
+        sha = kernel_source_sha(["decode_fp8.cu", "pa_common.cuh"])
+        short = "gqa_decode" if make is workloads.gqa_decode else "long_decode"
+        line = {"seed": b.seed, "pool_seed": [b.seed, 2], "num_splits": S, "stage1_ms": st1,
+                "stage1_warm_ms": warm, "reps": reps, "step_ms": both, "kv_bytes": kv,
+                "stage1_gbs": gbs, "frac_of_hbm_peak": gbs / pk["hbm_gbs"],
+                "step_gbs": kv / (both * 1e-3) / 1e9, "kernel": kname,
+                "l2": "2 rotating pool copies",
+                "roofline": roofline("hbm", gbs, pk, "GB/s", kname, kv,
+                                     profiled_traffic(f"decode_splitkv_fp8_{short}.md", sha))}
+        if check:
+            import oracle
+            step(pools[0])
+            torch.cuda.synchronize()
+            reqs = np.array([0, 5])
+            bs = b.block_size
+
+            def ref():
+                sp, st = sub_pool(host_pool, b.block_table, b.seq_lens, reqs)
+                sp = oracle.reshape_and_cache_fp8(b.key[reqs], b.value[reqs], sp,
+                                                  _new_slots(st, b.seq_lens, reqs, bs), bs, ks, vs)
+                part = oracle.split_partials_fp8(b.q[_last_rows(b)[reqs]], sp, st,
+                                                 b.seq_lens[reqs], b.scale, ks, vs, 1)
+                return oracle.lse_merge(part)
+            line["parity"], line["cpu_baseline"] = _decode_check(b, o, lo, reqs, ref,
+                                                                 b.num_kv_heads * d * 2)
+        res[b.name] = line
+        del pool, pools, q, ws, host_pool
         torch.cuda.empty_cache()
     return res
 
 
-def bench_cascade(pa, device, pk, flush, reps=10):
+def bench_cascade(pa, device, pk, flush, reps=SECONDARY_REPS, check=True):
     """Cascade attention on 64 decode requests sharing a prompt (4096 tokens:
     17 MB of K/V per layer, L2-resident; 32768 tokens: 134 MB, more than L2),
     against plain split-KV decode of the same batch, which reads the prompt
     once per request."""
     res = {}
     for prefix in (4096, 32768):
-        b = workloads.shared_prefix_decode(prefix_tokens=prefix, with_pool=False)
+        b = workloads.shared_prefix_decode(prefix_tokens=prefix)
         N, hq, d = b.num_seqs, b.num_q_heads, b.head_size
-        pool = device_pool((b.num_blocks, 2, b.block_size, b.num_kv_heads, d), 6, device)
+        pool = to_dev_bf16(b.pool, device)
+        pa.pa_reshape_and_cache(to_dev_bf16(b.key, device), to_dev_bf16(b.value, device), pool,
+                                to_dev(b.slot_mapping, torch.int64, device))
         q = to_dev_bf16(b.q, device)
         table = to_dev(b.block_table, torch.int32, device)
         qsl = to_dev(b.query_start_loc, torch.int32, device)
@@ -614,54 +958,52 @@ def bench_cascade(pa, device, pk, flush, reps=10):
         lo = torch.empty((N, hq), dtype=torch.float32, device=device)
         plain = _timed_with_flush(lambda: pa.pa_decode(q.view(N, hq, d), pool, table, seq, b.scale,
                                                        ws, o, lo, mx), flush, reps)
-        casc = _timed_with_flush(lambda: pa.pa_cascade_fwd(q, pool, table, qsl, seq, 1, P, b.scale,
-                                                           cws, S1, mx, out=o, lse=lo),
-                                 flush, reps)
+
+        def casc_call():
+            pa.pa_cascade_fwd(q, pool, table, qsl, seq, 1, P, b.scale, cws, S1, mx, out=o, lse=lo)
+        casc = _timed_with_flush(casc_call, flush, reps)
         row = b.num_kv_heads * d * 2 * 2
         unique = (prefix + int((b.seq_lens - prefix).astype(np.int64).sum())) * row
-        res[b.name] = {"prefix_tokens": prefix, "prefix_splits": S1, "suffix_splits": S2,
-                       "cascade_ms": casc, "plain_decode_ms": plain, "speedup": plain / casc,
-                       "unique_kv_bytes": unique,
-                       "cascade_unique_gbs": unique / (casc * 1e-3) / 1e9,
-                       "plain_kv_bytes": b.kv_bytes()}
+        gbs = unique / (casc * 1e-3) / 1e9
+        line = {"seed": b.seed, "prefix_tokens": prefix, "prefix_splits": S1,
+                "suffix_splits": S2, "cascade_ms": casc, "plain_decode_ms": plain,
+                "reps": reps, "speedup": plain / casc, "unique_kv_bytes": unique,
+                "cascade_unique_gbs": gbs, "plain_kv_bytes": b.kv_bytes(),
+                "l2": "flushed (256 MB write) before each launch",
+                "roofline": roofline("hbm", gbs, pk, "GB/s",
+                                     "varlen_tc_kernel (prefix) + decode_splitkv_kernel (suffix) "
+                                     "+ lse_merge", unique)}
+        if check:
+            import oracle
+            casc_call()
+            torch.cuda.synchronize()
+            reqs = np.array([0, 17, 63])
+            rows = _last_rows(b)[reqs]
+            mask = np.zeros(b.num_tokens, np.uint8)
+            mask[rows] = 1
+            ref_pool = oracle.reshape_and_cache(b.key, b.value, b.pool, b.slot_mapping,
+                                                b.block_size)
+
+            def ref():
+                ro, rl = oracle.paged_attention(b.q, ref_pool, b.block_table, b.query_start_loc,
+                                                b.seq_lens, b.scale, row_mask=mask)
+                return ro[rows], rl[rows]
+            line["parity"], line["cpu_baseline"] = _decode_check(b, o, lo, reqs, ref, row)
+        res[b.name] = line
         del pool, q, ws, cws
         torch.cuda.empty_cache()
     return res
 
 
-SECONDARY = {"chunked_prefill": bench_prefill, "long_decode": bench_long_decode,
-             "mla_decode": bench_mla, "fp8_decode": bench_fp8_decode, "cascade": bench_cascade,
+SECONDARY = {"tiny": bench_tiny, "chunked_prefill": bench_prefill,
+             "long_decode": bench_long_decode, "mla_decode": bench_mla,
+             "fp8_decode": bench_fp8_decode, "cascade": bench_cascade,
              "mla_prefill": bench_mla_prefill}
 
 
 def secondary(pa, device, pk):
     flush = l2_flusher(device)
     return {name: fn(pa, device, pk, flush) for name, fn in SECONDARY.items()}
-
-
-def mla_splits(m, sms):
-    """Splits for the MLA workload: each (request, split, 128-head group) runs
-    on a pair of SMs, so enough splits to give every pair slot one unit, and
-    no more (each split adds a 128 x 513 fp32 partial per request)."""
-    groups = max(1, (m.num_heads + 127) // 128)
-    return max(1, min(8, math.ceil((sms // 2) / (m.batch * groups))))
-
-
-def _timed_with_flush(fn, flush, reps):
-    """Median of reps event-timed launches, L2 flushed before each."""
-    for _ in range(3):
-        flush()
-        fn()
-    times = []
-    for _ in range(reps):
-        flush()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        fn()
-        e1.record()
-        torch.cuda.synchronize()
-        times.append(e0.elapsed_time(e1))
-    return statistics.median(times)
 
 
 # ---------------------------------------------------------------------------
@@ -697,7 +1039,8 @@ def main():
     pa.lib()
     pk = peaks()
     if args.only is not None:
-        rec = SECONDARY[args.only](pa, device, pk, l2_flusher(device), reps=args.steps)
+        rec = SECONDARY[args.only](pa, device, pk, l2_flusher(device), reps=args.steps,
+                                  check=False)
         if rank == 0:
             print(json.dumps({"only": args.only, **rec}), flush=True)
         return
@@ -706,7 +1049,7 @@ def main():
     step = DecodeStep(pa, b, device)
     kv_bytes = b.kv_bytes()
 
-    clocks = ClockSampler(local)
+    clocks = NvmlClockSampler(local)
     clocks.start()
     for k in range(warmup):
         step.run(k)
@@ -716,11 +1059,14 @@ def main():
     torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    h0 = time.perf_counter()
     t_start.record()
     for k in range(args.steps):
         step.run(k)
     t_end.record()
     torch.cuda.synchronize()
+    if hasattr(clocks, "mark"):
+        clocks.mark(h0, time.perf_counter())
     if dist is not None:
         dist.barrier()
     total_ms = t_start.elapsed_time(t_end)
@@ -730,10 +1076,15 @@ def main():
     # launches (about 8 us per step), so they stay out of the pass above.
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
+    h0 = time.perf_counter()
     for k in range(args.steps):
         step.run(k, ev[k])
     torch.cuda.synchronize()
+    if hasattr(clocks, "mark"):
+        clocks.mark(h0, time.perf_counter())
     clk = clocks.stop()
+    # The last step's result, for the parity pass of the oracle leg below.
+    head_out, head_lse = step.out.float().cpu().numpy(), step.lse.cpu().numpy()
     dec_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
     achieved = kv_bytes / (dec_ms * 1e-3) / 1e9
     sha = kernel_source_sha(["decode.cu", "pa_common.cuh"])
@@ -750,10 +1101,12 @@ def main():
     if not args.no_secondary and rank == 0:
         sec = secondary(pa, device, pk)
 
-    cpu = None
+    cpu = head_parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, cores, sample = cpu_baseline_sample(b)
+        v, cores, sample, (ref_o, ref_l) = cpu_baseline_sample(b)
         cpu = {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+        head_parity = parity(head_out, ref_o, head_lse, ref_l,
+                             f"all {b.num_seqs} requests x {b.num_q_heads} heads")
 
     if rank == 0:
         rec = {
@@ -761,7 +1114,8 @@ def main():
             "steps": args.steps, "warmup": warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded numpy N(0,1) rounded to bf16; random block permutation)",
-            "config": {"workload": b.name, "num_seqs": b.num_seqs, "seq_lens": "U[128,4096]",
+            "config": {"workload": b.name, "seed": b.seed, "num_seqs": b.num_seqs,
+                       "seq_lens": "U[128,4096]",
                        "num_q_heads": 32, "num_kv_heads": 8, "head_size": 128,
                        "block_size": 16, "num_splits": step.S, "kv_bytes_per_step": kv_bytes,
                        "step": "cache write (64 tokens) + split-KV stage 1 + LSE merge",
@@ -781,6 +1135,7 @@ def main():
                          "peak_source": "MEASURED_PEAKS hbm_gbs (of measured)"
                          if pk["source"] == "measured" else "fallback 6.8 TB/s (of fallback)"},
             "cpu_baseline": cpu,
+            "parity": head_parity,
             "secondary": sec,
         }
         print(json.dumps(rec), flush=True)

@@ -240,6 +240,23 @@ pa_status pa_mla_decode(const void* q, const void* kv_cache, const int32_t* bloc
                         float* lse, void* stream);
 
 /*
+ * A num_splits for pa_mla_decode, chosen from the batch, the head count, the
+ * longest sequence and the SM count (the split count of "Triton and MLA",
+ * key-files list, _compute_num_kv_splits, is likewise chosen from max_seq_len
+ * and sm_count; this rule is the library's for the MLA kernel).  One
+ * (split, request, group of 128 heads) unit runs on a pair of SMs, and each
+ * split adds a [128, kv_lora_rank + 1] fp32 partial per request and head
+ * group (written once and read once by the merge: ~456 tokens' worth of
+ * cache bytes), so the rule takes just enough splits to give every SM pair
+ * one unit, and never splits finer than the page's 512-token pieces:
+ *   units = batch * ceil(num_heads / 128),
+ *   S = min(ceil((sm_count / 2) / units), ceil(max_seq_len / 512)), at least 1.
+ * sm_count <= 0 means the current device's SM count; batch <= 0 or
+ * num_heads <= 0 gives 1.
+ */
+int pa_mla_num_kv_splits(int batch, int num_heads, int max_seq_len, int sm_count);
+
+/*
  * fp8 KV cache.  The pool holds e4m3 codes (OCP FP8 "fn": 1 sign, 4 exponent
  * bits with bias 7, 3 mantissa bits; largest finite 448; 0x7F / 0xFF NaN),
  * one byte per element, in the standard layout [num_blocks, 2, block_size,

@@ -389,6 +389,20 @@ int pa_num_kv_splits(int max_seq_len, int sm_count) {
   return static_cast<int>(s);
 }
 
+int pa_mla_num_kv_splits(int batch, int num_heads, int max_seq_len, int sm_count) {
+  if (batch <= 0 || num_heads <= 0) return 1;
+  if (sm_count <= 0) sm_count = pa_device_sm_count();
+  if (sm_count <= 0) sm_count = 1;
+  const long long units = static_cast<long long>(batch) * ((num_heads + 127) / 128);
+  const long long pairs = sm_count / 2 > 0 ? sm_count / 2 : 1;
+  long long s = (pairs + units - 1) / units;
+  const long long by_len = (static_cast<long long>(max_seq_len > 0 ? max_seq_len : 0) + 511) / 512;
+  if (s > by_len) s = by_len;
+  if (s < 1) s = 1;
+  if (s > kMaxSplits) s = kMaxSplits;
+  return static_cast<int>(s);
+}
+
 size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_splits, int dv) {
   if (num_seqs < 0 || num_q_heads <= 0 || num_splits <= 0 || dv <= 0) return 0;
   return static_cast<size_t>(num_seqs) * num_q_heads * num_splits * (static_cast<size_t>(dv) + 1) *

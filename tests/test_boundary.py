@@ -50,6 +50,22 @@ def test_split_rule_of_the_page(pa):
     assert pa.pa_num_kv_splits(0, 152) == 1
 
 
+def test_mla_split_planner(pa):
+    # S = min(ceil((SMs / 2) / (batch * ceil(H / 128))), ceil(max_seq / 512)), at least 1:
+    # one (split, request, head group) unit per SM pair, never finer than 512 tokens.
+    assert pa.pa_mla_num_kv_splits(128, 128, 8192, 152) == 1      # the DeepSeek-V3-shape batch
+    assert pa.pa_mla_num_kv_splits(8, 128, 8192, 152) == 10       # ceil(76 / 8)
+    assert pa.pa_mla_num_kv_splits(8, 256, 8192, 152) == 5        # two head groups per request
+    assert pa.pa_mla_num_kv_splits(1, 128, 131072, 152) == 76     # one request: every pair
+    assert pa.pa_mla_num_kv_splits(1, 128, 2048, 152) == 4        # capped at 512-token pieces
+    assert pa.pa_mla_num_kv_splits(1, 64, 100, 152) == 1
+    assert pa.pa_mla_num_kv_splits(76, 128, 8192, 152) == 1
+    assert pa.pa_mla_num_kv_splits(75, 128, 8192, 152) == 2
+    assert pa.pa_mla_num_kv_splits(4, 128, 0, 152) == 1
+    assert pa.pa_mla_num_kv_splits(0, 128, 4096, 152) == 1
+    assert pa.pa_mla_num_kv_splits(2, 128, 1 << 20, 1) == 1      # fewer than two SMs
+
+
 def test_workspace_bytes(pa):
     assert pa.pa_decode_workspace_bytes(8, 64, 256, 128) == 8 * 64 * 256 * 129 * 4
     assert pa.pa_decode_workspace_bytes(128, 128, 4, 512) == 128 * 128 * 4 * 513 * 4

@@ -7,7 +7,9 @@ imports the other.
 
 Recipe (the same for every workload):
   * numpy ``default_rng(seed)`` draws N(0, 1) float32 values, rounded to bf16
-    (round to nearest even) and kept as uint16 bit patterns;
+    (round to nearest even) and kept as uint16 bit patterns; arrays of more
+    than 2^22 values are drawn in 2^22-value chunks, chunk k from the k-th
+    child generator (``Generator.spawn``);
   * request lengths are integers drawn uniformly from inclusive ranges;
   * the pool holds exactly sum_i ceil(seq_i / bs) blocks (unless a size is
     given); a seeded permutation of the block ids is handed out to the
@@ -26,6 +28,8 @@ Recipe (the same for every workload):
 from __future__ import annotations
 
 import math
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -43,26 +47,47 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
+def _chunked_fill(rng: np.random.Generator, n: int, chunk: int, fill) -> None:
+    """Calls fill(gen, a, m) for the chunks [a, a + m) of n elements.  An
+    array of one chunk is drawn from ``rng`` itself; a larger one takes one
+    child generator of ``rng`` per chunk (``Generator.spawn``, in chunk
+    order), so the values do not depend on how many threads draw them, and
+    the chunks are drawn on all host cores (numpy releases the GIL while it
+    fills a buffer)."""
+    if n <= chunk:
+        fill(rng, 0, n)
+        return
+    starts = list(range(0, n, chunk))
+    kids = rng.spawn(len(starts))
+    work = [(kids[k], a, min(n, a + chunk) - a) for k, a in enumerate(starts)]
+    threads = max(1, min(len(work), os.cpu_count() or 1))
+    if threads == 1:
+        for w in work:
+            fill(*w)
+        return
+    with ThreadPoolExecutor(threads) as ex:
+        list(ex.map(lambda w: fill(*w), work))
+
+
 def randn_bf16(rng: np.random.Generator, shape, chunk: int = 1 << 22) -> np.ndarray:
     """N(0, 1) values rounded to bf16 (nearest even), as uint16 bits.  Drawn
-    in small chunks through reused buffers, so multi-GB pools need no float32
-    copy of the whole array."""
+    in chunks of ``chunk`` values (see _chunked_fill), so multi-GB pools need
+    no float32 copy of the whole array."""
     n = int(np.prod(shape))
     out = np.empty(n, np.uint16)
-    buf = np.empty(min(n, chunk), np.float32)
-    tmp = np.empty(min(n, chunk), np.uint32)
-    for a in range(0, n, chunk):
-        m = min(n, a + chunk) - a
-        f = buf[:m]
-        rng.standard_normal(m, dtype=np.float32, out=f)
+
+    def fill(gen, a, m):
+        f = np.empty(m, np.float32)
+        gen.standard_normal(m, dtype=np.float32, out=f)
         u = f.view(np.uint32)
-        t = tmp[:m]
-        np.right_shift(u, 16, out=t)
+        t = np.right_shift(u, 16)
         t &= 1
         t += 0x7FFF
         t += u
         t >>= 16
         out[a:a + m] = t
+
+    _chunked_fill(rng, n, chunk, fill)
     return out.reshape(shape)
 
 
@@ -391,14 +416,17 @@ FP8_V_SCALE = float(np.float32(0.0211))
 
 def e4m3_codes(rng: np.random.Generator, shape, chunk: int = 1 << 24) -> np.ndarray:
     """Uniformly random finite e4m3 codes as uint8: each of the 254 codes other
-    than the two NaN codes (0x7F, 0xFF) is equally likely."""
+    than the two NaN codes (0x7F, 0xFF) is equally likely.  Chunked as
+    randn_bf16."""
     n = int(np.prod(shape))
     out = np.empty(n, np.uint8)
-    for a in range(0, n, chunk):
-        m = min(n, a + chunk) - a
-        r = rng.integers(0, 254, size=m, dtype=np.uint8)
+
+    def fill(gen, a, m):
+        r = gen.integers(0, 254, size=m, dtype=np.uint8)
         r[r >= 0x7F] += 1
         out[a:a + m] = r
+
+    _chunked_fill(rng, n, chunk, fill)
     return out.reshape(shape)
 
 
