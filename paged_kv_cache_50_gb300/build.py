@@ -49,17 +49,23 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    """Compile and link libpa.so; returns its path."""
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(OUT_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=None, out_dir=None,
+          lib_name="libpa.so") -> str:
+    """Compile and link libpa.so; returns its path.  ``out_dir`` / ``lib_name``
+    build a variant elsewhere (the tests' timeout variant, with its own
+    defines in ``extra_flags``); the default build never includes one."""
+    out_dir = out_dir or OUT_DIR
+    lib = os.path.join(out_dir, lib_name)
+    if not force and os.path.exists(lib) and all(
+            os.path.getmtime(p) <= os.path.getmtime(lib) for p in _deps()):
+        return lib
+    os.makedirs(out_dir, exist_ok=True)
     cc = nvcc()
     flags = NVCC_FLAGS + list(extra_flags or [])
     objs = []
     cmds = []
     for src in _sources():
-        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         cmds.append([cc, *ARCH, *flags, "-c", src, "-o", obj])
 
@@ -74,10 +80,10 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=min(len(cmds), os.cpu_count() or 4)) as ex:
         list(ex.map(run, cmds))
-    tmp = LIB + f".{os.getpid()}.tmp"
+    tmp = lib + f".{os.getpid()}.tmp"
     run([cc, *ARCH, "-shared", "--cudart", "static", "-o", tmp, *objs])
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

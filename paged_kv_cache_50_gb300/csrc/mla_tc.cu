@@ -19,11 +19,12 @@
 // (st.async into the peer's buffer, completing bytes on the peer's barrier)
 // as 16-bit fixed point: the SM-to-SM path moves only ~12 bytes per clock,
 // and halving the bytes keeps the exchange behind the tensor core.  Each
-// head row of a tile is scaled by a power of two 2^(15 - E) with
-// 2^E > max |S_peer| over the row's visible tokens, rounded to int16 and
-// decoded exactly, so the error of a score is at most 2^(E - 16) <
-// max |S_peer| / 32768 (f16 would allow 2^-12 of each value, ~8x more for the
-// largest scores, which dominate the LSE).  CTA r then holds
+// head row of a tile travels in units of a = max |S_peer| / 32767 over the
+// row's visible tokens (the unit itself is sent with the row), rounded to
+// int16, so the error of a score is at most a / 2 = max |S_peer| / 65534
+// (f16 would allow 2^-12 of each value, ~16x more for the largest scores,
+// which dominate the LSE; a power-of-two unit would waste up to one bit).
+// CTA r then holds
 // S = S_r + decode(S_peer) and runs the online softmax on it; each CTA's
 // output half and row sum come from its own P, so each half is normalised
 // consistently.  The query's latent half is the A operand of the score MMAs
@@ -58,7 +59,7 @@
 //   K/V   4 stages x (4 latent chunks [64 tokens][128 B] + rope half
 //         [64 tokens][64 B])                                          144 KB
 //   X     2 buffers of the peer's partial scores, [9 chunks][128 heads]
-//         [16 B]: 8 chunks of 8 int16 scores, then the row's exponent E, so
+//         [16 B]: 8 chunks of 8 int16 scores, then the row's unit a, so
 //         that one warp-wide store or load covers 512 contiguous bytes 36 KB
 //   P     2 buffers [128 heads][64 tokens] bf16 (128-byte swizzle)     32 KB
 // TMEM: S buffers at columns 0 and 64, the query's latent half (bf16 pairs)
@@ -131,6 +132,14 @@ __device__ __forceinline__ float mex2(float x) {
   return y;
 }
 
+// x += a0 * b, y += a1 * b as one packed fp32 pair FMA.
+__device__ __forceinline__ void ffma2_acc(float& x, float& y, float a0, float a1, float b) {
+  asm("{\n.reg .b64 a, b, c;\nmov.b64 a, {%2, %3};\nmov.b64 b, {%4, %4};\n"
+      "mov.b64 c, {%0, %1};\nfma.rn.f32x2 c, a, b, c;\nmov.b64 {%0, %1}, c;\n}"
+      : "+f"(x), "+f"(y)
+      : "f"(a0), "f"(a1), "f"(b));
+}
+
 __device__ __forceinline__ float mmax3(float a, float b, float c) {
   float y;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
@@ -142,15 +151,17 @@ __device__ __forceinline__ uint32_t xoff(int t, int c) {
   return static_cast<uint32_t>(c * 2048 + t * 16);
 }
 
-// The exchange's 16-bit fixed point, offset binary: a partial score x with
-// |x| < 2^E travels as u = q + 32768, q = x * 2^(15-E) rounded to the
-// nearest integer (nearest even; +32768 clamped to 32767), two per 32-bit
-// word.  Integer <-> float conversions go through a bias, which keeps the
-// exchange on the FMA and integer pipes: x * 2^(15-E) + (1.5 * 2^23 + 32768),
-// rounded once by the FMA, is the float 1.5 * 2^23 + u, whose bits are
-// 0x4B40 << 16 | u for 0 <= u < 2^16.  One byte permute packs a pair's low
-// halves; the receiver rebuilds each float with one byte permute and
-// subtracts the bias exactly.
+// The exchange's 16-bit fixed point, offset binary: a partial score x of a
+// row with max |x| = amax travels as u = q + 32768, q = x * (32767 / amax)
+// rounded to the nearest integer (nearest even; +32768 clamped to 32767),
+// two per 32-bit word; the receiver scales q by a = amax / 32767.
+// Integer <-> float conversions go through a bias, which keeps the exchange
+// on the FMA and integer pipes: x * mul + (1.5 * 2^23 + 32768), rounded once
+// by the FMA, is the float 1.5 * 2^23 + u, whose bits are 0x4B40 << 16 | u
+// for 0 <= u < 2^16.  One byte permute packs a pair's low halves; the
+// receiver rebuilds each float with one byte permute, subtracts the bias
+// (exact: both are integers below 2^24) and adds q * a to its own partial
+// score with one FMA.
 constexpr float kXBias = 12615680.0f;   // 1.5 * 2^23 + 32768
 constexpr uint32_t kXBiasHi = 0x4B40u;  // upper 16 bits of the float 1.5 * 2^23 + u
 __device__ __forceinline__ uint32_t pack_q16(float lo, float hi, float mul) {
@@ -291,7 +302,9 @@ mla_tc_kernel(const __nv_bfloat16* __restrict__ q, const __grid_constant__ CUten
       tc::tc_fence_before();
       tc::mbar_arrive(BAR(kMQFull));
     }
-    float m_used = -CUDART_INF_F, l = 0.f;
+    // l: the row's sum of weights (for the LSE); lr: the sum of the same
+    // weights rounded to bf16, as PV multiplies them (for the output).
+    float m_used = -CUDART_INF_F, l = 0.f, lr = 0.f;
     for (int j = 0; j < ntiles; ++j) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
       const int buf = j & 1;
@@ -317,10 +330,9 @@ mla_tc_kernel(const __nv_bfloat16* __restrict__ q, const __grid_constant__ CUten
       if (!all_ok(tc::mbar_wait_cluster(BAR(kMXFull + buf), (j >> 1) & 1))) break;
       {
         const uint32_t xb = xs + buf * C::kXBytes;
-        int e_row;
-        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(e_row) : "r"(xb + xoff(t, 8)) : "memory");
-        const float unit = __uint_as_float(static_cast<uint32_t>(112 + e_row) << 23);  // 2^(E-15)
-        const float bias_unit = kXBias * unit;   // exact: kXBias < 2^24
+        uint32_t unit_bits;
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(unit_bits) : "r"(xb + xoff(t, 8)) : "memory");
+        const float unit = __uint_as_float(unit_bits);   // a = amax / 32767
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           uint32_t v[4];
@@ -330,14 +342,12 @@ mla_tc_kernel(const __nv_bfloat16* __restrict__ q, const __grid_constant__ CUten
                        : "memory");
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            // The pair's two values q times `unit`, exactly (unit a power of
-            // two): (1.5 * 2^23 + u) * unit - bias_unit = (u - 32768) * unit.
-            // Then added to this CTA's partial scores; both steps as packed
-            // pairs.
-            float d0, d1;
-            ffma2(d0, d1, __uint_as_float(__byte_perm(v[e], kXBiasHi, 0x5410)),
-                  __uint_as_float(__byte_perm(v[e], kXBiasHi, 0x5432)), unit, -bias_unit);
-            fadd2(sc[8 * c + 2 * e], sc[8 * c + 2 * e + 1], d0, d1);
+            // The pair's two values q = (1.5 * 2^23 + u) - bias (exact), then
+            // this CTA's partial scores += q * a; both steps as packed pairs.
+            float d0 = __uint_as_float(__byte_perm(v[e], kXBiasHi, 0x5410));
+            float d1 = __uint_as_float(__byte_perm(v[e], kXBiasHi, 0x5432));
+            fadd2(d0, d1, -kXBias, -kXBias);
+            ffma2_acc(sc[8 * c + 2 * e], sc[8 * c + 2 * e + 1], d0, d1, unit);
           }
         }
       }
@@ -410,11 +420,16 @@ mla_tc_kernel(const __nv_bfloat16* __restrict__ q, const __grid_constant__ CUten
       // P = exp2(s * scale_log2 - m_used) as bf16, row t of shared-memory
       // P buffer `buf` (128-byte swizzle, the A operand of PV), once PV(j-2)
       // has read it.  Keeping P out of TMEM lets S(j+2) reuse the S buffer
-      // as soon as S(j) has been read.
+      // as soon as S(j) has been read.  Two row sums: of the weights (the
+      // LSE), and of the bf16-rounded weights that PV multiplies (the
+      // output's divisor), so that the output is a weighted mean whose
+      // weights sum to 1: where one token dominates, its value comes out
+      // unscaled by the up to 2^-9 rounding of its weight.
       if (j >= 2 && !all_ok(tc::mbar_wait(BAR(kMPDone + buf), ((j >> 1) - 1) & 1))) break;
       {
         const uint32_t pb = sbase + C::kOffP + buf * C::kPBytes;
         float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        float r8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           uint32_t pk[4];
@@ -426,12 +441,15 @@ mla_tc_kernel(const __nv_bfloat16* __restrict__ q, const __grid_constant__ CUten
             const float p1 = mex2(x1);
             fadd2(l8[2 * e], l8[2 * e + 1], p0, p1);
             pk[e] = pack_bf16(p0, p1);
+            fadd2(r8[2 * e], r8[2 * e + 1], __uint_as_float(pk[e] << 16),
+                  __uint_as_float(pk[e] & 0xffff0000u));
           }
           asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(pb + msw128(t, c)),
                        "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3])
                        : "memory");
         }
         l = l * alpha + (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
+        lr = lr * alpha + (((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7])));
       }
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(BAR(kMPFull + buf));
@@ -449,7 +467,7 @@ mla_tc_kernel(const __nv_bfloat16* __restrict__ q, const __grid_constant__ CUten
                                            256 * rank);
     const float lse_v = (ok && l > 0.f) ? (m_used + log2f(l)) * kLn2 : -CUDART_INF_F;
     if (ok) {   // warp-uniform: TMEM loads are collective
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = lr > 0.f ? 1.f / lr : 0.f;
 #pragma unroll 1
       for (int c = 0; c < 256 / 32; ++c) {
         uint32_t r[32];
@@ -537,10 +555,10 @@ mla_tc_kernel(const __nv_bfloat16* __restrict__ q, const __grid_constant__ CUten
         for (int k = 0; k < 8; ++k) a8[k] = mmax3(a8[k], fabsf(v[e + k]), fabsf(v[e + 8 + k]));
       const float amax = mmax3(mmax3(a8[0], a8[1], a8[2]), mmax3(a8[3], a8[4], a8[5]),
                                fmaxf(a8[6], a8[7]));
-      // E with max |v| < 2^E (E = -100 for an all-zero row), and 2^(15 - E).
-      const int ebits = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu);
-      const int e_row = ebits == 0 ? -100 : min(ebits - 126, 127);
-      const float mul = __uint_as_float(static_cast<uint32_t>(142 - e_row) << 23);
+      // The row's unit a = amax / 32767 and its inverse (0 for an all-zero
+      // row, whose codes are then all 0).
+      const float unit = amax * (1.f / 32767.f);
+      const float mul = amax > 0.f ? 32767.f * __frcp_rn(amax) : 0.f;
       // The peer has consumed what this CTA sent into buffer `buf` two
       // tiles ago.
       if (j >= 2 &&
@@ -558,7 +576,7 @@ mla_tc_kernel(const __nv_bfloat16* __restrict__ q, const __grid_constant__ CUten
                         pack_q16(v[e + 2], v[e + 3], mul), pack_q16(v[e + 4], v[e + 5], mul),
                         pack_q16(v[e + 6], v[e + 7], mul), full);
       }
-      tc::st_async_v4(dst + xoff(t, 8), static_cast<uint32_t>(e_row), 0u, 0u, 0u, full);
+      tc::st_async_v4(dst + xoff(t, 8), __float_as_uint(unit), 0u, 0u, 0u, full);
     }
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issue

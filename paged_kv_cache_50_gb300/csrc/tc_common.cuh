@@ -43,8 +43,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Waits for the phase of `bar` with the given parity to complete, giving up
 // after a bounded number of polls (each poll may suspend the thread for a
-// while).  Returns false on timeout.
-constexpr int kWaitPolls = 1 << 20;
+// while).  Returns false on timeout.  PA_WAIT_POLLS overrides the bound (the
+// timeout test builds a variant with a short one).
+#ifndef PA_WAIT_POLLS
+#define PA_WAIT_POLLS (1 << 20)
+#endif
+constexpr int kWaitPolls = PA_WAIT_POLLS;
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   for (int i = 0; i < kWaitPolls; ++i)
     if (mbar_try_wait(bar, parity)) return true;

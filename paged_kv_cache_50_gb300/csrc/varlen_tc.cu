@@ -145,6 +145,14 @@ struct VarlenArgs {
 // flag (4 B, padded to 8) and a ring of 4 tile descriptors (4 B each).
 constexpr int kPieceRing = 4;
 
+#ifdef PA_TEST_HOOKS
+// Test builds only: the producer of the CTA whose linear block index is
+// g_test_skip.x issues no copies (and no byte count) for K/V tile
+// g_test_skip.y, so the waits on that tile's barriers can only end at their
+// poll limit.  Set by pa_test_skip_tile_loads; {-1, -1} = off.
+__device__ int2 g_test_skip = {-1, -1};
+#endif
+
 // EXT = false compiles the plain call (no window, split, offsets, virtual
 // request or partial output: those fields are ignored).
 // MLA = true: keys and values come from the contiguous expanded workspaces
@@ -676,18 +684,25 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
     auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, tc::mbar_wait(bar, parity));
     };
+#ifdef PA_TEST_HOOKS
+    const long long cta_id = blockIdx.x + static_cast<long long>(gridDim.x) *
+                                              (blockIdx.y + static_cast<long long>(gridDim.y) * blockIdx.z);
+    auto skipped = [&](int j) { return cta_id == g_test_skip.x && j == g_test_skip.y; };
+#else
+    auto skipped = [](int) { return false; };
+#endif
     // K(j) and V(j) go to stage j & 1; stage reuse waits for S(j-2) / PV(j-2).
     auto issue_k = [&](int j, int blk) -> bool {
       const int st = j & 1;
       if (j >= 2 && !wait_all(BAR(kKEmpty + st), ((j >> 1) - 1) & 1)) return false;
-      issue(j, blk, 0, sbase + C::kOffK + st * C::kKBytes, BAR(kKFull + st));
+      if (!skipped(j)) issue(j, blk, 0, sbase + C::kOffK + st * C::kKBytes, BAR(kKFull + st));
       return true;
     };
     auto issue_v = [&](int j, int blk) -> bool {
       const int vst = j % C::kVStages;
       if (j >= C::kVStages && !wait_all(BAR(kVEmpty + vst), ((j / C::kVStages) - 1) & 1))
         return false;
-      issue(j, blk, 1, sbase + C::kOffV + vst * C::kVBytes, BAR(kVFull + vst));
+      if (!skipped(j)) issue(j, blk, 1, sbase + C::kOffV + vst * C::kVBytes, BAR(kVFull + vst));
       return true;
     };
     int r0 = raw_of(0), r1 = raw_of(1), r2 = raw_of(2);   // tiles j, j+1, j+2 (raw)
@@ -864,6 +879,16 @@ static cudaError_t launch_varlen_tc_t(const VarlenLaunch& L, cudaStream_t stream
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, map, vmap, a);
 }
+
+#ifdef PA_TEST_HOOKS
+// Test builds only (not declared in pa.h): makes the producer of CTA `cta`
+// (linear block index) of the following varlen launches skip K/V tile `tile`;
+// cta < 0 turns it off.
+extern "C" int pa_test_skip_tile_loads(int cta, int tile) {
+  const int2 v = make_int2(cta, tile);
+  return cudaMemcpyToSymbol(g_test_skip, &v, sizeof(v)) == cudaSuccess ? 0 : 3;
+}
+#endif
 
 cudaError_t launch_varlen_tc(const VarlenLaunch& L, cudaStream_t stream) {
   if (L.mla_k != nullptr)   // MLA prefill attention: [nope | rope] keys, 128-wide values

@@ -152,14 +152,19 @@ def test_mla_prefill_workload_full_size_sampled(pa):
     b = workloads.mla_prefill()
     pool = _written_pool(b, poison=False)
     out, lse = _prefill(pa, b, pool)
+    # Every Q tile's first and last row (the MLA attention has one q head per
+    # kv head, so a 128-row tile is 128 query rows) plus 1 % random rows, in
+    # 8 heads spread over the 128.
     rng = np.random.default_rng(97)
     rows = np.zeros(b.num_tokens, np.uint8)
     for i in range(b.num_seqs):
         a, e = int(b.query_start_loc[i]), int(b.query_start_loc[i + 1])
-        rows[[a, e - 1]] = 1
-        rows[rng.integers(a, e, size=2)] = 1
+        starts = np.arange(a, e, 128)
+        rows[starts] = 1
+        rows[np.minimum(starts + 127, e - 1)] = 1
+    rows[rng.choice(b.num_tokens, b.num_tokens // 100, replace=False)] = 1
     heads = np.zeros(b.num_heads, np.uint8)
-    heads[[0, 77, 127]] = 1
+    heads[[0, 17, 38, 64, 77, 101, 126, 127]] = 1
     ref_o, ref_l = oracle.mla_prefill(b.q, pool, b.w_kv_b, b.block_table, b.query_start_loc,
                                       b.seq_lens, b.scale, head_mask=heads, row_mask=rows)
     r, h = rows.astype(bool), heads.astype(bool)
