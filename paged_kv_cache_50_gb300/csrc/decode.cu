@@ -50,7 +50,7 @@ struct DecodeCfg {
   // (= 4 mod 32: the fragment stores hit 32 distinct banks).
   static constexpr int kOStride = D + 4;
   static constexpr int kHeads = 8 * NT;
-  static constexpr int kCombineBytes = kWarps * (kHeads * kOStride + 2 * kHeads) * 4;
+  static constexpr int kCombineBytes = kWarps * (kHeads * kOStride + 3 * kHeads) * 4;
   static constexpr int kSmemBytes = kPipeBytes > kCombineBytes ? kPipeBytes : kCombineBytes;
 };
 
@@ -145,12 +145,15 @@ decode_splitkv_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
 
   // Per lane: heads nt*8 + 2 tid4 + j (j = 0, 1) -- running max (replicated
   // over the 8 token lanes), partial sums over the lane's tokens, and O^T.
-  float m_r[NT][2], l_r[NT][2];
+  // l_r: the weights' sums (for the LSE); lb_r: the sums of the weights
+  // rounded to bf16, as the PV product multiplies them (the output divisor).
+  float m_r[NT][2], l_r[NT][2], lb_r[NT][2];
   float o[NT][kK][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     m_r[nt][0] = m_r[nt][1] = -CUDART_INF_F;
     l_r[nt][0] = l_r[nt][1] = 0.f;
+    lb_r[nt][0] = lb_r[nt][1] = 0.f;
 #pragma unroll
     for (int md = 0; md < kK; ++md) o[nt][md][0] = o[nt][md][1] = o[nt][md][2] = o[nt][md][3] = 0.f;
   }
@@ -230,6 +233,7 @@ decode_splitkv_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
           const float alpha = fast_exp2(m_r[nt][j] - mx);   // 0 when m_r = -inf
           m_r[nt][j] = mx;
           l_r[nt][j] *= alpha;
+          lb_r[nt][j] *= alpha;
 #pragma unroll
           for (int md = 0; md < kK; ++md) {
             o[nt][md][j] *= alpha;
@@ -245,6 +249,8 @@ decode_splitkv_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
       // each lane gathers its head's four tokens.
       const uint32_t u_lo = pack_bf16(p[0], p[1]);   // token gid, heads 2 tid4, +1
       const uint32_t u_hi = pack_bf16(p[2], p[3]);   // token gid + 8
+      add_bf16x2_f32(lb_r[nt][0], lb_r[nt][1], u_lo);
+      add_bf16x2_f32(lb_r[nt][0], lb_r[nt][1], u_hi);
       const uint32_t xa = __shfl_sync(0xffffffffu, u_lo, srcA);
       const uint32_t xb = __shfl_sync(0xffffffffu, u_lo, srcB);
       const uint32_t ya = __shfl_sync(0xffffffffu, u_hi, srcA);
@@ -274,6 +280,9 @@ decode_splitkv_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
       l_r[nt][j] += __shfl_xor_sync(0xffffffffu, l_r[nt][j], 4);
       l_r[nt][j] += __shfl_xor_sync(0xffffffffu, l_r[nt][j], 8);
       l_r[nt][j] += __shfl_xor_sync(0xffffffffu, l_r[nt][j], 16);
+      lb_r[nt][j] += __shfl_xor_sync(0xffffffffu, lb_r[nt][j], 4);
+      lb_r[nt][j] += __shfl_xor_sync(0xffffffffu, lb_r[nt][j], 8);
+      lb_r[nt][j] += __shfl_xor_sync(0xffffffffu, lb_r[nt][j], 16);
     }
 
   // Merge the four warps' states through shared memory.
@@ -281,6 +290,7 @@ decode_splitkv_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
   float* cbuf = reinterpret_cast<float*>(smem);
   float* mbuf = cbuf + C::kWarps * C::kHeads * C::kOStride;  // [warp][kHeads]
   float* lbuf = mbuf + C::kWarps * C::kHeads;
+  float* rbuf = lbuf + C::kWarps * C::kHeads;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
@@ -295,6 +305,7 @@ decode_splitkv_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
       for (int j = 0; j < 2; ++j) {
         mbuf[warp * C::kHeads + nt * 8 + 2 * tid4 + j] = m_r[nt][j];
         lbuf[warp * C::kHeads + nt * 8 + 2 * tid4 + j] = l_r[nt][j];
+        rbuf[warp * C::kHeads + nt * 8 + 2 * tid4 + j] = lb_r[nt][j];
       }
     }
   }
@@ -311,14 +322,15 @@ decode_splitkv_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
       if (e == 0) dst[D] = -CUDART_INF_F;
       continue;
     }
-    float L = 0.f, acc = 0.f;
+    float L = 0.f, LB = 0.f, acc = 0.f;
 #pragma unroll
     for (int w = 0; w < C::kWarps; ++w) {
       const float f = fast_exp2(mbuf[w * C::kHeads + r] - M);
       L += f * lbuf[w * C::kHeads + r];
+      LB += f * rbuf[w * C::kHeads + r];
       acc += f * cbuf[(w * C::kHeads + r) * C::kOStride + e];
     }
-    dst[e] = acc / L;
+    dst[e] = acc / LB;
     if (e == 0) dst[D] = (M + log2f(L)) * kLn2;
   }
 }

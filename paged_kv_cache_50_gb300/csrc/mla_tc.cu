@@ -441,8 +441,7 @@ mla_tc_kernel(const __nv_bfloat16* __restrict__ q, const __grid_constant__ CUten
             const float p1 = mex2(x1);
             fadd2(l8[2 * e], l8[2 * e + 1], p0, p1);
             pk[e] = pack_bf16(p0, p1);
-            fadd2(r8[2 * e], r8[2 * e + 1], __uint_as_float(pk[e] << 16),
-                  __uint_as_float(pk[e] & 0xffff0000u));
+            add_bf16x2_f32(r8[2 * e], r8[2 * e + 1], pk[e]);
           }
           asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(pb + msw128(t, c)),
                        "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3])

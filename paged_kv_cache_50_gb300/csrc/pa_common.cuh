@@ -165,6 +165,15 @@ __device__ __forceinline__ void fadd2(float& x, float& y, float a0, float a1) {
       : "f"(a0), "f"(a1));
 }
 
+// lo += the low bf16 half of pk, hi += its high half (each widened exactly,
+// then one fp32 add): the row sums of the bf16-rounded softmax weights.
+__device__ __forceinline__ void add_bf16x2_f32(float& lo, float& hi, uint32_t pk) {
+  asm("{\n.reg .b16 l, h;\nmov.b32 {l, h}, %2;\nadd.rn.f32.bf16 %0, l, %0;\n"
+      "add.rn.f32.bf16 %1, h, %1;\n}"
+      : "+f"(lo), "+f"(hi)
+      : "r"(pk));
+}
+
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 

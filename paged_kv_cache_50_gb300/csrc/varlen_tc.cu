@@ -325,7 +325,10 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
       if (!w) fail();
       return w;
     };
-    float m_used = -CUDART_INF_F, l = 0.f;
+    // l: the row's sum of weights (for the LSE); lr: the same weights rounded
+    // to bf16, as PV multiplies them (the output's divisor, so that a
+    // dominant token's value is not scaled by the rounding of its weight).
+    float m_used = -CUDART_INF_F, l = 0.f, lr = 0.f;
     for (int j = 0; j < ntiles; ++j) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
       const int tok0 = tbase + j * C::kBN;
@@ -422,8 +425,10 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
       // columns of the S row, published in two halves (tokens 0-63, 64-127)
       // so that the first half of PV_x(j) runs while the second is computed.
       {
-        // Row sums in eight partial sums, four packed pairs.
+        // Row sums in eight partial sums, four packed pairs (and the same
+        // for the rounded weights).
         float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        float r8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c16 = 0; c16 < C::kBN / 32; ++c16) {
           uint32_t pk[16];
@@ -436,6 +441,7 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
             const float p1 = ex2(x1);
             fadd2(l8[2 * (e & 3)], l8[2 * (e & 3) + 1], p0, p1);
             pk[e] = pack_bf16(p0, p1);
+            add_bf16x2_f32(r8[2 * (e & 3)], r8[2 * (e & 3) + 1], pk[e]);
           }
           tc::tmem_st16(ts + c16 * 16, pk);
           if (c16 == C::kBN / 64 - 1 || c16 == C::kBN / 32 - 1) {
@@ -445,6 +451,7 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
           }
         }
         l = l * alpha + (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
+        lr = lr * alpha + (((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7])));
       }
     }
     // ------------------------------------------------------------ epilogue
@@ -456,7 +463,7 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
     float* wrow = ws == nullptr ? nullptr
                                 : ws + (qrow * a.ws_slots + a.ws_slot0 + split) * (DV + 1);
     if (ok && wrow != nullptr) {   // warp-uniform
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = lr > 0.f ? 1.f / lr : 0.f;
 #pragma unroll
       for (int c = 0; c < DV / 32; ++c) {
         uint32_t r[32];
@@ -474,7 +481,7 @@ varlen_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_consta
         wrow[DV] = -CUDART_INF_F;
       }
     } else if (ok) {   // warp-uniform
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = lr > 0.f ? 1.f / lr : 0.f;
       // A warp's store covers 32 rows (one per thread): 32-byte stores write
       // whole sectors where `out` is 32-byte aligned (rows are multiples of
       // 32 bytes), 16-byte ones otherwise.
