@@ -13,8 +13,10 @@
  *
  * Conventions for every entry point:
  *  - Every data pointer is a DEVICE pointer owned by the caller; the library
- *    allocates nothing, keeps no state beyond a cached SM count per device and
- *    a device error word, and never synchronises the host.
+ *    allocates nothing and never synchronises the host.  Its only state is a
+ *    cached SM count and tensor-map encoder per device, the device error word,
+ *    and the fixed 16 MiB device array of pa_decode_noalloc (present on every
+ *    device that loads the library, used only by that entry point).
  *  - bf16 tensors are passed as `const void*` / `void*` and hold IEEE
  *    bfloat16 values; every tensor is dense and row-major (C order) with the
  *    shape stated below.
