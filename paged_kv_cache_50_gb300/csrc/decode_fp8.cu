@@ -127,7 +127,8 @@ __global__ void __launch_bounds__(128)
 decode_splitkv_fp8_kernel(const __nv_bfloat16* __restrict__ q, const uint8_t* __restrict__ cache,
                           const int32_t* __restrict__ block_table,
                           const int32_t* __restrict__ seq_lens, int max_blocks, int Hq, int Hkv,
-                          int bs, int num_blocks, float scale_log2, float v_scale, int S,
+                          int bs, int bs_log2, int num_blocks, float scale_log2, float v_scale,
+                          int S,
                           int chunk, float* __restrict__ ws, int* err) {
   using C = DecodeFp8Cfg<D, STAGES, NT>;
   constexpr int kK = D / 16;   // k-steps of Q K^T = d-tiles of V^T P^T
@@ -149,7 +150,8 @@ decode_splitkv_fp8_kernel(const __nv_bfloat16* __restrict__ q, const uint8_t* __
   int first_blk[STAGES];
 #pragma unroll
   for (int n = 0; n < STAGES; ++n) {
-    const long long col = (a0 + (warp + n * C::kWarps) * 16) / bs;
+    const long long col = bs_log2 >= 0 ? (a0 + (warp + n * C::kWarps) * 16) >> bs_log2
+                                       : (a0 + (warp + n * C::kWarps) * 16) / bs;
     first_blk[n] = col < max_blocks ? block_at(table, static_cast<int>(col), max_blocks) : -1;
   }
   const int seq = seq_lens[i];
@@ -182,7 +184,7 @@ decode_splitkv_fp8_kernel(const __nv_bfloat16* __restrict__ q, const uint8_t* __
   // Block id of the warp's n-th sub-block (loaded one iteration before its
   // copies are issued, so the table read is off the critical path).
   auto lookup = [&](int n) {
-    return block_at(table, (t0 + (warp + n * C::kWarps) * 16) / bs, max_blocks);
+    return block_at(table, div_bs(t0 + (warp + n * C::kWarps) * 16, bs, bs_log2), max_blocks);
   };
   // Bit n % 32 of okbits: the n-th sub-block's block id was valid (at most
   // STAGES sub-blocks are between issue and use).
@@ -192,7 +194,7 @@ decode_splitkv_fp8_kernel(const __nv_bfloat16* __restrict__ q, const uint8_t* __
     const bool ok = blk >= 0 && blk < num_blocks;
     if (!ok && lane == 0) record_error(err, PA_DEVERR_BLOCK_ID);
     okbits = (okbits & ~(1u << (n & 31))) | (static_cast<uint32_t>(ok) << (n & 31));
-    const int off = tb % bs;
+    const int off = mod_bs(tb, bs, bs_log2);
     const uint8_t* kbase = cache + ((static_cast<int64_t>(ok ? blk : 0) * 2) * bs + off) * row_stride +
                            static_cast<int64_t>(kvh) * D;
     const uint8_t* vbase = kbase + static_cast<int64_t>(bs) * row_stride;
@@ -422,7 +424,7 @@ static cudaError_t launch_decode_fp8_t(const void* q, const void* cache,
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(S, Hkv, N), dim3(C::kThreads), C::kSmemBytes, stream,
                     static_cast<const __nv_bfloat16*>(q), static_cast<const uint8_t*>(cache),
-                    block_table, seq_lens, max_blocks, Hq, Hkv, bs, num_blocks,
+                    block_table, seq_lens, max_blocks, Hq, Hkv, bs, block_size_log2(bs), num_blocks,
                     scale * k_scale * kLog2e, v_scale, S, chunk, ws, err);
 }
 
