@@ -158,6 +158,19 @@ decode_splitkv_fp8_kernel(const __nv_bfloat16* __restrict__ q, const uint8_t* __
   const int t0 = static_cast<int>(a0 < seq ? a0 : seq);
   const int t1 = (s == S - 1) ? seq : static_cast<int>(a0 + chunk < seq ? a0 + chunk : seq);
   const int nsb = (t1 - t0 + 15) >> 4;
+  if (nsb == 0) {
+    // An empty split (the request ends before it starts): o = 0, lse = -inf
+    // for the group's heads, and nothing else.  With the split size taken
+    // from the batch's longest request, many of a ragged batch's splits are
+    // empty.
+    pdl_trigger();
+    for (int idx = threadIdx.x; idx < grp * (D + 1); idx += C::kThreads) {
+      const int r = idx / (D + 1), e = idx - r * (D + 1);
+      ws[((static_cast<int64_t>(i) * Hq + kvh * grp + r) * S + s) * (D + 1) + e] =
+          e == D ? -CUDART_INF_F : 0.f;
+    }
+    return;
+  }
   const int my_n = nsb > warp ? (nsb - warp + C::kWarps - 1) / C::kWarps : 0;
 
   // Q^T as the B operand: lane (gid, tid4) holds head nt*8 + gid (zero past
