@@ -629,7 +629,10 @@ def bench_prefill(pa, device, pk, flush, reps=SECONDARY_REPS, check=True):
            "frac_of_bf16_peak": tf / pk["bf16_tflops"],
            "l2": "flushed (256 MB write) before each launch",
            "roofline": roofline("tensor", tf, pk, "TFLOP/s", "varlen_tc_kernel",
-                                b.causal_flops())}
+                                b.causal_flops(),
+                                profiled_traffic("varlen_tc_chunked_prefill.md",
+                                                 kernel_source_sha(["varlen_tc.cu",
+                                                                    "tc_common.cuh"])))}
     if check:
         import oracle
         prefill()
