@@ -131,6 +131,22 @@ def test_decode_rejects(pa):
     assert L.pa_lse_merge(NULL, 2, 8, 4, 128, 1, NULL, NULL) == pa.PA_ERR_INVALID
 
 
+def test_limits_are_rejected_one_past(pa):
+    """One past each launch limit: 65536 requests, 16385 splits."""
+    L = pa.lib()
+    s = _shape(pa, num_seqs=65536)
+    assert L.pa_decode_splitkv(16, 16, 16, 16, ctypes.byref(s), 0.1, 4, 64, 16, NULL) == \
+        pa.PA_ERR_INVALID
+    assert L.pa_varlen_fwd(16, 16, 16, 16, 16, 1, 1, ctypes.byref(s), 0.1, 1, 16, NULL, NULL) == \
+        pa.PA_ERR_INVALID
+    ok = _shape(pa)
+    assert L.pa_decode_splitkv(16, 16, 16, 16, ctypes.byref(ok), 0.1, 16385, 64, 16, NULL) == \
+        pa.PA_ERR_INVALID
+    assert L.pa_lse_merge(16, 2, 8, 16385, 128, 16, NULL, NULL) == pa.PA_ERR_INVALID
+    assert L.pa_mla_decode(16, 16, 16, 16, 65536, 128, 512, 64, 64, 10, 10, 64, 0.1, 1, 16, 16,
+                           NULL, NULL) == pa.PA_ERR_INVALID
+
+
 def test_cache_write_rejects(pa):
     L = pa.lib()
     assert L.pa_reshape_and_cache(1, 1, 1, 1, 4, ctypes.byref(_shape(pa, block_size=24)),
