@@ -4,7 +4,7 @@ Headline workload: the GQA decode batch with the Llama-3-8B attention shape
 (64 requests x 1 query, seq_lens U[128, 4096], 32 q / 8 kv heads, head_size
 128, block_size 16, bf16).  One step = the whole decode hot path on that
 batch: the cache write of the step's 64 new tokens, split-KV stage 1 with the
-page's split rule, and the LSE merge.  ``value`` is decode KV throughput in
+split count of the library's planner, and the LSE merge.  ``value`` is decode KV throughput in
 GB/s: the bytes of K and V the step must read (4096 B per token per kv-head
 pair, summed over the batch) divided by the time per step.
 
@@ -257,7 +257,12 @@ class DecodeStep:
         self.table = to_dev(b.block_table, torch.int32, device)
         self.seq = to_dev(b.seq_lens, torch.int32, device)
         self.max_seq = int(b.seq_lens.max())
-        self.S = pa.pa_num_kv_splits(self.max_seq, pa.pa_device_sm_count())
+        # The library's decode planner (about twelve CTAs per SM, never more
+        # splits than the page's rule): 4 for this batch, where the page's
+        # rule gives 8 and each extra CTA costs start-up and combine time.
+        self.S = pa.pa_decode_num_kv_splits(N, b.num_kv_heads, self.max_seq,
+                                            pa.pa_device_sm_count())
+        self.S_page = pa.pa_num_kv_splits(self.max_seq, pa.pa_device_sm_count())
         self.ws = pa.decode_workspace(N, hq, self.S, d, device=device)
         self.out = torch.empty((N, hq, d), dtype=torch.bfloat16, device=device)
         self.lse = torch.empty((N, hq), dtype=torch.float32, device=device)
@@ -885,7 +890,11 @@ def bench_fp8_decode(pa, device, pk, flush, reps=SECONDARY_REPS, check=True):
         table = to_dev(b.block_table, torch.int32, device)
         seq = to_dev(b.seq_lens, torch.int32, device)
         mx = int(b.seq_lens.max())
-        S = pa.pa_num_kv_splits(mx, pa.pa_device_sm_count())
+        sms = pa.pa_device_sm_count()
+        # The long-context batch keeps the page's rule (its workload fixes
+        # S); the GQA batch takes the library's planner, as the headline.
+        S = (pa.pa_num_kv_splits(mx, sms) if make is workloads.long_decode
+             else pa.pa_decode_num_kv_splits(N, b.num_kv_heads, mx, sms))
         ws = pa.decode_workspace(N, hq, S, d, device=device)
         o = torch.empty((N, hq, d), dtype=torch.bfloat16, device=device)
         lo = torch.empty((N, hq), dtype=torch.float32, device=device)
@@ -1120,7 +1129,9 @@ def main():
             "config": {"workload": b.name, "seed": b.seed, "num_seqs": b.num_seqs,
                        "seq_lens": "U[128,4096]",
                        "num_q_heads": 32, "num_kv_heads": 8, "head_size": 128,
-                       "block_size": 16, "num_splits": step.S, "kv_bytes_per_step": kv_bytes,
+                       "block_size": 16, "num_splits": step.S,
+                       "splits_from": f"pa_decode_num_kv_splits (the page's rule: {step.S_page})",
+                       "kv_bytes_per_step": kv_bytes,
                        "step": "cache write (64 tokens) + split-KV stage 1 + LSE merge",
                        "l2": "inputs larger than L2: 4 rotating pool copies of "
                              f"{kv_bytes / 1e9:.2f} GB", "parallelism": f"replicas x{world}",

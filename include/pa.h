@@ -242,6 +242,20 @@ pa_status pa_mla_decode(const void* q, const void* kv_cache, const int32_t* bloc
                         float* lse, void* stream);
 
 /*
+ * A num_splits for pa_decode_splitkv / pa_decode_splitkv_fp8 chosen from the
+ * batch as well as max_seq_len and the SM count (the library's planner; the
+ * page's rule is pa_num_kv_splits).  Every (request, kv head, split) is one
+ * CTA, and each CTA pays a fixed start-up and combine cost, so the planner
+ * takes just enough splits for about twelve CTAs per SM, never more than
+ * the page's rule gives:
+ *   S = min(max(1, ceil(12 * sm_count / (num_seqs * num_kv_heads))),
+ *           pa_num_kv_splits(max_seq_len, sm_count)).
+ * sm_count <= 0 means the current device's SM count; num_seqs <= 0 or
+ * num_kv_heads <= 0 gives 1.
+ */
+int pa_decode_num_kv_splits(int num_seqs, int num_kv_heads, int max_seq_len, int sm_count);
+
+/*
  * A num_splits for pa_mla_decode, chosen from the batch, the head count, the
  * longest sequence and the SM count (the split count of "Triton and MLA",
  * key-files list, _compute_num_kv_splits, is likewise chosen from max_seq_len

@@ -60,6 +60,8 @@ def lib() -> ctypes.CDLL:
         L.pa_num_kv_splits.argtypes = [i32, i32]
         L.pa_num_kv_splits.restype = i32
         L.pa_mla_num_kv_splits.argtypes = [i32, i32, i32, i32]
+        L.pa_decode_num_kv_splits.argtypes = [i32, i32, i32, i32]
+        L.pa_decode_num_kv_splits.restype = i32
         L.pa_mla_num_kv_splits.restype = i32
         L.pa_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
         L.pa_decode_workspace_bytes.restype = ctypes.c_size_t
@@ -334,6 +336,12 @@ def pa_cascade_fwd(q, kv_cache, block_table, query_start_loc, seq_lens, max_quer
 
 def pa_num_kv_splits(max_seq_len: int, sm_count: int = 0) -> int:
     return int(lib().pa_num_kv_splits(int(max_seq_len), int(sm_count)))
+
+
+def pa_decode_num_kv_splits(num_seqs: int, num_kv_heads: int, max_seq_len: int,
+                            sm_count: int = 0) -> int:
+    return int(lib().pa_decode_num_kv_splits(int(num_seqs), int(num_kv_heads), int(max_seq_len),
+                                             int(sm_count)))
 
 
 def pa_mla_num_kv_splits(batch: int, num_heads: int, max_seq_len: int,

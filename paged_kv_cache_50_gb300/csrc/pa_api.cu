@@ -389,6 +389,18 @@ int pa_num_kv_splits(int max_seq_len, int sm_count) {
   return static_cast<int>(s);
 }
 
+int pa_decode_num_kv_splits(int num_seqs, int num_kv_heads, int max_seq_len, int sm_count) {
+  if (num_seqs <= 0 || num_kv_heads <= 0) return 1;
+  if (sm_count <= 0) sm_count = pa_device_sm_count();
+  if (sm_count <= 0) sm_count = 1;
+  const long long units = static_cast<long long>(num_seqs) * num_kv_heads;
+  long long s = (12LL * sm_count + units - 1) / units;
+  const int page = pa_num_kv_splits(max_seq_len, sm_count);
+  if (s > page) s = page;
+  if (s < 1) s = 1;
+  return static_cast<int>(s);
+}
+
 int pa_mla_num_kv_splits(int batch, int num_heads, int max_seq_len, int sm_count) {
   if (batch <= 0 || num_heads <= 0) return 1;
   if (sm_count <= 0) sm_count = pa_device_sm_count();

@@ -50,6 +50,17 @@ def test_split_rule_of_the_page(pa):
     assert pa.pa_num_kv_splits(0, 152) == 1
 
 
+def test_decode_split_planner(pa):
+    # S = min(max(1, ceil(12 * SMs / (N * Hkv))), page rule): ~12 CTAs per SM.
+    assert pa.pa_decode_num_kv_splits(64, 8, 4096, 152) == 4       # the GQA decode batch
+    assert pa.pa_decode_num_kv_splits(8, 8, 131072, 152) == 29     # long context (the page: 256)
+    assert pa.pa_decode_num_kv_splits(64, 8, 1000, 152) == 2       # capped by ceil(1000 / 512)
+    assert pa.pa_decode_num_kv_splits(4096, 8, 4096, 152) == 1
+    assert pa.pa_decode_num_kv_splits(1, 1, 1 << 20, 152) == 304   # capped at 2 x SMs
+    assert pa.pa_decode_num_kv_splits(0, 8, 4096, 152) == 1
+    assert pa.pa_decode_num_kv_splits(64, 8, 0, 152) == 1
+
+
 def test_mla_split_planner(pa):
     # S = min(ceil((SMs / 2) / (batch * ceil(H / 128))), ceil(max_seq / 512)), at least 1:
     # one (split, request, head group) unit per SM pair, never finer than 512 tokens.

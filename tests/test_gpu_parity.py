@@ -209,7 +209,8 @@ def test_decode_gqa_workload_all_requests(pa):
                                           b.seq_lens, b.scale)
     sms = pa.pa_device_sm_count()
     S_page = pa.pa_num_kv_splits(int(b.seq_lens.max()), sms)
-    for S in sorted({S_page, 1, 37}):
+    S_plan = pa.pa_decode_num_kv_splits(b.num_seqs, b.num_kv_heads, int(b.seq_lens.max()), sms)
+    for S in sorted({S_page, S_plan, 1, 37}):
         out, lse, ws = _decode(pa, d, S)
         assert_out_close(out, ref_o, f"gqa decode S={S}")
         assert_lse_close(lse, ref_l, f"gqa decode lse S={S}")
