@@ -66,7 +66,7 @@ template <int D, int STAGES, int NT>
 __global__ void __launch_bounds__(128)
 decode_splitkv_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ cache,
                       const int32_t* __restrict__ block_table, const int32_t* __restrict__ seq_lens,
-                      int max_blocks, int Hq, int Hkv, int bs, int num_blocks, float scale_log2,
+                      int max_blocks, int Hq, int Hkv, int bs, int bs_log2, int num_blocks, float scale_log2,
                       int S, int chunk, float* __restrict__ ws, int* err, DecodeExt ext) {
   using C = DecodeCfg<D, STAGES, NT>;
   constexpr int kK = D / 16;   // k-steps of K Q^T = d-tiles of V^T P^T
@@ -79,12 +79,25 @@ decode_splitkv_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
 
   // Every input may come from the previous kernel in the stream.
   pdl_wait();
-  // ext.seq_off tokens at the front of every request are skipped (their
-  // blocks are the first ext.table_col0 columns of the table row).
-  const int seq = max(0, seq_lens[i] - ext.seq_off);
   // Split s covers [s*chunk, (s+1)*chunk) of the request (the last split runs
   // to the end), chunk being one block-aligned size for the whole batch.
   const long long a0 = static_cast<long long>(s) * chunk;
+  // ext.seq_off tokens at the front of every request are skipped (their
+  // blocks are the first ext.table_col0 columns of the table row).
+  const int32_t* table = block_table + static_cast<int64_t>(i) * max_blocks + ext.table_col0;
+  const int cols = max_blocks - ext.table_col0;
+  // Block ids of the warp's first STAGES sub-blocks, read together with
+  // seq_len (they do not depend on it when the split is not empty, which
+  // then starts at a0); ids of sub-blocks the split does not have are never
+  // used.
+  int first_blk[STAGES];
+#pragma unroll
+  for (int n = 0; n < STAGES; ++n) {
+    const long long tok = a0 + (warp + n * C::kWarps) * 16;
+    const long long col = bs_log2 >= 0 ? tok >> bs_log2 : tok / bs;
+    first_blk[n] = col < cols ? block_at(table, static_cast<int>(col), cols) : -1;
+  }
+  const int seq = max(0, seq_lens[i] - ext.seq_off);
   const int t0 = static_cast<int>(a0 < seq ? a0 : seq);
   const int t1 = (s == S - 1) ? seq : static_cast<int>(a0 + chunk < seq ? a0 + chunk : seq);
   const int nsb = (t1 - t0 + 15) >> 4;
@@ -122,13 +135,11 @@ decode_splitkv_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
 
   const uint32_t wbase = smem_u32(smem) + warp * C::kWarpBytes;
   const int64_t row_stride = static_cast<int64_t>(Hkv) * D;
-  const int32_t* table = block_table + static_cast<int64_t>(i) * max_blocks + ext.table_col0;
-  const int cols = max_blocks - ext.table_col0;
 
   // Block id of the warp's n-th sub-block (loaded one iteration before its
   // copies are issued, so the table read is off the critical path).
   auto lookup = [&](int n) {
-    return block_at(table, (t0 + (warp + n * C::kWarps) * 16) / bs, cols);
+    return block_at(table, div_bs(t0 + (warp + n * C::kWarps) * 16, bs, bs_log2), cols);
   };
   // Bit n % 32 of okbits: the n-th sub-block's block id was valid (at most
   // STAGES sub-blocks are between issue and use).
@@ -138,7 +149,7 @@ decode_splitkv_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
     const bool ok = blk >= 0 && blk < num_blocks;
     if (!ok && lane == 0) record_error(err, PA_DEVERR_BLOCK_ID);
     okbits = (okbits & ~(1u << (n & 31))) | (static_cast<uint32_t>(ok) << (n & 31));
-    const int off = tb % bs;
+    const int off = mod_bs(tb, bs, bs_log2);
     const __nv_bfloat16* kbase =
         cache + ((static_cast<int64_t>(ok ? blk : 0) * 2) * bs + off) * row_stride +
         static_cast<int64_t>(kvh) * D;
@@ -173,10 +184,10 @@ decode_splitkv_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
 
 #pragma unroll
   for (int n = 0; n < STAGES - 1; ++n) {
-    if (n < my_n) issue(n, lookup(n));
+    if (n < my_n) issue(n, first_blk[n]);
     cp_async_commit();
   }
-  int next_blk = STAGES - 1 < my_n ? lookup(STAGES - 1) : -1;
+  int next_blk = STAGES - 1 < my_n ? first_blk[STAGES - 1] : -1;
 
   // Source lanes of the P^T operand: tokens 2 tid4 (srcA) and 2 tid4 + 1
   // (srcB) hold head gid in the lane of tid4' = gid / 2, half gid % 2.
@@ -361,7 +372,8 @@ static cudaError_t launch_decode_t(const void* q, const void* cache, const int32
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(S, Hkv, N), dim3(C::kThreads), C::kSmemBytes, stream,
                     static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(cache),
-                    block_table, seq_lens, max_blocks, Hq, Hkv, bs, num_blocks, scale * kLog2e, S,
+                    block_table, seq_lens, max_blocks, Hq, Hkv, bs, block_size_log2(bs), num_blocks,
+                    scale * kLog2e, S,
                     chunk, ws, err, ext);
 }
 

@@ -20,11 +20,9 @@ __device__ __forceinline__ void record_error(int* err, int bit) {
 
 // Block id of logical block `idx` of a request's table row; a column past the
 // row (a seq_len longer than the table allows) reads as an invalid id (-1).
-// log2(bs) if the block size is a power of two, else -1: the fp8 decode
-// kernel then splits a token index into (block, offset) with a shift and a
-// mask instead of an integer division per 16-token sub-block.  (The bf16
-// kernel keeps the division: with it removed the compiler scheduled its main
-// loop in fewer registers and the GQA batch ran 1.4 % slower.)
+// log2(bs) if the block size is a power of two, else -1: the decode kernels
+// then split a token index into (block, offset) with a shift and a mask
+// instead of an integer division per 16-token sub-block.
 inline int block_size_log2(int bs) {
   return (bs > 0 && (bs & (bs - 1)) == 0) ? __builtin_ctz(static_cast<unsigned>(bs)) : -1;
 }
