@@ -50,7 +50,10 @@
 //   warp 10    exchange helper: once the softmax warps have read the peer's
 //              partial scores of a tile, tells the peer its buffer is free
 //              (a thread with no remote stores of its own in flight, so the
-//              cluster-scope release does not wait for them).
+//              cluster-scope release does not wait for them).  The query's
+//              latent half is staged through the exchange buffers, so the
+//              first "buffer free" of each buffer comes from the softmax
+//              warps once they have read the query back.
 // O is rescaled only when a head's running max grows by more than 2^8
 // (exact: P keeps the older reference max).
 //
@@ -197,18 +200,25 @@ mla_tc_kernel(const __nv_bfloat16* __restrict__ q, const __grid_constant__ CUten
   // kMlaRankMax keep the grid order.
   int b = blockIdx.y;
   if (gridDim.y <= kMlaRankMax) {
-    const int nb = static_cast<int>(gridDim.y);
-    volatile int* sl = reinterpret_cast<volatile int*>(sgen + C::kOffX);
+    // The lengths are padded with -1 (below every length) to a multiple of
+    // four, so that each thread reads them as 16-byte vectors.
+    const int nb = static_cast<int>(gridDim.y), nb4 = (nb + 3) >> 2;
+    int* sl = reinterpret_cast<int*>(sgen + C::kOffX);
     volatile int* pick =
         reinterpret_cast<volatile int*>(sgen + C::kOffBar + 8 * kMNumBars + 16 + 4 * kMlaRing);
-    for (int i = threadIdx.x; i < nb; i += blockDim.x) sl[i] = seq_lens[i];
+    for (int i = threadIdx.x; i < 4 * nb4; i += blockDim.x) sl[i] = i < nb ? seq_lens[i] : -1;
     __syncthreads();
+    const int4* sl4 = reinterpret_cast<const int4*>(sl);
     for (int i = threadIdx.x; i < nb; i += blockDim.x) {
       const int v = sl[i];
       int rnk = 0;
-      for (int k = 0; k < nb; ++k) {
-        const int u = sl[k];
-        rnk += (u > v || (u == v && k < i)) ? 1 : 0;
+#pragma unroll 8
+      for (int k = 0; k < nb4; ++k) {
+        const int4 u = sl4[k];
+        rnk += (u.x > v || (u.x == v && 4 * k < i)) ? 1 : 0;
+        rnk += (u.y > v || (u.y == v && 4 * k + 1 < i)) ? 1 : 0;
+        rnk += (u.z > v || (u.z == v && 4 * k + 2 < i)) ? 1 : 0;
+        rnk += (u.w > v || (u.w == v && 4 * k + 3 < i)) ? 1 : 0;
       }
       if (rnk == static_cast<int>(blockIdx.y)) *pick = i;
     }
@@ -241,7 +251,7 @@ mla_tc_kernel(const __nv_bfloat16* __restrict__ q, const __grid_constant__ CUten
     tc::mbar_init(BAR(kMSFull + 1), 1);
     for (int k = 0; k < 2; ++k) {
       tc::mbar_init(BAR(kMXFull + k), 1);
-      tc::mbar_init(BAR(kMXEmpty + k), 1);   // the peer's exchange helper
+      tc::mbar_init(BAR(kMXEmpty + k), 1);   // the peer: its softmax warps, then its helper
       tc::mbar_init(BAR(kMXRead + k), 128);
     }
     for (int k = 0; k < 2; ++k) {
@@ -281,26 +291,43 @@ mla_tc_kernel(const __nv_bfloat16* __restrict__ q, const __grid_constant__ CUten
     {
       // Head t's latent half of the query, [256 r, 256 r + 256), as the A
       // operand of the score MMAs: TMEM lane t, two bf16 per column (the
-      // lower index in the low half).
+      // lower index in the low half).  The 512 bytes of each row come in
+      // with one round of 16-byte asynchronous copies into the exchange and
+      // P buffers (64 KB, unused until the first scores), chunk c of row t
+      // at t * 512 + (c ^ (t & 7)) * 16 so that the reads back are free of
+      // bank conflicts.
       const int head = hg * C::kH + t;
-      const uint4* src = reinterpret_cast<const uint4*>(
+      const char* src = reinterpret_cast<const char*>(
           q + (static_cast<int64_t>(b) * H + (head < H ? head : 0)) * C::kDk + 256 * rank);
+      const uint32_t stg = xs + static_cast<uint32_t>(t) * 512u;
+#pragma unroll
+      for (int c = 0; c < 32; ++c)
+        cp_async_16(stg + ((c ^ (t & 7)) << 4), src + 16 * c, head < H ? 16 : 0);
+      cp_async_commit();
+      cp_async_wait<0>();
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          const uint4 x = head < H ? __ldg(src + c * 8 + v) : make_uint4(0, 0, 0, 0);
-          r[4 * v] = x.x;
-          r[4 * v + 1] = x.y;
-          r[4 * v + 2] = x.z;
-          r[4 * v + 3] = x.w;
-        }
+        for (int v = 0; v < 8; ++v)
+          asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(r[4 * v]), "=r"(r[4 * v + 1]), "=r"(r[4 * v + 2]), "=r"(r[4 * v + 3])
+                       : "r"(stg + (((8 * c + v) ^ (t & 7)) << 4))
+                       : "memory");
         tc::tmem_st32(tmem + lane_base + C::kColQ + c * 32, r);
       }
       tc::tmem_wait_st();
       tc::tc_fence_before();
       tc::mbar_arrive(BAR(kMQFull));
+      // Once all 128 rows have been read back, the peer may send into the
+      // exchange buffers: the first phase of both of its "buffer consumed"
+      // barriers.
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (t == 0) {
+        const uint32_t xempty_peer = tc::map_to_rank(BAR(kMXEmpty), peer);
+        tc::mbar_arrive_remote(xempty_peer);
+        tc::mbar_arrive_remote(xempty_peer + 8u);
+      }
     }
     // l: the row's sum of weights (for the LSE); lr: the sum of the same
     // weights rounded to bf16, as PV multiplies them (for the output).
@@ -560,9 +587,7 @@ mla_tc_kernel(const __nv_bfloat16* __restrict__ q, const __grid_constant__ CUten
       const float mul = amax > 0.f ? 32767.f * __frcp_rn(amax) : 0.f;
       // The peer has consumed what this CTA sent into buffer `buf` two
       // tiles ago.
-      if (j >= 2 &&
-          !__all_sync(0xffffffffu,
-                      tc::mbar_wait_cluster(BAR(kMXEmpty + buf), ((j >> 1) - 1) & 1))) {
+      if (!__all_sync(0xffffffffu, tc::mbar_wait_cluster(BAR(kMXEmpty + buf), (j >> 1) & 1))) {
         fail();
         break;
       }
