@@ -70,8 +70,8 @@ typedef struct pa_shape {
   int num_kv_heads;       /* Hkv; Hq % Hkv == 0, q head h reads kv head h/(Hq/Hkv) */
   int head_size;          /* d                                                  */
   int block_size;         /* tokens per cache block; a positive multiple of 16  */
-  int num_blocks;         /* blocks in the pool                                 */
-  int max_blocks_per_seq; /* columns of block_table                             */
+  int num_blocks;         /* blocks in the pool; at least 1                     */
+  int max_blocks_per_seq; /* columns of block_table; at least 1                 */
 } pa_shape;
 
 /*
@@ -233,7 +233,9 @@ pa_status pa_lse_merge(const float* workspace, int num_seqs, int num_q_heads,
  * with num_splits == 1 and `out` 16-byte aligned it writes out and lse
  * directly and leaves the workspace untouched (it must still be passed).
  * Supported: kv_lora_rank == 512, rope_dim == 64, num_heads a multiple of 64,
- * block_size a multiple of 32.
+ * block_size a multiple of 32.  num_blocks and max_blocks_per_seq must be at
+ * least 1 (a pool with no blocks is PA_ERR_INVALID, even for a batch whose
+ * requests are all empty).
  */
 pa_status pa_mla_decode(const void* q, const void* kv_cache, const int32_t* block_table,
                         const int32_t* seq_lens, int batch, int num_heads, int kv_lora_rank,

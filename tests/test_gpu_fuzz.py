@@ -6,7 +6,8 @@ split count.  Each case draws the kv-head count, the group size (1-16), the
 head size (64 / 128), the block size (a multiple of 16, powers of two and
 not), the request count, lengths mixed with block-boundary values, and the
 query lengths; the parametrised tests elsewhere walk these axes one at a
-time, this one crosses them.
+time, this one crosses them.  A second set does the same for MLA latent
+decode (head count, block size, batch, lengths, split count).
 """
 
 import numpy as np
@@ -114,4 +115,38 @@ def test_random_shape(pa, seed):
     torch.cuda.synchronize()
     assert_out_close(bf16_to_f64(out), r8o, f"fp8 decode {what}")
     assert_lse_close(lse.cpu().numpy(), r8l, f"fp8 decode lse {what}")
+    assert pa.pa_get_device_error() == 0
+
+
+def draw_mla_case(seed):
+    """The shape of MLA case `seed`: head count, block size (a multiple of
+    32), batch, lengths (0 allowed, tile and block boundaries mixed in) and
+    split count."""
+    rng = np.random.default_rng(5000 + seed)
+    heads = int(rng.choice([64, 128, 256]))
+    bs = int(rng.choice([32, 64, 96, 128]))
+    batch = int(rng.integers(1, 10))
+    edges = [0, 1, 63, 64, 65, bs - 1, bs, bs + 1, 2 * bs]
+    seq = [int(rng.choice(edges)) if rng.random() < 0.4 else int(rng.integers(1, 2500))
+           for _ in range(batch)]
+    if max(seq) == 0:
+        seq[0] = 1   # a pool needs at least one block
+    splits = int(rng.integers(1, 4))
+    return dict(heads=heads, bs=bs, seq=seq, S=splits)
+
+
+@pytest.mark.parametrize("seed", list(range(24)))
+def test_random_mla_decode(pa, seed):
+    import math
+    c = draw_mla_case(seed)
+    m = workloads.make_mla_batch(f"mla_fuzz{seed}", 5100 + seed, c["seq"], c["heads"],
+                                 block_size=c["bs"], scale=1.0 / math.sqrt(192.0))
+    ref_o, ref_l = oracle.mla_decode(m.q, m.pool, m.block_table, m.seq_lens, m.scale)
+    ws = pa.decode_workspace(m.batch, c["heads"], c["S"], 512)
+    out, lse = pa.pa_mla_decode(to_dev_bf16(m.q), to_dev_bf16(m.pool),
+                                to_dev(m.block_table, torch.int32),
+                                to_dev(m.seq_lens, torch.int32), m.scale, ws)
+    torch.cuda.synchronize()
+    assert_out_close(bf16_to_f64(out), ref_o, f"mla seed {seed} {c}")
+    assert_lse_close(lse.cpu().numpy(), ref_l, f"mla lse seed {seed} {c}")
     assert pa.pa_get_device_error() == 0
