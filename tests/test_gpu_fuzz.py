@@ -6,8 +6,10 @@ split count.  Each case draws the kv-head count, the group size (1-16), the
 head size (64 / 128), the block size (a multiple of 16, powers of two and
 not), the request count, lengths mixed with block-boundary values, and the
 query lengths; the parametrised tests elsewhere walk these axes one at a
-time, this one crosses them.  A second set does the same for MLA latent
-decode (head count, block size, batch, lengths, split count).
+time, this one crosses them.  Further sets do the same for MLA latent
+decode (head count, block size, batch, lengths, split count), cascade
+attention (prefix length, suffixes, decode or prefill rows, masking, both
+split counts) and MLA prefill (head count, block size, lengths, masking).
 """
 
 import numpy as np
@@ -149,4 +151,116 @@ def test_random_mla_decode(pa, seed):
     torch.cuda.synchronize()
     assert_out_close(bf16_to_f64(out), ref_o, f"mla seed {seed} {c}")
     assert_lse_close(lse.cpu().numpy(), ref_l, f"mla lse seed {seed} {c}")
+    assert pa.pa_get_device_error() == 0
+
+
+def draw_cascade_case(seed):
+    """Shape of cascade case `seed`: a shared prefix of 1-39 blocks, 1-6
+    requests with their own suffixes, decode (one query each) or prefill
+    rows, causal or not, and the two split counts."""
+    rng = np.random.default_rng(6000 + seed)
+    hkv = int(rng.choice([1, 2, 4]))
+    g = int(rng.choice([1, 2, 4, 8, 16]))
+    while hkv * g > 32:
+        hkv //= 2
+    d = int(rng.choice([64, 128]))
+    bs = int(rng.choice([16, 32, 64]))
+    prefix_blocks = int(rng.integers(1, 40))
+    n = int(rng.integers(1, 7))
+    decode = bool(rng.random() < 0.5)
+    suf = [int(rng.integers(1, 400)) for _ in range(n)]
+    ql = [1] * n if decode else [int(min(x, rng.integers(1, 150))) for x in suf]
+    causal = True if decode else bool(rng.random() < 0.7)
+    return dict(hkv=hkv, g=g, d=d, bs=bs, P=prefix_blocks, suf=suf, ql=ql, causal=causal,
+                S1=int(rng.integers(1, 7)), S2=int(rng.integers(1, 5)))
+
+
+@pytest.mark.parametrize("seed", list(range(24)))
+def test_random_cascade(pa, seed):
+    from tests.test_gpu_parity import Dev
+    c = draw_cascade_case(seed)
+    hq = c["hkv"] * c["g"]
+    b = workloads.make_shared_prefix_batch(f"casc_fuzz{seed}", 6100 + seed, c["P"], c["suf"],
+                                           c["ql"], hq, c["hkv"], c["d"], c["bs"])
+    dev = Dev(pa, b)
+    pool = dev.ref_pool()
+    ref_o, ref_l = oracle.paged_attention(b.q, pool, b.block_table, b.query_start_loc,
+                                          b.seq_lens, b.scale, causal=c["causal"])
+    ws = pa.cascade_workspace(b.num_tokens, hq, c["S1"], c["S2"], c["d"])
+    out, lse = pa.pa_cascade_fwd(dev.q, dev.pool, dev.table, dev.qsl, dev.seq,
+                                 int(b.query_lens.max()), c["P"], b.scale, ws, c["S1"],
+                                 causal=c["causal"])
+    torch.cuda.synchronize()
+    assert_out_close(bf16_to_f64(out), ref_o, f"cascade seed {seed} {c}")
+    assert_lse_close(lse.cpu().numpy(), ref_l, f"cascade lse seed {seed} {c}")
+    assert pa.pa_get_device_error() == 0
+
+
+def draw_mla_prefill_case(seed):
+    """Shape of MLA prefill case `seed`: head count, block size, 1-4
+    requests, context and new-token lengths, causal or not."""
+    rng = np.random.default_rng(7000 + seed)
+    heads = int(rng.choice([4, 8, 16, 20, 32, 128]))
+    bs = int(rng.choice([16, 32, 64, 128]))
+    n = int(rng.integers(1, 5))
+    top = 200 if heads == 128 else 400
+    seq = [int(rng.integers(1, top)) for _ in range(n)]
+    ql = [int(min(x, rng.integers(1, 200))) for x in seq]
+    return dict(heads=heads, bs=bs, seq=seq, ql=ql, causal=bool(rng.random() < 0.8))
+
+
+@pytest.mark.parametrize("seed", list(range(12)))
+def test_random_mla_prefill(pa, seed):
+    """The output within the usual tolerance of the oracle's.  The LSE
+    within 1e-3 plus what the expansion's own rounding can move it by: the
+    kernel accumulates each expanded key element in fp32 and rounds it to
+    bf16, the oracle rounds the fp64 product, and where the sum lies that
+    close to a rounding boundary the two pick neighbouring bf16 values (the
+    expansion test bounds this by one unit in the last place).  A key that
+    moves by dK moves a score by at most scale * sum_e |q_e| |dK_e|, and the
+    LSE by at most the largest such score shift over the visible tokens; the
+    allowance is that shift, from the kernel's expanded keys (read back from
+    the workspace) against the oracle's."""
+    from tests.test_gpu_mla_prefill import _expanded_ref, _written_pool
+    c = draw_mla_prefill_case(seed)
+    b = workloads.make_mla_prefill_batch(f"mlap_fuzz{seed}", 7100 + seed, c["seq"], c["ql"],
+                                         c["heads"], block_size=c["bs"])
+    pool = _written_pool(b)
+    n_req, heads = b.num_seqs, b.num_heads
+    s_max = int(b.seq_lens.max())
+    ws = torch.empty(pa.pa_mla_prefill_workspace_bytes(n_req, s_max, heads), dtype=torch.uint8,
+                     device="cuda")
+    out, lse = pa.pa_mla_prefill(to_dev_bf16(b.q), to_dev_bf16(pool), to_dev_bf16(b.w_kv_b),
+                                 to_dev(b.block_table, torch.int32),
+                                 to_dev(b.query_start_loc, torch.int32),
+                                 to_dev(b.seq_lens, torch.int32), int(b.query_lens.max()),
+                                 b.scale, ws, causal=c["causal"])
+    torch.cuda.synchronize()
+    what = f"mla prefill seed {seed} {c}"
+    ref_o, ref_l = oracle.mla_prefill(b.q, pool, b.w_kv_b, b.block_table, b.query_start_loc,
+                                      b.seq_lens, b.scale, causal=c["causal"])
+    assert_out_close(bf16_to_f64(out), ref_o, what)
+    got_l = lse.cpu().numpy().astype(np.float64)
+    assert np.array_equal(np.isneginf(got_l), np.isneginf(ref_l)), what
+    k_gpu = bf16_to_f64(ws[: n_req * s_max * heads * 192 * 2].view(torch.bfloat16)
+                        .view(n_req, s_max, heads, 192))
+    q_abs = np.abs(workloads.bf16_bits_to_f32(b.q).astype(np.float64))
+    qsl = b.query_start_loc
+    for i in range(n_req):
+        rows = slice(int(qsl[i]), int(qsl[i + 1]))
+        n, ql = int(b.seq_lens[i]), int(qsl[i + 1] - qsl[i])
+        if ql == 0:
+            continue
+        k_ref, _, _ = _expanded_ref(b, pool, i, np.arange(heads))
+        dk = np.abs(k_gpu[i, :n] - k_ref)                                     # [n, h, 192]
+        shift = b.scale * np.einsum("rhe,phe->rhp", q_abs[rows], dk)          # [ql, h, n]
+        if c["causal"]:
+            pos = n - ql + np.arange(ql)
+            shift = np.where(np.arange(n)[None, None, :] <= pos[:, None, None], shift, 0.0)
+        allow = 1e-3 + shift.max(axis=2)
+        err = np.abs(got_l[rows] - ref_l[rows])
+        fin = np.isfinite(ref_l[rows])
+        bad = fin & (err > allow)
+        assert not bad.any(), (f"{what}: request {i}: LSE error {err[fin].max():.3e} beyond "
+                               f"1e-3 + the expansion's rounding shift")
     assert pa.pa_get_device_error() == 0
