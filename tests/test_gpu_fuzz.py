@@ -228,7 +228,9 @@ def test_random_mla_prefill(pa, seed):
     pool = _written_pool(b)
     n_req, heads = b.num_seqs, b.num_heads
     s_max = int(b.seq_lens.max())
-    ws = torch.empty(pa.pa_mla_prefill_workspace_bytes(n_req, s_max, heads), dtype=torch.uint8,
+    # Zeroed so that the slots past each request's length (never written)
+    # convert cleanly when the expanded keys are read back.
+    ws = torch.zeros(pa.pa_mla_prefill_workspace_bytes(n_req, s_max, heads), dtype=torch.uint8,
                      device="cuda")
     out, lse = pa.pa_mla_prefill(to_dev_bf16(b.q), to_dev_bf16(pool), to_dev_bf16(b.w_kv_b),
                                  to_dev(b.block_table, torch.int32),
