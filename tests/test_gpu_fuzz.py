@@ -9,7 +9,9 @@ query lengths; the parametrised tests elsewhere walk these axes one at a
 time, this one crosses them.  Further sets do the same for MLA latent
 decode (head count, block size, batch, lengths, split count), cascade
 attention (prefix length, suffixes, decode or prefill rows, masking, both
-split counts) and MLA prefill (head count, block size, lengths, masking).
+split counts) and MLA prefill (head count, block size, lengths, masking),
+and a last set takes larger batches (grids of thousands of CTAs) with the
+varlen rows sampled.
 """
 
 import numpy as np
@@ -265,4 +267,66 @@ def test_random_mla_prefill(pa, seed):
         bad = fin & (err > allow)
         assert not bad.any(), (f"{what}: request {i}: LSE error {err[fin].max():.3e} beyond "
                                f"1e-3 + the expansion's rounding shift")
+    assert pa.pa_get_device_error() == 0
+
+
+def draw_large_case(seed):
+    """A larger random batch: up to 64 requests of up to 8192 tokens, either
+    prefill-like (up to 2048 new rows each) or decode-like (up to 8), any
+    masking, up to 64 splits; grids of thousands of CTAs."""
+    rng = np.random.default_rng(9000 + seed)
+    hkv = int(rng.choice([1, 2, 4, 8]))
+    g = int(rng.choice([1, 2, 4, 8]))
+    d = int(rng.choice([64, 128]))
+    bs = int(rng.choice([16, 32, 64, 128]))
+    n = int(rng.integers(1, 65))
+    seq = rng.integers(1, 8193, size=n)
+    top = 2049 if rng.random() < 0.5 else 9
+    ql = np.minimum(seq, rng.integers(1, top, size=n))
+    causal = bool(rng.random() < 0.8)
+    return dict(hkv=hkv, g=g, d=d, bs=bs, seq=seq, ql=ql, causal=causal,
+                S=int(rng.integers(1, 65)), rng=rng)
+
+
+@pytest.mark.parametrize("seed", list(range(10)))
+def test_random_large_shape(pa, seed):
+    """Varlen attention on every request's first and last row and 300 random
+    rows, and split-KV decode of every request's last row, against the
+    oracle."""
+    c = draw_large_case(seed)
+    rng = c.pop("rng")
+    hq = c["hkv"] * c["g"]
+    b = workloads.make_paged_batch(f"large{seed}", 9100 + seed, c["seq"], c["ql"], hq, c["hkv"],
+                                   c["d"], c["bs"], causal=c["causal"])
+    what = f"seed {seed} hkv {c['hkv']} g {c['g']} d {c['d']} bs {c['bs']} n {len(c['seq'])} " \
+           f"T {b.num_tokens} causal {c['causal']} S {c['S']}"
+    pool = to_dev_bf16(b.pool)
+    pa.pa_reshape_and_cache(to_dev_bf16(b.key), to_dev_bf16(b.value), pool,
+                            to_dev(b.slot_mapping, torch.int64))
+    ref_pool = oracle.reshape_and_cache(b.key, b.value, b.pool, b.slot_mapping, c["bs"])
+    assert np.array_equal(bf16_bits(pool), ref_pool), what
+    table, seql = to_dev(b.block_table, torch.int32), to_dev(b.seq_lens, torch.int32)
+    qsl = b.query_start_loc
+    out, lse = pa.pa_varlen_fwd(to_dev_bf16(b.q), pool, table, to_dev(qsl, torch.int32), seql,
+                                int(b.query_lens.max()), b.scale, causal=c["causal"])
+    torch.cuda.synchronize()
+    mask = np.zeros(b.num_tokens, np.uint8)
+    mask[qsl[:-1]] = 1
+    mask[qsl[1:] - 1] = 1
+    mask[rng.choice(b.num_tokens, size=min(b.num_tokens, 300), replace=False)] = 1
+    ref_o, ref_l = oracle.paged_attention(b.q, ref_pool, b.block_table, qsl, b.seq_lens, b.scale,
+                                          causal=c["causal"], row_mask=mask)
+    sel = mask.astype(bool)
+    assert_out_close(bf16_to_f64(out)[sel], ref_o[sel], f"varlen {what}")
+    assert_lse_close(lse.cpu().numpy()[sel], ref_l[sel], f"varlen lse {what}")
+    last = qsl[1:] - 1
+    n = b.num_seqs
+    q = to_dev_bf16(b.q[last]).view(n, hq, c["d"])
+    ref_o, ref_l = oracle.lse_merge(
+        oracle.split_partials(b.q[last], ref_pool, b.block_table, b.seq_lens, b.scale, 1))
+    ws = pa.decode_workspace(n, hq, c["S"], c["d"])
+    out, lse = pa.pa_decode(q, pool, table, seql, b.scale, ws)
+    torch.cuda.synchronize()
+    assert_out_close(bf16_to_f64(out), ref_o, f"decode {what}")
+    assert_lse_close(lse.cpu().numpy(), ref_l, f"decode lse {what}")
     assert pa.pa_get_device_error() == 0
