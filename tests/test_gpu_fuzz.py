@@ -59,7 +59,15 @@ def draw_case(seed):
     mode = str(rng.choice(["causal", "noncausal", "window"]))
     window = int(rng.integers(1, 600))
     splits = int(rng.integers(1, 9))
-    return dict(hkv=hkv, g=g, d=d, bs=bs, seq=seq, ql=ql, mode=mode, window=window, S=splits)
+    # fp8 scales, log-uniform over [0.002, 0.04]: at the small end many new
+    # keys and values saturate at +-448 codes.  The pool's cached entries are
+    # random codes (up to 448 * scale), so the upper end keeps them below ~18:
+    # with values in the hundreds, an output that is a small difference of
+    # large weighted terms is only as exact as the weights (f16, 2^-11), and
+    # the absolute 1e-2 bar is meant for values of unit scale.
+    ks, vs = (float(np.exp(rng.uniform(np.log(0.002), np.log(0.04)))) for _ in range(2))
+    return dict(hkv=hkv, g=g, d=d, bs=bs, seq=seq, ql=ql, mode=mode, window=window, S=splits,
+                ks=ks, vs=vs)
 
 
 @pytest.mark.parametrize("seed", SEEDS)
@@ -105,17 +113,19 @@ def test_random_shape(pa, seed):
     torch.cuda.synchronize()
     assert_out_close(bf16_to_f64(out), ref_ld, f"decode {what}")
     assert_lse_close(lse.cpu().numpy(), ref_ll, f"decode lse {what}")
-    # The same batch over an fp8 pool: quantising write (bit-exact), decode.
+    # The same batch over an fp8 pool at the case's scales: quantising write
+    # (bit-exact), decode.
     p8 = workloads.fp8_pool(b)
     d8 = torch.from_numpy(p8.copy()).cuda()
+    ks, vs = c["ks"], c["vs"]
     pa.pa_reshape_and_cache_fp8(to_dev_bf16(b.key), to_dev_bf16(b.value), d8,
-                                to_dev(b.slot_mapping, torch.int64), KS, VS)
-    ref8 = oracle.reshape_and_cache_fp8(b.key, b.value, p8, b.slot_mapping, c["bs"], KS, VS)
+                                to_dev(b.slot_mapping, torch.int64), ks, vs)
+    ref8 = oracle.reshape_and_cache_fp8(b.key, b.value, p8, b.slot_mapping, c["bs"], ks, vs)
     assert np.array_equal(d8.cpu().numpy(), ref8), what
     r8o, r8l = oracle.lse_merge(oracle.split_partials_fp8(b.q[last], ref8, b.block_table,
-                                                          b.seq_lens, b.scale, KS, VS, 1))
+                                                          b.seq_lens, b.scale, ks, vs, 1))
     ws = pa.decode_workspace(n, hq, c["S"], c["d"])
-    out, lse = pa.pa_decode_fp8(q, d8, table, seql, b.scale, KS, VS, ws)
+    out, lse = pa.pa_decode_fp8(q, d8, table, seql, b.scale, ks, vs, ws)
     torch.cuda.synchronize()
     assert_out_close(bf16_to_f64(out), r8o, f"fp8 decode {what}")
     assert_lse_close(lse.cpu().numpy(), r8l, f"fp8 decode lse {what}")
