@@ -66,8 +66,11 @@ def draw_case(seed):
     # large weighted terms is only as exact as the weights (f16, 2^-11), and
     # the absolute 1e-2 bar is meant for values of unit scale.
     ks, vs = (float(np.exp(rng.uniform(np.log(0.002), np.log(0.04)))) for _ in range(2))
+    # Softmax scale, log-uniform over [1/4, 4] / sqrt(d): from flat rows to
+    # rows dominated by a few tokens.
+    scale = float(np.exp(rng.uniform(np.log(0.25), np.log(4.0)))) / np.sqrt(d)
     return dict(hkv=hkv, g=g, d=d, bs=bs, seq=seq, ql=ql, mode=mode, window=window, S=splits,
-                ks=ks, vs=vs)
+                ks=ks, vs=vs, scale=scale)
 
 
 @pytest.mark.parametrize("seed", SEEDS)
@@ -75,7 +78,8 @@ def test_random_shape(pa, seed):
     c = draw_case(seed)
     hq = c["hkv"] * c["g"]
     b = workloads.make_paged_batch(f"fuzz{seed}", 4100 + seed, c["seq"], c["ql"], hq, c["hkv"],
-                                   c["d"], c["bs"], causal=c["mode"] != "noncausal")
+                                   c["d"], c["bs"], causal=c["mode"] != "noncausal",
+                                   scale=c["scale"])
     what = f"seed {seed} {c}"
     # Cache write, bit-exact.
     pool = to_dev_bf16(b.pool)
@@ -146,15 +150,15 @@ def draw_mla_case(seed):
     if max(seq) == 0:
         seq[0] = 1   # a pool needs at least one block
     splits = int(rng.integers(1, 4))
-    return dict(heads=heads, bs=bs, seq=seq, S=splits)
+    scale = float(np.exp(rng.uniform(np.log(0.25), np.log(4.0)))) / np.sqrt(192.0)
+    return dict(heads=heads, bs=bs, seq=seq, S=splits, scale=scale)
 
 
 @pytest.mark.parametrize("seed", list(range(24)))
 def test_random_mla_decode(pa, seed):
-    import math
     c = draw_mla_case(seed)
     m = workloads.make_mla_batch(f"mla_fuzz{seed}", 5100 + seed, c["seq"], c["heads"],
-                                 block_size=c["bs"], scale=1.0 / math.sqrt(192.0))
+                                 block_size=c["bs"], scale=c["scale"])
     ref_o, ref_l = oracle.mla_decode(m.q, m.pool, m.block_table, m.seq_lens, m.scale)
     ws = pa.decode_workspace(m.batch, c["heads"], c["S"], 512)
     out, lse = pa.pa_mla_decode(to_dev_bf16(m.q), to_dev_bf16(m.pool),
